@@ -1,0 +1,303 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each check is chosen so that a plausible mistake in the oracle fails it:
+hand-derived routing and permutation cases (tests/golden/routing_hand.json),
+brute-force top-k by explicit rank counting, closed-form gates, permutation
+invariants, identity experts (combine must return x times the sum of kept
+gates), a dense every-expert-then-mask formulation of the layer, the k=1 single
+expert case against a textbook MLP written with torch.nn.functional, and
+central finite differences for every gradient.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as orc
+from synth import gen, workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "routing_hand.json")
+
+
+def _f(v):
+    return float("-inf") if v == "-inf" else float(v)
+
+
+# ---------------------------------------------------------------- golden
+def test_golden_topk_cases():
+    cases = json.load(open(GOLDEN))["topk"]
+    for c in cases:
+        l = np.array([[_f(v) for v in row] for row in c["logits"]], dtype=np.float32)
+        idx, g = orc.route_topk(l, c["k"])
+        assert idx.tolist() == c["idx"], c["name"]
+        np.testing.assert_allclose(g, np.array(c["gates"]), rtol=0, atol=1e-15, err_msg=c["name"])
+
+
+def test_golden_permute_cases():
+    cases = json.load(open(GOLDEN))["permute"]
+    for c in cases:
+        idx = np.array(c["idx"], dtype=np.int32)
+        p = orc.permute(idx, c["E"], c["capacity"])
+        for key in ("counts_raw", "counts", "offsets", "row_of_slot", "slot_of_row"):
+            assert p[key].tolist() == c[key], (c["name"], key)
+
+
+# ---------------------------------------------------------------- top-k
+def brute_force_topk(l: np.ndarray, k: int):
+    """rank_e = #{e': l_e' > l_e} + #{e' < e: l_e' == l_e}; slot = rank."""
+    T, E = l.shape
+    idx = np.full((T, k), -1, dtype=np.int64)
+    for t in range(T):
+        for e in range(E):
+            r = 0
+            for e2 in range(E):
+                if l[t, e2] > l[t, e] or (l[t, e2] == l[t, e] and e2 < e):
+                    r += 1
+            if r < k:
+                idx[t, r] = e
+    return idx
+
+
+def _adversarial_logits(T, E, seed):
+    rng = np.random.default_rng(seed)
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    l[0] = 0.0                                  # all equal
+    l[1, ::3] = 5.0                             # many maxima
+    l[2] = -0.0; l[2, E // 2] = 0.0             # signed zeros
+    l[3, : E // 2] = -np.inf                    # -inf columns
+    l[4] = np.round(l[4])                       # coarse values, many ties
+    l[5, E - 1] = np.float32(1e30)              # large value at the end
+    return l
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (8, 8), (64, 4), (128, 4), (256, 8), (5, 1)])
+def test_topk_matches_brute_force(E, k):
+    l = _adversarial_logits(12, E, seed=E * 31 + k)
+    idx, g = orc.route_topk(l, k)
+    assert np.array_equal(idx, brute_force_topk(l, k))
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (64, 4), (128, 4)])
+def test_gates_closed_form(E, k):
+    l = gen.random_logits(64, E)
+    idx, g = orc.route_topk(l, k)
+    # softmax over all E, then renormalise over the selected set
+    l64 = l.astype(np.float64)
+    p = np.exp(l64 - l64.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    sel = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+    np.testing.assert_allclose(g, sel / sel.sum(axis=1, keepdims=True), rtol=1e-12, atol=0)
+    np.testing.assert_allclose(g.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert np.all(np.diff(g, axis=1) <= 0)  # slot order = descending gate
+
+
+def test_random_routing_gates_are_softmax_over_the_k_drawn():
+    T, E, k = 256, 64, 4
+    l = gen.random_routing_logits(T, E, k)
+    assert np.all(np.isfinite(l).sum(axis=1) == k)
+    idx, g = orc.route_topk(l, k)
+    for t in range(T):
+        fin = np.nonzero(np.isfinite(l[t]))[0]
+        assert set(idx[t].tolist()) == set(fin.tolist())
+        z = l[t, fin].astype(np.float64)
+        sm = np.exp(z - z.max()) / np.exp(z - z.max()).sum()
+        np.testing.assert_allclose(sorted(g[t]), sorted(sm), rtol=1e-12)
+
+
+# ---------------------------------------------------------------- permutation
+@pytest.mark.parametrize("T,E,k,cap", [(300, 8, 2, 0), (300, 8, 2, 40), (1000, 64, 4, 0),
+                                       (1000, 64, 4, orc.capacity_of(1000, 4, 64)), (7, 4, 4, 1)])
+def test_permutation_invariants(T, E, k, cap):
+    l = gen.random_logits(T, E)
+    l[:, 0] += 1.0  # skew the load
+    idx, _ = orc.route_topk(l, k)
+    p = orc.permute(idx, E, cap)
+    R = int(p["offsets"][-1])
+    row = p["row_of_slot"]
+    kept = row >= 0
+    # bijection between kept slots and rows [0, R)
+    assert sorted(row[kept].tolist()) == list(range(R))
+    assert np.array_equal(p["slot_of_row"][row[kept]], np.nonzero(kept)[0])
+    assert p["counts"].sum() == R == T * k - (~kept).sum()
+    assert p["counts_raw"].sum() == T * k
+    if cap > 0:
+        assert np.all(p["counts"] <= cap)
+    # each segment holds expert e's tokens, in strictly increasing token order
+    for e in range(E):
+        seg = p["slot_of_row"][p["offsets"][e]:p["offsets"][e + 1]]
+        toks = seg // k
+        assert np.all(idx.reshape(-1)[seg] == e)
+        assert np.all(np.diff(toks) > 0)
+        # dropped slots of e are exactly its latest tokens beyond the capacity
+        all_toks = np.nonzero((idx == e).any(axis=1))[0]
+        n_keep = len(all_toks) if cap <= 0 else min(cap, len(all_toks))
+        assert np.array_equal(toks, all_toks[:n_keep])
+
+
+# ---------------------------------------------------------------- layer pins
+def _tiny_inputs(T, d, E, H, Hs, seed, learned=True):
+    rng = np.random.default_rng(seed)
+    inp = {
+        "x": rng.standard_normal((T, d)),
+        "W_g": 0.3 * rng.standard_normal((E, H, d)),
+        "W_u": 0.3 * rng.standard_normal((E, H, d)),
+        "W_d": 0.3 * rng.standard_normal((E, d, H)),
+        "dY": rng.standard_normal((T, d)),
+    }
+    if learned:
+        inp["W_r"] = 0.5 * rng.standard_normal((E, d))
+    if Hs:
+        inp["Ws_g"] = 0.3 * rng.standard_normal((Hs, d))
+        inp["Ws_u"] = 0.3 * rng.standard_normal((Hs, d))
+        inp["Ws_d"] = 0.3 * rng.standard_normal((d, Hs))
+    return inp
+
+
+@pytest.mark.parametrize("cap", [0, 3])
+def test_identity_experts_return_x_times_sum_of_kept_gates(cap):
+    w = workloads.WORKLOADS["tiny"]
+    inp = orc.inputs_to_f64(workloads.make_inputs(w))
+    inp.pop("Ws_g", None)
+    f = orc.layer_forward(inp, w.k, cap, expert_fn=lambda e, xr: xr)
+    kept_gate_sum = (f["gates"] * f["kept"]).sum(axis=1)
+    np.testing.assert_allclose(f["y"], inp["x"] * kept_gate_sum[:, None], rtol=1e-13, atol=1e-13)
+    if cap == 0:
+        np.testing.assert_allclose(kept_gate_sum, 1.0, atol=1e-12)
+    else:
+        assert (kept_gate_sum < 1.0 - 1e-9).any()
+
+
+def dense_masked_layer(inp, k, cap):
+    """Every expert on every token, then masked: y = s + sum_e m[t,e] G[t,e] f_e(x[t]).
+    The mask comes from explicit rank counting, the gates from the full
+    softmax renormalised over the mask, the capacity from a token-order count."""
+    x = inp["x"]
+    T, d = x.shape
+    l = (x @ inp["W_r"].T).astype(np.float32).astype(np.float64)
+    E = l.shape[1]
+    sel_idx = brute_force_topk(l.astype(np.float32), k)
+    mask = np.zeros((T, E), dtype=bool)
+    for t in range(T):
+        mask[t, sel_idx[t]] = True
+    p = np.exp(l - l.max(axis=1, keepdims=True))
+    G = np.where(mask, p, 0.0)
+    G /= G.sum(axis=1, keepdims=True)
+    keep = mask.copy()
+    if cap > 0:
+        seen = np.zeros(E, dtype=int)
+        for t in range(T):
+            for e in range(E):
+                if mask[t, e]:
+                    keep[t, e] = seen[e] < cap
+                    seen[e] += 1
+    y = np.zeros((T, d))
+    for e in range(E):
+        a = x @ inp["W_g"][e].T
+        u = x @ inp["W_u"][e].T
+        fe = (a / (1 + np.exp(-a)) * u) @ inp["W_d"][e].T
+        y += (keep[:, e] * G[:, e])[:, None] * fe
+    if "Ws_g" in inp:
+        a = x @ inp["Ws_g"].T
+        u = x @ inp["Ws_u"].T
+        y += (a / (1 + np.exp(-a)) * u) @ inp["Ws_d"].T
+    return y
+
+
+@pytest.mark.parametrize("cap", [0, 5])
+def test_routed_layer_equals_dense_masked_layer(cap):
+    inp = _tiny_inputs(T=24, d=16, E=6, H=12, Hs=8, seed=3)
+    f = orc.layer_forward(inp, 2, cap)
+    yd = dense_masked_layer(inp, 2, cap)
+    np.testing.assert_allclose(f["y"], yd, rtol=1e-12, atol=1e-12)
+
+
+def test_single_expert_k1_is_a_dense_swiglu_mlp():
+    inp = _tiny_inputs(T=10, d=16, E=1, H=24, Hs=8, seed=5)
+    f = orc.layer_forward(inp, 1, 0)
+    F = torch.nn.functional
+    x = torch.tensor(inp["x"])
+
+    def mlp(Wg, Wu, Wd):
+        return F.linear(F.silu(F.linear(x, torch.tensor(Wg))) * F.linear(x, torch.tensor(Wu)), torch.tensor(Wd))
+
+    y_ref = mlp(inp["W_g"][0], inp["W_u"][0], inp["W_d"][0]) + mlp(inp["Ws_g"], inp["Ws_u"], inp["Ws_d"])
+    np.testing.assert_allclose(f["gates"], 1.0)
+    np.testing.assert_allclose(f["y"], y_ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- backward
+def _loss(inp, k, cap, **kw):
+    f = orc.layer_forward(inp, k, cap, exact_router=True, **kw)
+    return float((f["y"] * inp["dY"]).sum()), f
+
+
+def _fd_setup(cap, seed0=11):
+    # reseed until no top-k decision is within 1e-3 of flipping
+    for seed in range(seed0, seed0 + 50):
+        inp = _tiny_inputs(T=8, d=12, E=4, H=8, Hs=6, seed=seed)
+        l = inp["x"] @ inp["W_r"].T
+        s = -np.sort(-l, axis=1)
+        if np.min(s[:, 1] - s[:, 2]) > 1e-3 and np.min(s[:, 0] - s[:, 1]) > 1e-3:
+            return inp
+    raise RuntimeError("no well-separated seed")
+
+
+@pytest.mark.parametrize("cap", [0, 3])
+def test_backward_matches_central_finite_differences(cap):
+    k = 2
+    inp = _fd_setup(cap)
+    _, f = _loss(inp, k, cap)
+    b = orc.layer_backward(inp, f)
+    eps = 1e-6
+    names = {"x": "dx", "W_r": "dW_r", "W_g": "dW_g", "W_u": "dW_u", "W_d": "dW_d",
+             "Ws_g": "dWs_g", "Ws_u": "dWs_u", "Ws_d": "dWs_d"}
+    for name, gname in names.items():
+        P = inp[name]
+        num = np.zeros_like(P)
+        it = np.nditer(P, flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            old = P[i]
+            P[i] = old + eps
+            lp, fp = _loss(inp, k, cap)
+            P[i] = old - eps
+            lm, fm = _loss(inp, k, cap)
+            P[i] = old
+            assert np.array_equal(fp["idx"], f["idx"]) and np.array_equal(fm["idx"], f["idx"])
+            num[i] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(b[gname], num, rtol=1e-6, atol=1e-7, err_msg=gname)
+    # gates treated as inputs
+    G = f["gates"].copy()
+    num = np.zeros_like(G)
+    for i in np.ndindex(G.shape):
+        Gp = G.copy(); Gp[i] += eps
+        Gm = G.copy(); Gm[i] -= eps
+        num[i] = (_loss(inp, k, cap, gates=Gp)[0] - _loss(inp, k, cap, gates=Gm)[0]) / (2 * eps)
+    np.testing.assert_allclose(b["dgates"], num, rtol=1e-6, atol=1e-7)
+    # logits treated as inputs
+    L = f["logits"].copy()
+    num = np.zeros_like(L)
+    for i in np.ndindex(L.shape):
+        Lp = L.copy(); Lp[i] += eps
+        Lm = L.copy(); Lm[i] -= eps
+        num[i] = (_loss(inp, k, cap, logits=Lp)[0] - _loss(inp, k, cap, logits=Lm)[0]) / (2 * eps)
+    np.testing.assert_allclose(b["dlogits"], num, rtol=1e-6, atol=1e-7)
+
+
+def test_swiglu_derivative_matches_torch_autograd():
+    a = torch.linspace(-30, 30, 601, dtype=torch.float64, requires_grad=True)
+    u = torch.linspace(-2, 3, 601, dtype=torch.float64)
+    h = torch.nn.functional.silu(a) * u
+    h.sum().backward()
+    sg = orc.sigmoid(a.detach().numpy())
+    da = u.numpy() * sg * (1 + a.detach().numpy() * (1 - sg))
+    np.testing.assert_allclose(da, a.grad.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_capacity_formula():
+    assert orc.capacity_of(8192, 4, 64) == 640          # 1.25 * 8192 * 4 / 64 exactly
+    assert orc.capacity_of(10, 1, 3) == math.ceil(1.25 * 10 / 3)
+    assert workloads.WORKLOADS["tiny64e_zipf_cap125"].capacity == 640
