@@ -1,0 +1,440 @@
+"""Benchmark of the MoE layer hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--cpu-sample-tokens N] [--no-cpu-baseline]
+
+One step = one full forward + backward of the layer (router, top-k gating,
+permutation, grouped SwiGLU experts + shared expert, combine, and every
+backward step) over one batch of seeded synthetic input, through the C ABI.
+Default workload: the 64-expert layer with random routing (T=8192, d=2048,
+E=64, top-4, H=Hs=1024).  Inputs are resident in HBM when the timed region
+starts; L2 (129 MB) is flushed by writing a 256 MB buffer before every step.
+
+Prints ONE JSON line (rank 0).  With --gpus N > 1 (torchrun) every rank runs an
+independent replica of the layer on its own tokens (weak scaling; the layer
+has no exchange step, so no collective runs on the data path).
+
+--impl reference times the CPU oracle (float64 numpy, the machine's host cores) on
+a bounded token sample of the same workload: rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import workloads  # noqa: E402
+
+METRIC = "MoE layer tokens/s fwd & fwd+bwd on 1 GB300; grouped-GEMM % BF16 peak"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="tiny64e_random", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--cpu-sample-tokens", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ accounting
+def gemm_flops(w, R):
+    """Algorithmic tensor-core FLOPs of one forward and one backward pass."""
+    fwd = 6.0 * R * w.d * w.H + 6.0 * w.T * w.d * w.Hs
+    bwd = 12.0 * R * w.d * w.H + 12.0 * w.T * w.d * w.Hs
+    if w.routing == "learned":
+        fwd += 2.0 * w.T * w.d * w.E
+        bwd += 4.0 * w.T * w.d * w.E
+    return fwd, bwd
+
+
+def call_flops(w, R):
+    """Algorithmic FLOPs of the tensor-core C-ABI calls."""
+    return {
+        "moe_grouped_swiglu": 6.0 * R * w.d * w.H + 6.0 * w.T * w.d * w.Hs,
+        "moe_grouped_swiglu_bwd": 12.0 * R * w.d * w.H + 12.0 * w.T * w.d * w.Hs,
+    }
+
+
+def call_bytes(w, R):
+    """Algorithmic HBM bytes of the bandwidth-bound C-ABI calls."""
+    T, d, E, k = w.T, w.d, w.E, w.k
+    route = T * E * 4 + T * k * 8 + (T * d * 2 + E * d * 2 + T * E * 4 if w.routing == "learned" else 0)
+    return {
+        "moe_route_topk": route,
+        "moe_permute": T * d * 2 + R * d * 2 + T * k * 4 * 4 + R * 4,
+        "moe_unpermute_combine": R * d * 2 + (T * d * 2 if w.Hs else 0) + T * d * 2 + T * k * 8,
+        "moe_unpermute_combine_bwd": T * d * 2 + 2 * R * d * 2 + T * k * 12,
+        "moe_permute_bwd": R * d * 2 + (T * d * 2 if w.Hs else 0) + T * d * 2 + T * k * 4,
+    }
+
+
+def launches_per_step(w):
+    n = 0
+    n += 1 + (1 if w.routing == "learned" else 0)          # route: [router GEMM] + top-k
+    n += 3                                                 # permute: hist, scan, scatter
+    n += 2                                                 # grouped swiglu: gate/up, down
+    n += 1                                                 # combine
+    n += 1                                                 # combine bwd
+    n += 4                                                 # swiglu bwd: dgrad-down, wgrad-down, dgrad-gu, wgrad-gu
+    if w.routing == "learned":
+        S = max(1, min(64, w.T // 512))
+        n += 2 + (1 if S > 1 else 0)                       # router bwd: dl, dW_r GEMM, split-K reduce
+        n += 2                                             # permute bwd: dl->bf16, router-dx GEMM + reduce
+    else:
+        n += 1 + 1                                         # router bwd dl; unpermute reduce
+    return n
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "",
+                                 f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                smax.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                               parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ reference arm
+def oracle_sample(w, inp, n_tokens):
+    """Inputs restricted to the first n_tokens tokens (weights unchanged)."""
+    sub = dict(inp)
+    for key in ("x", "dY", "logits_in"):
+        if key in sub:
+            sub[key] = sub[key][:n_tokens]
+    return sub
+
+
+def run_oracle_step(w, f64, n_tokens):
+    from oracle import moe_oracle as orc
+    cap = 0
+    if w.capacity > 0:
+        cap = orc.capacity_of(n_tokens, w.k, w.E)
+    t0 = time.perf_counter()
+    fwd = orc.layer_forward(f64, w.k, cap)
+    orc.layer_backward(f64, fwd)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, inp, n_tokens, steps=1):
+    from oracle import moe_oracle as orc
+    f64 = orc.inputs_to_f64(oracle_sample(w, inp, n_tokens))
+    times = [run_oracle_step(w, f64, n_tokens) for _ in range(steps)]
+    t = statistics.median(times)
+    return {"value": n_tokens / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {n_tokens} of {w.T} tokens of {w.name}, forward+backward, float64 numpy "
+                      f"(BLAS on all {os.cpu_count()} host cores), median of {steps}",
+            "seconds": t}
+
+
+def main_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = workloads.WORKLOADS[args.workload]
+    w = workloads.custom(w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, Hs=w.Hs, routing=w.routing,
+                         zipf_bias=w.zipf_bias, capacity_factor=w.capacity_factor, backward=True)
+    inp = workloads.make_inputs(w)
+    from oracle import moe_oracle as orc
+    n = args.cpu_sample_tokens
+    f64 = orc.inputs_to_f64(oracle_sample(w, inp, n))
+    for _ in range(args.warmup):
+        run_oracle_step(w, f64, n)
+    times = [run_oracle_step(w, f64, n) for _ in range(args.steps)]
+    total = sum(times)
+    value = n * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64/Box-Muller generator)",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "H": w.H, "Hs": w.Hs,
+                   "routing": w.routing, "capacity": w.capacity, "pass": "forward+backward",
+                   "sample_tokens": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"first {n} of {w.T} tokens per step, forward+backward, float64 numpy"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def main_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from top_routing_grouped_moe_gb300 import _binding as B
+    from top_routing_grouped_moe_gb300.layer import MoELayer
+
+    base = workloads.WORKLOADS[args.workload]
+    w = workloads.custom(base.name, T=base.T, d=base.d, E=base.E, k=base.k, H=base.H, Hs=base.Hs,
+                         routing=base.routing, zipf_bias=base.zipf_bias, capacity_factor=base.capacity_factor,
+                         backward=True)
+    # every rank draws its own tokens (weak scaling); weights are the same
+    seed = 20261202 + 7919 * rank
+    inp = workloads.make_inputs(w, base=seed)
+    dev = {}
+    for key, v in inp.items():
+        if key in ("bias", "logits_in"):
+            dev[key] = torch.from_numpy(v).cuda()
+        else:
+            dev[key] = torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16)
+    learned = w.routing == "learned"
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    calls = ["moe_route_topk", "moe_permute", "moe_grouped_swiglu", "moe_unpermute_combine",
+             "moe_unpermute_combine_bwd", "moe_grouped_swiglu_bwd", "moe_route_topk_bwd", "moe_permute_bwd"]
+
+    def step(evs=None):
+        x = dev["x"]
+        T, d, E, k, H, Hs = w.T, w.d, w.E, w.k, w.H, w.Hs
+        L = layer
+
+        def mark(i):
+            if evs is not None:
+                evs[i].record(stream)
+
+        mark(0)
+        B.moe_route_topk(x, dev.get("W_r"), dev.get("bias"), dev.get("logits_in"), T, d, E, k,
+                         L.logits if learned else None, L.idx, L.gates, L.ws, L.ws_bytes, stream)
+        mark(1)
+        B.moe_permute(x, L.idx, T, d, E, k, L.capacity, L.counts_raw, L.counts, L.offsets, L.row_of_slot,
+                      L.slot_of_row, L.x_perm, L.ws, L.ws_bytes, stream)
+        mark(2)
+        B.moe_grouped_swiglu(L.x_perm, L.offsets, x, T, d, E, k, H, Hs, dev["W_g"], dev["W_u"], dev["W_d"],
+                             dev.get("Ws_g"), dev.get("Ws_u"), dev.get("Ws_d"), L.au, L.h, L.o_perm, L.au_s,
+                             L.h_s, L.s, L.ws, L.ws_bytes, stream)
+        mark(3)
+        B.moe_unpermute_combine(L.o_perm, L.s, L.gates, L.row_of_slot, T, d, k, L.y, stream)
+        mark(4)
+        B.moe_unpermute_combine_bwd(dev["dY"], L.o_perm, L.gates, L.row_of_slot, T, d, k, L.dO_perm, L.dgates,
+                                    stream)
+        mark(5)
+        B.moe_grouped_swiglu_bwd(L.dO_perm, dev["dY"], L.offsets, L.x_perm, x, L.au, L.h, L.au_s, L.h_s, T, d, E,
+                                 k, H, Hs, dev["W_g"], dev["W_u"], dev["W_d"], dev.get("Ws_g"), dev.get("Ws_u"),
+                                 dev.get("Ws_d"), L.dx_perm, L.dx_s, L.dW_g, L.dW_u, L.dW_d, L.dWs_g, L.dWs_u,
+                                 L.dWs_d, L.ws, L.ws_bytes, stream)
+        mark(6)
+        B.moe_route_topk_bwd(L.dgates, L.gates, L.idx, x if learned else None, T, d, E, k, L.dlogits,
+                             L.dW_r if learned else None, L.ws, L.ws_bytes, stream)
+        mark(7)
+        B.moe_permute_bwd(L.dx_perm, L.dx_s, L.row_of_slot, L.dlogits if learned else None,
+                          dev.get("W_r") if learned else None, T, d, E, k, L.dx, L.ws, L.ws_bytes, stream)
+        mark(8)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = B.moe_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {B.status_string(st)}")
+    R = int(layer.offsets[-1].item())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        step(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [evs[i][0].elapsed_time(evs[i][8]) for i in range(args.steps)]
+    per_call = {c: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)] for j, c in enumerate(calls)}
+    fwd_ms = [evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms, sum(fwd_ms)], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, fwd_total = float(t[0]), float(t[1])
+    else:
+        fwd_total = sum(fwd_ms)
+    value = w.T * args.steps * world / (total_ms / 1000.0)
+    fwd_value = w.T * args.steps * world / (fwd_total / 1000.0)
+
+    # roofline of the dominant call (the grouped GEMMs, tensor bound)
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peaks = json.load(open(pk))
+    bf16_peak = peaks.get("bf16_tflops_sustained") or 1700.0
+    hbm_peak = peaks.get("hbm_gbs") or 6800.0
+    peak_src = "measured" if peaks else "fallback"
+    cf = call_flops(w, R)
+    cb = call_bytes(w, R)
+    avg = {c: statistics.mean(v) for c, v in per_call.items()}
+    dom = max(cf, key=lambda c: avg[c])
+    achieved = cf[dom] / (avg[dom] / 1000.0) / 1e12
+    calls_out = {}
+    for c in calls:
+        e = {"ms": round(avg[c], 4), "share": round(avg[c] / (total_ms / args.steps), 4)}
+        if c in cf:
+            e["tflops"] = round(cf[c] / (avg[c] / 1000.0) / 1e12, 1)
+            e["frac_bf16"] = round(e["tflops"] / bf16_peak, 3)
+        if c in cb:
+            e["gbs"] = round(cb[c] / (avg[c] / 1000.0) / 1e9, 1)
+            e["frac_hbm"] = round(e["gbs"] / hbm_peak, 3)
+        calls_out[c] = e
+    ffl, bfl = gemm_flops(w, R)
+
+    # e2e through the public layer API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {}
+        for key in ("x", "dY"):
+            pin[key] = torch.from_numpy(inp[key].view(np.int16)).view(torch.bfloat16).pin_memory()
+        if "logits_in" in inp:
+            pin["logits_in"] = torch.from_numpy(inp["logits_in"]).pin_memory()
+        y_host = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
+        dx_host = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
+        xin = torch.empty_like(dev["x"])
+        dyin = torch.empty_like(dev["dY"])
+        lin = torch.empty_like(dev["logits_in"]) if "logits_in" in dev else None
+        h2d = pin["x"].numel() * 2 + pin["dY"].numel() * 2 + (pin["logits_in"].numel() * 4 if lin is not None else 0)
+        d2h = 2 * w.T * w.d * 2
+
+        def e2e_step():
+            xin.copy_(pin["x"], non_blocking=True)
+            dyin.copy_(pin["dY"], non_blocking=True)
+            if lin is not None:
+                lin.copy_(pin["logits_in"], non_blocking=True)
+            p = dict(dev)
+            layer.forward(xin, p, logits_in=lin)
+            layer.backward(xin, dyin, p, learned_router=learned)
+            y_host.copy_(layer.y, non_blocking=True)
+            dx_host.copy_(layer.dx, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        el = time.perf_counter() - t0
+        if world > 1:
+            tt = torch.tensor([el], dtype=torch.float64, device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            el = float(tt[0])
+        e2e = {"value": w.T * args.steps * world / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp, args.cpu_sample_tokens)
+        cpu.pop("seconds", None)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded SplitMix64/Box-Muller generator)",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "H": w.H, "Hs": w.Hs,
+                       "routing": w.routing, "capacity": w.capacity, "pass": "forward+backward",
+                       "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}"},
+            "fwd_tokens_per_s": fwd_value,
+            "gemm_tflops_fwd_bwd": (ffl + bfl) / (total_ms / args.steps / 1000.0) / 1e12,
+            "roofline": {"bound": "tensor", "kernel": f"{dom} (tcgen05 grouped GEMM launches)",
+                         "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / bf16_peak, 4), "traffic": None,
+                         "peak_source": f"{peak_src} bf16 dense (sustained)"},
+            "calls": calls_out,
+            "clocks": clocks,
+            "gpu_launches": launches_per_step(w) * args.steps,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return main_reference(args)
+    return main_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,228 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE layer with top-k routing and one
+ * shared expert: router + top-k gating, token permutation into expert-
+ * contiguous order, grouped SwiGLU expert MLP (plus the shared expert), and
+ * the gate-weighted unpermute/combine, each with its backward.
+ *
+ * Sources.  The Olmo-core DDP MoE pages describe the layer this computes:
+ *   - "Olmo-core DDP MoE examples" README, "Production throughput runs": top-4
+ *     routing, one shared expert, sequence length 8192, random vs learned
+ *     routing, BF16;
+ *   - same README, "Interpreting the eight-layer DDP vs FSDP comparison":
+ *     capacity factor, router, shared-branch mixing and sparse kernels;
+ *   - "Olmo-core 3 Opens Large MoE Training", "Technical Deep Dive": experts
+ *     stay resident in GPU memory while tokens are routed to them;
+ *   - "Scaling Trillion-Parameter Models: The Architecture of Olmo-core 3",
+ *     "Code Snippet": a per-token expert-selection step (route_input /
+ *     select_expert).
+ * The pages give no formulas; each call below states the definition it
+ * implements.
+ *
+ * Conventions (all calls):
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     documented otherwise.  The library never allocates or frees device
+ *     memory; scratch space comes from a caller workspace of at least
+ *     moe_workspace_size() bytes, 256-byte aligned.
+ *   - Tensors are dense and row-major.  "bf16" = IEEE bfloat16 bit patterns
+ *     (uint16 storage).  Device pointers of bf16/fp32 tensors must be 16-byte
+ *     aligned.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*,
+ *     NULL = legacy default stream), performs no host synchronisation and
+ *     can be captured in a CUDA graph.
+ *   - Return value: MOE_OK, or an error code.  Argument errors are detected
+ *     on the host before anything is launched.  MOE_ERR_CUDA reports a launch
+ *     failure (moe_last_cuda_error() gives the cudaError_t value).  Device-side
+ *     problems (a bounded wait that expired, an index out of range) do not
+ *     fault: the kernel records a code in a device status word, skips the bad
+ *     access and returns; moe_device_status() reads it.
+ *   - Shape limits: 1 <= k <= 8, k <= E <= 256, E % 8 == 0 (rows of fp32/bf16
+ *     [T,E] tensors must be 16-byte multiples), d % 64 == 0, H % 128 == 0,
+ *     Hs % 128 == 0 (0 = no shared expert), T >= 1, T*k < 2^31.
+ *
+ * Shapes: T tokens, d model width, E experts, k experts per token, H routed
+ * expert hidden width, Hs shared expert hidden width, R = number of kept
+ * (token, slot) pairs (R = T*k when dropless), C = capacity (<= 0: dropless).
+ *
+ * Weight layouts (out_features x in_features):
+ *   W_r [E,d]; W_g, W_u [E,H,d]; W_d [E,d,H]; Ws_g, Ws_u [Hs,d]; Ws_d [d,Hs].
+ * Buffers sized for the dropless maximum R <= T*k (rows >= R are left as
+ * they were): x_perm, o_perm, dO_perm, dx_perm [T*k, d]; au [T*k, 2H];
+ * h [T*k, H]; slot_of_row [T*k].
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer where one is required, bad size */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape outside the limits above */
+  MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+  MOE_ERR_TIMEOUT = 5,      /* device status: a bounded wait expired */
+  MOE_ERR_DEVICE_BOUNDS = 6 /* device status: an index was out of range */
+};
+
+/* Library version, (major << 16) | minor.  No side effects. */
+MOE_API int moe_version(void);
+
+/* Static string for a status code; never NULL. */
+MOE_API const char* moe_status_string(int status);
+
+/* cudaError_t of the last failed CUDA call made by this library in the calling
+ * thread (0 if none). */
+MOE_API int moe_last_cuda_error(void);
+
+/* Reads and clears the device status word of the current device (a blocking
+ * copy; call it outside stream capture).  *status_out receives MOE_OK or the
+ * first device-side error recorded since the last call. */
+MOE_API int moe_device_status(int* status_out);
+
+/* Workspace bytes needed by every call below for this shape (the maximum
+ * over the calls; a single buffer can serve all of them in sequence on one
+ * stream).  Host only.  Returns MOE_ERR_UNSUPPORTED for shapes outside the
+ * limits. */
+MOE_API int moe_workspace_size(int T, int d, int E, int k, int H, int Hs, size_t* bytes);
+
+/* ---------------------------------------------------------------- forward */
+
+/* Router logits, softmax and top-k gating ("top-4 routing", README,
+ * "Production throughput runs"; the per-token selection step of "Code
+ * Snippet").
+ *   learned routing (logits_in == NULL):
+ *     logits[t,e] = fp32(sum_c x[t,c] * W_r[e,c]) + bias[e]   (bias may be NULL)
+ *     x [T,d] bf16, W_r [E,d] bf16, bias [E] fp32; logits [T,E] fp32 is
+ *     written (required).  The product runs on the tensor cores with fp32
+ *     accumulation.
+ *   given logits (logits_in != NULL, e.g. random routing): logits_in [T,E]
+ *     fp32 is used as is; x, W_r, bias and logits are ignored (may be NULL).
+ *     -inf entries are allowed.
+ *   top-k: the k experts first in the order (logit descending, expert index
+ *     ascending); -0.0 equals +0.0.  topk_idx [T,k] int32 in that order.
+ *   gates [T,k] fp32: exp(l_s - l_0) / sum_j exp(l_j - l_0) over the selected
+ *     logits, i.e. the fp32 softmax renormalised over the top-k.
+ * NaN logits are not supported. */
+MOE_API int moe_route_topk(const void* x, const void* W_r, const float* bias, const float* logits_in,
+                   int T, int d, int E, int k,
+                   float* logits, int32_t* topk_idx, float* gates,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* Token permutation into expert-contiguous order: per-expert histogram,
+ * capacity clamp, exclusive prefix sum, stable scatter (tokens stay resident
+ * experts are fed by routing, "Technical Deep Dive"; capacity factor, README
+ * "Interpreting the eight-layer DDP vs FSDP comparison").
+ *   rank(t,s)      = #{t' < t : topk_idx[t,s] is among t''s experts}
+ *   kept(t,s)      = capacity <= 0 || rank(t,s) < capacity
+ *   counts_raw[e]  = #{(t,s) : topk_idx[t,s] == e}            [E] int32
+ *   counts[e]      = #kept pairs of e = min(counts_raw[e], capacity)  [E]
+ *   offsets[e]     = sum_{e' < e} counts[e'];  offsets[E] = R   [E+1] int32
+ *   row_of_slot[t*k+s] = offsets[e] + rank(t,s) if kept, else -1   [T*k]
+ *   slot_of_row[row]   = t*k+s for every kept pair (rows [0,R))     [T*k]
+ *   x_perm[row, :]     = x[t, :]                                  [T*k, d] bf16
+ * Deterministic (no order-dependent atomics): the results are bit-exact. */
+MOE_API int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int k, int capacity,
+                int32_t* counts_raw, int32_t* counts, int32_t* offsets,
+                int32_t* row_of_slot, int32_t* slot_of_row, void* x_perm,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped SwiGLU expert MLP over the ragged per-expert row segments plus the
+ * shared expert ("one shared expert", README "Production throughput runs";
+ * "sparse kernels", "Interpreting the eight-layer ..."):
+ *   rows [offsets[e], offsets[e+1]) of x_perm go through expert e:
+ *     a = x W_g[e]^T, u = x W_u[e]^T (fp32 accumulate), h = silu(a) * u,
+ *     o = h W_d[e]^T;   silu(a) = a / (1 + exp(-a)).
+ *   au [T*k, 2H] bf16 receives a in columns [0,H) and u in [H,2H) (may be
+ *   NULL when no backward follows); h [T*k, H] bf16 (required);
+ *   o_perm [T*k, d] bf16.
+ *   Shared expert (Hs > 0): the same on every token of x [T,d] with Ws_*,
+ *   writing au_s [T,2Hs] (nullable), h_s [T,Hs] and s [T,d] bf16.
+ *   Hs == 0: the shared pointers are ignored.
+ * Tensor-core (tcgen05) grouped GEMMs fed by TMA; the per-expert tile
+ * schedule is read from `offsets` on the device. */
+MOE_API int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const void* x,
+                       int T, int d, int E, int k, int H, int Hs,
+                       const void* W_g, const void* W_u, const void* W_d,
+                       const void* Ws_g, const void* Ws_u, const void* Ws_d,
+                       void* au, void* h, void* o_perm,
+                       void* au_s, void* h_s, void* s,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Gate-weighted unpermute and combine:
+ *   y[t,:] = s[t,:] + sum_{s kept} gates[t,s] * o_perm[row_of_slot[t*k+s], :]
+ * fp32 accumulation, one bf16 rounding.  s may be NULL (no shared expert).
+ * y [T,d] bf16. */
+MOE_API int moe_unpermute_combine(const void* o_perm, const void* s, const float* gates,
+                          const int32_t* row_of_slot, int T, int d, int k,
+                          void* y, void* stream);
+
+/* --------------------------------------------------------------- backward */
+
+/* Backward of moe_unpermute_combine for upstream dY [T,d] bf16:
+ *   dO_perm[row,:] = bf16(gates[t,s] * dY[t,:])        for kept (t,s)
+ *   dgates[t,s]    = sum_c dY[t,c] * o_perm[row,c]     (fp32; 0 if dropped)
+ * The gradient reaching the shared expert output is dY itself. */
+MOE_API int moe_unpermute_combine_bwd(const void* dY, const void* o_perm, const float* gates,
+                              const int32_t* row_of_slot, int T, int d, int k,
+                              void* dO_perm, float* dgates, void* stream);
+
+/* Backward of moe_grouped_swiglu.  Inputs: dO_perm [T*k,d], dY [T,d] (the
+ * shared expert's upstream gradient; ignored if Hs == 0), offsets, x_perm, x,
+ * and the saved au, h (au_s, h_s) of the forward call.
+ *   dh = dO W_d[e];  da = dh * u * sig(a) * (1 + a (1 - sig(a)));
+ *   du = dh * silu(a);  dx_perm = da W_g[e] + du W_u[e];
+ *   dW_d[e] = dO_e^T h_e;  dW_g[e] = da_e^T x_e;  dW_u[e] = du_e^T x_e
+ * (the same for the shared expert over all T tokens).  Outputs (bf16):
+ * dx_perm [T*k,d], dx_s [T,d], dW_g, dW_u [E,H,d], dW_d [E,d,H] (zero for
+ * experts with no rows), dWs_g, dWs_u [Hs,d], dWs_d [d,Hs].  Each output
+ * element is owned by one tile: no atomics, deterministic. */
+MOE_API int moe_grouped_swiglu_bwd(const void* dO_perm, const void* dY, const int32_t* offsets,
+                           const void* x_perm, const void* x,
+                           const void* au, const void* h, const void* au_s, const void* h_s,
+                           int T, int d, int E, int k, int H, int Hs,
+                           const void* W_g, const void* W_u, const void* W_d,
+                           const void* Ws_g, const void* Ws_u, const void* Ws_d,
+                           void* dx_perm, void* dx_s,
+                           void* dW_g, void* dW_u, void* dW_d,
+                           void* dWs_g, void* dWs_u, void* dWs_d,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of the top-k softmax gating and of the router product:
+ *   dlogits[t,e] = g_s (dgates[t,s] - sum_j g_j dgates[t,j]) if e = topk_idx[t,s],
+ *                  0 for experts not selected by t             [T,E] fp32
+ *   dW_r[e,c]    = sum_t dlogits[t,e] x[t,c]                   [E,d] fp32
+ * (dropped slots have dgates = 0 but stay in the renormalisation set).  x may
+ * be NULL only together with dW_r == NULL (given-logits routing).  dW_r uses
+ * the tensor cores with dlogits rounded to bf16 and fp32 accumulation. */
+MOE_API int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
+                       const void* x, int T, int d, int E, int k,
+                       float* dlogits, float* dW_r, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of the permutation (gather-reduce) plus the router's input
+ * gradient:
+ *   dx[t,:] = sum_{s kept} dx_perm[row_of_slot[t*k+s], :] + dx_s[t,:]
+ *             + sum_e dlogits[t,e] W_r[e,:]
+ * fp32 accumulation, one bf16 rounding.  dx_s may be NULL (no shared
+ * expert); dlogits and W_r may both be NULL (given-logits routing).  The
+ * router term uses the tensor cores with dlogits rounded to bf16. */
+MOE_API int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot,
+                    const float* dlogits, const void* W_r,
+                    int T, int d, int E, int k, void* dx,
+                    void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -165,6 +165,57 @@ def swiglu_bwd(xr, Wg, Wu, Wd, a, u, h, dO):
 
 
 # --------------------------------------------------------------------------
+# combine / unpermute steps and their backward
+# --------------------------------------------------------------------------
+def combine(o, s, gates, row_of_slot, T, k):
+    """y[t] = s[t] + sum_{s kept} g[t,s] o[row(t,s)]  (s may be None)."""
+    d = o.shape[1]
+    y = np.zeros((T, d)) if s is None else np.array(s, dtype=np.float64, copy=True)
+    row = np.asarray(row_of_slot).reshape(T, k)
+    for s_ in range(k):
+        m = row[:, s_] >= 0
+        y[m] += gates[m, s_:s_ + 1] * o[row[m, s_]]
+    return y
+
+
+def combine_bwd(dY, o, gates, row_of_slot, T, k):
+    """dO[row] = g dY[t]; dg[t,s] = <dY[t], o[row]> (0 for dropped slots)."""
+    d = dY.shape[1]
+    row = np.asarray(row_of_slot).reshape(T, k)
+    R = o.shape[0]
+    dO = np.zeros((R, d))
+    dg = np.zeros((T, k))
+    for s_ in range(k):
+        m = row[:, s_] >= 0
+        dO[row[m, s_]] = gates[m, s_:s_ + 1] * dY[m]
+        dg[m, s_] = np.einsum("tc,tc->t", dY[m], o[row[m, s_]])
+    return dO, dg
+
+
+def topk_bwd(gates, idx, dg, E):
+    """Softmax-over-the-selected Jacobian: dl[t, idx[t,s]] = g_s (dg_s -
+    sum_j g_j dg_j), zero for experts outside the selection."""
+    T, k = idx.shape
+    dl = np.zeros((T, E))
+    sgd = (gates * dg).sum(axis=1, keepdims=True)
+    np.put_along_axis(dl, np.asarray(idx).astype(np.int64), gates * (dg - sgd), axis=1)
+    return dl
+
+
+def permute_bwd(dx_perm, dx_s, row_of_slot, T, k, dl=None, W_r=None):
+    """dx[t] = sum_{s kept} dx_perm[row(t,s)] + dx_s[t] + dl[t] W_r."""
+    d = dx_perm.shape[1]
+    dx = np.zeros((T, d)) if dx_s is None else np.array(dx_s, dtype=np.float64, copy=True)
+    row = np.asarray(row_of_slot).reshape(T, k)
+    for s_ in range(k):
+        m = row[:, s_] >= 0
+        dx[m] += dx_perm[row[m, s_]]
+    if dl is not None and W_r is not None:
+        dx += dl @ W_r
+    return dx
+
+
+# --------------------------------------------------------------------------
 # whole layer
 # --------------------------------------------------------------------------
 F64_KEYS = ("x", "W_r", "W_g", "W_u", "W_d", "Ws_g", "Ws_u", "Ws_d", "dY")
@@ -229,16 +280,11 @@ def layer_forward(inp: dict, k: int, capacity: int = 0, logits=None, exact_route
     if expert_fn is None:
         out.update({"a": a, "u": u, "h": h})
     out["o"] = o
-    y = np.zeros((T, d))
+    s = None
     if inp.get("Ws_g") is not None:
         a_s, u_s, h_s, s = swiglu_fwd(x, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"])
-        y += s
         out.update({"a_s": a_s, "u_s": u_s, "h_s": h_s, "s": s})
-    row = p["row_of_slot"].reshape(T, k)
-    for s_ in range(k):
-        m = row[:, s_] >= 0
-        y[m] += g[m, s_:s_ + 1] * o[row[m, s_]]
-    out["y"] = y
+    out["y"] = combine(o, s, g, p["row_of_slot"], T, k)
     return out
 
 
@@ -253,16 +299,8 @@ def layer_backward(inp: dict, fwd: dict, dY=None):
     idx, gates = fwd["idx"], fwd["gates"]
     k = idx.shape[1]
     E = fwd["logits"].shape[1]
-    row = fwd["row_of_slot"].reshape(T, k)
     R = int(fwd["offsets"][E])
-    o = fwd["o"]
-    # combine backward
-    dO = np.zeros((R, d))
-    dg = np.zeros((T, k))
-    for s_ in range(k):
-        m = row[:, s_] >= 0
-        dO[row[m, s_]] = gates[m, s_:s_ + 1] * dY[m]
-        dg[m, s_] = np.einsum("tc,tc->t", dY[m], o[row[m, s_]])
+    dO, dg = combine_bwd(dY, fwd["o"], gates, fwd["row_of_slot"], T, k)
     # experts
     H = inp["W_g"].shape[1]
     dx_perm = np.zeros((R, d))
@@ -276,25 +314,19 @@ def layer_backward(inp: dict, fwd: dict, dY=None):
             fwd["a"][r0:r1], fwd["u"][r0:r1], fwd["h"][r0:r1], dO[r0:r1])
         dx_perm[r0:r1] = dx_e
     out = {"dO": dO, "dgates": dg, "dx_perm": dx_perm, "dW_g": dWg, "dW_u": dWu, "dW_d": dWd}
-    dx = np.zeros((T, d))
+    dx_s = None
     if inp.get("Ws_g") is not None:
         dx_s, dWsg, dWsu, dWsd, _, _ = swiglu_bwd(
             x, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], fwd["a_s"], fwd["u_s"], fwd["h_s"], dY)
-        dx += dx_s
         out.update({"dx_s": dx_s, "dWs_g": dWsg, "dWs_u": dWsu, "dWs_d": dWsd})
-    for s_ in range(k):
-        m = row[:, s_] >= 0
-        dx[m] += dx_perm[row[m, s_]]
     # router: softmax-over-S Jacobian; dropped slots have dg = 0 but stay in S
-    dl = np.zeros((T, E))
-    sgd = (gates * dg).sum(axis=1, keepdims=True)
-    dsel = gates * (dg - sgd)
-    np.put_along_axis(dl, idx.astype(np.int64), dsel, axis=1)
+    dl = topk_bwd(gates, idx, dg, E)
     out["dlogits"] = dl
-    if inp.get("W_r") is not None and inp.get("logits_in") is None:
+    learned = inp.get("W_r") is not None and inp.get("logits_in") is None
+    if learned:
         out["dW_r"] = dl.T @ x
-        dx += dl @ inp["W_r"]
-    out["dx"] = dx
+    out["dx"] = permute_bwd(dx_perm, dx_s, fwd["row_of_slot"], T, k,
+                            dl if learned else None, inp["W_r"] if learned else None)
     return out
 
 

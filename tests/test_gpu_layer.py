@@ -1,0 +1,149 @@
+"""Whole-layer GPU parity (forward and backward) against the CPU oracle, at
+sizes the oracle finishes in seconds that still span several tiles, ragged
+per-expert segments, partial N tiles and capacity drops.
+
+Both sides start from the same seeded inputs and route on their own.  With
+learned routing the GPU computes the router product in fp32 on the tensor
+cores and the oracle in fp64 (rounded to fp32), so a top-k decision whose
+margin is below that rounding could legitimately differ: such near-tie tokens
+are allowed only where the oracle's own logits have a near tie, must be a
+valid top-k there, and are then left out of the per-token comparisons (and
+the experts they touch out of the weight-gradient comparisons)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as orc
+from synth import workloads
+from tests.gpu_util import assert_close, experts_touched, host_f64, routing_disagreements, upload
+
+pytestmark = pytest.mark.gpu
+
+LOGIT_TOL = 1e-4
+
+CASES = {
+    # name: workload (T, d, E, k, H, Hs, routing, zipf, capacity_factor)
+    "tiny": workloads.WORKLOADS["tiny"],
+    "shared_ragged": workloads.custom("shared_ragged", T=700, d=256, E=16, k=4, H=256, Hs=128),
+    "zipf_capacity": workloads.custom("zipf_capacity", T=700, d=256, E=16, k=2, H=256, Hs=128, zipf_bias=True,
+                                      capacity_factor=1.25),
+    "random_many_experts": workloads.custom("random_many_experts", T=512, d=256, E=64, k=4, H=128, Hs=128,
+                                            routing="random"),
+    "partial_tiles": workloads.custom("partial_tiles", T=300, d=384, E=8, k=2, H=384, Hs=384),
+}
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from top_routing_grouped_moe_gb300 import _binding
+    return _binding
+
+
+def run_layer(w, inp):
+    from top_routing_grouped_moe_gb300.layer import MoELayer
+    dev = upload(inp)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity)
+    layer.forward(dev["x"], dev, logits_in=dev.get("logits_in"))
+    layer.backward(dev["x"], dev["dY"], dev, learned_router=w.routing == "learned")
+    torch.cuda.synchronize()
+    return layer
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_layer_forward_backward_parity(B, name):
+    w = CASES[name]
+    if not w.backward:
+        w = workloads.custom(w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, Hs=w.Hs, routing=w.routing,
+                             zipf_bias=w.zipf_bias, capacity_factor=w.capacity_factor, backward=True)
+    inp = workloads.make_inputs(w)
+    layer = run_layer(w, inp)
+    assert B.moe_device_status() == 0
+    f64 = orc.inputs_to_f64(inp)
+    ref = orc.layer_forward(f64, w.k, w.capacity)
+    refb = orc.layer_backward(f64, ref)
+    T, k = w.T, w.k
+
+    gidx = layer.idx.cpu().numpy()
+    diff = np.zeros(T, dtype=bool)
+    if w.routing == "learned":
+        gl = layer.logits.cpu().numpy()
+        np.testing.assert_allclose(gl, ref["logits"], rtol=0, atol=LOGIT_TOL)
+        delta = max(float(np.abs(gl.astype(np.float64) - ref["logits"]).max()), 1e-7) * 4
+        diff = routing_disagreements(gidx, ref["idx"], ref["logits"], k, delta)
+        assert diff.sum() <= max(1, T // 100)
+    else:
+        assert np.array_equal(gidx, ref["idx"])
+    keep = ~diff
+    skip_e = experts_touched(diff, gidx, ref["idx"])
+    keep_e = np.setdiff1d(np.arange(w.E), skip_e)
+    if w.capacity > 0 and diff.any():
+        # a flipped token shifts the token-order ranks (and so the drops) of
+        # later tokens in the experts it touches
+        keep &= ~np.isin(ref["idx"], skip_e).any(axis=1) & ~np.isin(gidx, skip_e).any(axis=1)
+    if not diff.any():
+        # routing and permutation: bit-exact
+        for key in ("counts_raw", "counts", "offsets", "row_of_slot"):
+            assert np.array_equal(getattr(layer, key).cpu().numpy(), ref[key]), key
+        R = int(ref["offsets"][-1])
+        assert np.array_equal(layer.slot_of_row.cpu().numpy()[:R], ref["slot_of_row"])
+        assert_close("x_perm", host_f64(layer.x_perm)[:R], ref["x_perm"], atol=0, rtol=0, fro=0)
+        assert_close("h", host_f64(layer.h)[:R], ref["h"])
+        assert_close("a", host_f64(layer.au)[:R, :w.H], ref["a"])
+        assert_close("u", host_f64(layer.au)[:R, w.H:], ref["u"])
+        assert_close("o_perm", host_f64(layer.o_perm)[:R], ref["o"])
+        assert_close("dO", host_f64(layer.dO_perm)[:R], refb["dO"])
+        assert_close("dx_perm", host_f64(layer.dx_perm)[:R], refb["dx_perm"])
+    np.testing.assert_allclose(layer.gates.cpu().numpy()[keep], ref["gates"][keep], rtol=1e-5, atol=1e-6)
+
+    # forward values
+    if w.Hs:
+        assert_close("s", host_f64(layer.s), ref["s"])
+    assert_close("y", host_f64(layer.y)[keep], ref["y"][keep])
+
+    # backward
+    assert_close("dgates", layer.dgates.cpu().numpy()[keep], refb["dgates"][keep])
+    assert_close("dW_d", host_f64(layer.dW_d)[keep_e], refb["dW_d"][keep_e])
+    assert_close("dW_g", host_f64(layer.dW_g)[keep_e], refb["dW_g"][keep_e])
+    assert_close("dW_u", host_f64(layer.dW_u)[keep_e], refb["dW_u"][keep_e])
+    if w.Hs:
+        assert_close("dx_s", host_f64(layer.dx_s), refb["dx_s"])
+        assert_close("dWs_d", host_f64(layer.dWs_d), refb["dWs_d"])
+        assert_close("dWs_g", host_f64(layer.dWs_g), refb["dWs_g"])
+        assert_close("dWs_u", host_f64(layer.dWs_u), refb["dWs_u"])
+    assert_close("dlogits", layer.dlogits.cpu().numpy()[keep], refb["dlogits"][keep])
+    if w.routing == "learned":
+        assert_close("dW_r", layer.dW_r.cpu().numpy()[keep_e], refb["dW_r"][keep_e])
+    assert_close("dx", host_f64(layer.dx)[keep], refb["dx"][keep])
+
+
+def test_layer_is_deterministic(B):
+    w = workloads.custom("det", T=700, d=256, E=16, k=4, H=256, Hs=128)
+    inp = workloads.make_inputs(w)
+    a = run_layer(w, inp)
+    ya, dxa, dwa = a.y.clone(), a.dx.clone(), a.dW_g.clone()
+    b = run_layer(w, inp)
+    assert torch.equal(ya.view(torch.int16), b.y.view(torch.int16))
+    assert torch.equal(dxa.view(torch.int16), b.dx.view(torch.int16))
+    assert torch.equal(dwa.view(torch.int16), b.dW_g.view(torch.int16))
+
+
+def test_empty_experts_get_zero_weight_gradients(B):
+    """All tokens routed (random routing) to 4 of 32 experts: the other 28 have
+    no rows, and their dW must be exactly zero."""
+    from synth import gen
+    w = workloads.custom("empty", T=256, d=256, E=32, k=4, H=128, Hs=0, routing="random")
+    inp = workloads.make_inputs(w)
+    l = np.full((w.T, w.E), -np.inf, dtype=np.float32)
+    l[:, [3, 7, 20, 31]] = gen.random_logits(w.T, 4, tensor=400)
+    inp["logits_in"] = l
+    layer = run_layer(w, inp)
+    used = np.zeros(w.E, dtype=bool)
+    used[[3, 7, 20, 31]] = True
+    for name in ("dW_g", "dW_u", "dW_d"):
+        v = getattr(layer, name).float().cpu().numpy()
+        assert np.all(v[~used] == 0.0), name
+        assert np.all(np.abs(v[used]).sum(axis=(1, 2)) > 0), name
+    ref = orc.layer_forward(orc.inputs_to_f64(inp), w.k, 0)
+    assert_close("y", host_f64(layer.y), ref["y"])

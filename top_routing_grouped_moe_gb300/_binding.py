@@ -1,0 +1,174 @@
+"""ctypes binding of the C ABI (include/moe.h): the same function names,
+argument marshalling only.  Tensors are passed as device pointers
+(torch.Tensor.data_ptr()); every step runs in the CUDA library.
+
+Importing this module loads lib/libmoe_gb300.so; if the library has not been
+built, the import fails loudly (there is no fallback path)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libmoe_gb300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_DEVICE_BOUNDS = 6
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: status {status} ({msg})")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"CUDA library not built: {LIB_PATH} is missing "
+                          "(run `python -m top_routing_grouped_moe_gb300.build`)")
+    return ctypes.CDLL(LIB_PATH)
+
+
+_lib = _load()
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+# name -> argument kinds ('p' pointer/tensor, 'i' int, 'z' size_t, 's' stream)
+SIGNATURES = {
+    "moe_route_topk": "pppp" + "iiii" + "ppp" + "pz" + "s",
+    "moe_permute": "pp" + "iiiii" + "pppppp" + "pz" + "s",
+    "moe_grouped_swiglu": "ppp" + "iiiiii" + "pppppp" + "pppppp" + "pz" + "s",
+    "moe_unpermute_combine": "pppp" + "iii" + "p" + "s",
+    "moe_unpermute_combine_bwd": "pppp" + "iii" + "pp" + "s",
+    "moe_grouped_swiglu_bwd": "ppppppppp" + "iiiiii" + "pppppp" + "pp" + "pppppp" + "pz" + "s",
+    "moe_route_topk_bwd": "pppp" + "iiii" + "pp" + "pz" + "s",
+    "moe_permute_bwd": "ppppp" + "iiii" + "p" + "pz" + "s",
+}
+
+_CT = {"p": _P, "i": _I, "z": _SZ, "s": _P}
+
+for _name, _sig in SIGNATURES.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = [_CT[c] for c in _sig]
+    _f.restype = _I
+
+_lib.moe_version.restype = _I
+_lib.moe_version.argtypes = []
+_lib.moe_status_string.restype = ctypes.c_char_p
+_lib.moe_status_string.argtypes = [_I]
+_lib.moe_last_cuda_error.restype = _I
+_lib.moe_last_cuda_error.argtypes = []
+_lib.moe_device_status.restype = _I
+_lib.moe_device_status.argtypes = [ctypes.POINTER(_I)]
+_lib.moe_workspace_size.restype = _I
+_lib.moe_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
+
+
+def _ptr(v):
+    if v is None:
+        return None
+    if isinstance(v, torch.Tensor):
+        return ctypes.c_void_p(v.data_ptr())
+    return ctypes.c_void_p(int(v))
+
+
+def _stream(v):
+    if v is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(v, torch.cuda.Stream):
+        return ctypes.c_void_p(v.cuda_stream)
+    return ctypes.c_void_p(int(v))
+
+
+def status_string(status: int) -> str:
+    return _lib.moe_status_string(int(status)).decode()
+
+
+def _call(name: str, *args):
+    sig = SIGNATURES[name]
+    if len(args) != len(sig):
+        raise TypeError(f"{name} takes {len(sig)} arguments ({len(args)} given)")
+    conv = []
+    for kind, a in zip(sig, args):
+        if kind == "p":
+            conv.append(_ptr(a))
+        elif kind == "s":
+            conv.append(_stream(a))
+        else:
+            conv.append(int(a))
+    rc = getattr(_lib, name)(*conv)
+    if rc != MOE_OK:
+        msg = status_string(rc)
+        if rc == MOE_ERR_CUDA:
+            msg += f", cudaError {_lib.moe_last_cuda_error()}"
+        raise MoEError(name, rc, msg)
+    return rc
+
+
+def moe_version() -> int:
+    return _lib.moe_version()
+
+
+def moe_device_status() -> int:
+    v = _I(0)
+    rc = _lib.moe_device_status(ctypes.byref(v))
+    if rc != MOE_OK:
+        raise MoEError("moe_device_status", rc, status_string(rc))
+    return v.value
+
+
+def moe_workspace_size(T, d, E, k, H, Hs) -> int:
+    b = _SZ(0)
+    rc = _lib.moe_workspace_size(T, d, E, k, H, Hs, ctypes.byref(b))
+    if rc != MOE_OK:
+        raise MoEError("moe_workspace_size", rc, status_string(rc))
+    return b.value
+
+
+def moe_route_topk(x, W_r, bias, logits_in, T, d, E, k, logits, topk_idx, gates, ws, ws_bytes, stream=None):
+    return _call("moe_route_topk", x, W_r, bias, logits_in, T, d, E, k, logits, topk_idx, gates, ws, ws_bytes,
+                 stream)
+
+
+def moe_permute(x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, row_of_slot, slot_of_row, x_perm,
+                ws, ws_bytes, stream=None):
+    return _call("moe_permute", x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, row_of_slot,
+                 slot_of_row, x_perm, ws, ws_bytes, stream)
+
+
+def moe_grouped_swiglu(x_perm, offsets, x, T, d, E, k, H, Hs, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, au, h, o_perm,
+                       au_s, h_s, s, ws, ws_bytes, stream=None):
+    return _call("moe_grouped_swiglu", x_perm, offsets, x, T, d, E, k, H, Hs, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, au,
+                 h, o_perm, au_s, h_s, s, ws, ws_bytes, stream)
+
+
+def moe_unpermute_combine(o_perm, s, gates, row_of_slot, T, d, k, y, stream=None):
+    return _call("moe_unpermute_combine", o_perm, s, gates, row_of_slot, T, d, k, y, stream)
+
+
+def moe_unpermute_combine_bwd(dY, o_perm, gates, row_of_slot, T, d, k, dO_perm, dgates, stream=None):
+    return _call("moe_unpermute_combine_bwd", dY, o_perm, gates, row_of_slot, T, d, k, dO_perm, dgates, stream)
+
+
+def moe_grouped_swiglu_bwd(dO_perm, dY, offsets, x_perm, x, au, h, au_s, h_s, T, d, E, k, H, Hs, W_g, W_u, W_d,
+                           Ws_g, Ws_u, Ws_d, dx_perm, dx_s, dW_g, dW_u, dW_d, dWs_g, dWs_u, dWs_d, ws, ws_bytes,
+                           stream=None):
+    return _call("moe_grouped_swiglu_bwd", dO_perm, dY, offsets, x_perm, x, au, h, au_s, h_s, T, d, E, k, H, Hs,
+                 W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, dx_perm, dx_s, dW_g, dW_u, dW_d, dWs_g, dWs_u, dWs_d, ws,
+                 ws_bytes, stream)
+
+
+def moe_route_topk_bwd(dgates, gates, topk_idx, x, T, d, E, k, dlogits, dW_r, ws, ws_bytes, stream=None):
+    return _call("moe_route_topk_bwd", dgates, gates, topk_idx, x, T, d, E, k, dlogits, dW_r, ws, ws_bytes, stream)
+
+
+def moe_permute_bwd(dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream=None):
+    return _call("moe_permute_bwd", dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream)

@@ -1,0 +1,612 @@
+// Persistent, warp-specialised grouped GEMM on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in TMEM, operands staged by TMA with 128-byte
+// swizzle).  One CTA per SM; each CTA walks a device-side tile schedule built
+// from per-group row offsets that never leave the GPU.
+//
+//   warp 0      TMA producer (one lane): A and B tiles into a STAGES-deep ring
+//   warp 1      TMEM allocator + MMA issuer (one lane)
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane
+//               = one output row per thread), fused elementwise work, stores
+//
+// Two fp32 accumulators of 128 x 256 (all 512 TMEM columns) let the epilogue
+// of tile i overlap the main loop of tile i+1.
+//
+// Grouping modes:
+//   MGROUP  ragged M: group g owns rows [off[g], off[g+1]) of A and of the
+//           output, and its own B (3-D tensor map, group = 3rd coordinate).
+//           Forward expert GEMMs and activation-gradient (dgrad) GEMMs.
+//   KGROUP  ragged K: group g contracts over rows [off[g], off[g+1]) of A and
+//           B (both stored with K as the row index) into its own output slab.
+//           Weight-gradient (wgrad) GEMMs; tail rows of the last K step that
+//           belong to the next group are zeroed in shared memory.
+#pragma once
+#include <cuda.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;  // accumulator columns per tile
+constexpr int BK = 64;   // K per pipeline stage: 128 bytes of bf16 (one swizzle row)
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int NUM_THREADS = 192;
+constexpr int MAX_PROBLEMS = 2;
+constexpr int MAX_MAPS = 8;
+constexpr int MAX_G = kMaxE + 1;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) MN-major box: 8 KB
+
+enum Mode : int { MGROUP = 0, KGROUP = 1 };
+enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3, EPI_REDUCE_DX = 4 };
+
+struct Problem {
+  const int* offsets;  // [G+1] device; NULL: `extent` split evenly into G chunks
+  int G;
+  int extent;          // rows (MGROUP) or K (KGROUP) covered when offsets == NULL; also an upper clamp
+  int M, N, K;         // MGROUP uses N, K (M per group); KGROUP uses M, N (K per group)
+  int mma_n;           // instruction N (multiple of 16, <= 256)
+  int n_tile;          // output columns per tile (256; 128 h columns for EPI_SWIGLU_FWD)
+  int map_a, map_b, map_b2;  // tensor-map indices; map_b2 = second B map or -1
+  int ksplit;          // MN-major B: k >= ksplit reads map_b2 at k - ksplit (0 = off)
+  uint32_t tx_bytes;   // bytes landing per stage
+  // epilogue
+  void* out;
+  long long ldo;       // elements
+  long long gstride;   // elements between groups' output slabs (KGROUP)
+  void* out2;          // rows >= row_split go to out2 (KGROUP; 0 = off)
+  int row_split;
+  void* aux;           // SWIGLU_FWD: au out; SWIGLU_BWD: au in; REDUCE_DX: dx_perm in
+  long long ld_aux;
+  const void* aux2;    // REDUCE_DX: dx_s in (nullable)
+  const float* bias;   // EPI_F32 (nullable)
+  const int* row_of_slot;  // REDUCE_DX
+  int topk;
+  int aux_rows;        // REDUCE_DX: rows of the dx_perm buffer (bounds check)
+  int H;               // SWIGLU: column offset of u within au
+};
+
+struct Params {
+  CUtensorMap maps[MAX_MAPS];
+  Problem prob[MAX_PROBLEMS];
+  int num_problems;
+  int num_maps;
+  int* status;
+};
+
+struct Sched {
+  int tile_start[MAX_PROBLEMS + 1];
+  int off[MAX_PROBLEMS][MAX_G];
+  int tpre[MAX_PROBLEMS][MAX_G];  // MGROUP: exclusive prefix of tiles per group
+};
+
+struct SmemTail {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint32_t tmem_base;
+  int abort_flag;
+  Sched sched;
+};
+
+constexpr size_t kSmemBytes = 1024 + STAGES * (A_BYTES + B_BYTES) + sizeof(SmemTail);
+
+struct TileInfo {
+  int p, g, m0, n0, rows_end, k0, k1, nk;
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+template <int MODE>
+__device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int t) {
+  TileInfo ti;
+  int p = (P.num_problems > 1 && t >= S.tile_start[1]) ? 1 : 0;
+  const Problem& pr = P.prob[p];
+  int local = t - S.tile_start[p];
+  int nt = cdiv(pr.N, pr.n_tile);
+  ti.p = p;
+  if (MODE == MGROUP) {
+    int lo = 0, hi = pr.G - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (S.tpre[p][mid] <= local) lo = mid; else hi = mid - 1;
+    }
+    int g = lo;
+    int within = local - S.tpre[p][g];
+    int r0 = S.off[p][g], r1 = S.off[p][g + 1];
+    int mt = cdiv(r1 - r0, BM);
+    int n_idx = within / mt, m_idx = within - n_idx * mt;
+    ti.g = g;
+    ti.m0 = r0 + m_idx * BM;
+    ti.rows_end = r1;
+    ti.n0 = n_idx * pr.n_tile;
+    ti.k0 = 0;
+    ti.k1 = pr.K;
+    ti.nk = cdiv(pr.K, BK);
+  } else {
+    int mt = cdiv(pr.M, BM);
+    int per = mt * nt;
+    int g = local / per;
+    int within = local - g * per;
+    int m_idx = within / nt, n_idx = within - m_idx * nt;
+    ti.g = g;
+    ti.m0 = m_idx * BM;
+    ti.rows_end = pr.M;
+    ti.n0 = n_idx * pr.n_tile;
+    ti.k0 = S.off[p][g];
+    ti.k1 = S.off[p][g + 1];
+    ti.nk = cdiv(ti.k1 - ti.k0, BK);
+  }
+  return ti;
+}
+
+// Schedule set-up, run by every thread of the CTA before the roles start.
+template <int MODE>
+__device__ void build_schedule(const Params& P, Sched& S) {
+  const int tid = threadIdx.x;
+  for (int p = 0; p < P.num_problems; ++p) {
+    const Problem& pr = P.prob[p];
+    int chunk = pr.offsets ? 0 : cdiv(cdiv(pr.extent, pr.G), BK) * BK;
+    for (int i = tid; i <= pr.G; i += blockDim.x) {
+      int v = pr.offsets ? __ldg(pr.offsets + i) : min(i * chunk, pr.extent);
+      S.off[p][i] = v;
+    }
+  }
+  __syncthreads();
+  // clamp to a monotone sequence inside [0, extent]; count out-of-range
+  // offsets as a device error (they would index outside the caller buffers)
+  if (threadIdx.x < 32 * P.num_problems && (threadIdx.x & 31) == 0) {
+    int p = threadIdx.x >> 5;
+    const Problem& pr = P.prob[p];
+    int prev = 0;
+    bool bad = false;
+    for (int i = 0; i <= pr.G; ++i) {
+      int v = S.off[p][i];
+      if (v < prev || v > pr.extent || (i == 0 && v != 0)) bad = true;
+      v = min(max(v, prev), pr.extent);
+      if (i == 0) v = 0;
+      S.off[p][i] = v;
+      prev = v;
+    }
+    if (bad) record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int base = 0;
+    for (int p = 0; p < P.num_problems; ++p) {
+      const Problem& pr = P.prob[p];
+      int nt = cdiv(pr.N, pr.n_tile);
+      int total;
+      if (MODE == MGROUP) {
+        // warp scan of per-group tile counts
+        int per_lane = cdiv(pr.G, 32);
+        int g0 = lane * per_lane;
+        int local = 0;
+        for (int j = 0; j < per_lane; ++j) {
+          int g = g0 + j;
+          if (g < pr.G) local += cdiv(S.off[p][g + 1] - S.off[p][g], BM) * nt;
+        }
+        int incl = local;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+          int v = __shfl_up_sync(0xffffffffu, incl, s);
+          if (lane >= s) incl += v;
+        }
+        int run = incl - local;
+        for (int j = 0; j < per_lane; ++j) {
+          int g = g0 + j;
+          if (g < pr.G) {
+            S.tpre[p][g] = run;
+            run += cdiv(S.off[p][g + 1] - S.off[p][g], BM) * nt;
+          }
+        }
+        total = __shfl_sync(0xffffffffu, incl, 31);
+        if (lane == 0) S.tpre[p][pr.G] = total;
+      } else {
+        total = pr.G * cdiv(pr.M, BM) * nt;
+      }
+      if (lane == 0) S.tile_start[p] = base;
+      base += total;
+    }
+    if (lane == 0) S.tile_start[P.num_problems] = base;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + __expf(-a)); }
+
+template <int AMN, int BMN, int MODE, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  SmemTail* tail = reinterpret_cast<SmemTail*>(smem + STAGES * (A_BYTES + B_BYTES));
+  Sched& S = tail->sched;
+  volatile int* abort_flag = &tail->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&tail->full[s], 1);
+      ptx::mbar_init(&tail->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tail->tmem_full[a], 1);
+      ptx::mbar_init(&tail->tmem_empty[a], 128);
+    }
+    tail->abort_flag = 0;
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < P.num_maps; ++i) ptx::prefetch_tmap(&P.maps[i]);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&tail->tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  build_schedule<MODE>(P, S);  // contains __syncthreads
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = tail->tmem_base;
+  const int total = S.tile_start[P.num_problems];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase_mask = 0;  // bit s: parity of the last load issued into stage s
+      uint32_t issued_any = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        TileInfo ti = decode<MODE>(P, S, t);
+        const Problem& pr = P.prob[ti.p];
+        const CUtensorMap* mA = &P.maps[pr.map_a];
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!ptx::mbar_wait_bounded(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          uint64_t* fb = &tail->full[stage];
+          ptx::mbar_arrive_expect_tx(fb, pr.tx_bytes);
+          issued_any |= 1u << stage;
+          issued_phase_mask = (issued_phase_mask & ~(1u << stage)) | (phase << stage);
+          const int k = ti.k0 + kb * BK;
+          uint8_t* a_dst = sA + stage * A_BYTES;
+          uint8_t* b_dst = sB + stage * B_BYTES;
+          if (AMN == 0) {
+            ptx::tma_load_2d(a_dst, mA, fb, k, ti.m0);
+          } else {
+            ptx::tma_load_2d(a_dst, mA, fb, ti.m0, k);
+            ptx::tma_load_2d(a_dst + MN_BLOCK_BYTES, mA, fb, ti.m0 + 64, k);
+          }
+          if (EPI == EPI_SWIGLU_FWD) {
+            ptx::tma_load_3d(b_dst, &P.maps[pr.map_b], fb, k, ti.n0, ti.g);
+            ptx::tma_load_3d(b_dst + (B_BYTES / 2), &P.maps[pr.map_b2], fb, k, ti.n0, ti.g);
+          } else if (BMN == 0) {
+            ptx::tma_load_3d(b_dst, &P.maps[pr.map_b], fb, k, ti.n0, ti.g);
+          } else {
+            const int nblk = pr.n_tile / 64;
+            if (MODE == MGROUP) {
+              const CUtensorMap* mB = &P.maps[pr.map_b];
+              int kk = k;
+              if (pr.ksplit > 0 && k >= pr.ksplit) {
+                mB = &P.maps[pr.map_b2];
+                kk = k - pr.ksplit;
+              }
+              for (int j = 0; j < nblk; ++j) ptx::tma_load_3d(b_dst + j * MN_BLOCK_BYTES, mB, fb, ti.n0 + 64 * j, kk, ti.g);
+            } else {
+              const CUtensorMap* mB = &P.maps[pr.map_b];
+              for (int j = 0; j < nblk; ++j) ptx::tma_load_2d(b_dst + j * MN_BLOCK_BYTES, mB, fb, ti.n0 + 64 * j, k);
+            }
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_status(P.status, MOE_ERR_TIMEOUT);
+        // let copies already in flight land before the CTA's shared memory goes away
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_any & (1u << s)) {
+            volatile int never = 0;
+            ptx::mbar_wait_bounded(&tail->full[s], (issued_phase_mask >> s) & 1u, &never, 100000000ull);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    int it = 0;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+      TileInfo ti = decode<MODE>(P, S, t);
+      const Problem& pr = P.prob[ti.p];
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!ptx::mbar_wait_bounded(&tail->tmem_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      const uint32_t idesc = ptx::idesc_bf16(BM, pr.mma_n, AMN, BMN);
+      const int b_blocks = pr.n_tile / 64;
+      for (int kb = 0; kb < ti.nk; ++kb) {
+        if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        int valid = BK;
+        if (MODE == KGROUP) valid = min(BK, ti.k1 - (ti.k0 + kb * BK));
+        const int nsub = (valid + UMMA_K - 1) / UMMA_K;
+        uint8_t* a_st = sA + stage * A_BYTES;
+        uint8_t* b_st = sB + stage * B_BYTES;
+        if (MODE == KGROUP && valid < nsub * UMMA_K) {
+          // rows [valid, nsub*16) of this K step belong to the next group:
+          // zero them in both operands (whole 128-byte rows, so the swizzle
+          // pattern does not matter)
+          const int nrows = nsub * UMMA_K - valid;
+          const int chunks_per_blk = nrows * 8;  // 16-byte chunks
+          const int nblk = 2 + b_blocks;
+          for (int c = lane; c < chunks_per_blk * nblk; c += 32) {
+            int blk = c / chunks_per_blk;
+            int w = c - blk * chunks_per_blk;
+            int r = valid + (w >> 3);
+            uint8_t* base = blk < 2 ? a_st + blk * MN_BLOCK_BYTES : b_st + (blk - 2) * MN_BLOCK_BYTES;
+            *reinterpret_cast<uint4*>(base + r * 128 + (w & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const uint32_t a_addr = ptx::smem_u32(a_st);
+          const uint32_t b_addr = ptx::smem_u32(b_st);
+          for (int s = 0; s < nsub; ++s) {
+            const uint64_t ad = AMN ? ptx::smem_desc(a_addr + s * 2048, MN_BLOCK_BYTES, 1024)
+                                    : ptx::smem_desc(a_addr + s * 32, 16, 1024);
+            const uint64_t bd = BMN ? ptx::smem_desc(b_addr + s * 2048, MN_BLOCK_BYTES, 1024)
+                                    : ptx::smem_desc(b_addr + s * 32, 16, 1024);
+            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&tail->empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (ti.nk > 0) ptx::mma_commit(&tail->tmem_full[acc]);
+        else ptx::mbar_arrive(&tail->tmem_full[acc]);
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_status(P.status, MOE_ERR_TIMEOUT);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      TileInfo ti = decode<MODE>(P, S, t);
+      const Problem& pr = P.prob[ti.p];
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!ptx::mbar_wait_bounded(&tail->tmem_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
+        *abort_flag = 1;
+        record_status(P.status, MOE_ERR_TIMEOUT);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+      const int row = ti.m0 + r_in_tile;
+      const bool row_ok = row < ti.rows_end;
+      const bool has_acc = ti.nk > 0;
+
+      if (EPI == EPI_BF16) {
+        __nv_bfloat16* outp;
+        if (MODE == KGROUP && pr.row_split > 0 && ti.m0 >= pr.row_split)
+          outp = reinterpret_cast<__nv_bfloat16*>(pr.out2) + ti.g * pr.gstride + (long long)(row - pr.row_split) * pr.ldo;
+        else
+          outp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (MODE == KGROUP ? ti.g * pr.gstride : 0) + (long long)row * pr.ldo;
+        for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
+          if (ti.n0 + c0 >= pr.N) break;
+          uint32_t r[32];
+          if (has_acc) {
+            ptx::tmem_ld32(taddr + c0, r);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(outp + ti.n0 + c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+              v.y = pack_bf16(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+              v.z = pack_bf16(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+              v.w = pack_bf16(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+              dst[j] = v;
+            }
+          }
+        }
+      } else if (EPI == EPI_F32) {
+        float* outp = reinterpret_cast<float*>(pr.out) + (MODE == KGROUP ? ti.g * pr.gstride : 0) + (long long)row * pr.ldo;
+        for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
+          if (ti.n0 + c0 >= pr.N) break;
+          uint32_t r[32];
+          if (has_acc) {
+            ptx::tmem_ld32(taddr + c0, r);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int col = ti.n0 + c0 + 4 * j;
+              if (col < pr.N) {
+                float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                       __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                if (pr.bias) {
+                  v.x += __ldg(pr.bias + col); v.y += __ldg(pr.bias + col + 1);
+                  v.z += __ldg(pr.bias + col + 2); v.w += __ldg(pr.bias + col + 3);
+                }
+                *reinterpret_cast<float4*>(outp + col) = v;
+              }
+            }
+          }
+        }
+      } else if (EPI == EPI_SWIGLU_FWD) {
+        // accumulator columns [0,128) = a (gate), [128,256) = u (up)
+        __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row * pr.ldo + ti.n0;
+        __nv_bfloat16* ap = pr.aux ? reinterpret_cast<__nv_bfloat16*>(pr.aux) + (long long)row * pr.ld_aux + ti.n0 : nullptr;
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t ra[32], ru[32];
+          ptx::tmem_ld32(taddr + c0, ra);
+          ptx::tmem_ld32(taddr + 128 + c0, ru);
+          ptx::tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float h[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                float a = __uint_as_float(ra[8 * j + e]);
+                float u = __uint_as_float(ru[8 * j + e]);
+                h[e] = a * sigmoidf_(a) * u;
+              }
+              reinterpret_cast<uint4*>(hp + c0)[j] = pack8(h);
+              if (ap) {
+                uint4 va, vu;
+                va.x = pack_bf16(__uint_as_float(ra[8 * j + 0]), __uint_as_float(ra[8 * j + 1]));
+                va.y = pack_bf16(__uint_as_float(ra[8 * j + 2]), __uint_as_float(ra[8 * j + 3]));
+                va.z = pack_bf16(__uint_as_float(ra[8 * j + 4]), __uint_as_float(ra[8 * j + 5]));
+                va.w = pack_bf16(__uint_as_float(ra[8 * j + 6]), __uint_as_float(ra[8 * j + 7]));
+                vu.x = pack_bf16(__uint_as_float(ru[8 * j + 0]), __uint_as_float(ru[8 * j + 1]));
+                vu.y = pack_bf16(__uint_as_float(ru[8 * j + 2]), __uint_as_float(ru[8 * j + 3]));
+                vu.z = pack_bf16(__uint_as_float(ru[8 * j + 4]), __uint_as_float(ru[8 * j + 5]));
+                vu.w = pack_bf16(__uint_as_float(ru[8 * j + 6]), __uint_as_float(ru[8 * j + 7]));
+                reinterpret_cast<uint4*>(ap + c0)[j] = va;
+                reinterpret_cast<uint4*>(ap + pr.H + c0)[j] = vu;
+              }
+            }
+          }
+        }
+      } else if (EPI == EPI_SWIGLU_BWD) {
+        // accumulator = dh for H columns [n0, n0+256); au holds a | u
+        __nv_bfloat16* dp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row * pr.ldo + ti.n0;
+        const __nv_bfloat16* aup = reinterpret_cast<const __nv_bfloat16*>(pr.aux) + (long long)row * pr.ld_aux + ti.n0;
+        for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
+          if (ti.n0 + c0 >= pr.N) break;
+          uint32_t r[32];
+          ptx::tmem_ld32(taddr + c0, r);
+          ptx::tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 va = __ldg(reinterpret_cast<const uint4*>(aup + c0) + j);
+              uint4 vu = __ldg(reinterpret_cast<const uint4*>(aup + pr.H + c0) + j);
+              float a[8], u[8], da[8], du[8];
+              unpack8(va, a);
+              unpack8(vu, u);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                float dh = __uint_as_float(r[8 * j + e]);
+                float sg = sigmoidf_(a[e]);
+                da[e] = dh * u[e] * sg * (1.0f + a[e] * (1.0f - sg));
+                du[e] = dh * a[e] * sg;
+              }
+              reinterpret_cast<uint4*>(dp + c0)[j] = pack8(da);
+              reinterpret_cast<uint4*>(dp + pr.H + c0)[j] = pack8(du);
+            }
+          }
+        }
+      } else if (EPI == EPI_REDUCE_DX) {
+        // dx[t] = acc (router term) + dx_s[t] + sum_s dx_perm[row(t,s)]
+        int rows_s[kMaxK];
+        const int kk = pr.topk;
+        if (row_ok) {
+          for (int s = 0; s < kk; ++s) rows_s[s] = __ldg(pr.row_of_slot + (long long)row * kk + s);
+        }
+        __nv_bfloat16* dxp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row * pr.ldo + ti.n0;
+        const __nv_bfloat16* xs = pr.aux2 ? reinterpret_cast<const __nv_bfloat16*>(pr.aux2) + (long long)row * pr.ldo + ti.n0 : nullptr;
+        const __nv_bfloat16* xp = reinterpret_cast<const __nv_bfloat16*>(pr.aux);
+        for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
+          if (ti.n0 + c0 >= pr.N) break;
+          uint32_t r[32];
+          if (has_acc) {
+            ptx::tmem_ld32(taddr + c0, r);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[8 * j + e]);
+              if (xs) {
+                float f[8];
+                unpack8(__ldg(reinterpret_cast<const uint4*>(xs + c0) + j), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] += f[e];
+              }
+              for (int s = 0; s < kk; ++s) {
+                int rr = rows_s[s];
+                if (rr >= pr.aux_rows) {
+                  record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
+                  rr = -1;
+                }
+                if (rr >= 0) {
+                  float f[8];
+                  unpack8(__ldg(reinterpret_cast<const uint4*>(xp + (long long)rr * pr.ld_aux + ti.n0 + c0) + j), f);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) v[e] += f[e];
+                }
+              }
+              reinterpret_cast<uint4*>(dxp + c0)[j] = pack8(v);
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tail->tmem_empty[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace gemm
+}  // namespace moe

@@ -1,0 +1,132 @@
+// Backward expert GEMMs: dgrad of the down projection with the SwiGLU
+// backward epilogue, dgrad of gate/up, and the ragged-K weight gradients.
+#include "gemm_host.cuh"
+
+namespace moe {
+using namespace gemm;
+
+namespace {
+
+long long mgroup_tile_bound(int rows_total, int G, int N, int n_tile) {
+  return ((long long)rows_total / BM + G) * cdiv_h(N, n_tile);
+}
+
+bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
+  const int ia = P.num_maps++, ib = P.num_maps++;
+  if (!encode_2d(&P.maps[ia], a.dO, a.d, a.rows_total, (uint64_t)a.d * 2, 64, BM)) return false;
+  // B[n = j in H, k = c in d] = W_d[g][c][j]: MN-major, stored [G][K=d][N=H]
+  if (!encode_3d(&P.maps[ib], a.Wd, a.H, a.d, a.G, 64, 64)) return false;
+  pr = blank_problem();
+  pr.offsets = a.offsets;
+  pr.G = a.G;
+  pr.extent = a.rows_total;
+  pr.N = a.H;
+  pr.K = a.d;
+  pr.mma_n = 256;
+  pr.n_tile = 256;
+  pr.map_a = ia;
+  pr.map_b = ib;
+  pr.tx_bytes = A_BYTES + 4 * MN_BLOCK_BYTES;
+  pr.out = a.dau;
+  pr.ldo = 2LL * a.H;
+  pr.aux = const_cast<void*>(a.au);
+  pr.ld_aux = 2LL * a.H;
+  pr.H = a.H;
+  return true;
+}
+
+bool fill_dgrad_gu(Params& P, Problem& pr, const DgradGuArgs& a) {
+  const int ia = P.num_maps++, ig = P.num_maps++, iu = P.num_maps++;
+  if (!encode_2d(&P.maps[ia], a.dau, 2 * a.H, a.rows_total, (uint64_t)a.H * 4, 64, BM)) return false;
+  // B[n = c in d, k = j in 2H]: W_g[g][j][c] for j < H, W_u[g][j-H][c] after
+  if (!encode_3d(&P.maps[ig], a.Wg, a.d, a.H, a.G, 64, 64)) return false;
+  if (!encode_3d(&P.maps[iu], a.Wu, a.d, a.H, a.G, 64, 64)) return false;
+  pr = blank_problem();
+  pr.offsets = a.offsets;
+  pr.G = a.G;
+  pr.extent = a.rows_total;
+  pr.N = a.d;
+  pr.K = 2 * a.H;
+  pr.mma_n = 256;
+  pr.n_tile = 256;
+  pr.map_a = ia;
+  pr.map_b = ig;
+  pr.map_b2 = iu;
+  pr.ksplit = a.H;
+  pr.tx_bytes = A_BYTES + 4 * MN_BLOCK_BYTES;
+  pr.out = a.dx;
+  pr.ldo = a.d;
+  return true;
+}
+
+bool fill_wgrad(Params& P, Problem& pr, const WgradArgs& a) {
+  const int ia = P.num_maps++, ib = P.num_maps++;
+  if (!encode_2d(&P.maps[ia], a.A, a.M, a.rows_total, (uint64_t)a.M * 2, 64, 64)) return false;
+  if (!encode_2d(&P.maps[ib], a.B, a.N, a.rows_total, (uint64_t)a.N * 2, 64, 64)) return false;
+  pr = blank_problem();
+  pr.offsets = a.offsets;
+  pr.G = a.G;
+  pr.extent = a.rows_total;
+  pr.M = a.M;
+  pr.N = a.N;
+  pr.mma_n = 256;
+  pr.n_tile = 256;
+  pr.map_a = ia;
+  pr.map_b = ib;
+  pr.tx_bytes = 2 * MN_BLOCK_BYTES + 4 * MN_BLOCK_BYTES;
+  pr.out = a.out;
+  pr.out2 = a.out2;
+  pr.row_split = a.out2 ? a.row_split : 0;
+  pr.ldo = a.N;
+  pr.gstride = (long long)(a.out2 ? a.row_split : a.M) * a.N;
+  return true;
+}
+
+}  // namespace
+
+cudaError_t gemm_dgrad_down(const DgradDownArgs& routed, const DgradDownArgs* shared, int* status, cudaStream_t s) {
+  (void)status;
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  if (!fill_dgrad_down(P, P.prob[0], routed)) return cudaErrorInvalidValue;
+  long long bound = mgroup_tile_bound(routed.rows_total, routed.G, routed.H, 256);
+  P.num_problems = 1;
+  if (shared) {
+    if (!fill_dgrad_down(P, P.prob[1], *shared)) return cudaErrorInvalidValue;
+    bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->H, 256);
+    P.num_problems = 2;
+  }
+  return launch<0, 1, MGROUP, EPI_SWIGLU_BWD>(P, bound, s);
+}
+
+cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, int* status, cudaStream_t s) {
+  (void)status;
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  if (!fill_dgrad_gu(P, P.prob[0], routed)) return cudaErrorInvalidValue;
+  long long bound = mgroup_tile_bound(routed.rows_total, routed.G, routed.d, 256);
+  P.num_problems = 1;
+  if (shared) {
+    if (!fill_dgrad_gu(P, P.prob[1], *shared)) return cudaErrorInvalidValue;
+    bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->d, 256);
+    P.num_problems = 2;
+  }
+  return launch<0, 1, MGROUP, EPI_BF16>(P, bound, s);
+}
+
+cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* status, cudaStream_t s) {
+  (void)status;
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  if (!fill_wgrad(P, P.prob[0], routed)) return cudaErrorInvalidValue;
+  long long bound = (long long)routed.G * cdiv_h(routed.M, BM) * cdiv_h(routed.N, 256);
+  P.num_problems = 1;
+  if (shared) {
+    if (!fill_wgrad(P, P.prob[1], *shared)) return cudaErrorInvalidValue;
+    bound += (long long)shared->G * cdiv_h(shared->M, BM) * cdiv_h(shared->N, 256);
+    P.num_problems = 2;
+  }
+  return launch<1, 1, KGROUP, EPI_BF16>(P, bound, s);
+}
+
+}  // namespace moe

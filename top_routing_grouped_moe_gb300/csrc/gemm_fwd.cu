@@ -1,0 +1,90 @@
+// Forward expert GEMMs: gate/up with the SwiGLU epilogue, and down.
+#include "gemm_host.cuh"
+
+namespace moe {
+using namespace gemm;
+
+namespace {
+
+bool fill_swiglu_fwd(Params& P, Problem& pr, const SwigluFwdArgs& a) {
+  const int ia = P.num_maps++, ig = P.num_maps++, iu = P.num_maps++;
+  if (!encode_2d(&P.maps[ia], a.a, a.d, a.rows_total, (uint64_t)a.d * 2, 64, BM)) return false;
+  if (!encode_3d(&P.maps[ig], a.Wg, a.d, a.H, a.G, 64, 128)) return false;
+  if (!encode_3d(&P.maps[iu], a.Wu, a.d, a.H, a.G, 64, 128)) return false;
+  pr = blank_problem();
+  pr.offsets = a.offsets;
+  pr.G = a.G;
+  pr.extent = a.rows_total;
+  pr.N = a.H;
+  pr.K = a.d;
+  pr.mma_n = 256;
+  pr.n_tile = 128;  // 128 gate + 128 up accumulator columns -> 128 h columns
+  pr.map_a = ia;
+  pr.map_b = ig;
+  pr.map_b2 = iu;
+  pr.tx_bytes = A_BYTES + 2 * 128 * BK * 2;
+  pr.out = a.h;
+  pr.ldo = a.H;
+  pr.aux = a.au;
+  pr.ld_aux = 2LL * a.H;
+  pr.H = a.H;
+  return true;
+}
+
+bool fill_down_fwd(Params& P, Problem& pr, const DownFwdArgs& a) {
+  const int ia = P.num_maps++, ib = P.num_maps++;
+  if (!encode_2d(&P.maps[ia], a.h, a.H, a.rows_total, (uint64_t)a.H * 2, 64, BM)) return false;
+  if (!encode_3d(&P.maps[ib], a.Wd, a.H, a.d, a.G, 64, 256)) return false;
+  pr = blank_problem();
+  pr.offsets = a.offsets;
+  pr.G = a.G;
+  pr.extent = a.rows_total;
+  pr.N = a.d;
+  pr.K = a.H;
+  pr.mma_n = 256;
+  pr.n_tile = 256;
+  pr.map_a = ia;
+  pr.map_b = ib;
+  pr.tx_bytes = A_BYTES + 256 * BK * 2;
+  pr.out = a.o;
+  pr.ldo = a.d;
+  return true;
+}
+
+long long mgroup_tile_bound(int rows_total, int G, int N, int n_tile) {
+  return ((long long)rows_total / BM + G) * cdiv_h(N, n_tile);
+}
+
+}  // namespace
+
+cudaError_t gemm_swiglu_fwd(const SwigluFwdArgs& routed, const SwigluFwdArgs* shared, int* status, cudaStream_t s) {
+  (void)status;
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  if (!fill_swiglu_fwd(P, P.prob[0], routed)) return cudaErrorInvalidValue;
+  long long bound = mgroup_tile_bound(routed.rows_total, routed.G, routed.H, 128);
+  P.num_problems = 1;
+  if (shared) {
+    if (!fill_swiglu_fwd(P, P.prob[1], *shared)) return cudaErrorInvalidValue;
+    bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->H, 128);
+    P.num_problems = 2;
+  }
+  return launch<0, 0, MGROUP, EPI_SWIGLU_FWD>(P, bound, s);
+}
+
+cudaError_t gemm_down_fwd(const DownFwdArgs& routed, const DownFwdArgs* shared, int* status, cudaStream_t s) {
+  (void)status;
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  if (!fill_down_fwd(P, P.prob[0], routed)) return cudaErrorInvalidValue;
+  long long bound = mgroup_tile_bound(routed.rows_total, routed.G, routed.d, 256);
+  P.num_problems = 1;
+  if (shared) {
+    if (!fill_down_fwd(P, P.prob[1], *shared)) return cudaErrorInvalidValue;
+    bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->d, 256);
+    P.num_problems = 2;
+  }
+  return launch<0, 0, MGROUP, EPI_BF16>(P, bound, s);
+}
+
+}  // namespace moe

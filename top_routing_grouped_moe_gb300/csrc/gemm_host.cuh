@@ -1,0 +1,100 @@
+// Host helpers for the grouped GEMM: TMA tensor-map encoding (driver entry
+// point fetched through the runtime, so the library needs no link-time
+// libcuda) and the generic persistent launch.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "gemm.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace gemm {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [outer, inner] tensor with row pitch
+// `row_bytes`; box = box_inner x box_outer elements, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+inline bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                      uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 map over [d2, d1, d0] (d0 contiguous); box = b0 x b1 x 1.
+inline bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+                      uint32_t b1) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int cdiv_h(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+inline Problem blank_problem() {
+  Problem p;
+  std::memset(&p, 0, sizeof(p));
+  p.map_b2 = -1;
+  return p;
+}
+
+// Launch a persistent grid (<= one CTA per SM) for `tile_bound` tiles at most.
+template <int AMN, int BMN, int MODE, int EPI>
+cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static unsigned long long configured = 0;  // bit per device
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 64 && !(configured & (1ull << dev))) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+      if (e != cudaSuccess) return e;
+      configured |= 1ull << dev;
+    }
+  }
+  if (tile_bound <= 0) return cudaSuccess;
+  P.status = device_status_ptr();
+  int grid = device_sm_count();
+  if (tile_bound < grid) grid = static_cast<int>(tile_bound);
+  kern<<<grid, NUM_THREADS, kSmemBytes, s>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace gemm
+}  // namespace moe

@@ -1,0 +1,102 @@
+// Host-side interface between the C ABI (moe_abi.cu) and the kernel files.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// per-device facts and the device status word
+int device_sm_count();
+int* device_status_ptr();  // device address of the status word of the current device
+
+// ------------------------------------------------------------ SIMT kernels
+cudaError_t launch_topk_gating(const float* logits, int T, int E, int k, int32_t* idx, float* gates,
+                               int* status, cudaStream_t s);
+cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int E, int k, int capacity,
+                           int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
+                           int32_t* slot_of_row, void* x_perm, void* ws, int* status, cudaStream_t s);
+size_t permute_ws_bytes(int T, int E, int k);
+cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
+                           int T, int d, int k, void* y, int* status, cudaStream_t s);
+cudaError_t launch_combine_bwd(const void* dY, const void* o_perm, const float* gates, const int32_t* row_of_slot,
+                               int T, int d, int k, void* dO_perm, float* dgates, int* status, cudaStream_t s);
+cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot, int T, int d,
+                                    int k, void* dx, int* status, cudaStream_t s);
+// dlogits [T,E] fp32 (dense) and, if dl_bf16 != NULL, a bf16 copy [T,E]
+cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
+                                 float* dlogits, uint16_t* dl_bf16, cudaStream_t s);
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s);
+cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float* out, cudaStream_t s);
+
+// ------------------------------------------------------------ tensor-core GEMMs
+// All return cudaSuccess or an error; tensor-map encoding failures map to
+// cudaErrorInvalidValue.
+struct SwigluFwdArgs {
+  const void* a;        // [rows, d] bf16 (x_perm or x)
+  int rows_total;       // rows of the A buffer
+  const int32_t* offsets;  // [G+1] device, or NULL (dense: G = 1 over rows_total)
+  int G, d, H;
+  const void* Wg;       // [G, H, d]
+  const void* Wu;
+  void* au;             // [rows, 2H] or NULL
+  void* h;              // [rows, H]
+};
+struct DownFwdArgs {
+  const void* h;        // [rows, H]
+  int rows_total;
+  const int32_t* offsets;
+  int G, d, H;
+  const void* Wd;       // [G, d, H]
+  void* o;              // [rows, d]
+};
+// routed + (optional) shared in one persistent launch
+cudaError_t gemm_swiglu_fwd(const SwigluFwdArgs& routed, const SwigluFwdArgs* shared, int* status, cudaStream_t s);
+cudaError_t gemm_down_fwd(const DownFwdArgs& routed, const DownFwdArgs* shared, int* status, cudaStream_t s);
+// logits[T,E] = x W_r^T + bias
+cudaError_t gemm_router_fwd(const void* x, const void* W_r, const float* bias, int T, int d, int E, float* logits,
+                            int* status, cudaStream_t s);
+
+struct DgradDownArgs {    // dau = swiglu_bwd(dO W_d, au)
+  const void* dO;         // [rows, d]
+  int rows_total;
+  const int32_t* offsets;
+  int G, d, H;
+  const void* Wd;         // [G, d, H]
+  const void* au;         // [rows, 2H]
+  void* dau;              // [rows, 2H]
+};
+struct DgradGuArgs {      // dx = dau [W_g; W_u]
+  const void* dau;        // [rows, 2H]
+  int rows_total;
+  const int32_t* offsets;
+  int G, d, H;
+  const void* Wg;         // [G, H, d]
+  const void* Wu;
+  void* dx;               // [rows, d]
+};
+struct WgradArgs {        // out[g] = A_g^T B_g over rows [off[g], off[g+1])
+  const void* A;          // [rows, M] bf16
+  const void* B;          // [rows, N] bf16
+  int rows_total;
+  const int32_t* offsets; // or NULL: G = 1 over rows_total
+  int G, M, N;
+  void* out;              // [G, M, N] (rows < row_split), bf16
+  void* out2;             // rows >= row_split go here as [G, M - row_split, N]; NULL = none
+  int row_split;
+};
+cudaError_t gemm_dgrad_down(const DgradDownArgs& routed, const DgradDownArgs* shared, int* status, cudaStream_t s);
+cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, int* status, cudaStream_t s);
+cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* status, cudaStream_t s);
+// dW_r partials: part[S, E, d] = split-K pieces of dl^T x; dl_bf16 [T, E]
+cudaError_t gemm_router_dw(const uint16_t* dl_bf16, const void* x, int T, int d, int E, int S, float* part,
+                           int* status, cudaStream_t s);
+// dx = dl W_r + dx_s + sum_s dx_perm[row(t,s)]
+cudaError_t gemm_router_dx_reduce(const uint16_t* dl_bf16, const void* W_r, const void* dx_perm, const void* dx_s,
+                                  const int32_t* row_of_slot, int T, int d, int E, int k, void* dx, int* status,
+                                  cudaStream_t s);
+
+// split-K factor used for dW_r
+int router_dw_splits(int T, int d, int E);
+
+}  // namespace moe

@@ -1,0 +1,305 @@
+// C ABI of the MoE layer (include/moe.h): argument validation on the host,
+// workspace carving, and the launch sequence of each call.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// Device status word: kernels record the first device-side error here.
+__device__ int g_moe_status = 0;
+
+namespace {
+thread_local int t_last_cuda_error = 0;
+std::mutex g_dev_mu;
+int g_sm_count[64] = {0};
+int* g_status_ptr[64] = {nullptr};
+
+inline int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return MOE_ERR_CUDA;
+}
+inline int check(cudaError_t e) { return e == cudaSuccess ? MOE_OK : fail_cuda(e); }
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+int check_dims(int T, int d, int E, int k) {
+  if (T < 1 || d < 1 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || k > E || E > kMaxE || (E % 8) != 0 || (d % 64) != 0) return MOE_ERR_UNSUPPORTED;
+  if ((long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+int check_hidden(int H, int Hs) {
+  if (H < 128 || (H % 128) != 0) return MOE_ERR_UNSUPPORTED;
+  if (Hs < 0 || (Hs % 128) != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// workspace of each call
+size_t ws_route_topk_bwd(int T, int d, int E) {
+  const int S = router_dw_splits(T, d, E);
+  return align256((size_t)T * E * 2) + (S > 1 ? align256((size_t)S * E * d * 4) : 0);
+}
+size_t ws_permute_bwd(int T, int E) { return align256((size_t)T * E * 2); }
+size_t ws_swiglu_bwd(int T, int k, int H, int Hs) {
+  return align256((size_t)T * k * 2 * H * 2) + align256((size_t)T * 2 * Hs * 2);
+}
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+int* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_status) == cudaSuccess) g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_version(void) { return (1 << 16) | 0; }
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "shape outside the supported limits";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "device: bounded wait expired";
+    case MOE_ERR_DEVICE_BOUNDS: return "device: index out of range";
+    default: return "unknown status";
+  }
+}
+
+int moe_last_cuda_error(void) { return t_last_cuda_error; }
+
+int moe_device_status(int* status_out) {
+  if (!status_out) return MOE_ERR_INVALID_ARG;
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_moe_status, sizeof(int));
+  if (e != cudaSuccess) return fail_cuda(e);
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_moe_status, &zero, sizeof(int));
+  if (e != cudaSuccess) return fail_cuda(e);
+  *status_out = v;
+  return MOE_OK;
+}
+
+int moe_workspace_size(int T, int d, int E, int k, int H, int Hs, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  rc = check_hidden(H, Hs);
+  if (rc) return rc;
+  size_t b = permute_ws_bytes(T, E, k);
+  size_t v = ws_route_topk_bwd(T, d, E);
+  if (v > b) b = v;
+  v = ws_permute_bwd(T, E);
+  if (v > b) b = v;
+  v = ws_swiglu_bwd(T, k, H, Hs);
+  if (v > b) b = v;
+  *bytes = b;
+  return MOE_OK;
+}
+
+int moe_route_topk(const void* x, const void* W_r, const float* bias, const float* logits_in, int T, int d, int E,
+                   int k, float* logits, int32_t* topk_idx, float* gates, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (T < 1 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || k > E || E > kMaxE || (E % 8) != 0) return MOE_ERR_UNSUPPORTED;
+  if (!topk_idx || !gates) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float* src = logits_in;
+  if (!logits_in) {
+    int rc = check_dims(T, d, E, k);
+    if (rc) return rc;
+    if (!x || !W_r || !logits || !al16(x) || !al16(W_r) || !al16(logits)) return MOE_ERR_INVALID_ARG;
+    cudaError_t e = gemm_router_fwd(x, W_r, bias, T, d, E, logits, device_status_ptr(), s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    src = logits;
+  }
+  return check(launch_topk_gating(src, T, E, k, topk_idx, gates, device_status_ptr(), s));
+}
+
+int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int k, int capacity, int32_t* counts_raw,
+                int32_t* counts, int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row, void* x_perm, void* ws,
+                size_t ws_bytes, void* stream) {
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  if (!x || !topk_idx || !counts_raw || !counts || !offsets || !row_of_slot || !slot_of_row || !x_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(x_perm)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < permute_ws_bytes(T, E, k)) return MOE_ERR_WORKSPACE;
+  return check(launch_permute(x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, row_of_slot,
+                              slot_of_row, x_perm, ws, device_status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const void* x, int T, int d, int E, int k, int H,
+                       int Hs, const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
+                       const void* Ws_d, void* au, void* h, void* o_perm, void* au_s, void* h_s, void* s_out,
+                       void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  rc = check_hidden(H, Hs);
+  if (rc) return rc;
+  if (!x_perm || !offsets || !W_g || !W_u || !W_d || !h || !o_perm) return MOE_ERR_INVALID_ARG;
+  if (!al16(x_perm) || !al16(W_g) || !al16(W_u) || !al16(W_d) || !al16(h) || !al16(o_perm) || (au && !al16(au)))
+    return MOE_ERR_INVALID_ARG;
+  if (Hs > 0) {
+    if (!x || !Ws_g || !Ws_u || !Ws_d || !h_s || !s_out) return MOE_ERR_INVALID_ARG;
+    if (!al16(x) || !al16(Ws_g) || !al16(Ws_u) || !al16(Ws_d) || !al16(h_s) || !al16(s_out) ||
+        (au_s && !al16(au_s)))
+      return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = device_status_ptr();
+  SwigluFwdArgs r{x_perm, T * k, offsets, E, d, H, W_g, W_u, au, h};
+  SwigluFwdArgs sh{x, T, nullptr, 1, d, Hs, Ws_g, Ws_u, au_s, h_s};
+  cudaError_t e = gemm_swiglu_fwd(r, Hs > 0 ? &sh : nullptr, status, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  DownFwdArgs rd{h, T * k, offsets, E, d, H, W_d, o_perm};
+  DownFwdArgs sd{h_s, T, nullptr, 1, d, Hs, Ws_d, s_out};
+  return check(gemm_down_fwd(rd, Hs > 0 ? &sd : nullptr, status, st));
+}
+
+int moe_unpermute_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot, int T,
+                          int d, int k, void* y, void* stream) {
+  if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || (d % 64) != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!o_perm || !gates || !row_of_slot || !y) return MOE_ERR_INVALID_ARG;
+  if (!al16(o_perm) || !al16(y) || (s_out && !al16(s_out))) return MOE_ERR_INVALID_ARG;
+  return check(launch_combine(o_perm, s_out, gates, row_of_slot, T, d, k, y, device_status_ptr(),
+                              static_cast<cudaStream_t>(stream)));
+}
+
+int moe_unpermute_combine_bwd(const void* dY, const void* o_perm, const float* gates, const int32_t* row_of_slot,
+                              int T, int d, int k, void* dO_perm, float* dgates, void* stream) {
+  if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || (d % 64) != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!dY || !o_perm || !gates || !row_of_slot || !dO_perm || !dgates) return MOE_ERR_INVALID_ARG;
+  if (!al16(dY) || !al16(o_perm) || !al16(dO_perm)) return MOE_ERR_INVALID_ARG;
+  return check(launch_combine_bwd(dY, o_perm, gates, row_of_slot, T, d, k, dO_perm, dgates, device_status_ptr(),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_swiglu_bwd(const void* dO_perm, const void* dY, const int32_t* offsets, const void* x_perm,
+                           const void* x, const void* au, const void* h, const void* au_s, const void* h_s, int T,
+                           int d, int E, int k, int H, int Hs, const void* W_g, const void* W_u, const void* W_d,
+                           const void* Ws_g, const void* Ws_u, const void* Ws_d, void* dx_perm, void* dx_s,
+                           void* dW_g, void* dW_u, void* dW_d, void* dWs_g, void* dWs_u, void* dWs_d, void* ws,
+                           size_t ws_bytes, void* stream) {
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  rc = check_hidden(H, Hs);
+  if (rc) return rc;
+  const void* req[] = {dO_perm, offsets, x_perm, au, h, W_g, W_u, W_d, dx_perm, dW_g, dW_u, dW_d};
+  for (const void* p : req)
+    if (!p) return MOE_ERR_INVALID_ARG;
+  for (const void* p : req)
+    if (!al16(p)) return MOE_ERR_INVALID_ARG;
+  if (Hs > 0) {
+    const void* req_s[] = {dY, x, au_s, h_s, Ws_g, Ws_u, Ws_d, dx_s, dWs_g, dWs_u, dWs_d};
+    for (const void* p : req_s)
+      if (!p || !al16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!ws || ws_bytes < ws_swiglu_bwd(T, k, H, Hs)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = device_status_ptr();
+  char* w = static_cast<char*>(ws);
+  void* dau = w;
+  void* dau_s = w + align256((size_t)T * k * 2 * H * 2);
+
+  DgradDownArgs r1{dO_perm, T * k, offsets, E, d, H, W_d, au, dau};
+  DgradDownArgs s1{dY, T, nullptr, 1, d, Hs, Ws_d, au_s, dau_s};
+  cudaError_t e = gemm_dgrad_down(r1, Hs > 0 ? &s1 : nullptr, status, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+
+  WgradArgs r2{dO_perm, h, T * k, offsets, E, d, H, dW_d, nullptr, 0};
+  WgradArgs s2{dY, h_s, T, nullptr, 1, d, Hs, dWs_d, nullptr, 0};
+  e = gemm_wgrad(r2, Hs > 0 ? &s2 : nullptr, status, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+
+  DgradGuArgs r3{dau, T * k, offsets, E, d, H, W_g, W_u, dx_perm};
+  DgradGuArgs s3{dau_s, T, nullptr, 1, d, Hs, Ws_g, Ws_u, dx_s};
+  e = gemm_dgrad_gu(r3, Hs > 0 ? &s3 : nullptr, status, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+
+  WgradArgs r4{dau, x_perm, T * k, offsets, E, 2 * H, d, dW_g, dW_u, H};
+  WgradArgs s4{dau_s, x, T, nullptr, 1, 2 * Hs, d, dWs_g, dWs_u, Hs};
+  return check(gemm_wgrad(r4, Hs > 0 ? &s4 : nullptr, status, st));
+}
+
+int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* topk_idx, const void* x, int T, int d,
+                       int E, int k, float* dlogits, float* dW_r, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 1 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || k > E || E > kMaxE || (E % 8) != 0) return MOE_ERR_UNSUPPORTED;
+  if (!dgates || !gates || !topk_idx || !dlogits) return MOE_ERR_INVALID_ARG;
+  if ((x == nullptr) != (dW_r == nullptr)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!x) return check(launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits, nullptr, st));
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  if (!al16(x) || !al16(dW_r)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < ws_route_topk_bwd(T, d, E)) return MOE_ERR_WORKSPACE;
+  char* w = static_cast<char*>(ws);
+  uint16_t* dl_bf16 = reinterpret_cast<uint16_t*>(w);
+  cudaError_t e = launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits, dl_bf16, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const int S = router_dw_splits(T, d, E);
+  float* part = S > 1 ? reinterpret_cast<float*>(w + align256((size_t)T * E * 2)) : dW_r;
+  e = gemm_router_dw(dl_bf16, x, T, d, E, S, part, device_status_ptr(), st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (S > 1) return check(launch_splitk_reduce(part, S, (long long)E * d, dW_r, st));
+  return MOE_OK;
+}
+
+int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot, const float* dlogits,
+                    const void* W_r, int T, int d, int E, int k, void* dx, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || (d % 64) != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!dx_perm || !row_of_slot || !dx) return MOE_ERR_INVALID_ARG;
+  if (!al16(dx_perm) || !al16(dx) || (dx_s && !al16(dx_s))) return MOE_ERR_INVALID_ARG;
+  if ((dlogits == nullptr) != (W_r == nullptr)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!W_r) return check(launch_unpermute_reduce(dx_perm, dx_s, row_of_slot, T, d, k, dx, device_status_ptr(), st));
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  if (!al16(W_r)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < ws_permute_bwd(T, E)) return MOE_ERR_WORKSPACE;
+  uint16_t* dl_bf16 = static_cast<uint16_t*>(ws);
+  cudaError_t e = launch_f32_to_bf16(dlogits, dl_bf16, (long long)T * E, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return check(gemm_router_dx_reduce(dl_bf16, W_r, dx_perm, dx_s, row_of_slot, T, d, E, k, dx, device_status_ptr(),
+                                     st));
+}
+
+}  // extern "C"

@@ -1,0 +1,533 @@
+// SIMT kernels of the MoE layer: top-k gating, the deterministic permutation
+// (tile histogram + in-tile ranks, column scan, stable scatter), the
+// gate-weighted combine and the backward passes of those steps.  All of them
+// are bandwidth or latency bound: rows move as 16-byte vectors, one warp per
+// token, fp32 accumulation, and nothing depends on the order of atomics.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
+  // total order: value descending, then expert index ascending (-0.0 == +0.0)
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+// ------------------------------------------------------------------ top-k
+// One warp per token.  Lane l holds logits e = l + 32 j.  k rounds of a
+// warp arg-max (butterfly shuffles), ties to the lower expert index.
+template <int NJ>
+__global__ void topk_gating_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
+                                   float* __restrict__ gates) {
+  const int warp = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  const float* row = logits + (long long)warp * E;
+  float v[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    int e = lane + 32 * j;
+    v[j] = e < E ? __ldg(row + e) : 0.0f;
+  }
+  uint32_t taken = 0;
+  float sel_v[kMaxK];
+  int sel_i[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    if (s >= k) break;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      int e = lane + 32 * j;
+      if (e < E && !(taken & (1u << j)) && better(v[j], e, bv, bi)) {
+        bv = v[j];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    sel_v[s] = bv;
+    sel_i[s] = bi;
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+  }
+  // gates: softmax over the selected logits (max = the first one)
+  const float m = sel_v[0];
+  float den = 0.0f;
+  float ex[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    if (s >= k) break;
+    ex[s] = (sel_v[s] == -INFINITY) ? 0.0f : expf(sel_v[s] - m);
+    den += ex[s];
+  }
+  if (lane < k) {
+    float g = 0.0f;
+    int id = 0;
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s)
+      if (s == lane) {
+        g = ex[s] / den;
+        id = sel_i[s];
+      }
+    idx[(long long)warp * k + lane] = id;
+    gates[(long long)warp * k + lane] = g;
+  }
+}
+
+// ------------------------------------------------------------------ permutation
+// (1) per tile of kRouteTile tokens: a bitmask of the tile's tokens per expert
+// in shared memory gives the tile's per-expert counts and each (token, slot)'s
+// rank among the tile's tokens that picked the same expert.
+__global__ void perm_tile_hist_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                      int32_t* __restrict__ tile_counts, int32_t* __restrict__ inrank,
+                                      int* status) {
+  __shared__ uint32_t bits[kMaxE][kRouteTile / 32];
+  const int tile = blockIdx.x;
+  const int t_local = threadIdx.x;  // blockDim.x == kRouteTile
+  const int t = tile * kRouteTile + t_local;
+  for (int i = threadIdx.x; i < E * (kRouteTile / 32); i += blockDim.x) (&bits[0][0])[i] = 0u;
+  __syncthreads();
+  int ex[kMaxK];
+  if (t < T) {
+    for (int s = 0; s < k; ++s) {
+      int e = idx[(long long)t * k + s];
+      bool bad = e < 0 || e >= E;
+      for (int s2 = 0; s2 < s; ++s2) bad |= (ex[s2] == e);
+      if (bad) {
+        record_status(status, MOE_ERR_DEVICE_BOUNDS);
+        e = -1;
+      }
+      ex[s] = e;
+      if (e >= 0) atomicOr(&bits[e][t_local >> 5], 1u << (t_local & 31));
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kRouteTile / 32; ++w) c += __popc(bits[e][w]);
+    tile_counts[(long long)tile * E + e] = c;
+  }
+  if (t < T) {
+    const int w0 = t_local >> 5;
+    const uint32_t lt = (1u << (t_local & 31)) - 1u;
+    for (int s = 0; s < k; ++s) {
+      int e = ex[s];
+      int r = -1;
+      if (e >= 0) {
+        r = __popc(bits[e][w0] & lt);
+        for (int w = 0; w < w0; ++w) r += __popc(bits[e][w]);
+      }
+      inrank[(long long)t * k + s] = r;
+    }
+  }
+}
+
+// (2) one block: per expert, exclusive scan of the tile counts over tiles
+// (tile_base), totals (counts_raw), capacity clamp (counts) and offsets.
+__global__ void perm_scan_kernel(const int32_t* __restrict__ tile_counts, int ntile, int E, int capacity,
+                                 int32_t* __restrict__ tile_base, int32_t* __restrict__ counts_raw,
+                                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int seg[1024];
+  __shared__ int cnt[kMaxE];
+  const int P = blockDim.x / E;  // segments of tiles per expert
+  const int tid = threadIdx.x;
+  const int e = tid % E;
+  const int p = tid / E;
+  const int chunk = (ntile + P - 1) / P;
+  int sum = 0;
+  if (p < P) {
+    const int i0 = p * chunk, i1 = min(ntile, i0 + chunk);
+    for (int i = i0; i < i1; ++i) sum += tile_counts[(long long)i * E + e];
+  }
+  seg[tid] = sum;
+  __syncthreads();
+  if (p < P) {
+    int base = 0;
+    for (int q = 0; q < p; ++q) base += seg[q * E + e];
+    const int i0 = p * chunk, i1 = min(ntile, i0 + chunk);
+    for (int i = i0; i < i1; ++i) {
+      tile_base[(long long)i * E + e] = base;
+      base += tile_counts[(long long)i * E + e];
+    }
+    if (p == P - 1) {
+      counts_raw[e] = base;
+      int c = capacity > 0 ? min(base, capacity) : base;
+      counts[e] = c;
+      cnt[e] = c;
+    }
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // exclusive scan of cnt[0..E) by one warp
+    int per = (E + 31) / 32;
+    int loc = 0;
+    for (int j = 0; j < per; ++j) {
+      int i = tid * per + j;
+      if (i < E) loc += cnt[i];
+    }
+    int incl = loc;
+    for (int s = 1; s < 32; s <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, s);
+      if (tid >= s) incl += v;
+    }
+    int run = incl - loc;
+    for (int j = 0; j < per; ++j) {
+      int i = tid * per + j;
+      if (i < E) {
+        offsets[i] = run;
+        run += cnt[i];
+      }
+    }
+    if (tid == 31) offsets[E] = incl;
+  }
+}
+
+// (3) one warp per token: rows of its kept slots, row maps, and the copy of
+// x[t] into every destination row (the row is read once).
+__global__ void perm_scatter_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ idx,
+                                    const int32_t* __restrict__ inrank, const int32_t* __restrict__ tile_base,
+                                    const int32_t* __restrict__ offsets, int T, int d, int E, int k, int capacity,
+                                    int32_t* __restrict__ row_of_slot, int32_t* __restrict__ slot_of_row,
+                                    uint4* __restrict__ x_perm) {
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int row = -1;
+  if (lane < k) {
+    const long long slot = (long long)t * k + lane;
+    int e = idx[slot];
+    int r = inrank[slot];
+    if (e >= 0 && e < E && r >= 0) {
+      int rank = tile_base[(long long)(t / kRouteTile) * E + e] + r;
+      if (capacity <= 0 || rank < capacity) row = offsets[e] + rank;
+    }
+    row_of_slot[slot] = row;
+    if (row >= 0) slot_of_row[row] = static_cast<int32_t>(slot);
+  }
+  int rows[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
+  const int vec_per_row = d / 8;  // uint4 = 8 bf16
+  const uint4* src = x + (long long)t * vec_per_row;
+  for (int c = lane; c < vec_per_row; c += 32 * 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (c + 32 * u < vec_per_row) v[u] = __ldg(src + c + 32 * u);
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      if (s >= k) break;
+      if (rows[s] < 0) continue;
+      uint4* dst = x_perm + (long long)rows[s] * vec_per_row;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < vec_per_row) dst[c + 32 * u] = v[u];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ combine
+__global__ void combine_kernel(const uint4* __restrict__ o_perm, const uint4* __restrict__ s_out,
+                               const float* __restrict__ gates, const int32_t* __restrict__ row_of_slot, int T, int d,
+                               int k, long long max_rows, uint4* __restrict__ y, int* status) {
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int row = -1;
+  float g = 0.0f;
+  if (lane < k) {
+    row = row_of_slot[(long long)t * k + lane];
+    g = gates[(long long)t * k + lane];
+    if (row >= max_rows) {
+      record_status(status, MOE_ERR_DEVICE_BOUNDS);
+      row = -1;
+    }
+  }
+  int rows[kMaxK];
+  float gs[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
+    gs[s] = __shfl_sync(0xffffffffu, g, s < k ? s : 0);
+  }
+  const int vpr = d / 8;
+  for (int c = lane; c < vpr; c += 32) {
+    float acc[8];
+    if (s_out) {
+      unpack8(__ldg(s_out + (long long)t * vpr + c), acc);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    }
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      if (s >= k) break;
+      if (rows[s] < 0) continue;
+      float f[8];
+      unpack8(__ldg(o_perm + (long long)rows[s] * vpr + c), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(gs[s], f[e], acc[e]);
+    }
+    y[(long long)t * vpr + c] = pack8(acc);
+  }
+}
+
+__global__ void combine_bwd_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ o_perm,
+                                   const float* __restrict__ gates, const int32_t* __restrict__ row_of_slot, int T,
+                                   int d, int k, long long max_rows, uint4* __restrict__ dO_perm,
+                                   float* __restrict__ dgates, int* status) {
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int row = -1;
+  float g = 0.0f;
+  if (lane < k) {
+    row = row_of_slot[(long long)t * k + lane];
+    g = gates[(long long)t * k + lane];
+    if (row >= max_rows) {
+      record_status(status, MOE_ERR_DEVICE_BOUNDS);
+      row = -1;
+    }
+  }
+  int rows[kMaxK];
+  float gs[kMaxK], dot[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
+    gs[s] = __shfl_sync(0xffffffffu, g, s < k ? s : 0);
+    dot[s] = 0.0f;
+  }
+  const int vpr = d / 8;
+  for (int c = lane; c < vpr; c += 32) {
+    float dy[8];
+    unpack8(__ldg(dY + (long long)t * vpr + c), dy);
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      if (s >= k) break;
+      if (rows[s] < 0) continue;
+      float o[8], dO[8];
+      unpack8(__ldg(o_perm + (long long)rows[s] * vpr + c), o);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        dot[s] = fmaf(dy[e], o[e], dot[s]);
+        dO[e] = gs[s] * dy[e];
+      }
+      dO_perm[(long long)rows[s] * vpr + c] = pack8(dO);
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    if (s >= k) break;
+    float v = dot[s];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == s) dgates[(long long)t * k + s] = rows[s] >= 0 ? v : 0.0f;
+  }
+}
+
+__global__ void unpermute_reduce_kernel(const uint4* __restrict__ dx_perm, const uint4* __restrict__ dx_s,
+                                        const int32_t* __restrict__ row_of_slot, int T, int d, int k,
+                                        long long max_rows, uint4* __restrict__ dx, int* status) {
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int row = -1;
+  if (lane < k) {
+    row = row_of_slot[(long long)t * k + lane];
+    if (row >= max_rows) {
+      record_status(status, MOE_ERR_DEVICE_BOUNDS);
+      row = -1;
+    }
+  }
+  int rows[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
+  const int vpr = d / 8;
+  for (int c = lane; c < vpr; c += 32) {
+    float acc[8];
+    if (dx_s) {
+      unpack8(__ldg(dx_s + (long long)t * vpr + c), acc);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    }
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      if (s >= k) break;
+      if (rows[s] < 0) continue;
+      float f[8];
+      unpack8(__ldg(dx_perm + (long long)rows[s] * vpr + c), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += f[e];
+    }
+    dx[(long long)t * vpr + c] = pack8(acc);
+  }
+}
+
+// ------------------------------------------------------------------ router backward
+// One warp per token: dl_s = g_s (dg_s - sum_j g_j dg_j) scattered into a dense
+// [T,E] row (zeros elsewhere), plus an optional bf16 copy for the GEMMs.
+__global__ void router_bwd_dl_kernel(const float* __restrict__ dgates, const float* __restrict__ gates,
+                                     const int32_t* __restrict__ idx, int T, int E, int k, float* __restrict__ dl,
+                                     uint16_t* __restrict__ dl_bf16) {
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  float g = 0.0f, dg = 0.0f;
+  int e = -1;
+  if (lane < k) {
+    g = gates[(long long)t * k + lane];
+    dg = dgates[(long long)t * k + lane];
+    e = idx[(long long)t * k + lane];
+  }
+  float sgd = g * dg;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sgd += __shfl_xor_sync(0xffffffffu, sgd, off);
+  const float mine = g * (dg - sgd);
+  int es[kMaxK];
+  float vs[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    es[s] = __shfl_sync(0xffffffffu, e, s < k ? s : 0);
+    vs[s] = __shfl_sync(0xffffffffu, mine, s < k ? s : 0);
+  }
+  for (int c = lane; c < E; c += 32) {
+    float v = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s)
+      if (s < k && es[s] == c) v = vs[s];
+    dl[(long long)t * E + c] = v;
+    if (dl_bf16) {
+      __nv_bfloat16 b = __float2bfloat16_rn(v);
+      dl_bf16[(long long)t * E + c] = *reinterpret_cast<uint16_t*>(&b);
+    }
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    __nv_bfloat16 b = __float2bfloat16_rn(src[i]);
+    dst[i] = *reinterpret_cast<uint16_t*>(&b);
+  }
+}
+
+__global__ void splitk_reduce_kernel(const float4* __restrict__ part, int S, long long n4, float4* __restrict__ out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    float4 a = part[i];
+    for (int s = 1; s < S; ++s) {
+      float4 b = part[(long long)s * n4 + i];
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    out[i] = a;
+  }
+}
+
+inline unsigned warp_blocks(long long n) { return static_cast<unsigned>((n + kWarpsPerBlock - 1) / kWarpsPerBlock); }
+inline unsigned flat_blocks(long long n, int per) {
+  long long b = (n + per - 1) / per;
+  long long cap = 8LL * device_sm_count();
+  return static_cast<unsigned>(b < cap ? (b > 0 ? b : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_topk_gating(const float* logits, int T, int E, int k, int32_t* idx, float* gates, int* status,
+                               cudaStream_t s) {
+  (void)status;
+  const unsigned grid = warp_blocks(T);
+  const int nj = (E + 31) / 32;
+  switch (nj) {
+    case 1: topk_gating_kernel<1><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
+    case 2: topk_gating_kernel<2><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
+    case 3:
+    case 4: topk_gating_kernel<4><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
+    default: topk_gating_kernel<8><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
+  }
+  return cudaGetLastError();
+}
+
+static inline size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+size_t permute_ws_bytes(int T, int E, int k) {
+  const size_t ntile = (T + kRouteTile - 1) / kRouteTile;
+  return 2 * align256(ntile * E * sizeof(int32_t)) + align256((size_t)T * k * sizeof(int32_t));
+}
+
+cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int E, int k, int capacity,
+                           int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
+                           int32_t* slot_of_row, void* x_perm, void* ws, int* status, cudaStream_t s) {
+  const int ntile = (T + kRouteTile - 1) / kRouteTile;
+  char* w = static_cast<char*>(ws);
+  int32_t* tile_counts = reinterpret_cast<int32_t*>(w);
+  int32_t* tile_base = reinterpret_cast<int32_t*>(w + align256((size_t)ntile * E * 4));
+  int32_t* inrank = reinterpret_cast<int32_t*>(w + 2 * align256((size_t)ntile * E * 4));
+  perm_tile_hist_kernel<<<ntile, kRouteTile, 0, s>>>(idx, T, E, k, tile_counts, inrank, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  perm_scan_kernel<<<1, 1024, 0, s>>>(tile_counts, ntile, E, capacity, tile_base, counts_raw, counts, offsets);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  perm_scatter_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+      static_cast<const uint4*>(x), idx, inrank, tile_base, offsets, T, d, E, k, capacity, row_of_slot, slot_of_row,
+      static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
+                           int T, int d, int k, void* y, int* status, cudaStream_t s) {
+  combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+      static_cast<const uint4*>(o_perm), static_cast<const uint4*>(s_out), gates, row_of_slot, T, d, k,
+      (long long)T * k, static_cast<uint4*>(y), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const void* dY, const void* o_perm, const float* gates, const int32_t* row_of_slot,
+                               int T, int d, int k, void* dO_perm, float* dgates, int* status, cudaStream_t s) {
+  combine_bwd_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+      static_cast<const uint4*>(dY), static_cast<const uint4*>(o_perm), gates, row_of_slot, T, d, k,
+      (long long)T * k, static_cast<uint4*>(dO_perm), dgates, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot, int T, int d,
+                                    int k, void* dx, int* status, cudaStream_t s) {
+  unpermute_reduce_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+      static_cast<const uint4*>(dx_perm), static_cast<const uint4*>(dx_s), row_of_slot, T, d, k, (long long)T * k,
+      static_cast<uint4*>(dx), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
+                                 float* dlogits, uint16_t* dl_bf16, cudaStream_t s) {
+  router_bwd_dl_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(dgates, gates, idx, T, E, k, dlogits, dl_bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s) {
+  f32_to_bf16_kernel<<<flat_blocks(n, 256), 256, 0, s>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float* out, cudaStream_t s) {
+  const long long n4 = n / 4;
+  splitk_reduce_kernel<<<flat_blocks(n4, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(partial), S, n4,
+                                                            reinterpret_cast<float4*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe
