@@ -42,11 +42,11 @@ L2_FLUSH_BYTES = 256 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="tiny64e_random", choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--cpu-sample-tokens", type=int, default=1024)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -79,7 +79,7 @@ def call_bytes(w, R):
         "moe_route_topk": route,
         "moe_permute": T * d * 2 + R * d * 2 + T * k * 4 * 4 + R * 4,
         "moe_unpermute_combine": R * d * 2 + (T * d * 2 if w.Hs else 0) + T * d * 2 + T * k * 8,
-        "moe_unpermute_combine_bwd": T * d * 2 + 2 * R * d * 2 + T * k * 12,
+        "moe_unpermute_combine_bwd": T * d * 2 + R * d * 2 + T * k * 4,
         "moe_permute_bwd": R * d * 2 + (T * d * 2 if w.Hs else 0) + T * d * 2 + T * k * 4,
     }
 
@@ -90,8 +90,8 @@ def launches_per_step(w):
     n += 3                                                 # permute: hist, scan, scatter
     n += 2                                                 # grouped swiglu: gate/up, down
     n += 1                                                 # combine
-    n += 1                                                 # combine bwd
-    n += 4                                                 # swiglu bwd: dgrad-down, wgrad-down, dgrad-gu, wgrad-gu
+    n += 1                                                 # combine bwd (gather)
+    n += 5                                                 # swiglu bwd: dgrad-down, dgates, wgrad-down, dgrad-gu, wgrad-gu
     if w.routing == "learned":
         S = max(1, min(64, w.T // 512))
         n += 2 + (1 if S > 1 else 0)                       # router bwd: dl, dW_r GEMM, split-K reduce
@@ -118,7 +118,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -275,13 +275,12 @@ def main_ours(args):
         mark(3)
         B.moe_unpermute_combine(L.o_perm, L.s, L.gates, L.row_of_slot, T, d, k, L.y, stream)
         mark(4)
-        B.moe_unpermute_combine_bwd(dev["dY"], L.o_perm, L.gates, L.row_of_slot, T, d, k, L.dO_perm, L.dgates,
-                                    stream)
+        B.moe_unpermute_combine_bwd(dev["dY"], L.row_of_slot, T, d, k, L.dY_perm, stream)
         mark(5)
-        B.moe_grouped_swiglu_bwd(L.dO_perm, dev["dY"], L.offsets, L.x_perm, x, L.au, L.h, L.au_s, L.h_s, T, d, E,
-                                 k, H, Hs, dev["W_g"], dev["W_u"], dev["W_d"], dev.get("Ws_g"), dev.get("Ws_u"),
-                                 dev.get("Ws_d"), L.dx_perm, L.dx_s, L.dW_g, L.dW_u, L.dW_d, L.dWs_g, L.dWs_u,
-                                 L.dWs_d, L.ws, L.ws_bytes, stream)
+        B.moe_grouped_swiglu_bwd(L.dY_perm, dev["dY"], L.gates, L.row_of_slot, L.slot_of_row, L.offsets, L.x_perm,
+                                 x, L.au, L.au_s, T, d, E, k, H, Hs, dev["W_g"], dev["W_u"], dev["W_d"],
+                                 dev.get("Ws_g"), dev.get("Ws_u"), dev.get("Ws_d"), L.dx_perm, L.dx_s, L.dW_g,
+                                 L.dW_u, L.dW_d, L.dWs_g, L.dWs_u, L.dWs_d, L.dgates, L.ws, L.ws_bytes, stream)
         mark(6)
         B.moe_route_topk_bwd(L.dgates, L.gates, L.idx, x if learned else None, T, d, E, k, L.dlogits,
                              L.dW_r if learned else None, L.ws, L.ws_bytes, stream)

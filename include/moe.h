@@ -46,7 +46,7 @@
  * Weight layouts (out_features x in_features):
  *   W_r [E,d]; W_g, W_u [E,H,d]; W_d [E,d,H]; Ws_g, Ws_u [Hs,d]; Ws_d [d,Hs].
  * Buffers sized for the dropless maximum R <= T*k (rows >= R are left as
- * they were): x_perm, o_perm, dO_perm, dx_perm [T*k, d]; au [T*k, 2H];
+ * they were): x_perm, o_perm, dY_perm, dx_perm [T*k, d]; au [T*k, 2H] fp32;
  * h [T*k, H]; slot_of_row [T*k].
  */
 #ifndef MOE_GB300_H
@@ -143,20 +143,21 @@ MOE_API int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, in
  *   rows [offsets[e], offsets[e+1]) of x_perm go through expert e:
  *     a = x W_g[e]^T, u = x W_u[e]^T (fp32 accumulate), h = silu(a) * u,
  *     o = h W_d[e]^T;   silu(a) = a / (1 + exp(-a)).
- *   au [T*k, 2H] bf16 receives a in columns [0,H) and u in [H,2H) (may be
- *   NULL when no backward follows); h [T*k, H] bf16 (required);
+ *   au [T*k, 2H] FP32 receives a in columns [0,H) and u in [H,2H), kept for
+ *   the backward pass (may be NULL when no backward follows);
+ *   h [T*k, H] bf16 (the down projection's input, required);
  *   o_perm [T*k, d] bf16.
  *   Shared expert (Hs > 0): the same on every token of x [T,d] with Ws_*,
- *   writing au_s [T,2Hs] (nullable), h_s [T,Hs] and s [T,d] bf16.
+ *   writing au_s [T,2Hs] fp32 (nullable), h_s [T,Hs] and s [T,d] bf16.
  *   Hs == 0: the shared pointers are ignored.
  * Tensor-core (tcgen05) grouped GEMMs fed by TMA; the per-expert tile
- * schedule is read from `offsets` on the device. */
+ * schedule is read from `offsets` on the device.  ws is unused (may be NULL). */
 MOE_API int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const void* x,
                        int T, int d, int E, int k, int H, int Hs,
                        const void* W_g, const void* W_u, const void* W_d,
                        const void* Ws_g, const void* Ws_u, const void* Ws_d,
-                       void* au, void* h, void* o_perm,
-                       void* au_s, void* h_s, void* s,
+                       float* au, void* h, void* o_perm,
+                       float* au_s, void* h_s, void* s,
                        void* ws, size_t ws_bytes, void* stream);
 
 /* Gate-weighted unpermute and combine:
@@ -169,34 +170,49 @@ MOE_API int moe_unpermute_combine(const void* o_perm, const void* s, const float
 
 /* --------------------------------------------------------------- backward */
 
-/* Backward of moe_unpermute_combine for upstream dY [T,d] bf16:
- *   dO_perm[row,:] = bf16(gates[t,s] * dY[t,:])        for kept (t,s)
- *   dgates[t,s]    = sum_c dY[t,c] * o_perm[row,c]     (fp32; 0 if dropped)
- * The gradient reaching the shared expert output is dY itself. */
-MOE_API int moe_unpermute_combine_bwd(const void* dY, const void* o_perm, const float* gates,
-                              const int32_t* row_of_slot, int T, int d, int k,
-                              void* dO_perm, float* dgates, void* stream);
+/* Backward of moe_unpermute_combine, first half: the upstream gradient of
+ * every token is gathered into its kept rows,
+ *   dY_perm[row_of_slot[t*k+s], :] = dY[t, :]      (bit copies, bf16)
+ * The other two factors of the combine backward -- dO_perm = gates * dY_perm
+ * and dgates[t,s] = <dY[t], o_perm[row]> -- are formed inside
+ * moe_grouped_swiglu_bwd, from fp32 accumulators (dgates = <dY W_d, h>, the
+ * same quantity), so that neither the gate factor nor the rounding of o_perm
+ * to bf16 limits their precision.  The gradient reaching the shared expert's
+ * output is dY itself. */
+MOE_API int moe_unpermute_combine_bwd(const void* dY, const int32_t* row_of_slot, int T, int d, int k,
+                              void* dY_perm, void* stream);
 
-/* Backward of moe_grouped_swiglu.  Inputs: dO_perm [T*k,d], dY [T,d] (the
- * shared expert's upstream gradient; ignored if Hs == 0), offsets, x_perm, x,
- * and the saved au, h (au_s, h_s) of the forward call.
- *   dh = dO W_d[e];  da = dh * u * sig(a) * (1 + a (1 - sig(a)));
- *   du = dh * silu(a);  dx_perm = da W_g[e] + du W_u[e];
- *   dW_d[e] = dO_e^T h_e;  dW_g[e] = da_e^T x_e;  dW_u[e] = du_e^T x_e
- * (the same for the shared expert over all T tokens).  Outputs (bf16):
- * dx_perm [T*k,d], dx_s [T,d], dW_g, dW_u [E,H,d], dW_d [E,d,H] (zero for
- * experts with no rows), dWs_g, dWs_u [Hs,d], dWs_d [d,Hs].  Each output
- * element is owned by one tile: no atomics, deterministic. */
-MOE_API int moe_grouped_swiglu_bwd(const void* dO_perm, const void* dY, const int32_t* offsets,
-                           const void* x_perm, const void* x,
-                           const void* au, const void* h, const void* au_s, const void* h_s,
+/* Backward of moe_grouped_swiglu and of the gate factor of the combine.
+ * Inputs: dY_perm [T*k,d] (from moe_unpermute_combine_bwd), dY [T,d] (the
+ * shared expert's upstream gradient; ignored if Hs == 0), gates [T,k],
+ * row_of_slot, slot_of_row, offsets, x_perm, x and the fp32 au (au_s) saved by
+ * the forward call.  For each kept row r of expert e, with g = gates of its
+ * slot and a, u from au:
+ *   dh' = dY_perm[r] W_d[e]          (fp32 accumulate)
+ *   dgates[slot] = sum_j dh'_j h_j,  h = silu(a) u   (= <dY, o_perm[r]>)
+ *   dh = g dh';  da = dh * u * sig(a) * (1 + a (1 - sig(a)));  du = dh * silu(a)
+ *   dx_perm[r] = da W_g[e] + du W_u[e]
+ *   dW_d[e] = sum_r dY_perm[r]^T (g h_r);  dW_g[e] = sum_r da_r^T x_perm[r];
+ *   dW_u[e] = sum_r du_r^T x_perm[r]
+ * and the same for the shared expert over all T tokens with g = 1 (no gate
+ * gradient).  The weight-gradient products take their derived operand (g h,
+ * da | du) as a bf16 hi + lo pair, so the result keeps ~16 bits over sums of
+ * thousands of rows.  Outputs: dx_perm [T*k,d], dx_s [T,d], dW_g, dW_u
+ * [E,H,d], dW_d [E,d,H] (zero for experts with no rows), dWs_g, dWs_u [Hs,d],
+ * dWs_d [d,Hs] (all bf16) and dgates [T,k] fp32 (0 for dropped slots).  Each
+ * output element is owned by one tile: no atomics, deterministic.
+ * ws >= moe_workspace_size() bytes. */
+MOE_API int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gates,
+                           const int32_t* row_of_slot, const int32_t* slot_of_row,
+                           const int32_t* offsets, const void* x_perm, const void* x,
+                           const float* au, const float* au_s,
                            int T, int d, int E, int k, int H, int Hs,
                            const void* W_g, const void* W_u, const void* W_d,
                            const void* Ws_g, const void* Ws_u, const void* Ws_d,
                            void* dx_perm, void* dx_s,
                            void* dW_g, void* dW_u, void* dW_d,
                            void* dWs_g, void* dWs_u, void* dWs_d,
-                           void* ws, size_t ws_bytes, void* stream);
+                           float* dgates, void* ws, size_t ws_bytes, void* stream);
 
 /* Backward of the top-k softmax gating and of the router product:
  *   dlogits[t,e] = g_s (dgates[t,s] - sum_j g_j dgates[t,j]) if e = topk_idx[t,s],
@@ -204,7 +220,8 @@ MOE_API int moe_grouped_swiglu_bwd(const void* dO_perm, const void* dY, const in
  *   dW_r[e,c]    = sum_t dlogits[t,e] x[t,c]                   [E,d] fp32
  * (dropped slots have dgates = 0 but stay in the renormalisation set).  x may
  * be NULL only together with dW_r == NULL (given-logits routing).  dW_r uses
- * the tensor cores with dlogits rounded to bf16 and fp32 accumulation. */
+ * the tensor cores with dlogits as a bf16 hi + lo pair and fp32
+ * accumulation. */
 MOE_API int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
                        const void* x, int T, int d, int E, int k,
                        float* dlogits, float* dW_r, void* ws, size_t ws_bytes, void* stream);

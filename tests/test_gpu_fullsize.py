@@ -1,0 +1,64 @@
+"""Full-size GPU parity: every layer configuration of the workload table
+(64-expert random and learned/Zipf routing with and without capacity, the
+expert-count sweep E in {8, 32, 64, 128} at T=16384, and the d=4096 E=128
+layer), forward and backward, in the launch configuration bench.py times.
+
+The oracle is cheap enough in float64 BLAS to run the whole layer at these
+sizes on the host, so every output element is compared (not a sample).  The
+dense float64 weight copies need up to ~20 GB of host memory (the d=4096
+layer); tests whose copy would not fit in the host's available memory are
+skipped with the reason."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as orc
+from synth import workloads
+from tests.gpu_util import compare_layer, upload
+
+pytestmark = pytest.mark.gpu
+
+FULL = ["tiny64e_random", "tiny64e_zipf", "tiny64e_zipf_cap125", "scale_E8", "scale_E32", "scale_E64",
+        "scale_E128", "large_E128"]
+
+
+def _avail_bytes():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 1 << 62
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_layer_parity(name):
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from top_routing_grouped_moe_gb300 import _binding as B
+    from top_routing_grouped_moe_gb300.layer import MoELayer
+
+    base = workloads.WORKLOADS[name]
+    w = workloads.custom(base.name, T=base.T, d=base.d, E=base.E, k=base.k, H=base.H, Hs=base.Hs,
+                         routing=base.routing, zipf_bias=base.zipf_bias, capacity_factor=base.capacity_factor,
+                         backward=True)
+    f64_weight_bytes = 8 * (3 * w.E * w.d * w.H + 3 * w.d * w.Hs)
+    need = 3 * f64_weight_bytes + 24 * w.T * w.k * max(w.d, 2 * w.H) * 8
+    if need > _avail_bytes():
+        pytest.skip(f"oracle needs ~{need / 2**30:.0f} GiB of host memory")
+    inp = workloads.make_inputs(w)
+    dev = upload(inp)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity)
+    layer.forward(dev["x"], dev, logits_in=dev.get("logits_in"))
+    layer.backward(dev["x"], dev["dY"], dev, learned_router=w.routing == "learned")
+    torch.cuda.synchronize()
+    assert B.moe_device_status() == 0
+    del dev
+    f64 = orc.inputs_to_f64(inp)
+    ref = orc.layer_forward(f64, w.k, w.capacity)
+    refb = orc.layer_backward(f64, ref)
+    flips = compare_layer(w, inp, layer, ref, refb)
+    print(f"{name}: {flips} near-tie routing flips excluded")

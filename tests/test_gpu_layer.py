@@ -15,11 +15,10 @@ import torch
 
 from oracle import moe_oracle as orc
 from synth import workloads
-from tests.gpu_util import assert_close, experts_touched, host_f64, routing_disagreements, upload
+from tests.gpu_util import assert_close, compare_layer, host_f64, upload
 
 pytestmark = pytest.mark.gpu
 
-LOGIT_TOL = 1e-4
 
 CASES = {
     # name: workload (T, d, E, k, H, Hs, routing, zipf, capacity_factor)
@@ -63,59 +62,7 @@ def test_layer_forward_backward_parity(B, name):
     f64 = orc.inputs_to_f64(inp)
     ref = orc.layer_forward(f64, w.k, w.capacity)
     refb = orc.layer_backward(f64, ref)
-    T, k = w.T, w.k
-
-    gidx = layer.idx.cpu().numpy()
-    diff = np.zeros(T, dtype=bool)
-    if w.routing == "learned":
-        gl = layer.logits.cpu().numpy()
-        np.testing.assert_allclose(gl, ref["logits"], rtol=0, atol=LOGIT_TOL)
-        delta = max(float(np.abs(gl.astype(np.float64) - ref["logits"]).max()), 1e-7) * 4
-        diff = routing_disagreements(gidx, ref["idx"], ref["logits"], k, delta)
-        assert diff.sum() <= max(1, T // 100)
-    else:
-        assert np.array_equal(gidx, ref["idx"])
-    keep = ~diff
-    skip_e = experts_touched(diff, gidx, ref["idx"])
-    keep_e = np.setdiff1d(np.arange(w.E), skip_e)
-    if w.capacity > 0 and diff.any():
-        # a flipped token shifts the token-order ranks (and so the drops) of
-        # later tokens in the experts it touches
-        keep &= ~np.isin(ref["idx"], skip_e).any(axis=1) & ~np.isin(gidx, skip_e).any(axis=1)
-    if not diff.any():
-        # routing and permutation: bit-exact
-        for key in ("counts_raw", "counts", "offsets", "row_of_slot"):
-            assert np.array_equal(getattr(layer, key).cpu().numpy(), ref[key]), key
-        R = int(ref["offsets"][-1])
-        assert np.array_equal(layer.slot_of_row.cpu().numpy()[:R], ref["slot_of_row"])
-        assert_close("x_perm", host_f64(layer.x_perm)[:R], ref["x_perm"], atol=0, rtol=0, fro=0)
-        assert_close("h", host_f64(layer.h)[:R], ref["h"])
-        assert_close("a", host_f64(layer.au)[:R, :w.H], ref["a"])
-        assert_close("u", host_f64(layer.au)[:R, w.H:], ref["u"])
-        assert_close("o_perm", host_f64(layer.o_perm)[:R], ref["o"])
-        assert_close("dO", host_f64(layer.dO_perm)[:R], refb["dO"])
-        assert_close("dx_perm", host_f64(layer.dx_perm)[:R], refb["dx_perm"])
-    np.testing.assert_allclose(layer.gates.cpu().numpy()[keep], ref["gates"][keep], rtol=1e-5, atol=1e-6)
-
-    # forward values
-    if w.Hs:
-        assert_close("s", host_f64(layer.s), ref["s"])
-    assert_close("y", host_f64(layer.y)[keep], ref["y"][keep])
-
-    # backward
-    assert_close("dgates", layer.dgates.cpu().numpy()[keep], refb["dgates"][keep])
-    assert_close("dW_d", host_f64(layer.dW_d)[keep_e], refb["dW_d"][keep_e])
-    assert_close("dW_g", host_f64(layer.dW_g)[keep_e], refb["dW_g"][keep_e])
-    assert_close("dW_u", host_f64(layer.dW_u)[keep_e], refb["dW_u"][keep_e])
-    if w.Hs:
-        assert_close("dx_s", host_f64(layer.dx_s), refb["dx_s"])
-        assert_close("dWs_d", host_f64(layer.dWs_d), refb["dWs_d"])
-        assert_close("dWs_g", host_f64(layer.dWs_g), refb["dWs_g"])
-        assert_close("dWs_u", host_f64(layer.dWs_u), refb["dWs_u"])
-    assert_close("dlogits", layer.dlogits.cpu().numpy()[keep], refb["dlogits"][keep])
-    if w.routing == "learned":
-        assert_close("dW_r", layer.dW_r.cpu().numpy()[keep_e], refb["dW_r"][keep_e])
-    assert_close("dx", host_f64(layer.dx)[keep], refb["dx"][keep])
+    compare_layer(w, inp, layer, ref, refb)
 
 
 def test_layer_is_deterministic(B):

@@ -132,7 +132,9 @@ def test_identity_expert_combine(B, cap):
     assert_close("y", host_f64(y), ref["y"], atol=1e-2, rtol=1e-2, fro=4e-3)
 
 
-def test_combine_bwd_and_reduce(B):
+def test_combine_bwd_gather_and_reduce(B):
+    """moe_unpermute_combine_bwd gathers dY into the kept rows (bit copies);
+    moe_permute_bwd sums rows back per token."""
     T, E, k, d = 600, 32, 4, 256
     l = gen.random_logits(T, E, tensor=306)
     idx, g = run_topk(B, l, k)
@@ -142,9 +144,8 @@ def test_combine_bwd_and_reduce(B):
     o_bits = gen.normal_bf16(308, (T * k, d))
     dY_bits = gen.normal_bf16(309, (T, d))
     row = torch.from_numpy(p["row_of_slot"]).cuda()
-    dO = torch.zeros(T * k, d, dtype=torch.bfloat16, device="cuda")
-    dg = torch.empty(T, k, dtype=torch.float32, device="cuda")
-    B.moe_unpermute_combine_bwd(dev_bf16(dY_bits), dev_bf16(o_bits), dev_f32(g), row, T, d, k, dO, dg)
+    dYp = torch.zeros(T * k, d, dtype=torch.bfloat16, device="cuda")
+    B.moe_unpermute_combine_bwd(dev_bf16(dY_bits), row, T, d, k, dYp)
     # reduce: dx = sum_s dx_perm[row] + dx_s, with dx_perm = o, dx_s = dY
     dx = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
     B.moe_permute_bwd(dev_bf16(o_bits), dev_bf16(dY_bits), row, None, None, T, d, E, k, dx, None, 0)
@@ -153,14 +154,11 @@ def test_combine_bwd_and_reduce(B):
     ridx, rg = orc.route_topk(l, k)
     rp = orc.permute(ridx, E, 20)
     assert int(rp["offsets"][-1]) == R
+    got = dYp.view(torch.int16).cpu().numpy().view(np.uint16)[:R]
+    assert np.array_equal(got, dY_bits[rp["slot_of_row"] // k])
     o = orc.bf16_to_f64(o_bits)
     dY = orc.bf16_to_f64(dY_bits)
-    rowm = rp["row_of_slot"].reshape(T, k)
-    ref_dO, ref_dg = orc.combine_bwd(dY, o[:R], rg, rp["row_of_slot"], T, k)
     ref_dx = orc.permute_bwd(o[:R], dY, rp["row_of_slot"], T, k)
-    assert_close("dO", host_f64(dO)[:R], ref_dO)
-    assert_close("dgates", dg.cpu().numpy(), ref_dg)
-    assert np.all(dg.cpu().numpy()[rowm < 0] == 0.0)
     assert_close("dx", host_f64(dx), ref_dx)
 
 

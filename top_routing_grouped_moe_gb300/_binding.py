@@ -47,8 +47,8 @@ SIGNATURES = {
     "moe_permute": "pp" + "iiiii" + "pppppp" + "pz" + "s",
     "moe_grouped_swiglu": "ppp" + "iiiiii" + "pppppp" + "pppppp" + "pz" + "s",
     "moe_unpermute_combine": "pppp" + "iii" + "p" + "s",
-    "moe_unpermute_combine_bwd": "pppp" + "iii" + "pp" + "s",
-    "moe_grouped_swiglu_bwd": "ppppppppp" + "iiiiii" + "pppppp" + "pp" + "pppppp" + "pz" + "s",
+    "moe_unpermute_combine_bwd": "pp" + "iii" + "p" + "s",
+    "moe_grouped_swiglu_bwd": "pppppppppp" + "iiiiii" + "pppppp" + "pp" + "pppppp" + "p" + "pz" + "s",
     "moe_route_topk_bwd": "pppp" + "iiii" + "pp" + "pz" + "s",
     "moe_permute_bwd": "ppppp" + "iiii" + "p" + "pz" + "s",
 }
@@ -154,16 +154,16 @@ def moe_unpermute_combine(o_perm, s, gates, row_of_slot, T, d, k, y, stream=None
     return _call("moe_unpermute_combine", o_perm, s, gates, row_of_slot, T, d, k, y, stream)
 
 
-def moe_unpermute_combine_bwd(dY, o_perm, gates, row_of_slot, T, d, k, dO_perm, dgates, stream=None):
-    return _call("moe_unpermute_combine_bwd", dY, o_perm, gates, row_of_slot, T, d, k, dO_perm, dgates, stream)
+def moe_unpermute_combine_bwd(dY, row_of_slot, T, d, k, dY_perm, stream=None):
+    return _call("moe_unpermute_combine_bwd", dY, row_of_slot, T, d, k, dY_perm, stream)
 
 
-def moe_grouped_swiglu_bwd(dO_perm, dY, offsets, x_perm, x, au, h, au_s, h_s, T, d, E, k, H, Hs, W_g, W_u, W_d,
-                           Ws_g, Ws_u, Ws_d, dx_perm, dx_s, dW_g, dW_u, dW_d, dWs_g, dWs_u, dWs_d, ws, ws_bytes,
-                           stream=None):
-    return _call("moe_grouped_swiglu_bwd", dO_perm, dY, offsets, x_perm, x, au, h, au_s, h_s, T, d, E, k, H, Hs,
-                 W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, dx_perm, dx_s, dW_g, dW_u, dW_d, dWs_g, dWs_u, dWs_d, ws,
-                 ws_bytes, stream)
+def moe_grouped_swiglu_bwd(dY_perm, dY, gates, row_of_slot, slot_of_row, offsets, x_perm, x, au, au_s, T, d, E, k,
+                           H, Hs, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, dx_perm, dx_s, dW_g, dW_u, dW_d, dWs_g, dWs_u,
+                           dWs_d, dgates, ws, ws_bytes, stream=None):
+    return _call("moe_grouped_swiglu_bwd", dY_perm, dY, gates, row_of_slot, slot_of_row, offsets, x_perm, x, au,
+                 au_s, T, d, E, k, H, Hs, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, dx_perm, dx_s, dW_g, dW_u, dW_d, dWs_g,
+                 dWs_u, dWs_d, dgates, ws, ws_bytes, stream)
 
 
 def moe_route_topk_bwd(dgates, gates, topk_idx, x, T, d, E, k, dlogits, dW_r, ws, ws_bytes, stream=None):

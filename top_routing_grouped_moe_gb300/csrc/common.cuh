@@ -43,4 +43,17 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
 }
 
+// v = hi + lo with hi = bf16(v), lo = bf16(v - hi): about 16 significant bits
+// in two bf16 halves (8 values each, packed).
+__device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
+  float h[8], l[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    h[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
+    l[e] = v[e] - h[e];
+  }
+  hi = pack8(h);
+  lo = pack8(l);
+}
+
 }  // namespace moe

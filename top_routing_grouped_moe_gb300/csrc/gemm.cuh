@@ -19,6 +19,13 @@
 //           B (both stored with K as the row index) into its own output slab.
 //           Weight-gradient (wgrad) GEMMs; tail rows of the last K step that
 //           belong to the next group are zeroed in shared memory.
+//
+// Split precision (nsplit = 2): one operand is given as a pair of bf16
+// tensors hi + lo (hi = bf16(v), lo = bf16(v - hi), together ~16 mantissa
+// bits); every K step is issued twice, once with each half, into the same
+// fp32 accumulator.  Used where a derived operand feeds a long reduction
+// (weight gradients), so that bf16 rounding of that operand does not grow
+// with the number of rows summed.
 #pragma once
 #include <cuda.h>
 
@@ -54,6 +61,8 @@ struct Problem {
   int n_tile;          // output columns per tile (256; 128 h columns for EPI_SWIGLU_FWD)
   int map_a, map_b, map_b2;  // tensor-map indices; map_b2 = second B map or -1
   int ksplit;          // MN-major B: k >= ksplit reads map_b2 at k - ksplit (0 = off)
+  int map_a_lo, map_b_lo;  // lo halves of a split operand (-1 = none)
+  int nsplit;          // 1, or 2 = every K step issued with the hi and the lo half
   uint32_t tx_bytes;   // bytes landing per stage
   // epilogue
   void* out;
@@ -69,6 +78,15 @@ struct Problem {
   int topk;
   int aux_rows;        // REDUCE_DX: rows of the dx_perm buffer (bounds check)
   int H;               // SWIGLU: column offset of u within au
+  // EPI_SWIGLU_BWD
+  const float* gates;      // per-slot gate (nullable: g = 1)
+  const int* slot_of_row;  // row -> slot (with gates)
+  int gate_slots;          // number of valid slots (bounds check)
+  void* out_lo;            // lo half of da | du
+  void* gh_hi;             // g*h, hi / lo halves, [rows, H]
+  void* gh_lo;
+  float* dgp;              // per-row partials of the gate gradient, [rows, ld_dgp] (nullable)
+  int ld_dgp;
 };
 
 struct Params {
@@ -128,7 +146,7 @@ __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int 
     ti.n0 = n_idx * pr.n_tile;
     ti.k0 = 0;
     ti.k1 = pr.K;
-    ti.nk = cdiv(pr.K, BK);
+    ti.nk = cdiv(pr.K, BK) * pr.nsplit;
   } else {
     int mt = cdiv(pr.M, BM);
     int per = mt * nt;
@@ -141,7 +159,7 @@ __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int 
     ti.n0 = n_idx * pr.n_tile;
     ti.k0 = S.off[p][g];
     ti.k1 = S.off[p][g + 1];
-    ti.nk = cdiv(ti.k1 - ti.k0, BK);
+    ti.nk = cdiv(ti.k1 - ti.k0, BK) * pr.nsplit;
   }
   return ti;
 }
@@ -281,14 +299,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           ptx::mbar_arrive_expect_tx(fb, pr.tx_bytes);
           issued_any |= 1u << stage;
           issued_phase_mask = (issued_phase_mask & ~(1u << stage)) | (phase << stage);
-          const int k = ti.k0 + kb * BK;
+          const int part = pr.nsplit == 2 ? (kb & 1) : 0;
+          const int k = ti.k0 + (pr.nsplit == 2 ? (kb >> 1) : kb) * BK;
           uint8_t* a_dst = sA + stage * A_BYTES;
           uint8_t* b_dst = sB + stage * B_BYTES;
+          const CUtensorMap* mAk = (part && pr.map_a_lo >= 0) ? &P.maps[pr.map_a_lo] : mA;
           if (AMN == 0) {
-            ptx::tma_load_2d(a_dst, mA, fb, k, ti.m0);
+            ptx::tma_load_2d(a_dst, mAk, fb, k, ti.m0);
           } else {
-            ptx::tma_load_2d(a_dst, mA, fb, ti.m0, k);
-            ptx::tma_load_2d(a_dst + MN_BLOCK_BYTES, mA, fb, ti.m0 + 64, k);
+            ptx::tma_load_2d(a_dst, mAk, fb, ti.m0, k);
+            ptx::tma_load_2d(a_dst + MN_BLOCK_BYTES, mAk, fb, ti.m0 + 64, k);
           }
           if (EPI == EPI_SWIGLU_FWD) {
             ptx::tma_load_3d(b_dst, &P.maps[pr.map_b], fb, k, ti.n0, ti.g);
@@ -306,7 +326,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
               }
               for (int j = 0; j < nblk; ++j) ptx::tma_load_3d(b_dst + j * MN_BLOCK_BYTES, mB, fb, ti.n0 + 64 * j, kk, ti.g);
             } else {
-              const CUtensorMap* mB = &P.maps[pr.map_b];
+              const CUtensorMap* mB = (part && pr.map_b_lo >= 0) ? &P.maps[pr.map_b_lo] : &P.maps[pr.map_b];
               for (int j = 0; j < nblk; ++j) ptx::tma_load_2d(b_dst + j * MN_BLOCK_BYTES, mB, fb, ti.n0 + 64 * j, k);
             }
           }
@@ -353,7 +373,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         }
         ptx::tc_fence_after();
         int valid = BK;
-        if (MODE == KGROUP) valid = min(BK, ti.k1 - (ti.k0 + kb * BK));
+        if (MODE == KGROUP) valid = min(BK, ti.k1 - (ti.k0 + (pr.nsplit == 2 ? (kb >> 1) : kb) * BK));
         const int nsub = (valid + UMMA_K - 1) / UMMA_K;
         uint8_t* a_st = sA + stage * A_BYTES;
         uint8_t* b_st = sB + stage * B_BYTES;
@@ -482,9 +502,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           }
         }
       } else if (EPI == EPI_SWIGLU_FWD) {
-        // accumulator columns [0,128) = a (gate), [128,256) = u (up)
+        // accumulator columns [0,128) = a (gate), [128,256) = u (up); a and u
+        // are kept in fp32 for the backward pass
         __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row * pr.ldo + ti.n0;
-        __nv_bfloat16* ap = pr.aux ? reinterpret_cast<__nv_bfloat16*>(pr.aux) + (long long)row * pr.ld_aux + ti.n0 : nullptr;
+        float* ap = pr.aux ? reinterpret_cast<float*>(pr.aux) + (long long)row * pr.ld_aux + ti.n0 : nullptr;
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t ra[32], ru[32];
           ptx::tmem_ld32(taddr + c0, ra);
@@ -501,26 +522,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
                 h[e] = a * sigmoidf_(a) * u;
               }
               reinterpret_cast<uint4*>(hp + c0)[j] = pack8(h);
-              if (ap) {
-                uint4 va, vu;
-                va.x = pack_bf16(__uint_as_float(ra[8 * j + 0]), __uint_as_float(ra[8 * j + 1]));
-                va.y = pack_bf16(__uint_as_float(ra[8 * j + 2]), __uint_as_float(ra[8 * j + 3]));
-                va.z = pack_bf16(__uint_as_float(ra[8 * j + 4]), __uint_as_float(ra[8 * j + 5]));
-                va.w = pack_bf16(__uint_as_float(ra[8 * j + 6]), __uint_as_float(ra[8 * j + 7]));
-                vu.x = pack_bf16(__uint_as_float(ru[8 * j + 0]), __uint_as_float(ru[8 * j + 1]));
-                vu.y = pack_bf16(__uint_as_float(ru[8 * j + 2]), __uint_as_float(ru[8 * j + 3]));
-                vu.z = pack_bf16(__uint_as_float(ru[8 * j + 4]), __uint_as_float(ru[8 * j + 5]));
-                vu.w = pack_bf16(__uint_as_float(ru[8 * j + 6]), __uint_as_float(ru[8 * j + 7]));
-                reinterpret_cast<uint4*>(ap + c0)[j] = va;
-                reinterpret_cast<uint4*>(ap + pr.H + c0)[j] = vu;
+            }
+            if (ap) {
+              float4* da4 = reinterpret_cast<float4*>(ap + c0);
+              float4* du4 = reinterpret_cast<float4*>(ap + pr.H + c0);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                da4[j] = make_float4(__uint_as_float(ra[4 * j]), __uint_as_float(ra[4 * j + 1]),
+                                     __uint_as_float(ra[4 * j + 2]), __uint_as_float(ra[4 * j + 3]));
+                du4[j] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
+                                     __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
               }
             }
           }
         }
       } else if (EPI == EPI_SWIGLU_BWD) {
-        // accumulator = dh for H columns [n0, n0+256); au holds a | u
-        __nv_bfloat16* dp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row * pr.ldo + ti.n0;
-        const __nv_bfloat16* aup = reinterpret_cast<const __nv_bfloat16*>(pr.aux) + (long long)row * pr.ld_aux + ti.n0;
+        // accumulator = dY_perm W_d for H columns [n0, n0+256) (no gate yet);
+        // au = fp32 a | u of the forward.  Per element:
+        //   h = silu(a) u;  dg += acc * h;  dh = g acc;
+        //   da = dh u sig(a) (1 + a (1 - sig(a)));  du = dh silu(a)
+        // da | du go out as bf16 hi + lo, g*h as bf16 hi + lo (operands of the
+        // weight-gradient GEMMs), and the gate-gradient partial per row.
+        float g = 1.0f;
+        if (row_ok && pr.gates) {
+          int slot = __ldg(pr.slot_of_row + row);
+          if (slot < 0 || slot >= pr.gate_slots) {
+            record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
+            g = 0.0f;
+          } else {
+            g = __ldg(pr.gates + slot);
+          }
+        }
+        const long long ro = (long long)row * pr.ldo + ti.n0;         // into [rows, 2H]
+        const long long rh = (long long)row * pr.H + ti.n0;           // into [rows, H]
+        const float* aup = reinterpret_cast<const float*>(pr.aux) + (long long)row * pr.ld_aux + ti.n0;
+        float dgacc = 0.0f;
         for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
           if (ti.n0 + c0 >= pr.N) break;
           uint32_t r[32];
@@ -529,23 +565,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           if (row_ok) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              uint4 va = __ldg(reinterpret_cast<const uint4*>(aup + c0) + j);
-              uint4 vu = __ldg(reinterpret_cast<const uint4*>(aup + pr.H + c0) + j);
-              float a[8], u[8], da[8], du[8];
-              unpack8(va, a);
-              unpack8(vu, u);
+              const float4* a4 = reinterpret_cast<const float4*>(aup + c0 + 8 * j);
+              const float4* u4 = reinterpret_cast<const float4*>(aup + pr.H + c0 + 8 * j);
+              float4 a0 = __ldg(a4), a1 = __ldg(a4 + 1), u0 = __ldg(u4), u1 = __ldg(u4 + 1);
+              const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+              const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+              float da[8], du[8], gh[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                float dh = __uint_as_float(r[8 * j + e]);
-                float sg = sigmoidf_(a[e]);
+                const float acc = __uint_as_float(r[8 * j + e]);
+                const float sg = sigmoidf_(a[e]);
+                const float si = a[e] * sg;
+                const float h = si * u[e];
+                dgacc = fmaf(acc, h, dgacc);
+                const float dh = g * acc;
                 da[e] = dh * u[e] * sg * (1.0f + a[e] * (1.0f - sg));
-                du[e] = dh * a[e] * sg;
+                du[e] = dh * si;
+                gh[e] = g * h;
               }
-              reinterpret_cast<uint4*>(dp + c0)[j] = pack8(da);
-              reinterpret_cast<uint4*>(dp + pr.H + c0)[j] = pack8(du);
+              uint4 hi, lo;
+              split8(da, hi, lo);
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.out) + ro + c0 + 8 * j) = hi;
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.out_lo) + ro + c0 + 8 * j) = lo;
+              split8(du, hi, lo);
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.out) + ro + pr.H + c0 + 8 * j) = hi;
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.out_lo) + ro + pr.H + c0 + 8 * j) = lo;
+              split8(gh, hi, lo);
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.gh_hi) + rh + c0 + 8 * j) = hi;
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.gh_lo) + rh + c0 + 8 * j) = lo;
             }
           }
         }
+        if (row_ok && pr.dgp) pr.dgp[(long long)row * pr.ld_dgp + ti.n0 / pr.n_tile] = dgacc;
       } else if (EPI == EPI_REDUCE_DX) {
         // dx[t] = acc (router term) + dx_s[t] + sum_s dx_perm[row(t,s)]
         int rows_s[kMaxK];

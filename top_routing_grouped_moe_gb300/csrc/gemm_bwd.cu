@@ -13,7 +13,7 @@ long long mgroup_tile_bound(int rows_total, int G, int N, int n_tile) {
 
 bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
   const int ia = P.num_maps++, ib = P.num_maps++;
-  if (!encode_2d(&P.maps[ia], a.dO, a.d, a.rows_total, (uint64_t)a.d * 2, 64, BM)) return false;
+  if (!encode_2d(&P.maps[ia], a.dY, a.d, a.rows_total, (uint64_t)a.d * 2, 64, BM)) return false;
   // B[n = j in H, k = c in d] = W_d[g][c][j]: MN-major, stored [G][K=d][N=H]
   if (!encode_3d(&P.maps[ib], a.Wd, a.H, a.d, a.G, 64, 64)) return false;
   pr = blank_problem();
@@ -27,11 +27,19 @@ bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
   pr.map_a = ia;
   pr.map_b = ib;
   pr.tx_bytes = A_BYTES + 4 * MN_BLOCK_BYTES;
-  pr.out = a.dau;
+  pr.out = a.dau_hi;
+  pr.out_lo = a.dau_lo;
   pr.ldo = 2LL * a.H;
-  pr.aux = const_cast<void*>(a.au);
+  pr.aux = const_cast<float*>(a.au);
   pr.ld_aux = 2LL * a.H;
   pr.H = a.H;
+  pr.gh_hi = a.gh_hi;
+  pr.gh_lo = a.gh_lo;
+  pr.gates = a.gates;
+  pr.slot_of_row = a.slot_of_row;
+  pr.gate_slots = a.gate_slots;
+  pr.dgp = a.dgp;
+  pr.ld_dgp = cdiv_h(a.H, 256);
   return true;
 }
 
@@ -64,6 +72,15 @@ bool fill_wgrad(Params& P, Problem& pr, const WgradArgs& a) {
   if (!encode_2d(&P.maps[ia], a.A, a.M, a.rows_total, (uint64_t)a.M * 2, 64, 64)) return false;
   if (!encode_2d(&P.maps[ib], a.B, a.N, a.rows_total, (uint64_t)a.N * 2, 64, 64)) return false;
   pr = blank_problem();
+  if (a.A_lo) {
+    pr.map_a_lo = P.num_maps++;
+    if (!encode_2d(&P.maps[pr.map_a_lo], a.A_lo, a.M, a.rows_total, (uint64_t)a.M * 2, 64, 64)) return false;
+  }
+  if (a.B_lo) {
+    pr.map_b_lo = P.num_maps++;
+    if (!encode_2d(&P.maps[pr.map_b_lo], a.B_lo, a.N, a.rows_total, (uint64_t)a.N * 2, 64, 64)) return false;
+  }
+  pr.nsplit = (a.A_lo || a.B_lo) ? 2 : 1;
   pr.offsets = a.offsets;
   pr.G = a.G;
   pr.extent = a.rows_total;

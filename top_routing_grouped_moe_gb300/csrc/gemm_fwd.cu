@@ -25,7 +25,7 @@ bool fill_swiglu_fwd(Params& P, Problem& pr, const SwigluFwdArgs& a) {
   pr.tx_bytes = A_BYTES + 2 * 128 * BK * 2;
   pr.out = a.h;
   pr.ldo = a.H;
-  pr.aux = a.au;
+  pr.aux = a.au;  // fp32
   pr.ld_aux = 2LL * a.H;
   pr.H = a.H;
   return true;

@@ -68,6 +68,9 @@ inline Problem blank_problem() {
   Problem p;
   std::memset(&p, 0, sizeof(p));
   p.map_b2 = -1;
+  p.map_a_lo = -1;
+  p.map_b_lo = -1;
+  p.nsplit = 1;
   return p;
 }
 

@@ -41,16 +41,19 @@ int router_dw_splits(int T, int d, int E) {
   return S;
 }
 
-cudaError_t gemm_router_dw(const uint16_t* dl_bf16, const void* x, int T, int d, int E, int S, float* part,
-                           int* status, cudaStream_t s) {
+cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* x, int T, int d, int E, int S,
+                           float* part, int* status, cudaStream_t s) {
   (void)status;
   Params P;
   std::memset(&P, 0, sizeof(P));
-  P.num_maps = 2;
-  if (!encode_2d(&P.maps[0], dl_bf16, E, T, (uint64_t)E * 2, 64, 64)) return cudaErrorInvalidValue;
+  P.num_maps = 3;
+  if (!encode_2d(&P.maps[0], dl_hi, E, T, (uint64_t)E * 2, 64, 64)) return cudaErrorInvalidValue;
   if (!encode_2d(&P.maps[1], x, d, T, (uint64_t)d * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!encode_2d(&P.maps[2], dl_lo, E, T, (uint64_t)E * 2, 64, 64)) return cudaErrorInvalidValue;
   Problem& pr = P.prob[0];
   pr = blank_problem();
+  pr.map_a_lo = 2;
+  pr.nsplit = 2;
   pr.G = S;
   pr.extent = T;
   pr.M = E;

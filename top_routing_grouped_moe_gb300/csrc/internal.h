@@ -19,13 +19,17 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
 size_t permute_ws_bytes(int T, int E, int k);
 cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
                            int T, int d, int k, void* y, int* status, cudaStream_t s);
-cudaError_t launch_combine_bwd(const void* dY, const void* o_perm, const float* gates, const int32_t* row_of_slot,
-                               int T, int d, int k, void* dO_perm, float* dgates, int* status, cudaStream_t s);
+// dY_perm[row_of_slot[t*k+s]] = dY[t] for every kept slot
+cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
+                               int* status, cudaStream_t s);
+// dgates[t,s] = sum_p dgp[row_of_slot[t*k+s], p] (0 for dropped slots)
+cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_slot, int T, int k, float* dgates,
+                                 cudaStream_t s);
 cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot, int T, int d,
                                     int k, void* dx, int* status, cudaStream_t s);
-// dlogits [T,E] fp32 (dense) and, if dl_bf16 != NULL, a bf16 copy [T,E]
+// dlogits [T,E] fp32 (dense) and, if dl_hi != NULL, its bf16 hi + lo halves [T,E]
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
-                                 float* dlogits, uint16_t* dl_bf16, cudaStream_t s);
+                                 float* dlogits, uint16_t* dl_hi, uint16_t* dl_lo, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float* out, cudaStream_t s);
 
@@ -39,7 +43,7 @@ struct SwigluFwdArgs {
   int G, d, H;
   const void* Wg;       // [G, H, d]
   const void* Wu;
-  void* au;             // [rows, 2H] or NULL
+  float* au;            // [rows, 2H] fp32 (a | u) or NULL
   void* h;              // [rows, H]
 };
 struct DownFwdArgs {
@@ -57,14 +61,21 @@ cudaError_t gemm_down_fwd(const DownFwdArgs& routed, const DownFwdArgs* shared, 
 cudaError_t gemm_router_fwd(const void* x, const void* W_r, const float* bias, int T, int d, int E, float* logits,
                             int* status, cudaStream_t s);
 
-struct DgradDownArgs {    // dau = swiglu_bwd(dO W_d, au)
-  const void* dO;         // [rows, d]
+struct DgradDownArgs {    // dau = swiglu_bwd(g * (dY_perm W_d), au), plus g*h and the gate-gradient partials
+  const void* dY;         // [rows, d] (gathered upstream gradient, no gate)
   int rows_total;
   const int32_t* offsets;
   int G, d, H;
   const void* Wd;         // [G, d, H]
-  const void* au;         // [rows, 2H]
-  void* dau;              // [rows, 2H]
+  const float* au;        // [rows, 2H] fp32
+  void* dau_hi;           // [rows, 2H] bf16
+  void* dau_lo;
+  void* gh_hi;            // [rows, H] bf16
+  void* gh_lo;
+  const float* gates;     // per-slot gates or NULL (g = 1)
+  const int32_t* slot_of_row;
+  int gate_slots;
+  float* dgp;             // [rows, ceil(H/256)] or NULL
 };
 struct DgradGuArgs {      // dx = dau [W_g; W_u]
   const void* dau;        // [rows, 2H]
@@ -77,7 +88,9 @@ struct DgradGuArgs {      // dx = dau [W_g; W_u]
 };
 struct WgradArgs {        // out[g] = A_g^T B_g over rows [off[g], off[g+1])
   const void* A;          // [rows, M] bf16
+  const void* A_lo;       // lo half of A (split precision) or NULL
   const void* B;          // [rows, N] bf16
+  const void* B_lo;       // lo half of B or NULL
   int rows_total;
   const int32_t* offsets; // or NULL: G = 1 over rows_total
   int G, M, N;
@@ -88,9 +101,9 @@ struct WgradArgs {        // out[g] = A_g^T B_g over rows [off[g], off[g+1])
 cudaError_t gemm_dgrad_down(const DgradDownArgs& routed, const DgradDownArgs* shared, int* status, cudaStream_t s);
 cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, int* status, cudaStream_t s);
 cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* status, cudaStream_t s);
-// dW_r partials: part[S, E, d] = split-K pieces of dl^T x; dl_bf16 [T, E]
-cudaError_t gemm_router_dw(const uint16_t* dl_bf16, const void* x, int T, int d, int E, int S, float* part,
-                           int* status, cudaStream_t s);
+// dW_r partials: part[S, E, d] = split-K pieces of (dl_hi + dl_lo)^T x; dl halves [T, E] bf16
+cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* x, int T, int d, int E, int S,
+                           float* part, int* status, cudaStream_t s);
 // dx = dl W_r + dx_s + sum_s dx_perm[row(t,s)]
 cudaError_t gemm_router_dx_reduce(const uint16_t* dl_bf16, const void* W_r, const void* dx_perm, const void* dx_s,
                                   const int32_t* row_of_slot, int T, int d, int E, int k, void* dx, int* status,

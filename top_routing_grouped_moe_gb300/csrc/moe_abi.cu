@@ -44,12 +44,34 @@ int check_hidden(int H, int Hs) {
 // workspace of each call
 size_t ws_route_topk_bwd(int T, int d, int E) {
   const int S = router_dw_splits(T, d, E);
-  return align256((size_t)T * E * 2) + (S > 1 ? align256((size_t)S * E * d * 4) : 0);
+  return 2 * align256((size_t)T * E * 2) + (S > 1 ? align256((size_t)S * E * d * 4) : 0);
 }
 size_t ws_permute_bwd(int T, int E) { return align256((size_t)T * E * 2); }
-size_t ws_swiglu_bwd(int T, int k, int H, int Hs) {
-  return align256((size_t)T * k * 2 * H * 2) + align256((size_t)T * 2 * Hs * 2);
+
+// grouped SwiGLU backward scratch: da|du hi+lo [rows,2H] x2, g*h hi+lo [rows,H] x2,
+// gate-gradient partials [rows, ceil(H/256)], for the routed rows (T*k) and the
+// shared expert (T rows).
+struct SwigluBwdWs {
+  size_t dau_hi, dau_lo, gh_hi, gh_lo, dgp, s_dau_hi, s_dau_lo, s_gh_hi, s_gh_lo, total;
+};
+SwigluBwdWs swiglu_bwd_ws(int T, int k, int H, int Hs) {
+  SwigluBwdWs w;
+  const size_t R = (size_t)T * k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += align256(bytes); return o; };
+  w.dau_hi = take(R * 2 * H * 2);
+  w.dau_lo = take(R * 2 * H * 2);
+  w.gh_hi = take(R * H * 2);
+  w.gh_lo = take(R * H * 2);
+  w.dgp = take(R * ((H + 255) / 256) * 4);
+  w.s_dau_hi = take((size_t)T * 2 * Hs * 2);
+  w.s_dau_lo = take((size_t)T * 2 * Hs * 2);
+  w.s_gh_hi = take((size_t)T * Hs * 2);
+  w.s_gh_lo = take((size_t)T * Hs * 2);
+  w.total = off;
+  return w;
 }
+size_t ws_swiglu_bwd(int T, int k, int H, int Hs) { return swiglu_bwd_ws(T, k, H, Hs).total; }
 
 }  // namespace
 
@@ -163,7 +185,7 @@ int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int
 
 int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const void* x, int T, int d, int E, int k, int H,
                        int Hs, const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
-                       const void* Ws_d, void* au, void* h, void* o_perm, void* au_s, void* h_s, void* s_out,
+                       const void* Ws_d, float* au, void* h, void* o_perm, float* au_s, void* h_s, void* s_out,
                        void* ws, size_t ws_bytes, void* stream) {
   (void)ws;
   (void)ws_bytes;
@@ -201,60 +223,72 @@ int moe_unpermute_combine(const void* o_perm, const void* s_out, const float* ga
                               static_cast<cudaStream_t>(stream)));
 }
 
-int moe_unpermute_combine_bwd(const void* dY, const void* o_perm, const float* gates, const int32_t* row_of_slot,
-                              int T, int d, int k, void* dO_perm, float* dgates, void* stream) {
+int moe_unpermute_combine_bwd(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
+                              void* stream) {
   if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
   if (k > kMaxK || (d % 64) != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
-  if (!dY || !o_perm || !gates || !row_of_slot || !dO_perm || !dgates) return MOE_ERR_INVALID_ARG;
-  if (!al16(dY) || !al16(o_perm) || !al16(dO_perm)) return MOE_ERR_INVALID_ARG;
-  return check(launch_combine_bwd(dY, o_perm, gates, row_of_slot, T, d, k, dO_perm, dgates, device_status_ptr(),
+  if (!dY || !row_of_slot || !dY_perm) return MOE_ERR_INVALID_ARG;
+  if (!al16(dY) || !al16(dY_perm)) return MOE_ERR_INVALID_ARG;
+  return check(launch_gather_rows(dY, row_of_slot, T, d, k, dY_perm, device_status_ptr(),
                                   static_cast<cudaStream_t>(stream)));
 }
 
-int moe_grouped_swiglu_bwd(const void* dO_perm, const void* dY, const int32_t* offsets, const void* x_perm,
-                           const void* x, const void* au, const void* h, const void* au_s, const void* h_s, int T,
-                           int d, int E, int k, int H, int Hs, const void* W_g, const void* W_u, const void* W_d,
-                           const void* Ws_g, const void* Ws_u, const void* Ws_d, void* dx_perm, void* dx_s,
-                           void* dW_g, void* dW_u, void* dW_d, void* dWs_g, void* dWs_u, void* dWs_d, void* ws,
-                           size_t ws_bytes, void* stream) {
+int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gates, const int32_t* row_of_slot,
+                           const int32_t* slot_of_row, const int32_t* offsets, const void* x_perm, const void* x,
+                           const float* au, const float* au_s, int T, int d, int E, int k, int H, int Hs,
+                           const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
+                           const void* Ws_d, void* dx_perm, void* dx_s, void* dW_g, void* dW_u, void* dW_d,
+                           void* dWs_g, void* dWs_u, void* dWs_d, float* dgates, void* ws, size_t ws_bytes,
+                           void* stream) {
   int rc = check_dims(T, d, E, k);
   if (rc) return rc;
   rc = check_hidden(H, Hs);
   if (rc) return rc;
-  const void* req[] = {dO_perm, offsets, x_perm, au, h, W_g, W_u, W_d, dx_perm, dW_g, dW_u, dW_d};
+  const void* req[] = {dY_perm, gates, row_of_slot, slot_of_row, offsets, x_perm, au, W_g, W_u, W_d,
+                       dx_perm, dW_g, dW_u, dW_d, dgates};
   for (const void* p : req)
     if (!p) return MOE_ERR_INVALID_ARG;
-  for (const void* p : req)
+  const void* req16[] = {dY_perm, x_perm, au, W_g, W_u, W_d, dx_perm, dW_g, dW_u, dW_d};
+  for (const void* p : req16)
     if (!al16(p)) return MOE_ERR_INVALID_ARG;
   if (Hs > 0) {
-    const void* req_s[] = {dY, x, au_s, h_s, Ws_g, Ws_u, Ws_d, dx_s, dWs_g, dWs_u, dWs_d};
+    const void* req_s[] = {dY, x, au_s, Ws_g, Ws_u, Ws_d, dx_s, dWs_g, dWs_u, dWs_d};
     for (const void* p : req_s)
       if (!p || !al16(p)) return MOE_ERR_INVALID_ARG;
   }
-  if (!ws || ws_bytes < ws_swiglu_bwd(T, k, H, Hs)) return MOE_ERR_WORKSPACE;
+  const SwigluBwdWs L = swiglu_bwd_ws(T, k, H, Hs);
+  if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = device_status_ptr();
   char* w = static_cast<char*>(ws);
-  void* dau = w;
-  void* dau_s = w + align256((size_t)T * k * 2 * H * 2);
+  const int R = T * k;
+  float* dgp = reinterpret_cast<float*>(w + L.dgp);
 
-  DgradDownArgs r1{dO_perm, T * k, offsets, E, d, H, W_d, au, dau};
-  DgradDownArgs s1{dY, T, nullptr, 1, d, Hs, Ws_d, au_s, dau_s};
+  // 1. dgrad of the down projection with the SwiGLU backward epilogue
+  DgradDownArgs r1{dY_perm, R, offsets, E, d, H, W_d, au, w + L.dau_hi, w + L.dau_lo, w + L.gh_hi, w + L.gh_lo,
+                   gates, slot_of_row, R, dgp};
+  DgradDownArgs s1{dY, T, nullptr, 1, d, Hs, Ws_d, au_s, w + L.s_dau_hi, w + L.s_dau_lo, w + L.s_gh_hi,
+                   w + L.s_gh_lo, nullptr, nullptr, 0, nullptr};
   cudaError_t e = gemm_dgrad_down(r1, Hs > 0 ? &s1 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_dgates_reduce(dgp, (H + 255) / 256, row_of_slot, T, k, dgates, st);
+  if (e != cudaSuccess) return fail_cuda(e);
 
-  WgradArgs r2{dO_perm, h, T * k, offsets, E, d, H, dW_d, nullptr, 0};
-  WgradArgs s2{dY, h_s, T, nullptr, 1, d, Hs, dWs_d, nullptr, 0};
+  // 2. dW_d = dY_perm^T (g h), g h split into bf16 hi + lo
+  WgradArgs r2{dY_perm, nullptr, w + L.gh_hi, w + L.gh_lo, R, offsets, E, d, H, dW_d, nullptr, 0};
+  WgradArgs s2{dY, nullptr, w + L.s_gh_hi, w + L.s_gh_lo, T, nullptr, 1, d, Hs, dWs_d, nullptr, 0};
   e = gemm_wgrad(r2, Hs > 0 ? &s2 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
 
-  DgradGuArgs r3{dau, T * k, offsets, E, d, H, W_g, W_u, dx_perm};
-  DgradGuArgs s3{dau_s, T, nullptr, 1, d, Hs, Ws_g, Ws_u, dx_s};
+  // 3. dx_perm = [da|du] [W_g; W_u]
+  DgradGuArgs r3{w + L.dau_hi, R, offsets, E, d, H, W_g, W_u, dx_perm};
+  DgradGuArgs s3{w + L.s_dau_hi, T, nullptr, 1, d, Hs, Ws_g, Ws_u, dx_s};
   e = gemm_dgrad_gu(r3, Hs > 0 ? &s3 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
 
-  WgradArgs r4{dau, x_perm, T * k, offsets, E, 2 * H, d, dW_g, dW_u, H};
-  WgradArgs s4{dau_s, x, T, nullptr, 1, 2 * Hs, d, dWs_g, dWs_u, Hs};
+  // 4. [dW_g; dW_u] = [da|du]^T x_perm, [da|du] split into bf16 hi + lo
+  WgradArgs r4{w + L.dau_hi, w + L.dau_lo, x_perm, nullptr, R, offsets, E, 2 * H, d, dW_g, dW_u, H};
+  WgradArgs s4{w + L.s_dau_hi, w + L.s_dau_lo, x, nullptr, T, nullptr, 1, 2 * Hs, d, dWs_g, dWs_u, Hs};
   return check(gemm_wgrad(r4, Hs > 0 ? &s4 : nullptr, status, st));
 }
 
@@ -265,18 +299,19 @@ int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* t
   if (!dgates || !gates || !topk_idx || !dlogits) return MOE_ERR_INVALID_ARG;
   if ((x == nullptr) != (dW_r == nullptr)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (!x) return check(launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits, nullptr, st));
+  if (!x) return check(launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits, nullptr, nullptr, st));
   int rc = check_dims(T, d, E, k);
   if (rc) return rc;
   if (!al16(x) || !al16(dW_r)) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < ws_route_topk_bwd(T, d, E)) return MOE_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
-  uint16_t* dl_bf16 = reinterpret_cast<uint16_t*>(w);
-  cudaError_t e = launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits, dl_bf16, st);
+  uint16_t* dl_hi = reinterpret_cast<uint16_t*>(w);
+  uint16_t* dl_lo = reinterpret_cast<uint16_t*>(w + align256((size_t)T * E * 2));
+  cudaError_t e = launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits, dl_hi, dl_lo, st);
   if (e != cudaSuccess) return fail_cuda(e);
   const int S = router_dw_splits(T, d, E);
-  float* part = S > 1 ? reinterpret_cast<float*>(w + align256((size_t)T * E * 2)) : dW_r;
-  e = gemm_router_dw(dl_bf16, x, T, d, E, S, part, device_status_ptr(), st);
+  float* part = S > 1 ? reinterpret_cast<float*>(w + 2 * align256((size_t)T * E * 2)) : dW_r;
+  e = gemm_router_dw(dl_hi, dl_lo, x, T, d, E, S, part, device_status_ptr(), st);
   if (e != cudaSuccess) return fail_cuda(e);
   if (S > 1) return check(launch_splitk_reduce(part, S, (long long)E * d, dW_r, st));
   return MOE_OK;

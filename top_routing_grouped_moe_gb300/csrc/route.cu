@@ -287,56 +287,54 @@ __global__ void combine_kernel(const uint4* __restrict__ o_perm, const uint4* __
   }
 }
 
-__global__ void combine_bwd_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ o_perm,
-                                   const float* __restrict__ gates, const int32_t* __restrict__ row_of_slot, int T,
-                                   int d, int k, long long max_rows, uint4* __restrict__ dO_perm,
-                                   float* __restrict__ dgates, int* status) {
+// Backward of the unpermute: the upstream gradient of each token is gathered
+// into its kept rows (the gate factor and the gate gradient are applied in the
+// expert backward, where they can be formed from fp32 values).
+__global__ void gather_rows_kernel(const uint4* __restrict__ dY, const int32_t* __restrict__ row_of_slot, int T,
+                                   int d, int k, long long max_rows, uint4* __restrict__ dY_perm, int* status) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   int row = -1;
-  float g = 0.0f;
   if (lane < k) {
     row = row_of_slot[(long long)t * k + lane];
-    g = gates[(long long)t * k + lane];
     if (row >= max_rows) {
       record_status(status, MOE_ERR_DEVICE_BOUNDS);
       row = -1;
     }
   }
   int rows[kMaxK];
-  float gs[kMaxK], dot[kMaxK];
 #pragma unroll
-  for (int s = 0; s < kMaxK; ++s) {
-    rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
-    gs[s] = __shfl_sync(0xffffffffu, g, s < k ? s : 0);
-    dot[s] = 0.0f;
-  }
+  for (int s = 0; s < kMaxK; ++s) rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
   const int vpr = d / 8;
-  for (int c = lane; c < vpr; c += 32) {
-    float dy[8];
-    unpack8(__ldg(dY + (long long)t * vpr + c), dy);
+  const uint4* src = dY + (long long)t * vpr;
+  for (int c = lane; c < vpr; c += 32 * 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (c + 32 * u < vpr) v[u] = __ldg(src + c + 32 * u);
 #pragma unroll
     for (int s = 0; s < kMaxK; ++s) {
       if (s >= k) break;
       if (rows[s] < 0) continue;
-      float o[8], dO[8];
-      unpack8(__ldg(o_perm + (long long)rows[s] * vpr + c), o);
+      uint4* dst = dY_perm + (long long)rows[s] * vpr;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        dot[s] = fmaf(dy[e], o[e], dot[s]);
-        dO[e] = gs[s] * dy[e];
-      }
-      dO_perm[(long long)rows[s] * vpr + c] = pack8(dO);
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < vpr) dst[c + 32 * u] = v[u];
     }
   }
-#pragma unroll
-  for (int s = 0; s < kMaxK; ++s) {
-    if (s >= k) break;
-    float v = dot[s];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == s) dgates[(long long)t * k + s] = rows[s] >= 0 ? v : 0.0f;
+}
+
+// dgates[slot] = sum of the per-N-tile partials of its row (0 if dropped)
+__global__ void dgates_reduce_kernel(const float* __restrict__ dgp, int P, const int32_t* __restrict__ row_of_slot,
+                                     long long n_slots, float* __restrict__ dgates) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_slots;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int row = row_of_slot[i];
+    float v = 0.0f;
+    if (row >= 0)
+      for (int p = 0; p < P; ++p) v += dgp[(long long)row * P + p];
+    dgates[i] = v;
   }
 }
 
@@ -381,10 +379,10 @@ __global__ void unpermute_reduce_kernel(const uint4* __restrict__ dx_perm, const
 
 // ------------------------------------------------------------------ router backward
 // One warp per token: dl_s = g_s (dg_s - sum_j g_j dg_j) scattered into a dense
-// [T,E] row (zeros elsewhere), plus an optional bf16 copy for the GEMMs.
+// [T,E] row (zeros elsewhere), plus optional bf16 hi + lo halves for the GEMMs.
 __global__ void router_bwd_dl_kernel(const float* __restrict__ dgates, const float* __restrict__ gates,
                                      const int32_t* __restrict__ idx, int T, int E, int k, float* __restrict__ dl,
-                                     uint16_t* __restrict__ dl_bf16) {
+                                     uint16_t* __restrict__ dl_hi, uint16_t* __restrict__ dl_lo) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -412,9 +410,11 @@ __global__ void router_bwd_dl_kernel(const float* __restrict__ dgates, const flo
     for (int s = 0; s < kMaxK; ++s)
       if (s < k && es[s] == c) v = vs[s];
     dl[(long long)t * E + c] = v;
-    if (dl_bf16) {
-      __nv_bfloat16 b = __float2bfloat16_rn(v);
-      dl_bf16[(long long)t * E + c] = *reinterpret_cast<uint16_t*>(&b);
+    if (dl_hi) {
+      __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      dl_hi[(long long)t * E + c] = *reinterpret_cast<uint16_t*>(&hi);
+      dl_lo[(long long)t * E + c] = *reinterpret_cast<uint16_t*>(&lo);
     }
   }
 }
@@ -496,11 +496,17 @@ cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* g
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_bwd(const void* dY, const void* o_perm, const float* gates, const int32_t* row_of_slot,
-                               int T, int d, int k, void* dO_perm, float* dgates, int* status, cudaStream_t s) {
-  combine_bwd_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-      static_cast<const uint4*>(dY), static_cast<const uint4*>(o_perm), gates, row_of_slot, T, d, k,
-      (long long)T * k, static_cast<uint4*>(dO_perm), dgates, status);
+cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
+                               int* status, cudaStream_t s) {
+  gather_rows_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+      static_cast<const uint4*>(dY), row_of_slot, T, d, k, (long long)T * k, static_cast<uint4*>(dY_perm), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_slot, int T, int k, float* dgates,
+                                 cudaStream_t s) {
+  const long long n = (long long)T * k;
+  dgates_reduce_kernel<<<flat_blocks(n, 256), 256, 0, s>>>(dgp, P, row_of_slot, n, dgates);
   return cudaGetLastError();
 }
 
@@ -513,8 +519,9 @@ cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const
 }
 
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
-                                 float* dlogits, uint16_t* dl_bf16, cudaStream_t s) {
-  router_bwd_dl_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(dgates, gates, idx, T, E, k, dlogits, dl_bf16);
+                                 float* dlogits, uint16_t* dl_hi, uint16_t* dl_lo, cudaStream_t s) {
+  router_bwd_dl_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(dgates, gates, idx, T, E, k, dlogits, dl_hi,
+                                                                       dl_lo);
   return cudaGetLastError();
 }
 

@@ -33,17 +33,17 @@ class MoELayer:
         self.row_of_slot = e(R, dt=torch.int32)
         self.slot_of_row = e(R, dt=torch.int32)
         self.x_perm = e(R, d)
-        self.au = e(R, 2 * H) if backward else None
+        self.au = e(R, 2 * H, dt=torch.float32) if backward else None
         self.h = e(R, H)
         self.o_perm = e(R, d)
-        self.au_s = e(T, 2 * Hs) if (Hs and backward) else None
+        self.au_s = e(T, 2 * Hs, dt=torch.float32) if (Hs and backward) else None
         self.h_s = e(T, Hs) if Hs else None
         self.s = e(T, d) if Hs else None
         self.y = e(T, d)
         self.ws_bytes = B.moe_workspace_size(T, d, E, k, H, Hs)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         if backward:
-            self.dO_perm = e(R, d)
+            self.dY_perm = e(R, d)
             self.dgates = e(T, k, dt=torch.float32)
             self.dx_perm = e(R, d)
             self.dx_s = e(T, d) if Hs else None
@@ -77,12 +77,12 @@ class MoELayer:
         """Backward of the last forward for upstream dY [T,d] bf16.  Fills
         dx, dW_g/u/d, dWs_*, dgates, dlogits and (learned router) dW_r."""
         T, d, E, k, H, Hs = self.T, self.d, self.E, self.k, self.H, self.Hs
-        B.moe_unpermute_combine_bwd(dY, self.o_perm, self.gates, self.row_of_slot, T, d, k, self.dO_perm,
-                                    self.dgates, stream)
-        B.moe_grouped_swiglu_bwd(self.dO_perm, dY, self.offsets, self.x_perm, x, self.au, self.h, self.au_s,
-                                 self.h_s, T, d, E, k, H, Hs, p["W_g"], p["W_u"], p["W_d"], p.get("Ws_g"),
-                                 p.get("Ws_u"), p.get("Ws_d"), self.dx_perm, self.dx_s, self.dW_g, self.dW_u,
-                                 self.dW_d, self.dWs_g, self.dWs_u, self.dWs_d, self.ws, self.ws_bytes, stream)
+        B.moe_unpermute_combine_bwd(dY, self.row_of_slot, T, d, k, self.dY_perm, stream)
+        B.moe_grouped_swiglu_bwd(self.dY_perm, dY, self.gates, self.row_of_slot, self.slot_of_row, self.offsets,
+                                 self.x_perm, x, self.au, self.au_s, T, d, E, k, H, Hs, p["W_g"], p["W_u"],
+                                 p["W_d"], p.get("Ws_g"), p.get("Ws_u"), p.get("Ws_d"), self.dx_perm, self.dx_s,
+                                 self.dW_g, self.dW_u, self.dW_d, self.dWs_g, self.dWs_u, self.dWs_d, self.dgates,
+                                 self.ws, self.ws_bytes, stream)
         lr = learned_router and p.get("W_r") is not None
         B.moe_route_topk_bwd(self.dgates, self.gates, self.idx, x if lr else None, T, d, E, k, self.dlogits,
                              self.dW_r if lr else None, self.ws, self.ws_bytes, stream)
