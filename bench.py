@@ -78,9 +78,9 @@ def call_bytes(w, R):
     return {
         "moe_route_topk": route,
         "moe_permute": T * d * 2 + R * d * 2 + T * k * 4 * 4 + R * 4,
-        "moe_unpermute_combine": R * d * 2 + (T * d * 2 if w.Hs else 0) + T * d * 2 + T * k * 8,
+        "moe_unpermute_combine": R * d * 4 + (T * d * 4 if w.Hs else 0) + T * d * 2 + T * k * 8,
         "moe_unpermute_combine_bwd": T * d * 2 + R * d * 2 + T * k * 4,
-        "moe_permute_bwd": R * d * 2 + (T * d * 2 if w.Hs else 0) + T * d * 2 + T * k * 4,
+        "moe_permute_bwd": R * d * 4 + (T * d * 4 if w.Hs else 0) + T * d * 2 + T * k * 4,
     }
 
 
@@ -99,6 +99,24 @@ def launches_per_step(w):
     else:
         n += 1 + 1                                         # router bwd dl; unpermute reduce
     return n
+
+
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(values, device):
+    """Element-wise max of a list of floats over all ranks (identity with one
+    rank).  The timed region of every rank is compared, the slowest counts."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def tokens_per_s(T, steps, world, total_ms):
+    """Whole-job throughput: every rank processes T tokens per step."""
+    return T * steps * world / (total_ms / 1000.0)
 
 
 # ------------------------------------------------------------------ clocks
@@ -317,15 +335,9 @@ def main_ours(args):
     step_ms = [evs[i][0].elapsed_time(evs[i][8]) for i in range(args.steps)]
     per_call = {c: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)] for j, c in enumerate(calls)}
     fwd_ms = [evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms, sum(fwd_ms)], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, fwd_total = float(t[0]), float(t[1])
-    else:
-        fwd_total = sum(fwd_ms)
-    value = w.T * args.steps * world / (total_ms / 1000.0)
-    fwd_value = w.T * args.steps * world / (fwd_total / 1000.0)
+    total_ms, fwd_total = max_over_ranks([sum(step_ms), sum(fwd_ms)], "cuda")
+    value = tokens_per_s(w.T, args.steps, world, total_ms)
+    fwd_value = tokens_per_s(w.T, args.steps, world, fwd_total)
 
     # roofline of the dominant call (the grouped GEMMs, tensor bound)
     peaks = {}
@@ -387,12 +399,9 @@ def main_ours(args):
         t0 = time.perf_counter()
         for _ in range(args.steps):
             e2e_step()
-        el = time.perf_counter() - t0
-        if world > 1:
-            tt = torch.tensor([el], dtype=torch.float64, device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            el = float(tt[0])
-        e2e = {"value": w.T * args.steps * world / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        el = max_over_ranks([time.perf_counter() - t0], "cuda")[0]
+        e2e = {"value": tokens_per_s(w.T, args.steps, world, el * 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
     cpu = None

@@ -46,8 +46,8 @@
  * Weight layouts (out_features x in_features):
  *   W_r [E,d]; W_g, W_u [E,H,d]; W_d [E,d,H]; Ws_g, Ws_u [Hs,d]; Ws_d [d,Hs].
  * Buffers sized for the dropless maximum R <= T*k (rows >= R are left as
- * they were): x_perm, o_perm, dY_perm, dx_perm [T*k, d]; au [T*k, 2H] fp32;
- * h [T*k, H]; slot_of_row [T*k].
+ * they were): x_perm, dY_perm [T*k, d] bf16; o_perm, dx_perm [T*k, d] fp32;
+ * au [T*k, 2H] fp32; h [T*k, H] bf16; slot_of_row [T*k].
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -103,7 +103,7 @@ MOE_API int moe_workspace_size(int T, int d, int E, int k, int H, int Hs, size_t
  * Snippet").
  *   learned routing (logits_in == NULL):
  *     logits[t,e] = fp32(sum_c x[t,c] * W_r[e,c]) + bias[e]   (bias may be NULL)
- *     x [T,d] bf16, W_r [E,d] bf16, bias [E] fp32; logits [T,E] fp32 is
+ *     x [T,d] bf16, W_r [E,d] bf16, bias [E] fp32 (16-byte aligned); logits [T,E] fp32 is
  *     written (required).  The product runs on the tensor cores with fp32
  *     accumulation.
  *   given logits (logits_in != NULL, e.g. random routing): logits_in [T,E]
@@ -146,9 +146,10 @@ MOE_API int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, in
  *   au [T*k, 2H] FP32 receives a in columns [0,H) and u in [H,2H), kept for
  *   the backward pass (may be NULL when no backward follows);
  *   h [T*k, H] bf16 (the down projection's input, required);
- *   o_perm [T*k, d] bf16.
+ *   o_perm [T*k, d] FP32 (kept in fp32 so that the combine adds unrounded
+ *   expert outputs).
  *   Shared expert (Hs > 0): the same on every token of x [T,d] with Ws_*,
- *   writing au_s [T,2Hs] fp32 (nullable), h_s [T,Hs] and s [T,d] bf16.
+ *   writing au_s [T,2Hs] fp32 (nullable), h_s [T,Hs] bf16 and s [T,d] fp32.
  *   Hs == 0: the shared pointers are ignored.
  * Tensor-core (tcgen05) grouped GEMMs fed by TMA; the per-expert tile
  * schedule is read from `offsets` on the device.  ws is unused (may be NULL). */
@@ -156,15 +157,15 @@ MOE_API int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const
                        int T, int d, int E, int k, int H, int Hs,
                        const void* W_g, const void* W_u, const void* W_d,
                        const void* Ws_g, const void* Ws_u, const void* Ws_d,
-                       float* au, void* h, void* o_perm,
-                       float* au_s, void* h_s, void* s,
+                       float* au, void* h, float* o_perm,
+                       float* au_s, void* h_s, float* s,
                        void* ws, size_t ws_bytes, void* stream);
 
 /* Gate-weighted unpermute and combine:
  *   y[t,:] = s[t,:] + sum_{s kept} gates[t,s] * o_perm[row_of_slot[t*k+s], :]
- * fp32 accumulation, one bf16 rounding.  s may be NULL (no shared expert).
- * y [T,d] bf16. */
-MOE_API int moe_unpermute_combine(const void* o_perm, const void* s, const float* gates,
+ * o_perm [T*k,d] and s [T,d] fp32 (s may be NULL: no shared expert); fp32
+ * accumulation, one bf16 rounding: y [T,d] bf16. */
+MOE_API int moe_unpermute_combine(const float* o_perm, const float* s, const float* gates,
                           const int32_t* row_of_slot, int T, int d, int k,
                           void* y, void* stream);
 
@@ -195,10 +196,11 @@ MOE_API int moe_unpermute_combine_bwd(const void* dY, const int32_t* row_of_slot
  *   dW_d[e] = sum_r dY_perm[r]^T (g h_r);  dW_g[e] = sum_r da_r^T x_perm[r];
  *   dW_u[e] = sum_r du_r^T x_perm[r]
  * and the same for the shared expert over all T tokens with g = 1 (no gate
- * gradient).  The weight-gradient products take their derived operand (g h,
- * da | du) as a bf16 hi + lo pair, so the result keeps ~16 bits over sums of
- * thousands of rows.  Outputs: dx_perm [T*k,d], dx_s [T,d], dW_g, dW_u
- * [E,H,d], dW_d [E,d,H] (zero for experts with no rows), dWs_g, dWs_u [Hs,d],
+ * gradient).  The products take their derived operand (g h, da | du) as a
+ * bf16 hi + lo pair, so the result keeps ~16 bits over sums of thousands of
+ * rows (weight gradients) or of 2H products (input gradients).  Outputs: dx_perm [T*k,d] and dx_s [T,d] in fp32 (summed
+ * per token by moe_permute_bwd before any rounding), dW_g, dW_u [E,H,d],
+ * dW_d [E,d,H] (zero for experts with no rows), dWs_g, dWs_u [Hs,d],
  * dWs_d [d,Hs] (all bf16) and dgates [T,k] fp32 (0 for dropped slots).  Each
  * output element is owned by one tile: no atomics, deterministic.
  * ws >= moe_workspace_size() bytes. */
@@ -209,7 +211,7 @@ MOE_API int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const fl
                            int T, int d, int E, int k, int H, int Hs,
                            const void* W_g, const void* W_u, const void* W_d,
                            const void* Ws_g, const void* Ws_u, const void* Ws_d,
-                           void* dx_perm, void* dx_s,
+                           float* dx_perm, float* dx_s,
                            void* dW_g, void* dW_u, void* dW_d,
                            void* dWs_g, void* dWs_u, void* dWs_d,
                            float* dgates, void* ws, size_t ws_bytes, void* stream);
@@ -230,10 +232,11 @@ MOE_API int moe_route_topk_bwd(const float* dgates, const float* gates, const in
  * gradient:
  *   dx[t,:] = sum_{s kept} dx_perm[row_of_slot[t*k+s], :] + dx_s[t,:]
  *             + sum_e dlogits[t,e] W_r[e,:]
- * fp32 accumulation, one bf16 rounding.  dx_s may be NULL (no shared
- * expert); dlogits and W_r may both be NULL (given-logits routing).  The
- * router term uses the tensor cores with dlogits rounded to bf16. */
-MOE_API int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot,
+ * dx_perm [T*k,d] and dx_s [T,d] fp32; fp32 accumulation, one bf16 rounding:
+ * dx [T,d] bf16.  dx_s may be NULL (no shared expert); dlogits and W_r may
+ * both be NULL (given-logits routing).  The router term uses the tensor
+ * cores with dlogits as a bf16 hi + lo pair. */
+MOE_API int moe_permute_bwd(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot,
                     const float* dlogits, const void* W_r,
                     int T, int d, int E, int k, void* dx,
                     void* ws, size_t ws_bytes, void* stream);

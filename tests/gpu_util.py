@@ -36,15 +36,22 @@ def upload(inp: dict) -> dict:
     return out
 
 
+MARGINS = {}  # name -> (max err/(atol + rtol|ref|), relative Frobenius), of the last comparison
+
+
 def assert_close(name, gpu: np.ndarray, ref: np.ndarray, atol=ATOL, rtol=RTOL, fro=FRO):
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert gpu.shape == ref.shape, (name, gpu.shape, ref.shape)
     assert np.all(np.isfinite(gpu)), f"{name}: non-finite values"
     err = np.abs(gpu - ref)
-    bad = err > atol + rtol * np.abs(ref)
+    bound = atol + rtol * np.abs(ref)
+    bad = err > bound
     nref = np.linalg.norm(ref)
     rel = np.linalg.norm(gpu - ref) / nref if nref > 0 else np.linalg.norm(gpu)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = float(np.max(np.where(bound > 0, err / np.where(bound > 0, bound, 1), np.where(err > 0, np.inf, 0))))
+    MARGINS[name] = (ratio, float(rel))
     if bad.any():
         i = np.unravel_index(np.argmax(err - (atol + rtol * np.abs(ref))), err.shape)
         raise AssertionError(f"{name}: {bad.sum()} of {bad.size} elements out of tolerance; worst at {i}: "
@@ -109,6 +116,7 @@ def compare_layer(w, inp, layer, ref, refb):
     routing, which are excluded from the per-token and per-expert checks),
     floating outputs within the layer tolerance."""
     import torch
+    MARGINS.clear()
     T, k = w.T, w.k
 
     gidx = layer.idx.cpu().numpy()
@@ -163,4 +171,6 @@ def compare_layer(w, inp, layer, ref, refb):
     if w.routing == "learned":
         assert_close("dW_r", layer.dW_r.cpu().numpy()[keep_e], refb["dW_r"][keep_e])
     assert_close("dx", host_f64(layer.dx)[keep], refb["dx"][keep])
+    worst = ", ".join(f"{n} {r:.2f}/{f:.1e}" for n, (r, f) in sorted(MARGINS.items(), key=lambda kv: -kv[1][0]))
+    print(f"[margins: max err/bound / rel fro] {worst}")
     return int(diff.sum())

@@ -1,0 +1,94 @@
+"""Host-side checks of the C ABI (no GPU): the library loads and exports every
+function include/*.h declares, and argument errors come back as the
+documented status codes before anything touches a device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from top_routing_grouped_moe_gb300 import _binding
+    return _binding
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names.update(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 13
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    # and the binding covers every compute entry point
+    for n in names:
+        if n not in ("moe_version", "moe_status_string", "moe_last_cuda_error", "moe_device_status",
+                     "moe_workspace_size"):
+            assert n in lib.SIGNATURES, n
+
+
+def test_status_strings(lib):
+    for code in range(0, 8):
+        s = lib.status_string(code)
+        assert isinstance(s, str) and s
+    assert lib.moe_version() >> 16 >= 1
+
+
+def test_workspace_size(lib):
+    a = lib.moe_workspace_size(8192, 2048, 64, 4, 1024, 1024)
+    b = lib.moe_workspace_size(16384, 2048, 64, 4, 1024, 1024)
+    assert 0 < a < b
+    with pytest.raises(lib.MoEError) as e:
+        lib.moe_workspace_size(8192, 2048, 63, 4, 1024, 1024)   # E % 8 != 0
+    assert e.value.status == lib.MOE_ERR_UNSUPPORTED
+    with pytest.raises(lib.MoEError) as e:
+        lib.moe_workspace_size(8192, 2048, 64, 4, 1000, 0)      # H % 128 != 0
+    assert e.value.status == lib.MOE_ERR_UNSUPPORTED
+
+
+P = 1 << 12  # stand-in device addresses (16-byte aligned); never dereferenced
+
+
+@pytest.mark.parametrize("call,expect", [
+    # k > 8
+    (lambda L: L.moe_route_topk(None, None, None, P, 16, 0, 64, 9, None, P, P, None, 0, 0), 2),
+    # missing outputs
+    (lambda L: L.moe_route_topk(None, None, None, P, 16, 0, 64, 4, None, None, P, None, 0, 0), 1),
+    # learned routing without logits buffer
+    (lambda L: L.moe_route_topk(P, P, None, None, 16, 256, 64, 4, None, P, P, None, 0, 0), 1),
+    # d not a multiple of 64
+    (lambda L: L.moe_permute(P, P, 16, 100, 64, 4, 0, P, P, P, P, P, P, P, 1 << 20, 0), 2),
+    # workspace too small
+    (lambda L: L.moe_permute(P, P, 16, 128, 64, 4, 0, P, P, P, P, P, P, P, 16, 0), 3),
+    # misaligned x
+    (lambda L: L.moe_permute(P + 2, P, 16, 128, 64, 4, 0, P, P, P, P, P, P, P, 1 << 20, 0), 1),
+    # shared expert without its buffers
+    (lambda L: L.moe_grouped_swiglu(P, P, None, 16, 128, 8, 2, 128, 128, P, P, P, None, None, None,
+                                    P, P, P, None, None, None, None, 0, 0), 1),
+    # combine: null y
+    (lambda L: L.moe_unpermute_combine(P, None, P, P, 16, 128, 2, None, 0), 1),
+    # backward workspace too small
+    (lambda L: L.moe_grouped_swiglu_bwd(P, P, P, P, P, P, P, P, P, P, 16, 128, 8, 2, 128, 128, P, P, P, P, P, P,
+                                        P, P, P, P, P, P, P, P, P, P, 64, 0), 3),
+    # router backward: x without dW_r
+    (lambda L: L.moe_route_topk_bwd(P, P, P, P, 16, 128, 8, 2, P, None, P, 1 << 20, 0), 1),
+    # permute backward: dlogits without W_r
+    (lambda L: L.moe_permute_bwd(P, None, P, P, None, 16, 128, 8, 2, P, P, 1 << 20, 0), 1),
+])
+def test_argument_errors_are_reported_on_the_host(lib, call, expect):
+    with pytest.raises(lib.MoEError) as e:
+        call(lib)
+    assert e.value.status == expect

@@ -124,7 +124,7 @@ def test_identity_expert_combine(B, cap):
     idx, g = run_topk(B, l, k)
     x_bits = gen.normal_bf16(305, (T, d))
     p = run_permute(B, x_bits, idx, E, cap)
-    x_perm = dev_bf16(p["x_perm"])
+    x_perm = dev_bf16(p["x_perm"]).float()   # expert outputs are fp32
     y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
     B.moe_unpermute_combine(x_perm, None, dev_f32(g), torch.from_numpy(p["row_of_slot"]).cuda(), T, d, k, y)
     torch.cuda.synchronize()
@@ -146,9 +146,9 @@ def test_combine_bwd_gather_and_reduce(B):
     row = torch.from_numpy(p["row_of_slot"]).cuda()
     dYp = torch.zeros(T * k, d, dtype=torch.bfloat16, device="cuda")
     B.moe_unpermute_combine_bwd(dev_bf16(dY_bits), row, T, d, k, dYp)
-    # reduce: dx = sum_s dx_perm[row] + dx_s, with dx_perm = o, dx_s = dY
+    # reduce: dx = sum_s dx_perm[row] + dx_s, with dx_perm = o, dx_s = dY (fp32 inputs)
     dx = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
-    B.moe_permute_bwd(dev_bf16(o_bits), dev_bf16(dY_bits), row, None, None, T, d, E, k, dx, None, 0)
+    B.moe_permute_bwd(dev_bf16(o_bits).float(), dev_bf16(dY_bits).float(), row, None, None, T, d, E, k, dx, None, 0)
     torch.cuda.synchronize()
     # the oracle routes the same generator logits on its own
     ridx, rg = orc.route_topk(l, k)

@@ -104,6 +104,7 @@ struct Sched {
 };
 
 struct SmemTail {
+  float tbuf[4][32 * 36];  // per epilogue warp: 32x32 fp32 staging chunk, rows padded to 36
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
@@ -239,6 +240,61 @@ __device__ void build_schedule(const Params& P, Sched& S) {
 }
 
 __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + __expf(-a)); }
+
+template <int EPI>
+struct OutSel {
+  using type = __nv_bfloat16;
+};
+template <>
+struct OutSel<EPI_F32> {
+  using type = float;
+};
+template <int EPI>
+using OutT = typename OutSel<EPI>::type;
+
+// Epilogue register layout ("quad layout"): for a warp's 32 rows x 32
+// columns, lane l holds, for j = 0..7, the four consecutive columns
+// 4*(l%8) .. 4*(l%8)+3 of row 4*j + l/8.  Eight lanes cover one row, so every
+// global access of an instruction is four rows x 128 contiguous bytes (fp32)
+// or 64 bytes (bf16).
+constexpr int TB_STRIDE = 36;  // floats per row of the staging buffer (16-byte aligned, conflict-free)
+
+// 32 accumulator columns at `taddr` (row-per-thread in TMEM) -> quad layout,
+// through the warp's 32 x 36 shared-memory buffer (float4 writes and reads,
+// free of bank conflicts).
+__device__ __forceinline__ void tmem_chunk_quad(uint32_t taddr, float* tb, int lane, float4 (&v)[8]) {
+  uint32_t r[32];
+  ptx::tmem_ld32(taddr, r);
+  ptx::tmem_ld_wait();
+  __syncwarp();
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+    *reinterpret_cast<float4*>(tb + lane * TB_STRIDE + 4 * m) =
+        make_float4(__uint_as_float(r[4 * m]), __uint_as_float(r[4 * m + 1]), __uint_as_float(r[4 * m + 2]),
+                    __uint_as_float(r[4 * m + 3]));
+  __syncwarp();
+  const int rs = lane >> 3, cq = (lane & 7) * 4;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const float4*>(tb + (4 * j + rs) * TB_STRIDE + cq);
+}
+
+__device__ __forceinline__ void zero_quad(float4 (&v)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+}
+// v = hi + lo, hi = bf16(v), lo = bf16(v - hi), four values
+__device__ __forceinline__ void split_store4(__nv_bfloat16* hi, __nv_bfloat16* lo, float4 v) {
+  const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
+  const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+  *reinterpret_cast<uint2*>(hi) = make_uint2(*reinterpret_cast<const uint32_t*>(&h01),
+                                             *reinterpret_cast<const uint32_t*>(&h23));
+  *reinterpret_cast<uint2*>(lo) = make_uint2(pack_bf16(v.x - f01.x, v.y - f01.y), pack_bf16(v.z - f23.x, v.w - f23.y));
+}
 
 template <int AMN, int BMN, int MODE, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params P) {
@@ -425,8 +481,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r_in_tile = q * 32 + lane;
+    // Warp w owns TMEM lanes [32q, 32q+32) (q = w % 4) = tile rows
+    // [32q, 32q+32).  Each 32-column accumulator chunk goes TMEM -> registers
+    // (row per thread) -> shared memory -> quad layout (tmem_chunk_quad), so
+    // that all global traffic is vectorised and coalesced.
+    const int q = warp & 3;
+    float* tb = &tail->tbuf[q][0];
+    const unsigned FULL = 0xffffffffu;
+    const int rs = lane >> 3;         // row within each group of four
+    const int cq = (lane & 7) * 4;    // first of this lane's four columns
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       TileInfo ti = decode<MODE>(P, S, t);
@@ -440,98 +503,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       }
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-      const int row = ti.m0 + r_in_tile;
-      const bool row_ok = row < ti.rows_end;
+      const int row0 = ti.m0 + q * 32;
+      const int nrows = max(0, min(32, ti.rows_end - row0));
       const bool has_acc = ti.nk > 0;
 
-      if (EPI == EPI_BF16) {
-        __nv_bfloat16* outp;
-        if (MODE == KGROUP && pr.row_split > 0 && ti.m0 >= pr.row_split)
-          outp = reinterpret_cast<__nv_bfloat16*>(pr.out2) + ti.g * pr.gstride + (long long)(row - pr.row_split) * pr.ldo;
-        else
-          outp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (MODE == KGROUP ? ti.g * pr.gstride : 0) + (long long)row * pr.ldo;
-        for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
-          if (ti.n0 + c0 >= pr.N) break;
-          uint32_t r[32];
-          if (has_acc) {
-            ptx::tmem_ld32(taddr + c0, r);
-            ptx::tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = 0u;
-          }
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(outp + ti.n0 + c0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-              v.y = pack_bf16(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-              v.z = pack_bf16(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-              v.w = pack_bf16(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
-              dst[j] = v;
-            }
-          }
+      if (EPI == EPI_BF16 || EPI == EPI_F32) {
+        long long base;  // element offset of (row0, 0)
+        OutT<EPI>* outp;
+        if (MODE == KGROUP && pr.row_split > 0 && ti.m0 >= pr.row_split) {
+          outp = reinterpret_cast<OutT<EPI>*>(pr.out2);
+          base = ti.g * pr.gstride + (long long)(row0 - pr.row_split) * pr.ldo;
+        } else {
+          outp = reinterpret_cast<OutT<EPI>*>(pr.out);
+          base = (MODE == KGROUP ? ti.g * pr.gstride : 0) + (long long)row0 * pr.ldo;
         }
-      } else if (EPI == EPI_F32) {
-        float* outp = reinterpret_cast<float*>(pr.out) + (MODE == KGROUP ? ti.g * pr.gstride : 0) + (long long)row * pr.ldo;
         for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
           if (ti.n0 + c0 >= pr.N) break;
-          uint32_t r[32];
-          if (has_acc) {
-            ptx::tmem_ld32(taddr + c0, r);
-            ptx::tmem_ld_wait();
-          } else {
+          float4 v[8];
+          if (has_acc) tmem_chunk_quad(taddr + c0, tb, lane, v);
+          else zero_quad(v);
+          const int col = ti.n0 + c0 + cq;
+          const bool col_ok = col < pr.N;  // N is a multiple of 4
+          float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (EPI == EPI_F32 && pr.bias && col_ok) b = __ldg(reinterpret_cast<const float4*>(pr.bias + col));
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = 0u;
-          }
-          if (row_ok) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int col = ti.n0 + c0 + 4 * j;
-              if (col < pr.N) {
-                float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                       __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                if (pr.bias) {
-                  v.x += __ldg(pr.bias + col); v.y += __ldg(pr.bias + col + 1);
-                  v.z += __ldg(pr.bias + col + 2); v.w += __ldg(pr.bias + col + 3);
-                }
-                *reinterpret_cast<float4*>(outp + col) = v;
-              }
-            }
+          for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + rs;
+            if (r < nrows && col_ok)
+              store4(outp + base + (long long)r * pr.ldo + col,
+                     make_float4(v[j].x + b.x, v[j].y + b.y, v[j].z + b.z, v[j].w + b.w));
           }
         }
       } else if (EPI == EPI_SWIGLU_FWD) {
-        // accumulator columns [0,128) = a (gate), [128,256) = u (up); a and u
-        // are kept in fp32 for the backward pass
-        __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row * pr.ldo + ti.n0;
-        float* ap = pr.aux ? reinterpret_cast<float*>(pr.aux) + (long long)row * pr.ld_aux + ti.n0 : nullptr;
+        // accumulator columns [0,128) = a (gate), [128,256) = u (up); h goes
+        // out in bf16 (down-projection input), a and u in fp32 (backward)
+        __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row0 * pr.ldo + ti.n0;
+        float* ap = pr.aux ? reinterpret_cast<float*>(pr.aux) + (long long)row0 * pr.ld_aux + ti.n0 : nullptr;
         for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t ra[32], ru[32];
-          ptx::tmem_ld32(taddr + c0, ra);
-          ptx::tmem_ld32(taddr + 128 + c0, ru);
-          ptx::tmem_ld_wait();
-          if (row_ok) {
+          float4 va[8], vu[8];
+          tmem_chunk_quad(taddr + c0, tb, lane, va);
+          tmem_chunk_quad(taddr + 128 + c0, tb, lane, vu);
+          const int c = c0 + cq;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              float h[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                float a = __uint_as_float(ra[8 * j + e]);
-                float u = __uint_as_float(ru[8 * j + e]);
-                h[e] = a * sigmoidf_(a) * u;
-              }
-              reinterpret_cast<uint4*>(hp + c0)[j] = pack8(h);
-            }
-            if (ap) {
-              float4* da4 = reinterpret_cast<float4*>(ap + c0);
-              float4* du4 = reinterpret_cast<float4*>(ap + pr.H + c0);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                da4[j] = make_float4(__uint_as_float(ra[4 * j]), __uint_as_float(ra[4 * j + 1]),
-                                     __uint_as_float(ra[4 * j + 2]), __uint_as_float(ra[4 * j + 3]));
-                du4[j] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
-                                     __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
+          for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + rs;
+            if (r < nrows) {
+              const float4 a = va[j], u = vu[j];
+              const float4 h = make_float4(a.x * sigmoidf_(a.x) * u.x, a.y * sigmoidf_(a.y) * u.y,
+                                           a.z * sigmoidf_(a.z) * u.z, a.w * sigmoidf_(a.w) * u.w);
+              store4(hp + (long long)r * pr.ldo + c, h);
+              if (ap) {
+                store4(ap + (long long)r * pr.ld_aux + c, a);
+                store4(ap + (long long)r * pr.ld_aux + pr.H + c, u);
               }
             }
           }
@@ -543,108 +566,157 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         //   da = dh u sig(a) (1 + a (1 - sig(a)));  du = dh silu(a)
         // da | du go out as bf16 hi + lo, g*h as bf16 hi + lo (operands of the
         // weight-gradient GEMMs), and the gate-gradient partial per row.
-        float g = 1.0f;
-        if (row_ok && pr.gates) {
-          int slot = __ldg(pr.slot_of_row + row);
+        float g_mine = 1.0f;  // gate of row row0 + lane
+        if (pr.gates && lane < nrows) {
+          const int slot = __ldg(pr.slot_of_row + row0 + lane);
           if (slot < 0 || slot >= pr.gate_slots) {
             record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
-            g = 0.0f;
+            g_mine = 0.0f;
           } else {
-            g = __ldg(pr.gates + slot);
+            g_mine = __ldg(pr.gates + slot);
           }
         }
-        const long long ro = (long long)row * pr.ldo + ti.n0;         // into [rows, 2H]
-        const long long rh = (long long)row * pr.H + ti.n0;           // into [rows, H]
-        const float* aup = reinterpret_cast<const float*>(pr.aux) + (long long)row * pr.ld_aux + ti.n0;
-        float dgacc = 0.0f;
-        for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
-          if (ti.n0 + c0 >= pr.N) break;
-          uint32_t r[32];
-          ptx::tmem_ld32(taddr + c0, r);
-          ptx::tmem_ld_wait();
-          if (row_ok) {
+        float gj[8], part[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float4* a4 = reinterpret_cast<const float4*>(aup + c0 + 8 * j);
-              const float4* u4 = reinterpret_cast<const float4*>(aup + pr.H + c0 + 8 * j);
-              float4 a0 = __ldg(a4), a1 = __ldg(a4 + 1), u0 = __ldg(u4), u1 = __ldg(u4 + 1);
-              const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-              const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-              float da[8], du[8], gh[8];
+        for (int j = 0; j < 8; ++j) {
+          gj[j] = __shfl_sync(FULL, g_mine, 4 * j + rs);
+          part[j] = 0.0f;
+        }
+        const float* aup = reinterpret_cast<const float*>(pr.aux) + (long long)row0 * pr.ld_aux + ti.n0;
+        const long long ro = (long long)row0 * pr.ldo + ti.n0;  // into [rows, 2H]
+        const long long rh = (long long)row0 * pr.H + ti.n0;    // into [rows, H]
+        __nv_bfloat16* dhi = reinterpret_cast<__nv_bfloat16*>(pr.out) + ro;
+        __nv_bfloat16* dlo = reinterpret_cast<__nv_bfloat16*>(pr.out_lo) + ro;
+        __nv_bfloat16* ghh = reinterpret_cast<__nv_bfloat16*>(pr.gh_hi) + rh;
+        __nv_bfloat16* ghl = reinterpret_cast<__nv_bfloat16*>(pr.gh_lo) + rh;
+        const int ncols = min(pr.n_tile, pr.N - ti.n0);
+        // a, u of the next chunk are loaded while the current one is processed
+        float4 na[8], nu[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float acc = __uint_as_float(r[8 * j + e]);
+        for (int j = 0; j < 8; ++j) {
+          const int r = 4 * j + rs;
+          if (r < nrows) {
+            na[j] = __ldg(reinterpret_cast<const float4*>(aup + (long long)r * pr.ld_aux + cq));
+            nu[j] = __ldg(reinterpret_cast<const float4*>(aup + (long long)r * pr.ld_aux + pr.H + cq));
+          }
+        }
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
+          float4 ca[8], cu[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            ca[j] = na[j];
+            cu[j] = nu[j];
+          }
+          if (c0 + 32 < ncols) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int r = 4 * j + rs;
+              if (r < nrows) {
+                na[j] = __ldg(reinterpret_cast<const float4*>(aup + (long long)r * pr.ld_aux + c0 + 32 + cq));
+                nu[j] = __ldg(reinterpret_cast<const float4*>(aup + (long long)r * pr.ld_aux + pr.H + c0 + 32 + cq));
+              }
+            }
+          }
+          float4 vd[8];
+          tmem_chunk_quad(taddr + c0, tb, lane, vd);
+          const int c = c0 + cq;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + rs;
+            if (r < nrows) {
+              const float a[4] = {ca[j].x, ca[j].y, ca[j].z, ca[j].w}, u[4] = {cu[j].x, cu[j].y, cu[j].z, cu[j].w};
+              const float dv[4] = {vd[j].x, vd[j].y, vd[j].z, vd[j].w};
+              float da[4], du[4], gh[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
                 const float sg = sigmoidf_(a[e]);
                 const float si = a[e] * sg;
                 const float h = si * u[e];
-                dgacc = fmaf(acc, h, dgacc);
-                const float dh = g * acc;
+                part[j] = fmaf(dv[e], h, part[j]);
+                const float dh = gj[j] * dv[e];
                 da[e] = dh * u[e] * sg * (1.0f + a[e] * (1.0f - sg));
                 du[e] = dh * si;
-                gh[e] = g * h;
+                gh[e] = gj[j] * h;
               }
-              uint4 hi, lo;
-              split8(da, hi, lo);
-              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.out) + ro + c0 + 8 * j) = hi;
-              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.out_lo) + ro + c0 + 8 * j) = lo;
-              split8(du, hi, lo);
-              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.out) + ro + pr.H + c0 + 8 * j) = hi;
-              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.out_lo) + ro + pr.H + c0 + 8 * j) = lo;
-              split8(gh, hi, lo);
-              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.gh_hi) + rh + c0 + 8 * j) = hi;
-              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pr.gh_lo) + rh + c0 + 8 * j) = lo;
+              const long long o2 = (long long)r * pr.ldo + c;
+              const long long o1 = (long long)r * pr.H + c;
+              split_store4(dhi + o2, dlo + o2, make_float4(da[0], da[1], da[2], da[3]));
+              split_store4(dhi + o2 + pr.H, dlo + o2 + pr.H, make_float4(du[0], du[1], du[2], du[3]));
+              split_store4(ghh + o1, ghl + o1, make_float4(gh[0], gh[1], gh[2], gh[3]));
             }
           }
         }
-        if (row_ok && pr.dgp) pr.dgp[(long long)row * pr.ld_dgp + ti.n0 / pr.n_tile] = dgacc;
+        if (pr.dgp) {
+          // sum each row's partials over its eight lanes
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float v = part[j];
+            v += __shfl_xor_sync(FULL, v, 1);
+            v += __shfl_xor_sync(FULL, v, 2);
+            v += __shfl_xor_sync(FULL, v, 4);
+            const int r = 4 * j + rs;
+            if ((lane & 7) == 0 && r < nrows) pr.dgp[(long long)(row0 + r) * pr.ld_dgp + ti.n0 / pr.n_tile] = v;
+          }
+        }
       } else if (EPI == EPI_REDUCE_DX) {
         // dx[t] = acc (router term) + dx_s[t] + sum_s dx_perm[row(t,s)]
-        int rows_s[kMaxK];
         const int kk = pr.topk;
-        if (row_ok) {
-          for (int s = 0; s < kk; ++s) rows_s[s] = __ldg(pr.row_of_slot + (long long)row * kk + s);
+        int my_rows[kMaxK];
+#pragma unroll
+        for (int s = 0; s < kMaxK; ++s) {
+          my_rows[s] = -1;
+          if (s < kk && lane < nrows) {
+            int rr = __ldg(pr.row_of_slot + (long long)(row0 + lane) * kk + s);
+            if (rr >= pr.aux_rows) {
+              record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
+              rr = -1;
+            }
+            my_rows[s] = rr;
+          }
         }
-        __nv_bfloat16* dxp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row * pr.ldo + ti.n0;
-        const __nv_bfloat16* xs = pr.aux2 ? reinterpret_cast<const __nv_bfloat16*>(pr.aux2) + (long long)row * pr.ldo + ti.n0 : nullptr;
-        const __nv_bfloat16* xp = reinterpret_cast<const __nv_bfloat16*>(pr.aux);
+        int rows_j[8][kMaxK];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int s = 0; s < kMaxK; ++s) rows_j[j][s] = __shfl_sync(FULL, my_rows[s], 4 * j + rs);
+        __nv_bfloat16* dxp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row0 * pr.ldo;
+        const float* xs = pr.aux2 ? reinterpret_cast<const float*>(pr.aux2) + (long long)row0 * pr.ldo : nullptr;
+        const float* xp = reinterpret_cast<const float*>(pr.aux);
         for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
           if (ti.n0 + c0 >= pr.N) break;
-          uint32_t r[32];
-          if (has_acc) {
-            ptx::tmem_ld32(taddr + c0, r);
-            ptx::tmem_ld_wait();
-          } else {
+          float4 v[8];
+          if (has_acc) tmem_chunk_quad(taddr + c0, tb, lane, v);
+          else zero_quad(v);
+          const int col = ti.n0 + c0 + cq;
+          // one term at a time for all eight rows, so eight loads are in flight
+          if (xs) {
+            float4 b[8];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = 0u;
-          }
-          if (row_ok) {
+            for (int j = 0; j < 8; ++j)
+              if (4 * j + rs < nrows) b[j] = __ldg(reinterpret_cast<const float4*>(xs + (long long)(4 * j + rs) * pr.ldo + col));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              float v[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[8 * j + e]);
-              if (xs) {
-                float f[8];
-                unpack8(__ldg(reinterpret_cast<const uint4*>(xs + c0) + j), f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] += f[e];
+            for (int j = 0; j < 8; ++j)
+              if (4 * j + rs < nrows) {
+                v[j].x += b[j].x; v[j].y += b[j].y; v[j].z += b[j].z; v[j].w += b[j].w;
               }
-              for (int s = 0; s < kk; ++s) {
-                int rr = rows_s[s];
-                if (rr >= pr.aux_rows) {
-                  record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
-                  rr = -1;
-                }
-                if (rr >= 0) {
-                  float f[8];
-                  unpack8(__ldg(reinterpret_cast<const uint4*>(xp + (long long)rr * pr.ld_aux + ti.n0 + c0) + j), f);
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) v[e] += f[e];
-                }
-              }
-              reinterpret_cast<uint4*>(dxp + c0)[j] = pack8(v);
-            }
           }
+#pragma unroll
+          for (int s = 0; s < kMaxK; ++s) {
+            if (s >= kk) break;
+            float4 b[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (4 * j + rs < nrows && rows_j[j][s] >= 0)
+                b[j] = __ldg(reinterpret_cast<const float4*>(xp + (long long)rows_j[j][s] * pr.ld_aux + col));
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (4 * j + rs < nrows && rows_j[j][s] >= 0) {
+                v[j].x += b[j].x; v[j].y += b[j].y; v[j].z += b[j].z; v[j].w += b[j].w;
+              }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (4 * j + rs < nrows) store4(dxp + (long long)(4 * j + rs) * pr.ldo + col, v[j]);
         }
       }
       ptx::tc_fence_before();

@@ -50,6 +50,11 @@ bool fill_dgrad_gu(Params& P, Problem& pr, const DgradGuArgs& a) {
   if (!encode_3d(&P.maps[ig], a.Wg, a.d, a.H, a.G, 64, 64)) return false;
   if (!encode_3d(&P.maps[iu], a.Wu, a.d, a.H, a.G, 64, 64)) return false;
   pr = blank_problem();
+  if (a.dau_lo) {
+    pr.map_a_lo = P.num_maps++;
+    if (!encode_2d(&P.maps[pr.map_a_lo], a.dau_lo, 2 * a.H, a.rows_total, (uint64_t)a.H * 4, 64, BM)) return false;
+    pr.nsplit = 2;
+  }
   pr.offsets = a.offsets;
   pr.G = a.G;
   pr.extent = a.rows_total;
@@ -128,7 +133,7 @@ cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, 
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->d, 256);
     P.num_problems = 2;
   }
-  return launch<0, 1, MGROUP, EPI_BF16>(P, bound, s);
+  return launch<0, 1, MGROUP, EPI_F32>(P, bound, s);
 }
 
 cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* status, cudaStream_t s) {

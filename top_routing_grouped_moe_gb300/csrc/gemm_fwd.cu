@@ -84,7 +84,7 @@ cudaError_t gemm_down_fwd(const DownFwdArgs& routed, const DownFwdArgs* shared, 
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->d, 256);
     P.num_problems = 2;
   }
-  return launch<0, 0, MGROUP, EPI_BF16>(P, bound, s);
+  return launch<0, 0, MGROUP, EPI_F32>(P, bound, s);
 }
 
 }  // namespace moe

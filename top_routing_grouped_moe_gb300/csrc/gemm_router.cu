@@ -70,17 +70,20 @@ cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const v
   return launch<1, 1, KGROUP, EPI_F32>(P, (long long)S * cdiv_h(E, BM) * cdiv_h(d, 256), s);
 }
 
-cudaError_t gemm_router_dx_reduce(const uint16_t* dl_bf16, const void* W_r, const void* dx_perm, const void* dx_s,
-                                  const int32_t* row_of_slot, int T, int d, int E, int k, void* dx, int* status,
-                                  cudaStream_t s) {
+cudaError_t gemm_router_dx_reduce(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, const float* dx_perm,
+                                  const float* dx_s, const int32_t* row_of_slot, int T, int d, int E, int k, void* dx,
+                                  int* status, cudaStream_t s) {
   (void)status;
   Params P;
   std::memset(&P, 0, sizeof(P));
-  P.num_maps = 2;
-  if (!encode_2d(&P.maps[0], dl_bf16, E, T, (uint64_t)E * 2, 64, BM)) return cudaErrorInvalidValue;
+  P.num_maps = 3;
+  if (!encode_2d(&P.maps[0], dl_hi, E, T, (uint64_t)E * 2, 64, BM)) return cudaErrorInvalidValue;
   if (!encode_3d(&P.maps[1], W_r, d, E, 1, 64, 64)) return cudaErrorInvalidValue;
+  if (!encode_2d(&P.maps[2], dl_lo, E, T, (uint64_t)E * 2, 64, BM)) return cudaErrorInvalidValue;
   Problem& pr = P.prob[0];
   pr = blank_problem();
+  pr.map_a_lo = 2;
+  pr.nsplit = 2;
   pr.G = 1;
   pr.extent = T;
   pr.N = d;
@@ -92,7 +95,7 @@ cudaError_t gemm_router_dx_reduce(const uint16_t* dl_bf16, const void* W_r, cons
   pr.tx_bytes = A_BYTES + 4 * MN_BLOCK_BYTES;
   pr.out = dx;
   pr.ldo = d;
-  pr.aux = const_cast<void*>(dx_perm);
+  pr.aux = const_cast<float*>(dx_perm);
   pr.ld_aux = d;
   pr.aux2 = dx_s;
   pr.row_of_slot = row_of_slot;

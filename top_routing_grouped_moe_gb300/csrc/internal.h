@@ -17,7 +17,8 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
                            int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
                            int32_t* slot_of_row, void* x_perm, void* ws, int* status, cudaStream_t s);
 size_t permute_ws_bytes(int T, int E, int k);
-cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
+// o_perm, s_out fp32; y bf16
+cudaError_t launch_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
                            int T, int d, int k, void* y, int* status, cudaStream_t s);
 // dY_perm[row_of_slot[t*k+s]] = dY[t] for every kept slot
 cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
@@ -25,12 +26,14 @@ cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T
 // dgates[t,s] = sum_p dgp[row_of_slot[t*k+s], p] (0 for dropped slots)
 cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_slot, int T, int k, float* dgates,
                                  cudaStream_t s);
-cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot, int T, int d,
+// dx_perm, dx_s fp32; dx bf16
+cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, int T, int d,
                                     int k, void* dx, int* status, cudaStream_t s);
 // dlogits [T,E] fp32 (dense) and, if dl_hi != NULL, its bf16 hi + lo halves [T,E]
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
                                  float* dlogits, uint16_t* dl_hi, uint16_t* dl_lo, cudaStream_t s);
-cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s);
+// v -> bf16 hi + lo halves
+cudaError_t launch_f32_to_bf16_split(const float* src, uint16_t* hi, uint16_t* lo, long long n, cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float* out, cudaStream_t s);
 
 // ------------------------------------------------------------ tensor-core GEMMs
@@ -52,7 +55,7 @@ struct DownFwdArgs {
   const int32_t* offsets;
   int G, d, H;
   const void* Wd;       // [G, d, H]
-  void* o;              // [rows, d]
+  float* o;             // [rows, d] fp32
 };
 // routed + (optional) shared in one persistent launch
 cudaError_t gemm_swiglu_fwd(const SwigluFwdArgs& routed, const SwigluFwdArgs* shared, int* status, cudaStream_t s);
@@ -77,14 +80,15 @@ struct DgradDownArgs {    // dau = swiglu_bwd(g * (dY_perm W_d), au), plus g*h a
   int gate_slots;
   float* dgp;             // [rows, ceil(H/256)] or NULL
 };
-struct DgradGuArgs {      // dx = dau [W_g; W_u]
-  const void* dau;        // [rows, 2H]
+struct DgradGuArgs {      // dx = (dau_hi + dau_lo) [W_g; W_u]
+  const void* dau;        // [rows, 2H] bf16 hi half
+  const void* dau_lo;     // lo half (split precision) or NULL
   int rows_total;
   const int32_t* offsets;
   int G, d, H;
   const void* Wg;         // [G, H, d]
   const void* Wu;
-  void* dx;               // [rows, d]
+  float* dx;              // [rows, d] fp32
 };
 struct WgradArgs {        // out[g] = A_g^T B_g over rows [off[g], off[g+1])
   const void* A;          // [rows, M] bf16
@@ -104,8 +108,9 @@ cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* st
 // dW_r partials: part[S, E, d] = split-K pieces of (dl_hi + dl_lo)^T x; dl halves [T, E] bf16
 cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* x, int T, int d, int E, int S,
                            float* part, int* status, cudaStream_t s);
-// dx = dl W_r + dx_s + sum_s dx_perm[row(t,s)]
-cudaError_t gemm_router_dx_reduce(const uint16_t* dl_bf16, const void* W_r, const void* dx_perm, const void* dx_s,
+// dx = (dl_hi + dl_lo) W_r + dx_s + sum_s dx_perm[row(t,s)]   (dx_perm, dx_s fp32)
+cudaError_t gemm_router_dx_reduce(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, const float* dx_perm,
+                                  const float* dx_s,
                                   const int32_t* row_of_slot, int T, int d, int E, int k, void* dx, int* status,
                                   cudaStream_t s);
 

@@ -46,7 +46,7 @@ size_t ws_route_topk_bwd(int T, int d, int E) {
   const int S = router_dw_splits(T, d, E);
   return 2 * align256((size_t)T * E * 2) + (S > 1 ? align256((size_t)S * E * d * 4) : 0);
 }
-size_t ws_permute_bwd(int T, int E) { return align256((size_t)T * E * 2); }
+size_t ws_permute_bwd(int T, int E) { return 2 * align256((size_t)T * E * 2); }
 
 // grouped SwiGLU backward scratch: da|du hi+lo [rows,2H] x2, g*h hi+lo [rows,H] x2,
 // gate-gradient partials [rows, ceil(H/256)], for the routed rows (T*k) and the
@@ -162,7 +162,8 @@ int moe_route_topk(const void* x, const void* W_r, const float* bias, const floa
   if (!logits_in) {
     int rc = check_dims(T, d, E, k);
     if (rc) return rc;
-    if (!x || !W_r || !logits || !al16(x) || !al16(W_r) || !al16(logits)) return MOE_ERR_INVALID_ARG;
+    if (!x || !W_r || !logits || !al16(x) || !al16(W_r) || !al16(logits) || (bias && !al16(bias)))
+      return MOE_ERR_INVALID_ARG;
     cudaError_t e = gemm_router_fwd(x, W_r, bias, T, d, E, logits, device_status_ptr(), s);
     if (e != cudaSuccess) return fail_cuda(e);
     src = logits;
@@ -185,7 +186,7 @@ int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int
 
 int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const void* x, int T, int d, int E, int k, int H,
                        int Hs, const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
-                       const void* Ws_d, float* au, void* h, void* o_perm, float* au_s, void* h_s, void* s_out,
+                       const void* Ws_d, float* au, void* h, float* o_perm, float* au_s, void* h_s, float* s_out,
                        void* ws, size_t ws_bytes, void* stream) {
   (void)ws;
   (void)ws_bytes;
@@ -213,8 +214,8 @@ int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const void* x
   return check(gemm_down_fwd(rd, Hs > 0 ? &sd : nullptr, status, st));
 }
 
-int moe_unpermute_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot, int T,
-                          int d, int k, void* y, void* stream) {
+int moe_unpermute_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
+                          int T, int d, int k, void* y, void* stream) {
   if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
   if (k > kMaxK || (d % 64) != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   if (!o_perm || !gates || !row_of_slot || !y) return MOE_ERR_INVALID_ARG;
@@ -237,7 +238,7 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
                            const int32_t* slot_of_row, const int32_t* offsets, const void* x_perm, const void* x,
                            const float* au, const float* au_s, int T, int d, int E, int k, int H, int Hs,
                            const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
-                           const void* Ws_d, void* dx_perm, void* dx_s, void* dW_g, void* dW_u, void* dW_d,
+                           const void* Ws_d, float* dx_perm, float* dx_s, void* dW_g, void* dW_u, void* dW_d,
                            void* dWs_g, void* dWs_u, void* dWs_d, float* dgates, void* ws, size_t ws_bytes,
                            void* stream) {
   int rc = check_dims(T, d, E, k);
@@ -280,9 +281,9 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   e = gemm_wgrad(r2, Hs > 0 ? &s2 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
 
-  // 3. dx_perm = [da|du] [W_g; W_u]
-  DgradGuArgs r3{w + L.dau_hi, R, offsets, E, d, H, W_g, W_u, dx_perm};
-  DgradGuArgs s3{w + L.s_dau_hi, T, nullptr, 1, d, Hs, Ws_g, Ws_u, dx_s};
+  // 3. dx_perm = [da|du] [W_g; W_u], [da|du] split into bf16 hi + lo
+  DgradGuArgs r3{w + L.dau_hi, w + L.dau_lo, R, offsets, E, d, H, W_g, W_u, dx_perm};
+  DgradGuArgs s3{w + L.s_dau_hi, w + L.s_dau_lo, T, nullptr, 1, d, Hs, Ws_g, Ws_u, dx_s};
   e = gemm_dgrad_gu(r3, Hs > 0 ? &s3 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
 
@@ -317,7 +318,7 @@ int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* t
   return MOE_OK;
 }
 
-int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot, const float* dlogits,
+int moe_permute_bwd(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, const float* dlogits,
                     const void* W_r, int T, int d, int E, int k, void* dx, void* ws, size_t ws_bytes, void* stream) {
   if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
   if (k > kMaxK || (d % 64) != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
@@ -330,11 +331,12 @@ int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of
   if (rc) return rc;
   if (!al16(W_r)) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < ws_permute_bwd(T, E)) return MOE_ERR_WORKSPACE;
-  uint16_t* dl_bf16 = static_cast<uint16_t*>(ws);
-  cudaError_t e = launch_f32_to_bf16(dlogits, dl_bf16, (long long)T * E, st);
+  uint16_t* dl_hi = static_cast<uint16_t*>(ws);
+  uint16_t* dl_lo = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + align256((size_t)T * E * 2));
+  cudaError_t e = launch_f32_to_bf16_split(dlogits, dl_hi, dl_lo, (long long)T * E, st);
   if (e != cudaSuccess) return fail_cuda(e);
-  return check(gemm_router_dx_reduce(dl_bf16, W_r, dx_perm, dx_s, row_of_slot, T, d, E, k, dx, device_status_ptr(),
-                                     st));
+  return check(gemm_router_dx_reduce(dl_hi, dl_lo, W_r, dx_perm, dx_s, row_of_slot, T, d, E, k, dx,
+                                     device_status_ptr(), st));
 }
 
 }  // extern "C"

@@ -242,7 +242,8 @@ __global__ void perm_scatter_kernel(const uint4* __restrict__ x, const int32_t* 
 }
 
 // ------------------------------------------------------------------ combine
-__global__ void combine_kernel(const uint4* __restrict__ o_perm, const uint4* __restrict__ s_out,
+// fp32 expert / shared outputs, fp32 accumulation, one bf16 rounding of y.
+__global__ void combine_kernel(const float4* __restrict__ o_perm, const float4* __restrict__ s_out,
                                const float* __restrict__ gates, const int32_t* __restrict__ row_of_slot, int T, int d,
                                int k, long long max_rows, uint4* __restrict__ y, int* status) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -265,11 +266,12 @@ __global__ void combine_kernel(const uint4* __restrict__ o_perm, const uint4* __
     rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
     gs[s] = __shfl_sync(0xffffffffu, g, s < k ? s : 0);
   }
-  const int vpr = d / 8;
+  const int vpr = d / 8;  // 8 elements per step: two float4 in, one uint4 out
   for (int c = lane; c < vpr; c += 32) {
     float acc[8];
     if (s_out) {
-      unpack8(__ldg(s_out + (long long)t * vpr + c), acc);
+      float4 a = __ldg(s_out + (long long)t * 2 * vpr + 2 * c), b = __ldg(s_out + (long long)t * 2 * vpr + 2 * c + 1);
+      acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w; acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
@@ -278,10 +280,12 @@ __global__ void combine_kernel(const uint4* __restrict__ o_perm, const uint4* __
     for (int s = 0; s < kMaxK; ++s) {
       if (s >= k) break;
       if (rows[s] < 0) continue;
-      float f[8];
-      unpack8(__ldg(o_perm + (long long)rows[s] * vpr + c), f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = fmaf(gs[s], f[e], acc[e]);
+      const float4* src = o_perm + (long long)rows[s] * 2 * vpr + 2 * c;
+      float4 a = __ldg(src), b = __ldg(src + 1);
+      acc[0] = fmaf(gs[s], a.x, acc[0]); acc[1] = fmaf(gs[s], a.y, acc[1]);
+      acc[2] = fmaf(gs[s], a.z, acc[2]); acc[3] = fmaf(gs[s], a.w, acc[3]);
+      acc[4] = fmaf(gs[s], b.x, acc[4]); acc[5] = fmaf(gs[s], b.y, acc[5]);
+      acc[6] = fmaf(gs[s], b.z, acc[6]); acc[7] = fmaf(gs[s], b.w, acc[7]);
     }
     y[(long long)t * vpr + c] = pack8(acc);
   }
@@ -338,7 +342,7 @@ __global__ void dgates_reduce_kernel(const float* __restrict__ dgp, int P, const
   }
 }
 
-__global__ void unpermute_reduce_kernel(const uint4* __restrict__ dx_perm, const uint4* __restrict__ dx_s,
+__global__ void unpermute_reduce_kernel(const float4* __restrict__ dx_perm, const float4* __restrict__ dx_s,
                                         const int32_t* __restrict__ row_of_slot, int T, int d, int k,
                                         long long max_rows, uint4* __restrict__ dx, int* status) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -359,7 +363,8 @@ __global__ void unpermute_reduce_kernel(const uint4* __restrict__ dx_perm, const
   for (int c = lane; c < vpr; c += 32) {
     float acc[8];
     if (dx_s) {
-      unpack8(__ldg(dx_s + (long long)t * vpr + c), acc);
+      float4 a = __ldg(dx_s + (long long)t * 2 * vpr + 2 * c), b = __ldg(dx_s + (long long)t * 2 * vpr + 2 * c + 1);
+      acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w; acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
@@ -368,10 +373,10 @@ __global__ void unpermute_reduce_kernel(const uint4* __restrict__ dx_perm, const
     for (int s = 0; s < kMaxK; ++s) {
       if (s >= k) break;
       if (rows[s] < 0) continue;
-      float f[8];
-      unpack8(__ldg(dx_perm + (long long)rows[s] * vpr + c), f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += f[e];
+      const float4* src = dx_perm + (long long)rows[s] * 2 * vpr + 2 * c;
+      float4 a = __ldg(src), b = __ldg(src + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
     }
     dx[(long long)t * vpr + c] = pack8(acc);
   }
@@ -419,10 +424,15 @@ __global__ void router_bwd_dl_kernel(const float* __restrict__ dgates, const flo
   }
 }
 
-__global__ void f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, long long n) {
+// v -> hi = bf16(v), lo = bf16(v - hi)
+__global__ void f32_to_bf16_split_kernel(const float* __restrict__ src, uint16_t* __restrict__ hi,
+                                         uint16_t* __restrict__ lo, long long n) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    __nv_bfloat16 b = __float2bfloat16_rn(src[i]);
-    dst[i] = *reinterpret_cast<uint16_t*>(&b);
+    const float v = src[i];
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
+    hi[i] = *reinterpret_cast<uint16_t*>(&h);
+    lo[i] = *reinterpret_cast<uint16_t*>(&l);
   }
 }
 
@@ -488,10 +498,10 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
+cudaError_t launch_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
                            int T, int d, int k, void* y, int* status, cudaStream_t s) {
   combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-      static_cast<const uint4*>(o_perm), static_cast<const uint4*>(s_out), gates, row_of_slot, T, d, k,
+      reinterpret_cast<const float4*>(o_perm), reinterpret_cast<const float4*>(s_out), gates, row_of_slot, T, d, k,
       (long long)T * k, static_cast<uint4*>(y), status);
   return cudaGetLastError();
 }
@@ -510,10 +520,11 @@ cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot, int T, int d,
+cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, int T, int d,
                                     int k, void* dx, int* status, cudaStream_t s) {
   unpermute_reduce_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-      static_cast<const uint4*>(dx_perm), static_cast<const uint4*>(dx_s), row_of_slot, T, d, k, (long long)T * k,
+      reinterpret_cast<const float4*>(dx_perm), reinterpret_cast<const float4*>(dx_s), row_of_slot, T, d, k,
+      (long long)T * k,
       static_cast<uint4*>(dx), status);
   return cudaGetLastError();
 }
@@ -525,8 +536,8 @@ cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const 
   return cudaGetLastError();
 }
 
-cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s) {
-  f32_to_bf16_kernel<<<flat_blocks(n, 256), 256, 0, s>>>(src, dst, n);
+cudaError_t launch_f32_to_bf16_split(const float* src, uint16_t* hi, uint16_t* lo, long long n, cudaStream_t s) {
+  f32_to_bf16_split_kernel<<<flat_blocks(n, 256), 256, 0, s>>>(src, hi, lo, n);
   return cudaGetLastError();
 }
 

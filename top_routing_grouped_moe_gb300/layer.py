@@ -35,18 +35,18 @@ class MoELayer:
         self.x_perm = e(R, d)
         self.au = e(R, 2 * H, dt=torch.float32) if backward else None
         self.h = e(R, H)
-        self.o_perm = e(R, d)
+        self.o_perm = e(R, d, dt=torch.float32)
         self.au_s = e(T, 2 * Hs, dt=torch.float32) if (Hs and backward) else None
         self.h_s = e(T, Hs) if Hs else None
-        self.s = e(T, d) if Hs else None
+        self.s = e(T, d, dt=torch.float32) if Hs else None
         self.y = e(T, d)
         self.ws_bytes = B.moe_workspace_size(T, d, E, k, H, Hs)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         if backward:
             self.dY_perm = e(R, d)
             self.dgates = e(T, k, dt=torch.float32)
-            self.dx_perm = e(R, d)
-            self.dx_s = e(T, d) if Hs else None
+            self.dx_perm = e(R, d, dt=torch.float32)
+            self.dx_s = e(T, d, dt=torch.float32) if Hs else None
             self.dW_g = e(E, H, d)
             self.dW_u = e(E, H, d)
             self.dW_d = e(E, d, H)
