@@ -6,6 +6,7 @@ in parallel and linked (static CUDA runtime) into lib/libmoe_gb300.so.
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -40,11 +41,25 @@ def _deps():
             + glob.glob(os.path.join(ROOT, "include", "*.h")) + [os.path.abspath(__file__)])
 
 
+STAMP = LIB + ".stamp"
+
+
+def _fingerprint() -> str:
+    """Hash of every source file's path and contents plus the flags."""
+    h = hashlib.sha256()
+    for p in sorted(_deps()):
+        h.update(os.path.relpath(p, ROOT).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    return h.hexdigest()
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    with open(STAMP) as f:
+        return f.read().strip() == _fingerprint()
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
@@ -73,6 +88,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(_fingerprint())
     return LIB
 
 
