@@ -137,6 +137,31 @@ MOE_API int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, in
                 int32_t* row_of_slot, int32_t* slot_of_row, void* x_perm,
                 void* ws, size_t ws_bytes, void* stream);
 
+/* moe_permute without a workspace (no counterpart in the pages: it exists
+ * for callers, not for the method).  Same arguments, results and determinism
+ * as moe_permute, minus ws / ws_bytes.
+ *
+ * Who needs it: callers that cannot allocate device memory for scratch --
+ * plug-in hosts that give a library nothing but their own tensors and a
+ * stream, and processes whose device memory is entirely held by a framework
+ * pool, where one more cudaMalloc would fail or fragment that pool.  Nothing
+ * is allocated by this call or by the library on its behalf.
+ *
+ * Scratch: a fixed 4 MiB array inside the library, present on every GPU that
+ * loads the library until the process exits.  Shapes whose scratch
+ * (per-tile counts and bases, ceil(T/128) x E ints each, plus T*k in-tile
+ * ranks) exceeds 4 MiB are rejected with MOE_ERR_UNSUPPORTED before anything
+ * runs -- e.g. T*k up to about 512K slots at E = 64 fits.
+ * The first call on a device looks up that array's device address (once per
+ * device, with the device current); make that first call outside any stream
+ * capture.  All calls on a device share the array: calls whose kernels can
+ * overlap on the GPU (different streams without ordering) race and must be
+ * serialised by the caller.  The array keeps the previous call's contents;
+ * no part of it has to start at zero. */
+MOE_API int moe_permute_static(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
+                       int capacity, int32_t* counts_raw, int32_t* counts, int32_t* offsets,
+                       int32_t* row_of_slot, int32_t* slot_of_row, void* x_perm, void* stream);
+
 /* Grouped SwiGLU expert MLP over the ragged per-expert row segments plus the
  * shared expert ("one shared expert", README "Production throughput runs";
  * "sparse kernels", "Interpreting the eight-layer ..."):

@@ -75,6 +75,8 @@ P = 1 << 12  # stand-in device addresses (16-byte aligned); never dereferenced
     (lambda L: L.moe_permute(P, P, 16, 128, 64, 4, 0, P, P, P, P, P, P, P, 16, 0), 3),
     # misaligned x
     (lambda L: L.moe_permute(P + 2, P, 16, 128, 64, 4, 0, P, P, P, P, P, P, P, 1 << 20, 0), 1),
+    # E > 256
+    (lambda L: L.moe_permute_static(P, P, 16, 128, 264, 4, 0, P, P, P, P, P, P, 0), 2),
     # shared expert without its buffers
     (lambda L: L.moe_grouped_swiglu(P, P, None, 16, 128, 8, 2, 128, 128, P, P, P, None, None, None,
                                     P, P, P, None, None, None, None, 0, 0), 1),

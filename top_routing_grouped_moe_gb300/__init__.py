@@ -6,7 +6,7 @@ loaded on first use: if the CUDA library has not been built, that use raises
 ImportError (there is no CPU fallback)."""
 
 _BINDING_NAMES = {
-    "moe_route_topk", "moe_permute", "moe_grouped_swiglu", "moe_unpermute_combine",
+    "moe_route_topk", "moe_permute", "moe_permute_static", "moe_grouped_swiglu", "moe_unpermute_combine",
     "moe_unpermute_combine_bwd", "moe_grouped_swiglu_bwd", "moe_route_topk_bwd", "moe_permute_bwd",
     "moe_workspace_size", "moe_version", "moe_device_status", "MoEError", "status_string",
 }

@@ -45,6 +45,7 @@ _SZ = ctypes.c_size_t
 SIGNATURES = {
     "moe_route_topk": "pppp" + "iiii" + "ppp" + "pz" + "s",
     "moe_permute": "pp" + "iiiii" + "pppppp" + "pz" + "s",
+    "moe_permute_static": "pp" + "iiiii" + "pppppp" + "s",
     "moe_grouped_swiglu": "ppp" + "iiiiii" + "pppppp" + "pppppp" + "pz" + "s",
     "moe_unpermute_combine": "pppp" + "iii" + "p" + "s",
     "moe_unpermute_combine_bwd": "pp" + "iii" + "p" + "s",
@@ -142,6 +143,12 @@ def moe_permute(x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, 
                 ws, ws_bytes, stream=None):
     return _call("moe_permute", x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, row_of_slot,
                  slot_of_row, x_perm, ws, ws_bytes, stream)
+
+
+def moe_permute_static(x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, row_of_slot, slot_of_row,
+                       x_perm, stream=None):
+    return _call("moe_permute_static", x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets,
+                 row_of_slot, slot_of_row, x_perm, stream)
 
 
 def moe_grouped_swiglu(x_perm, offsets, x, T, d, E, k, H, Hs, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, au, h, o_perm,

@@ -9,6 +9,7 @@ namespace moe {
 // per-device facts and the device status word
 int device_sm_count();
 int* device_status_ptr();  // device address of the status word of the current device
+void record_cuda_error(cudaError_t e);  // what moe_last_cuda_error() reports in this thread
 
 // ------------------------------------------------------------ SIMT kernels
 cudaError_t launch_topk_gating(const float* logits, int T, int E, int k, int32_t* idx, float* gates,

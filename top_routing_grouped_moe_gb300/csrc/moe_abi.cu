@@ -75,6 +75,8 @@ size_t ws_swiglu_bwd(int T, int k, int H, int Hs) { return swiglu_bwd_ws(T, k, H
 
 }  // namespace
 
+void record_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
