@@ -39,9 +39,7 @@ constexpr int BM = 128;
 constexpr int BN = 256;  // accumulator columns per tile
 constexpr int BK = 64;   // K per pipeline stage: 128 bytes of bf16 (one swizzle row)
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB: this CTA's A tile per stage
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_PROBLEMS = 2;
 constexpr int MAX_MAPS = 8;
@@ -103,10 +101,22 @@ struct Sched {
   int tpre[MAX_PROBLEMS][MAX_G];  // MGROUP: exclusive prefix of tiles per group
 };
 
-struct SmemTail {
+// PAIR = 1: one CTA computes a 128 x 256 tile.  PAIR = 2: a cluster of two
+// CTAs computes a 256 x 256 tile with pair MMAs (tcgen05 cta_group::2): each
+// CTA holds 128 rows of A and 128 of the 256 columns of B, so a stage is
+// 32 KB instead of 48 KB and six stages fit where four did.
+template <int PAIR>
+struct PairCfg {
+  static constexpr int STAGES = PAIR == 2 ? 6 : 4;
+  static constexpr int B_BYTES = BN * BK * 2 / PAIR;  // this CTA's share of the B tile per stage
+  static constexpr int TILE_M = BM * PAIR;
+};
+
+template <int STG>
+struct SmemTailT {
   float tbuf[4][32 * 36];  // per epilogue warp: 32x32 fp32 staging chunk, rows padded to 36
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[STG];      // the stage's data landed (PAIR = 2: the leader's counts both CTAs)
+  uint64_t empty[STG];     // stage consumed by the MMAs (both CTAs, PAIR = 2)
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint32_t tmem_base;
@@ -114,7 +124,11 @@ struct SmemTail {
   Sched sched;
 };
 
-constexpr size_t kSmemBytes = 1024 + STAGES * (A_BYTES + B_BYTES) + sizeof(SmemTail);
+template <int PAIR>
+constexpr size_t smem_bytes() {
+  return 1024 + PairCfg<PAIR>::STAGES * (A_BYTES + PairCfg<PAIR>::B_BYTES) +
+         sizeof(SmemTailT<PairCfg<PAIR>::STAGES>);
+}
 
 struct TileInfo {
   int p, g, m0, n0, rows_end, k0, k1, nk;
@@ -122,7 +136,7 @@ struct TileInfo {
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-template <int MODE>
+template <int MODE, int TILE_M>
 __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int t) {
   TileInfo ti;
   int p = (P.num_problems > 1 && t >= S.tile_start[1]) ? 1 : 0;
@@ -139,23 +153,24 @@ __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int 
     int g = lo;
     int within = local - S.tpre[p][g];
     int r0 = S.off[p][g], r1 = S.off[p][g + 1];
-    int mt = cdiv(r1 - r0, BM);
-    int n_idx = within / mt, m_idx = within - n_idx * mt;
+    // n fastest: tiles that run at the same time share one slab of A rows and
+    // walk the group's weights, which stay in L2 across slabs
+    int m_idx = within / nt, n_idx = within - m_idx * nt;
     ti.g = g;
-    ti.m0 = r0 + m_idx * BM;
+    ti.m0 = r0 + m_idx * TILE_M;
     ti.rows_end = r1;
     ti.n0 = n_idx * pr.n_tile;
     ti.k0 = 0;
     ti.k1 = pr.K;
     ti.nk = cdiv(pr.K, BK) * pr.nsplit;
   } else {
-    int mt = cdiv(pr.M, BM);
+    int mt = cdiv(pr.M, TILE_M);
     int per = mt * nt;
     int g = local / per;
     int within = local - g * per;
     int m_idx = within / nt, n_idx = within - m_idx * nt;
     ti.g = g;
-    ti.m0 = m_idx * BM;
+    ti.m0 = m_idx * TILE_M;
     ti.rows_end = pr.M;
     ti.n0 = n_idx * pr.n_tile;
     ti.k0 = S.off[p][g];
@@ -166,7 +181,7 @@ __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int 
 }
 
 // Schedule set-up, run by every thread of the CTA before the roles start.
-template <int MODE>
+template <int MODE, int TILE_M>
 __device__ void build_schedule(const Params& P, Sched& S) {
   const int tid = threadIdx.x;
   for (int p = 0; p < P.num_problems; ++p) {
@@ -210,7 +225,7 @@ __device__ void build_schedule(const Params& P, Sched& S) {
         int local = 0;
         for (int j = 0; j < per_lane; ++j) {
           int g = g0 + j;
-          if (g < pr.G) local += cdiv(S.off[p][g + 1] - S.off[p][g], BM) * nt;
+          if (g < pr.G) local += cdiv(S.off[p][g + 1] - S.off[p][g], TILE_M) * nt;
         }
         int incl = local;
 #pragma unroll
@@ -223,13 +238,13 @@ __device__ void build_schedule(const Params& P, Sched& S) {
           int g = g0 + j;
           if (g < pr.G) {
             S.tpre[p][g] = run;
-            run += cdiv(S.off[p][g + 1] - S.off[p][g], BM) * nt;
+            run += cdiv(S.off[p][g + 1] - S.off[p][g], TILE_M) * nt;
           }
         }
         total = __shfl_sync(0xffffffffu, incl, 31);
         if (lane == 0) S.tpre[p][pr.G] = total;
       } else {
-        total = pr.G * cdiv(pr.M, BM) * nt;
+        total = pr.G * cdiv(pr.M, TILE_M) * nt;
       }
       if (lane == 0) S.tile_start[p] = base;
       base += total;
@@ -296,18 +311,47 @@ __device__ __forceinline__ void split_store4(__nv_bfloat16* hi, __nv_bfloat16* l
   *reinterpret_cast<uint2*>(lo) = make_uint2(pack_bf16(v.x - f01.x, v.y - f01.y), pack_bf16(v.z - f23.x, v.w - f23.y));
 }
 
-template <int AMN, int BMN, int MODE, int EPI>
+// TMA load into this CTA's shared memory.  PAIR = 1: bytes counted on this
+// CTA's barrier.  PAIR = 2: bytes counted on the leader CTA's barrier (so the
+// leader's single wait covers both halves of the stage).
+template <int PAIR>
+__device__ __forceinline__ void load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, uint32_t bar_leader, int c0,
+                                        int c1) {
+  if (PAIR == 1) ptx::tma_load_2d(dst, m, bar, c0, c1);
+  else ptx::tma_load_2d_pair(dst, m, bar_leader, c0, c1);
+}
+template <int PAIR>
+__device__ __forceinline__ void load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, uint32_t bar_leader, int c0,
+                                        int c1, int c2) {
+  if (PAIR == 1) ptx::tma_load_3d(dst, m, bar, c0, c1, c2);
+  else ptx::tma_load_3d_pair(dst, m, bar_leader, c0, c1, c2);
+}
+
+template <int AMN, int BMN, int MODE, int EPI, int PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params P) {
+  // ragged-K problems zero tail rows in shared memory before the MMAs; with a
+  // CTA pair the peer's rows could not be zeroed in time, so they stay single
+  static_assert(!(MODE == KGROUP && PAIR == 2), "ragged-K GEMMs run on single CTAs");
+  using Cfg = PairCfg<PAIR>;
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr int B_BYTES = Cfg::B_BYTES;
+  constexpr int TILE_M = Cfg::TILE_M;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  SmemTail* tail = reinterpret_cast<SmemTail*>(smem + STAGES * (A_BYTES + B_BYTES));
+  using Tail = SmemTailT<STAGES>;
+  Tail* tail = reinterpret_cast<Tail*>(smem + STAGES * (A_BYTES + B_BYTES));
   Sched& S = tail->sched;
   volatile int* abort_flag = &tail->abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // PAIR = 2: rank 0 (leader) issues the pair MMAs; rank 1 loads the other
+  // halves of A and B, whose bytes are counted on the leader's barriers.
+  const int rank = PAIR == 2 ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+  const int tile0 = blockIdx.x / PAIR;
+  const int tile_step = gridDim.x / PAIR;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -316,7 +360,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tail->tmem_full[a], 1);
-      ptx::mbar_init(&tail->tmem_empty[a], 128);
+      ptx::mbar_init(&tail->tmem_empty[a], 4 * PAIR);  // one arrival per epilogue warp of each CTA
     }
     tail->abort_flag = 0;
     ptx::fence_mbarrier_init();
@@ -325,14 +369,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     for (int i = 0; i < P.num_maps; ++i) ptx::prefetch_tmap(&P.maps[i]);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&tail->tmem_base, TMEM_COLS);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc<PAIR>(&tail->tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish<PAIR>();
     ptx::tc_fence_before();
   }
-  build_schedule<MODE>(P, S);  // contains __syncthreads
+  build_schedule<MODE, TILE_M>(P, S);  // contains __syncthreads
+  if (PAIR == 2) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
   const int total = S.tile_start[P.num_problems];
+  const int row_half = rank * BM;  // this CTA's first row (or M column) within a tile
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -342,8 +388,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       uint32_t issued_phase_mask = 0;  // bit s: parity of the last load issued into stage s
       uint32_t issued_any = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        TileInfo ti = decode<MODE>(P, S, t);
+      for (int t = tile0; t < total && ok; t += tile_step) {
+        TileInfo ti = decode<MODE, TILE_M>(P, S, t);
         const Problem& pr = P.prob[ti.p];
         const CUtensorMap* mA = &P.maps[pr.map_a];
         for (int kb = 0; kb < ti.nk; ++kb) {
@@ -352,7 +398,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             break;
           }
           uint64_t* fb = &tail->full[stage];
-          ptx::mbar_arrive_expect_tx(fb, pr.tx_bytes);
+          const uint32_t fbl = PAIR == 2 ? ptx::mapa(ptx::smem_u32(fb), 0) : 0u;
+          if (rank == 0) ptx::mbar_arrive_expect_tx(fb, pr.tx_bytes * PAIR);
           issued_any |= 1u << stage;
           issued_phase_mask = (issued_phase_mask & ~(1u << stage)) | (phase << stage);
           const int part = pr.nsplit == 2 ? (kb & 1) : 0;
@@ -360,19 +407,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           uint8_t* a_dst = sA + stage * A_BYTES;
           uint8_t* b_dst = sB + stage * B_BYTES;
           const CUtensorMap* mAk = (part && pr.map_a_lo >= 0) ? &P.maps[pr.map_a_lo] : mA;
+          const int am = ti.m0 + row_half;
           if (AMN == 0) {
-            ptx::tma_load_2d(a_dst, mAk, fb, k, ti.m0);
+            load_2d<PAIR>(a_dst, mAk, fb, fbl, k, am);
           } else {
-            ptx::tma_load_2d(a_dst, mAk, fb, ti.m0, k);
-            ptx::tma_load_2d(a_dst + MN_BLOCK_BYTES, mAk, fb, ti.m0 + 64, k);
+            load_2d<PAIR>(a_dst, mAk, fb, fbl, am, k);
+            load_2d<PAIR>(a_dst + MN_BLOCK_BYTES, mAk, fb, fbl, am + 64, k);
           }
           if (EPI == EPI_SWIGLU_FWD) {
-            ptx::tma_load_3d(b_dst, &P.maps[pr.map_b], fb, k, ti.n0, ti.g);
-            ptx::tma_load_3d(b_dst + (B_BYTES / 2), &P.maps[pr.map_b2], fb, k, ti.n0, ti.g);
+            // B tile = [128 rows of W_g ; 128 rows of W_u]; with a CTA pair
+            // each CTA holds one of the two halves
+            if (PAIR == 1) {
+              load_3d<PAIR>(b_dst, &P.maps[pr.map_b], fb, fbl, k, ti.n0, ti.g);
+              load_3d<PAIR>(b_dst + (B_BYTES / 2), &P.maps[pr.map_b2], fb, fbl, k, ti.n0, ti.g);
+            } else {
+              load_3d<PAIR>(b_dst, &P.maps[rank == 0 ? pr.map_b : pr.map_b2], fb, fbl, k, ti.n0, ti.g);
+            }
           } else if (BMN == 0) {
-            ptx::tma_load_3d(b_dst, &P.maps[pr.map_b], fb, k, ti.n0, ti.g);
+            load_3d<PAIR>(b_dst, &P.maps[pr.map_b], fb, fbl, k, ti.n0 + row_half, ti.g);
           } else {
-            const int nblk = pr.n_tile / 64;
+            const int nblk = pr.n_tile / 64 / PAIR;
+            const int bn = ti.n0 + row_half;
             if (MODE == MGROUP) {
               const CUtensorMap* mB = &P.maps[pr.map_b];
               int kk = k;
@@ -380,10 +435,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
                 mB = &P.maps[pr.map_b2];
                 kk = k - pr.ksplit;
               }
-              for (int j = 0; j < nblk; ++j) ptx::tma_load_3d(b_dst + j * MN_BLOCK_BYTES, mB, fb, ti.n0 + 64 * j, kk, ti.g);
+              for (int j = 0; j < nblk; ++j) load_3d<PAIR>(b_dst + j * MN_BLOCK_BYTES, mB, fb, fbl, bn + 64 * j, kk, ti.g);
             } else {
               const CUtensorMap* mB = (part && pr.map_b_lo >= 0) ? &P.maps[pr.map_b_lo] : &P.maps[pr.map_b];
-              for (int j = 0; j < nblk; ++j) ptx::tma_load_2d(b_dst + j * MN_BLOCK_BYTES, mB, fb, ti.n0 + 64 * j, k);
+              for (int j = 0; j < nblk; ++j) load_2d<PAIR>(b_dst + j * MN_BLOCK_BYTES, mB, fb, fbl, bn + 64 * j, k);
             }
           }
           if (++stage == STAGES) {
@@ -395,9 +450,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       if (!ok) {
         *abort_flag = 1;
         record_status(P.status, MOE_ERR_TIMEOUT);
-        // let copies already in flight land before the CTA's shared memory goes away
+        // let copies already in flight land before the CTA's shared memory goes
+        // away (the leader's barriers count the peer's copies too)
         for (int s = 0; s < STAGES; ++s)
-          if (issued_any & (1u << s)) {
+          if (rank == 0 && (issued_any & (1u << s))) {
             volatile int never = 0;
             ptx::mbar_wait_bounded(&tail->full[s], (issued_phase_mask >> s) & 1u, &never, 100000000ull);
           }
@@ -405,23 +461,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // PAIR = 1: this CTA issues.  PAIR = 2: only the leader issues; its full
+    // barriers count both CTAs' bytes, and its commits arrive on the barriers
+    // of both CTAs.
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     int it = 0;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-      TileInfo ti = decode<MODE>(P, S, t);
+    for (int t = tile0; t < total && ok && rank == 0; t += tile_step, ++it) {
+      TileInfo ti = decode<MODE, TILE_M>(P, S, t);
       const Problem& pr = P.prob[ti.p];
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      if (!ptx::mbar_wait_bounded(&tail->tmem_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+      if (!ptx::mbar_wait_cluster_bounded(&tail->tmem_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      const uint32_t idesc = ptx::idesc_bf16(BM, pr.mma_n, AMN, BMN);
-      const int b_blocks = pr.n_tile / 64;
+      const uint32_t idesc = ptx::idesc_bf16(TILE_M, pr.mma_n, AMN, BMN);
+      const int b_blocks = pr.n_tile / 64 / PAIR;
       for (int kb = 0; kb < ti.nk; ++kb) {
         if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
           ok = false;
@@ -448,8 +507,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             *reinterpret_cast<uint4*>(base + r * 128 + (w & 7) * 16) = make_uint4(0, 0, 0, 0);
           }
           ptx::fence_proxy_async_smem();
-          __syncwarp();
         }
+        __syncwarp();
         if (lane == 0) {
           const uint32_t a_addr = ptx::smem_u32(a_st);
           const uint32_t b_addr = ptx::smem_u32(b_st);
@@ -458,9 +517,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
                                     : ptx::smem_desc(a_addr + s * 32, 16, 1024);
             const uint64_t bd = BMN ? ptx::smem_desc(b_addr + s * 2048, MN_BLOCK_BYTES, 1024)
                                     : ptx::smem_desc(b_addr + s * 32, 16, 1024);
-            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+            if (PAIR == 1) ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+            else ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(&tail->empty[stage]);
+          if (PAIR == 1) ptx::mma_commit(&tail->empty[stage]);
+          else ptx::mma_commit_pair(&tail->empty[stage], 0x3);
         }
         __syncwarp();
         if (++stage == STAGES) {
@@ -470,8 +531,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       }
       if (!ok) break;
       if (lane == 0) {
-        if (ti.nk > 0) ptx::mma_commit(&tail->tmem_full[acc]);
-        else ptx::mbar_arrive(&tail->tmem_full[acc]);
+        if (ti.nk > 0) {
+          if (PAIR == 1) ptx::mma_commit(&tail->tmem_full[acc]);
+          else ptx::mma_commit_pair(&tail->tmem_full[acc], 0x3);
+        } else {
+          ptx::mbar_arrive(&tail->tmem_full[acc]);
+          if (PAIR == 2) ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&tail->tmem_full[acc]), 1));
+        }
       }
       __syncwarp();
     }
@@ -481,36 +547,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Warp w owns TMEM lanes [32q, 32q+32) (q = w % 4) = tile rows
-    // [32q, 32q+32).  Each 32-column accumulator chunk goes TMEM -> registers
-    // (row per thread) -> shared memory -> quad layout (tmem_chunk_quad), so
-    // that all global traffic is vectorised and coalesced.
+    // Warp w owns TMEM lanes [32q, 32q+32) (q = w % 4) = rows
+    // [32q, 32q+32) of this CTA's 128 rows of the tile.  Each 32-column
+    // accumulator chunk goes TMEM -> registers (row per thread) -> shared
+    // memory -> quad layout (tmem_chunk_quad), so that all global traffic is
+    // vectorised and coalesced.
     const int q = warp & 3;
     float* tb = &tail->tbuf[q][0];
     const unsigned FULL = 0xffffffffu;
     const int rs = lane >> 3;         // row within each group of four
     const int cq = (lane & 7) * 4;    // first of this lane's four columns
     int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      TileInfo ti = decode<MODE>(P, S, t);
+    for (int t = tile0; t < total; t += tile_step, ++it) {
+      TileInfo ti = decode<MODE, TILE_M>(P, S, t);
       const Problem& pr = P.prob[ti.p];
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      if (!ptx::mbar_wait_bounded(&tail->tmem_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
+      if (!ptx::mbar_wait_cluster_bounded(&tail->tmem_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
         *abort_flag = 1;
         record_status(P.status, MOE_ERR_TIMEOUT);
         break;
       }
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-      const int row0 = ti.m0 + q * 32;
+      const int m_cta = ti.m0 + row_half;  // first row (KGROUP: first M index) of this CTA
+      const int row0 = m_cta + q * 32;
       const int nrows = max(0, min(32, ti.rows_end - row0));
       const bool has_acc = ti.nk > 0;
 
       if (EPI == EPI_BF16 || EPI == EPI_F32) {
         long long base;  // element offset of (row0, 0)
         OutT<EPI>* outp;
-        if (MODE == KGROUP && pr.row_split > 0 && ti.m0 >= pr.row_split) {
+        if (MODE == KGROUP && pr.row_split > 0 && m_cta >= pr.row_split) {
           outp = reinterpret_cast<OutT<EPI>*>(pr.out2);
           base = ti.g * pr.gstride + (long long)(row0 - pr.row_split) * pr.ldo;
         } else {
@@ -720,14 +788,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         }
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&tail->tmem_empty[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR == 1 || rank == 0) ptx::mbar_arrive(&tail->tmem_empty[acc]);
+        else ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&tail->tmem_empty[acc]), 0));
+      }
     }
   }
 
   __syncthreads();
+  if (PAIR == 2) ptx::cluster_sync();  // no remote arrive is still in flight to a CTA that exits
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    ptx::tmem_dealloc<PAIR>(tmem_base, TMEM_COLS);
   }
 }
 

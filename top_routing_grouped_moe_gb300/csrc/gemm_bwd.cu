@@ -7,8 +7,10 @@ using namespace gemm;
 
 namespace {
 
+constexpr int kPair = 2;  // expert GEMMs run on CTA pairs
+
 long long mgroup_tile_bound(int rows_total, int G, int N, int n_tile) {
-  return ((long long)rows_total / BM + G) * cdiv_h(N, n_tile);
+  return ((long long)rows_total / PairCfg<kPair>::TILE_M + G) * cdiv_h(N, n_tile);
 }
 
 bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
@@ -26,7 +28,7 @@ bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
   pr.n_tile = 256;
   pr.map_a = ia;
   pr.map_b = ib;
-  pr.tx_bytes = A_BYTES + 4 * MN_BLOCK_BYTES;
+  pr.tx_bytes = A_BYTES + PairCfg<kPair>::B_BYTES;
   pr.out = a.dau_hi;
   pr.out_lo = a.dau_lo;
   pr.ldo = 2LL * a.H;
@@ -66,7 +68,7 @@ bool fill_dgrad_gu(Params& P, Problem& pr, const DgradGuArgs& a) {
   pr.map_b = ig;
   pr.map_b2 = iu;
   pr.ksplit = a.H;
-  pr.tx_bytes = A_BYTES + 4 * MN_BLOCK_BYTES;
+  pr.tx_bytes = A_BYTES + PairCfg<kPair>::B_BYTES;
   pr.out = a.dx;
   pr.ldo = a.d;
   return true;
@@ -95,7 +97,7 @@ bool fill_wgrad(Params& P, Problem& pr, const WgradArgs& a) {
   pr.n_tile = 256;
   pr.map_a = ia;
   pr.map_b = ib;
-  pr.tx_bytes = 2 * MN_BLOCK_BYTES + 4 * MN_BLOCK_BYTES;
+  pr.tx_bytes = A_BYTES + PairCfg<1>::B_BYTES;
   pr.out = a.out;
   pr.out2 = a.out2;
   pr.row_split = a.out2 ? a.row_split : 0;
@@ -118,7 +120,7 @@ cudaError_t gemm_dgrad_down(const DgradDownArgs& routed, const DgradDownArgs* sh
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->H, 256);
     P.num_problems = 2;
   }
-  return launch<0, 1, MGROUP, EPI_SWIGLU_BWD>(P, bound, s);
+  return launch<0, 1, MGROUP, EPI_SWIGLU_BWD, kPair>(P, bound, s);
 }
 
 cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, int* status, cudaStream_t s) {
@@ -133,7 +135,7 @@ cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, 
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->d, 256);
     P.num_problems = 2;
   }
-  return launch<0, 1, MGROUP, EPI_F32>(P, bound, s);
+  return launch<0, 1, MGROUP, EPI_F32, kPair>(P, bound, s);
 }
 
 cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* status, cudaStream_t s) {
@@ -148,7 +150,7 @@ cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* st
     bound += (long long)shared->G * cdiv_h(shared->M, BM) * cdiv_h(shared->N, 256);
     P.num_problems = 2;
   }
-  return launch<1, 1, KGROUP, EPI_BF16>(P, bound, s);
+  return launch<1, 1, KGROUP, EPI_BF16, 1>(P, bound, s);  // ragged K: single CTAs
 }
 
 }  // namespace moe

@@ -6,6 +6,8 @@ using namespace gemm;
 
 namespace {
 
+constexpr int kPair = 2;  // expert GEMMs run on CTA pairs
+
 bool fill_swiglu_fwd(Params& P, Problem& pr, const SwigluFwdArgs& a) {
   const int ia = P.num_maps++, ig = P.num_maps++, iu = P.num_maps++;
   if (!encode_2d(&P.maps[ia], a.a, a.d, a.rows_total, (uint64_t)a.d * 2, 64, BM)) return false;
@@ -22,7 +24,7 @@ bool fill_swiglu_fwd(Params& P, Problem& pr, const SwigluFwdArgs& a) {
   pr.map_a = ia;
   pr.map_b = ig;
   pr.map_b2 = iu;
-  pr.tx_bytes = A_BYTES + 2 * 128 * BK * 2;
+  pr.tx_bytes = A_BYTES + PairCfg<kPair>::B_BYTES;
   pr.out = a.h;
   pr.ldo = a.H;
   pr.aux = a.au;  // fp32
@@ -34,7 +36,7 @@ bool fill_swiglu_fwd(Params& P, Problem& pr, const SwigluFwdArgs& a) {
 bool fill_down_fwd(Params& P, Problem& pr, const DownFwdArgs& a) {
   const int ia = P.num_maps++, ib = P.num_maps++;
   if (!encode_2d(&P.maps[ia], a.h, a.H, a.rows_total, (uint64_t)a.H * 2, 64, BM)) return false;
-  if (!encode_3d(&P.maps[ib], a.Wd, a.H, a.d, a.G, 64, 256)) return false;
+  if (!encode_3d(&P.maps[ib], a.Wd, a.H, a.d, a.G, 64, 256 / kPair)) return false;
   pr = blank_problem();
   pr.offsets = a.offsets;
   pr.G = a.G;
@@ -45,14 +47,14 @@ bool fill_down_fwd(Params& P, Problem& pr, const DownFwdArgs& a) {
   pr.n_tile = 256;
   pr.map_a = ia;
   pr.map_b = ib;
-  pr.tx_bytes = A_BYTES + 256 * BK * 2;
+  pr.tx_bytes = A_BYTES + PairCfg<kPair>::B_BYTES;
   pr.out = a.o;
   pr.ldo = a.d;
   return true;
 }
 
 long long mgroup_tile_bound(int rows_total, int G, int N, int n_tile) {
-  return ((long long)rows_total / BM + G) * cdiv_h(N, n_tile);
+  return ((long long)rows_total / PairCfg<kPair>::TILE_M + G) * cdiv_h(N, n_tile);
 }
 
 }  // namespace
@@ -69,7 +71,7 @@ cudaError_t gemm_swiglu_fwd(const SwigluFwdArgs& routed, const SwigluFwdArgs* sh
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->H, 128);
     P.num_problems = 2;
   }
-  return launch<0, 0, MGROUP, EPI_SWIGLU_FWD>(P, bound, s);
+  return launch<0, 0, MGROUP, EPI_SWIGLU_FWD, kPair>(P, bound, s);
 }
 
 cudaError_t gemm_down_fwd(const DownFwdArgs& routed, const DownFwdArgs* shared, int* status, cudaStream_t s) {
@@ -84,7 +86,7 @@ cudaError_t gemm_down_fwd(const DownFwdArgs& routed, const DownFwdArgs* shared, 
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->d, 256);
     P.num_problems = 2;
   }
-  return launch<0, 0, MGROUP, EPI_F32>(P, bound, s);
+  return launch<0, 0, MGROUP, EPI_F32, kPair>(P, bound, s);
 }
 
 }  // namespace moe

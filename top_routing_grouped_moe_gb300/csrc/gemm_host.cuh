@@ -74,29 +74,68 @@ inline Problem blank_problem() {
   return p;
 }
 
-// Launch a persistent grid (<= one CTA per SM) for `tile_bound` tiles at most.
-template <int AMN, int BMN, int MODE, int EPI>
+// Launch a persistent grid for `tile_bound` tiles at most: one CTA per SM
+// (PAIR = 1), or clusters of two CTAs sized by the number of clusters that can
+// be resident at once (PAIR = 2).
+template <int AMN, int BMN, int MODE, int EPI, int PAIR>
 cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI>;
+  auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR>;
+  constexpr size_t smem = smem_bytes<PAIR>();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static std::mutex mu;
   static unsigned long long configured = 0;  // bit per device
+  static int max_clusters[64] = {0};
   {
     std::lock_guard<std::mutex> lk(mu);
-    if (dev < 64 && !(configured & (1ull << dev))) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!(configured & (1ull << dev))) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;
+      if (PAIR == 2) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        max_clusters[dev] = n > 0 ? n : 1;
+      }
       configured |= 1ull << dev;
     }
   }
   if (tile_bound <= 0) return cudaSuccess;
   P.status = device_status_ptr();
-  int grid = device_sm_count();
-  if (tile_bound < grid) grid = static_cast<int>(tile_bound);
-  kern<<<grid, NUM_THREADS, kSmemBytes, s>>>(P);
-  return cudaGetLastError();
+  if (PAIR == 1) {
+    int grid = device_sm_count();
+    if (tile_bound < grid) grid = static_cast<int>(tile_bound);
+    kern<<<grid, NUM_THREADS, smem, s>>>(P);
+    return cudaGetLastError();
+  }
+  int clusters = max_clusters[dev];
+  if (tile_bound < clusters) clusters = static_cast<int>(tile_bound);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 }  // namespace gemm

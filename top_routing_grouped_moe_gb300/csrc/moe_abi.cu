@@ -283,8 +283,10 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   e = gemm_wgrad(r2, Hs > 0 ? &s2 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
 
-  // 3. dx_perm = [da|du] [W_g; W_u], [da|du] split into bf16 hi + lo
-  DgradGuArgs r3{w + L.dau_hi, w + L.dau_lo, R, offsets, E, d, H, W_g, W_u, dx_perm};
+  // 3. dx_perm = [da|du] [W_g; W_u]
+  // routed rows carry their gate factor (g < 1), so their bf16 da|du error is
+  // small next to the shared expert's; only the shared operand is split
+  DgradGuArgs r3{w + L.dau_hi, nullptr, R, offsets, E, d, H, W_g, W_u, dx_perm};
   DgradGuArgs s3{w + L.s_dau_hi, w + L.s_dau_lo, T, nullptr, 1, d, Hs, Ws_g, Ws_u, dx_s};
   e = gemm_dgrad_gu(r3, Hs > 0 ? &s3 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
