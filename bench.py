@@ -102,6 +102,26 @@ def launches_per_step(w):
 
 
 # ------------------------------------------------------------------ ranks
+def profiled_traffic(workload_name, call):
+    """DRAM bytes per call of `call` from the committed ncu summaries under
+    profiles/, or None when no summary covers this workload or the kernels
+    have changed since it was taken (its source fingerprint differs)."""
+    import glob
+    from top_routing_grouped_moe_gb300 import build
+    fp = build._fingerprint()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        kv, traffic = {}, {}
+        for line in open(path):
+            parts = line.split()
+            if len(parts) == 2 and parts[0] in ("traffic_fingerprint", "traffic_workload"):
+                kv[parts[0]] = parts[1]
+            elif len(parts) == 3 and parts[0] == "traffic_bytes":
+                traffic[parts[1]] = int(parts[2])
+        if kv.get("traffic_fingerprint") == fp and kv.get("traffic_workload") == workload_name and call in traffic:
+            return traffic[call]
+    return None
+
+
 def max_over_ranks(values, device):
     """Element-wise max of a list of floats over all ranks (identity with one
     rank).  The timed region of every rank is compared, the slowest counts."""
@@ -422,7 +442,8 @@ def main_ours(args):
             "gemm_tflops_fwd_bwd": (ffl + bfl) / (total_ms / args.steps / 1000.0) / 1e12,
             "roofline": {"bound": "tensor", "kernel": f"{dom} (tcgen05 grouped GEMM launches)",
                          "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / bf16_peak, 4), "traffic": None,
+                         "frac": round(achieved / bf16_peak, 4), "traffic": profiled_traffic(w.name, dom),
+                         "traffic_unit": "bytes per call (ncu dram read + write)",
                          "peak_source": f"{peak_src} bf16 dense (sustained)"},
             "calls": calls_out,
             "clocks": clocks,
