@@ -22,10 +22,18 @@
 //
 // Split precision (nsplit = 2): one operand is given as a pair of bf16
 // tensors hi + lo (hi = bf16(v), lo = bf16(v - hi), together ~16 mantissa
-// bits); every K step is issued twice, once with each half, into the same
-// fp32 accumulator.  Used where a derived operand feeds a long reduction
-// (weight gradients), so that bf16 rounding of that operand does not grow
-// with the number of rows summed.
+// bits); every K step is issued with each half into the same fp32
+// accumulator.  Used where a derived operand feeds a long reduction (weight
+// gradients), so that bf16 rounding of that operand does not grow with the
+// number of rows summed.  Ragged-M problems load the halves in consecutive
+// stages; ragged-K problems load both halves and the other operand in one
+// stage (32 K rows), so the unsplit operand is read once.
+//
+// Tile schedule: static round-robin (tile t to CTA t mod grid), or, when the
+// launch passes a zeroed tile counter (ragged K), dynamic: each CTA's first
+// tile is its index, later ones come from an atomic counter; the producer
+// publishes each tile index to the MMA and epilogue warps through a small
+// ring in shared memory.  Tiles are numbered heaviest problem first.
 #pragma once
 #include <cuda.h>
 
@@ -47,6 +55,16 @@ constexpr int MAX_G = kMaxE + 1;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) MN-major box: 8 KB
 
+// Ragged-K stage: 32 K rows of A (128 M) | B (256 N) | the lo half of the
+// split operand.  MN-major boxes of 64 (MN) x 32 (K): 4 KB each.
+constexpr int BKK = 32;
+constexpr int KG_BLOCK_BYTES = 64 * BKK * 2;
+constexpr int KG_A_BYTES = 2 * KG_BLOCK_BYTES;
+constexpr int KG_B_BYTES = 4 * KG_BLOCK_BYTES;
+constexpr int KG_STAGE_BYTES = KG_A_BYTES + 2 * KG_B_BYTES;  // 40 KB
+constexpr int KG_STAGES = 5;
+constexpr int RING = 4;  // tile indices in flight from the producer to the other roles
+
 enum Mode : int { MGROUP = 0, KGROUP = 1 };
 enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3, EPI_REDUCE_DX = 4 };
 
@@ -61,6 +79,7 @@ struct Problem {
   int ksplit;          // MN-major B: k >= ksplit reads map_b2 at k - ksplit (0 = off)
   int map_a_lo, map_b_lo;  // lo halves of a split operand (-1 = none)
   int nsplit;          // 1, or 2 = every K step issued with the hi and the lo half
+  int blk3d;           // ragged K: A, B (and lo) maps are 64-column block views, one box per operand
   uint32_t tx_bytes;   // bytes landing per stage
   // epilogue
   void* out;
@@ -93,6 +112,7 @@ struct Params {
   int num_problems;
   int num_maps;
   int* status;
+  int* tile_counter;  // zeroed device int: dynamic schedule (ragged K); NULL: static
 };
 
 struct Sched {
@@ -119,15 +139,24 @@ struct SmemTailT {
   uint64_t empty[STG];     // stage consumed by the MMAs (both CTAs, PAIR = 2)
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
+  uint64_t ring_full[RING];   // dynamic schedule: tile index published
+  uint64_t ring_empty[RING];  // ... and read by the MMA warp and the four epilogue warps
+  int ring[RING];
   uint32_t tmem_base;
   int abort_flag;
   Sched sched;
 };
 
-template <int PAIR>
+template <int MODE, int PAIR>
+struct StageCfg {
+  static constexpr int STAGES = MODE == KGROUP ? KG_STAGES : PairCfg<PAIR>::STAGES;
+  static constexpr int BYTES = MODE == KGROUP ? KG_STAGE_BYTES : A_BYTES + PairCfg<PAIR>::B_BYTES;
+};
+
+template <int MODE, int PAIR>
 constexpr size_t smem_bytes() {
-  return 1024 + PairCfg<PAIR>::STAGES * (A_BYTES + PairCfg<PAIR>::B_BYTES) +
-         sizeof(SmemTailT<PairCfg<PAIR>::STAGES>);
+  return 1024 + StageCfg<MODE, PAIR>::STAGES * StageCfg<MODE, PAIR>::BYTES +
+         sizeof(SmemTailT<StageCfg<MODE, PAIR>::STAGES>);
 }
 
 struct TileInfo {
@@ -175,7 +204,7 @@ __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int 
     ti.n0 = n_idx * pr.n_tile;
     ti.k0 = S.off[p][g];
     ti.k1 = S.off[p][g + 1];
-    ti.nk = cdiv(ti.k1 - ti.k0, BK) * pr.nsplit;
+    ti.nk = cdiv(ti.k1 - ti.k0, BKK);
   }
   return ti;
 }
@@ -327,21 +356,37 @@ __device__ __forceinline__ void load_3d(void* dst, const CUtensorMap* m, uint64_
   else ptx::tma_load_3d_pair(dst, m, bar_leader, c0, c1, c2);
 }
 
+// Ragged K: rows [valid, valid + nrows) of `nblk` consecutive 64 x 32 boxes
+// at `base` belong to the next group (or lie past the end); zero them, whole
+// 128-byte rows (the swizzle permutes within a row only).  One full warp.
+__device__ __forceinline__ void zero_box_rows(uint8_t* base, int nblk, int valid, int nrows, int lane) {
+  const int per_blk = nrows * 8;  // 16-byte chunks
+  for (int c = lane; c < per_blk * nblk; c += 32) {
+    const int blk = c / per_blk;
+    const int w = c - blk * per_blk;
+    *reinterpret_cast<uint4*>(base + blk * KG_BLOCK_BYTES + (valid + (w >> 3)) * 128 + (w & 7) * 16) =
+        make_uint4(0, 0, 0, 0);
+  }
+}
+
 template <int AMN, int BMN, int MODE, int EPI, int PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params P) {
-  // ragged-K problems zero tail rows in shared memory before the MMAs; with a
-  // CTA pair the peer's rows could not be zeroed in time, so they stay single
+  // ragged-K problems zero tail rows in shared memory before the MMAs, which
+  // a CTA pair cannot do for the peer's rows without a round trip, so they
+  // run on single CTAs
   static_assert(!(MODE == KGROUP && PAIR == 2), "ragged-K GEMMs run on single CTAs");
+  static_assert(MODE == MGROUP || (AMN == 1 && BMN == 1), "ragged-K operands are MN-major");
   using Cfg = PairCfg<PAIR>;
-  constexpr int STAGES = Cfg::STAGES;
+  constexpr int STAGES = StageCfg<MODE, PAIR>::STAGES;
   constexpr int B_BYTES = Cfg::B_BYTES;
   constexpr int TILE_M = Cfg::TILE_M;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // ragged M: A ring then B ring; ragged K: stage s at smem + s * KG_STAGE_BYTES
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   using Tail = SmemTailT<STAGES>;
-  Tail* tail = reinterpret_cast<Tail*>(smem + STAGES * (A_BYTES + B_BYTES));
+  Tail* tail = reinterpret_cast<Tail*>(smem + STAGES * StageCfg<MODE, PAIR>::BYTES);
   Sched& S = tail->sched;
   volatile int* abort_flag = &tail->abort_flag;
 
@@ -362,6 +407,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       ptx::mbar_init(&tail->tmem_full[a], 1);
       ptx::mbar_init(&tail->tmem_empty[a], 4 * PAIR);  // one arrival per epilogue warp of each CTA
     }
+    for (int r = 0; r < RING; ++r) {
+      ptx::mbar_init(&tail->ring_full[r], 1);
+      ptx::mbar_init(&tail->ring_empty[r], 5);  // the MMA warp and the four epilogue warps
+    }
     tail->abort_flag = 0;
     ptx::fence_mbarrier_init();
   }
@@ -379,6 +428,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
   const uint32_t tmem_base = tail->tmem_base;
   const int total = S.tile_start[P.num_problems];
   const int row_half = rank * BM;  // this CTA's first row (or M column) within a tile
+  const bool dyn = MODE == KGROUP && P.tile_counter != nullptr;
+
+  // The i-th tile of this CTA, for the MMA and epilogue warps (whole warp):
+  // static, or read from the ring the producer fills.  False on timeout.
+  auto take_tile = [&](int i, int& t) -> bool {
+    if (!dyn) {
+      t = tile0 + i * tile_step;
+      return true;
+    }
+    const int slot = i & (RING - 1);
+    if (!ptx::mbar_wait_bounded(&tail->ring_full[slot], (i / RING) & 1, abort_flag, kWaitLimitNs)) return false;
+    t = *reinterpret_cast<volatile int*>(&tail->ring[slot]);
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&tail->ring_empty[slot]);
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -388,7 +453,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       uint32_t issued_phase_mask = 0;  // bit s: parity of the last load issued into stage s
       uint32_t issued_any = 0;
       bool ok = true;
-      for (int t = tile0; t < total && ok; t += tile_step) {
+      int fetched = 0;
+      for (int i = 0; ok; ++i) {
+        int t;
+        if (dyn) {
+          // publish this tile's index, then fetch the next one (its latency
+          // is hidden behind this tile's loads)
+          const int slot = i & (RING - 1);
+          if (!ptx::mbar_wait_bounded(&tail->ring_empty[slot], ((i / RING) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          t = i == 0 ? tile0 : fetched;
+          *reinterpret_cast<volatile int*>(&tail->ring[slot]) = t;
+          ptx::mbar_arrive(&tail->ring_full[slot]);
+          if (t >= total) break;
+          fetched = atomicAdd(P.tile_counter, 1) + tile_step;
+        } else {
+          t = tile0 + i * tile_step;
+          if (t >= total) break;
+        }
         TileInfo ti = decode<MODE, TILE_M>(P, S, t);
         const Problem& pr = P.prob[ti.p];
         const CUtensorMap* mA = &P.maps[pr.map_a];
@@ -402,33 +486,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           if (rank == 0) ptx::mbar_arrive_expect_tx(fb, pr.tx_bytes * PAIR);
           issued_any |= 1u << stage;
           issued_phase_mask = (issued_phase_mask & ~(1u << stage)) | (phase << stage);
-          const int part = pr.nsplit == 2 ? (kb & 1) : 0;
-          const int k = ti.k0 + (pr.nsplit == 2 ? (kb >> 1) : kb) * BK;
-          uint8_t* a_dst = sA + stage * A_BYTES;
-          uint8_t* b_dst = sB + stage * B_BYTES;
-          const CUtensorMap* mAk = (part && pr.map_a_lo >= 0) ? &P.maps[pr.map_a_lo] : mA;
-          const int am = ti.m0 + row_half;
-          if (AMN == 0) {
-            load_2d<PAIR>(a_dst, mAk, fb, fbl, k, am);
-          } else {
-            load_2d<PAIR>(a_dst, mAk, fb, fbl, am, k);
-            load_2d<PAIR>(a_dst + MN_BLOCK_BYTES, mAk, fb, fbl, am + 64, k);
-          }
-          if (EPI == EPI_SWIGLU_FWD) {
-            // B tile = [128 rows of W_g ; 128 rows of W_u]; with a CTA pair
-            // each CTA holds one of the two halves
-            if (PAIR == 1) {
-              load_3d<PAIR>(b_dst, &P.maps[pr.map_b], fb, fbl, k, ti.n0, ti.g);
-              load_3d<PAIR>(b_dst + (B_BYTES / 2), &P.maps[pr.map_b2], fb, fbl, k, ti.n0, ti.g);
+          if (MODE == KGROUP) {
+            // A (2 blocks) | B (n_tile / 64 blocks) | lo half of A or of B
+            const int k = ti.k0 + kb * BKK;
+            uint8_t* st = smem + stage * KG_STAGE_BYTES;
+            const int nblk = pr.n_tile / 64;
+            const CUtensorMap* mB = &P.maps[pr.map_b];
+            uint8_t* lo = st + KG_A_BYTES + KG_B_BYTES;
+            if (pr.blk3d) {
+              // one instruction per operand (a TMA load's issue cost barely
+              // depends on its size)
+              ptx::tma_load_3d(st, mA, fb, 0, k, ti.m0 / 64);
+              ptx::tma_load_3d(st + KG_A_BYTES, mB, fb, 0, k, ti.n0 / 64);
+              if (pr.map_a_lo >= 0) ptx::tma_load_3d(lo, &P.maps[pr.map_a_lo], fb, 0, k, ti.m0 / 64);
+              else if (pr.map_b_lo >= 0) ptx::tma_load_3d(lo, &P.maps[pr.map_b_lo], fb, 0, k, ti.n0 / 64);
             } else {
-              load_3d<PAIR>(b_dst, &P.maps[rank == 0 ? pr.map_b : pr.map_b2], fb, fbl, k, ti.n0, ti.g);
+              ptx::tma_load_2d(st, mA, fb, ti.m0, k);
+              ptx::tma_load_2d(st + KG_BLOCK_BYTES, mA, fb, ti.m0 + 64, k);
+              for (int j = 0; j < nblk; ++j)
+                ptx::tma_load_2d(st + KG_A_BYTES + j * KG_BLOCK_BYTES, mB, fb, ti.n0 + 64 * j, k);
+              if (pr.map_a_lo >= 0) {
+                ptx::tma_load_2d(lo, &P.maps[pr.map_a_lo], fb, ti.m0, k);
+                ptx::tma_load_2d(lo + KG_BLOCK_BYTES, &P.maps[pr.map_a_lo], fb, ti.m0 + 64, k);
+              } else if (pr.map_b_lo >= 0) {
+                for (int j = 0; j < nblk; ++j)
+                  ptx::tma_load_2d(lo + j * KG_BLOCK_BYTES, &P.maps[pr.map_b_lo], fb, ti.n0 + 64 * j, k);
+              }
             }
-          } else if (BMN == 0) {
-            load_3d<PAIR>(b_dst, &P.maps[pr.map_b], fb, fbl, k, ti.n0 + row_half, ti.g);
           } else {
-            const int nblk = pr.n_tile / 64 / PAIR;
-            const int bn = ti.n0 + row_half;
-            if (MODE == MGROUP) {
+            const int part = pr.nsplit == 2 ? (kb & 1) : 0;
+            const int k = ti.k0 + (pr.nsplit == 2 ? (kb >> 1) : kb) * BK;
+            uint8_t* a_dst = sA + stage * A_BYTES;
+            uint8_t* b_dst = sB + stage * B_BYTES;
+            const CUtensorMap* mAk = (part && pr.map_a_lo >= 0) ? &P.maps[pr.map_a_lo] : mA;
+            const int am = ti.m0 + row_half;
+            if (AMN == 0) {
+              load_2d<PAIR>(a_dst, mAk, fb, fbl, k, am);
+            } else {
+              load_2d<PAIR>(a_dst, mAk, fb, fbl, am, k);
+              load_2d<PAIR>(a_dst + MN_BLOCK_BYTES, mAk, fb, fbl, am + 64, k);
+            }
+            if (EPI == EPI_SWIGLU_FWD) {
+              // B tile = [128 rows of W_g ; 128 rows of W_u]; with a CTA pair
+              // each CTA holds one of the two halves
+              if (PAIR == 1) {
+                load_3d<PAIR>(b_dst, &P.maps[pr.map_b], fb, fbl, k, ti.n0, ti.g);
+                load_3d<PAIR>(b_dst + (B_BYTES / 2), &P.maps[pr.map_b2], fb, fbl, k, ti.n0, ti.g);
+              } else {
+                load_3d<PAIR>(b_dst, &P.maps[rank == 0 ? pr.map_b : pr.map_b2], fb, fbl, k, ti.n0, ti.g);
+              }
+            } else if (BMN == 0) {
+              load_3d<PAIR>(b_dst, &P.maps[pr.map_b], fb, fbl, k, ti.n0 + row_half, ti.g);
+            } else {
+              const int nblk = pr.n_tile / 64 / PAIR;
+              const int bn = ti.n0 + row_half;
               const CUtensorMap* mB = &P.maps[pr.map_b];
               int kk = k;
               if (pr.ksplit > 0 && k >= pr.ksplit) {
@@ -436,9 +547,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
                 kk = k - pr.ksplit;
               }
               for (int j = 0; j < nblk; ++j) load_3d<PAIR>(b_dst + j * MN_BLOCK_BYTES, mB, fb, fbl, bn + 64 * j, kk, ti.g);
-            } else {
-              const CUtensorMap* mB = (part && pr.map_b_lo >= 0) ? &P.maps[pr.map_b_lo] : &P.maps[pr.map_b];
-              for (int j = 0; j < nblk; ++j) load_2d<PAIR>(b_dst + j * MN_BLOCK_BYTES, mB, fb, fbl, bn + 64 * j, k);
             }
           }
           if (++stage == STAGES) {
@@ -467,8 +575,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    int it = 0;
-    for (int t = tile0; t < total && ok && rank == 0; t += tile_step, ++it) {
+    for (int it = 0; ok && rank == 0; ++it) {
+      int t;
+      if (!take_tile(it, t)) {
+        ok = false;
+        break;
+      }
+      if (t >= total) break;
       TileInfo ti = decode<MODE, TILE_M>(P, S, t);
       const Problem& pr = P.prob[ti.p];
       const int acc = it & 1;
@@ -480,50 +593,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       const uint32_t idesc = ptx::idesc_bf16(TILE_M, pr.mma_n, AMN, BMN);
-      const int b_blocks = pr.n_tile / 64 / PAIR;
       for (int kb = 0; kb < ti.nk; ++kb) {
         if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        int valid = BK;
-        if (MODE == KGROUP) valid = min(BK, ti.k1 - (ti.k0 + (pr.nsplit == 2 ? (kb >> 1) : kb) * BK));
-        const int nsub = (valid + UMMA_K - 1) / UMMA_K;
-        uint8_t* a_st = sA + stage * A_BYTES;
-        uint8_t* b_st = sB + stage * B_BYTES;
-        if (MODE == KGROUP && valid < nsub * UMMA_K) {
-          // rows [valid, nsub*16) of this K step belong to the next group:
-          // zero them in both operands (whole 128-byte rows, so the swizzle
-          // pattern does not matter)
-          const int nrows = nsub * UMMA_K - valid;
-          const int chunks_per_blk = nrows * 8;  // 16-byte chunks
-          const int nblk = 2 + b_blocks;
-          for (int c = lane; c < chunks_per_blk * nblk; c += 32) {
-            int blk = c / chunks_per_blk;
-            int w = c - blk * chunks_per_blk;
-            int r = valid + (w >> 3);
-            uint8_t* base = blk < 2 ? a_st + blk * MN_BLOCK_BYTES : b_st + (blk - 2) * MN_BLOCK_BYTES;
-            *reinterpret_cast<uint4*>(base + r * 128 + (w & 7) * 16) = make_uint4(0, 0, 0, 0);
+        if (MODE == KGROUP) {
+          // 32 K rows: per 16-row sub-step one MMA, plus one with the lo half
+          // of the split operand
+          uint8_t* st = smem + stage * KG_STAGE_BYTES;
+          const int valid = min(BKK, ti.k1 - (ti.k0 + kb * BKK));
+          const int nsub = (valid + UMMA_K - 1) / UMMA_K;
+          const int nblk = pr.n_tile / 64;
+          const bool a_lo = pr.map_a_lo >= 0, b_lo = !a_lo && pr.map_b_lo >= 0;
+          if (valid < nsub * UMMA_K) {
+            const int nrows = nsub * UMMA_K - valid;
+            zero_box_rows(st, 2, valid, nrows, lane);
+            zero_box_rows(st + KG_A_BYTES, nblk, valid, nrows, lane);
+            zero_box_rows(st + KG_A_BYTES + KG_B_BYTES, a_lo ? 2 : (b_lo ? nblk : 0), valid, nrows, lane);
+            ptx::fence_proxy_async_smem();
           }
-          ptx::fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t a_addr = ptx::smem_u32(a_st);
-          const uint32_t b_addr = ptx::smem_u32(b_st);
-          for (int s = 0; s < nsub; ++s) {
-            const uint64_t ad = AMN ? ptx::smem_desc(a_addr + s * 2048, MN_BLOCK_BYTES, 1024)
-                                    : ptx::smem_desc(a_addr + s * 32, 16, 1024);
-            const uint64_t bd = BMN ? ptx::smem_desc(b_addr + s * 2048, MN_BLOCK_BYTES, 1024)
-                                    : ptx::smem_desc(b_addr + s * 32, 16, 1024);
-            if (PAIR == 1) ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
-            else ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t sa = ptx::smem_u32(st), sb = sa + KG_A_BYTES, sl = sb + KG_B_BYTES;
+            for (int s = 0; s < nsub; ++s) {
+              const uint64_t ad = ptx::smem_desc(sa + s * 2048, KG_BLOCK_BYTES, 1024);
+              const uint64_t bd = ptx::smem_desc(sb + s * 2048, KG_BLOCK_BYTES, 1024);
+              ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+              if (a_lo) ptx::mma_bf16(d_tmem, ptx::smem_desc(sl + s * 2048, KG_BLOCK_BYTES, 1024), bd, idesc, 1u);
+              if (b_lo) ptx::mma_bf16(d_tmem, ad, ptx::smem_desc(sl + s * 2048, KG_BLOCK_BYTES, 1024), idesc, 1u);
+            }
+            ptx::mma_commit(&tail->empty[stage]);
           }
-          if (PAIR == 1) ptx::mma_commit(&tail->empty[stage]);
-          else ptx::mma_commit_pair(&tail->empty[stage], 0x3);
+          __syncwarp();
+        } else {
+          const int nsub = BK / UMMA_K;
+          uint8_t* a_st = sA + stage * A_BYTES;
+          uint8_t* b_st = sB + stage * B_BYTES;
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t a_addr = ptx::smem_u32(a_st);
+            const uint32_t b_addr = ptx::smem_u32(b_st);
+            for (int s = 0; s < nsub; ++s) {
+              const uint64_t ad = AMN ? ptx::smem_desc(a_addr + s * 2048, MN_BLOCK_BYTES, 1024)
+                                      : ptx::smem_desc(a_addr + s * 32, 16, 1024);
+              const uint64_t bd = BMN ? ptx::smem_desc(b_addr + s * 2048, MN_BLOCK_BYTES, 1024)
+                                      : ptx::smem_desc(b_addr + s * 32, 16, 1024);
+              if (PAIR == 1) ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+              else ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+            }
+            if (PAIR == 1) ptx::mma_commit(&tail->empty[stage]);
+            else ptx::mma_commit_pair(&tail->empty[stage], 0x3);
+          }
+          __syncwarp();
         }
-        __syncwarp();
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -557,8 +681,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     const unsigned FULL = 0xffffffffu;
     const int rs = lane >> 3;         // row within each group of four
     const int cq = (lane & 7) * 4;    // first of this lane's four columns
-    int it = 0;
-    for (int t = tile0; t < total; t += tile_step, ++it) {
+    for (int it = 0;; ++it) {
+      int t;
+      if (!take_tile(it, t)) {
+        *abort_flag = 1;
+        record_status(P.status, MOE_ERR_TIMEOUT);
+        break;
+      }
+      if (t >= total) break;
       TileInfo ti = decode<MODE, TILE_M>(P, S, t);
       const Problem& pr = P.prob[ti.p];
       const int acc = it & 1;

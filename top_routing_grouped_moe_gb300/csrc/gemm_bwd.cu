@@ -76,18 +76,20 @@ bool fill_dgrad_gu(Params& P, Problem& pr, const DgradGuArgs& a) {
 
 bool fill_wgrad(Params& P, Problem& pr, const WgradArgs& a) {
   const int ia = P.num_maps++, ib = P.num_maps++;
-  if (!encode_2d(&P.maps[ia], a.A, a.M, a.rows_total, (uint64_t)a.M * 2, 64, 64)) return false;
-  if (!encode_2d(&P.maps[ib], a.B, a.N, a.rows_total, (uint64_t)a.N * 2, 64, 64)) return false;
+  // 64-column block views: one TMA box per operand and stage (A: 2 blocks, B: 4)
+  if (!encode_blocks(&P.maps[ia], a.A, a.M, a.rows_total, BKK, 2)) return false;
+  if (!encode_blocks(&P.maps[ib], a.B, a.N, a.rows_total, BKK, 4)) return false;
   pr = blank_problem();
   if (a.A_lo) {
     pr.map_a_lo = P.num_maps++;
-    if (!encode_2d(&P.maps[pr.map_a_lo], a.A_lo, a.M, a.rows_total, (uint64_t)a.M * 2, 64, 64)) return false;
+    if (!encode_blocks(&P.maps[pr.map_a_lo], a.A_lo, a.M, a.rows_total, BKK, 2)) return false;
   }
   if (a.B_lo) {
     pr.map_b_lo = P.num_maps++;
-    if (!encode_2d(&P.maps[pr.map_b_lo], a.B_lo, a.N, a.rows_total, (uint64_t)a.N * 2, 64, 64)) return false;
+    if (!encode_blocks(&P.maps[pr.map_b_lo], a.B_lo, a.N, a.rows_total, BKK, 4)) return false;
   }
   pr.nsplit = (a.A_lo || a.B_lo) ? 2 : 1;
+  pr.blk3d = 1;
   pr.offsets = a.offsets;
   pr.G = a.G;
   pr.extent = a.rows_total;
@@ -97,7 +99,8 @@ bool fill_wgrad(Params& P, Problem& pr, const WgradArgs& a) {
   pr.n_tile = 256;
   pr.map_a = ia;
   pr.map_b = ib;
-  pr.tx_bytes = A_BYTES + PairCfg<1>::B_BYTES;
+  // one ragged-K stage: A (2 blocks), B (4), and the lo half of A (2) or of B (4)
+  pr.tx_bytes = (2 + 4 + (a.A_lo ? 2 : a.B_lo ? 4 : 0)) * KG_BLOCK_BYTES;
   pr.out = a.out;
   pr.out2 = a.out2;
   pr.row_split = a.out2 ? a.row_split : 0;
@@ -138,18 +141,21 @@ cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, 
   return launch<0, 1, MGROUP, EPI_F32, kPair>(P, bound, s);
 }
 
-cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* status, cudaStream_t s) {
+cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* tile_counter, int* status,
+                       cudaStream_t s) {
   (void)status;
   Params P;
   std::memset(&P, 0, sizeof(P));
-  if (!fill_wgrad(P, P.prob[0], routed)) return cudaErrorInvalidValue;
-  long long bound = (long long)routed.G * cdiv_h(routed.M, BM) * cdiv_h(routed.N, 256);
-  P.num_problems = 1;
-  if (shared) {
-    if (!fill_wgrad(P, P.prob[1], *shared)) return cudaErrorInvalidValue;
-    bound += (long long)shared->G * cdiv_h(shared->M, BM) * cdiv_h(shared->N, 256);
-    P.num_problems = 2;
+  // the shared expert's tiles (K = all tokens) are numbered first, so the
+  // dynamic schedule starts the heaviest tiles first
+  const WgradArgs* order[2] = {shared ? shared : &routed, shared ? &routed : nullptr};
+  long long bound = 0;
+  for (int i = 0; i < 2 && order[i]; ++i) {
+    if (!fill_wgrad(P, P.prob[i], *order[i])) return cudaErrorInvalidValue;
+    bound += (long long)order[i]->G * cdiv_h(order[i]->M, BM) * cdiv_h(order[i]->N, 256);
+    P.num_problems = i + 1;
   }
+  P.tile_counter = tile_counter;
   return launch<1, 1, KGROUP, EPI_BF16, 1>(P, bound, s);  // ragged K: single CTAs
 }
 

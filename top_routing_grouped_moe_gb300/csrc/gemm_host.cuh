@@ -48,6 +48,24 @@ inline bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t 
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A row-major [rows, cols] bf16 matrix (cols a multiple of 64) seen as 64-column
+// blocks: dims (64, rows, cols / 64), the block index outermost although its
+// stride (128 bytes) is the smallest.  One box of 64 x box_rows x box_blocks
+// lands in shared memory as box_blocks consecutive 64 x box_rows blocks: the
+// MN-major operand layout, in one TMA instruction instead of box_blocks.
+inline bool encode_blocks(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                          uint32_t box_blocks) {
+  EncodeTiledFn f = encode_fn();
+  if (!f || cols % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_blocks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D bf16 map over [d2, d1, d0] (d0 contiguous); box = b0 x b1 x 1.
 inline bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
                       uint32_t b1) {
@@ -80,7 +98,8 @@ inline Problem blank_problem() {
 template <int AMN, int BMN, int MODE, int EPI, int PAIR>
 cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR>;
-  constexpr size_t smem = smem_bytes<PAIR>();
+  constexpr size_t smem = smem_bytes<MODE, PAIR>();
+  static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -115,6 +134,10 @@ cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s) {
   }
   if (tile_bound <= 0) return cudaSuccess;
   P.status = device_status_ptr();
+  if (P.tile_counter) {
+    e = cudaMemsetAsync(P.tile_counter, 0, sizeof(int), s);
+    if (e != cudaSuccess) return e;
+  }
   if (PAIR == 1) {
     int grid = device_sm_count();
     if (tile_bound < grid) grid = static_cast<int>(tile_bound);
