@@ -66,6 +66,9 @@ constexpr int KG_STAGES = 5;
 constexpr int RING = 4;  // tile indices in flight from the producer to the other roles
 
 enum Mode : int { MGROUP = 0, KGROUP = 1 };
+// Ragged K: which operand comes as hi + lo halves (a compile-time choice, so
+// that each kernel issues its MMAs from one straight-line sequence)
+enum Split : int { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2 };
 enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3, EPI_REDUCE_DX = 4 };
 
 struct Problem {
@@ -369,13 +372,14 @@ __device__ __forceinline__ void zero_box_rows(uint8_t* base, int nblk, int valid
   }
 }
 
-template <int AMN, int BMN, int MODE, int EPI, int PAIR>
+template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params P) {
   // ragged-K problems zero tail rows in shared memory before the MMAs, which
   // a CTA pair cannot do for the peer's rows without a round trip, so they
   // run on single CTAs
   static_assert(!(MODE == KGROUP && PAIR == 2), "ragged-K GEMMs run on single CTAs");
   static_assert(MODE == MGROUP || (AMN == 1 && BMN == 1), "ragged-K operands are MN-major");
+  static_assert(MODE == KGROUP || SPLIT == SPLIT_NONE, "ragged-M split operands use consecutive stages");
   using Cfg = PairCfg<PAIR>;
   constexpr int STAGES = StageCfg<MODE, PAIR>::STAGES;
   constexpr int B_BYTES = Cfg::B_BYTES;
@@ -474,52 +478,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           if (t >= total) break;
         }
         TileInfo ti = decode<MODE, TILE_M>(P, S, t);
+        // Everything the stage loop needs, read once per tile: a parameter
+        // read inside the loop would be repeated after every asm statement
+        // (they all clobber memory), which cost as much as the MMAs.
         const Problem& pr = P.prob[ti.p];
+        const uint32_t tx = pr.tx_bytes * PAIR;
+        const int nsplit = pr.nsplit, ksplit = pr.ksplit, blk3d = pr.blk3d;
+        const int nblk = pr.n_tile / 64 / PAIR;
         const CUtensorMap* mA = &P.maps[pr.map_a];
-        for (int kb = 0; kb < ti.nk; ++kb) {
+        const CUtensorMap* mB = &P.maps[pr.map_b];
+        const CUtensorMap* mB2 = &P.maps[pr.map_b2 >= 0 ? pr.map_b2 : pr.map_b];
+        const CUtensorMap* mAlo = pr.map_a_lo >= 0 ? &P.maps[pr.map_a_lo] : nullptr;
+        const CUtensorMap* mBlo = pr.map_b_lo >= 0 ? &P.maps[pr.map_b_lo] : nullptr;
+        const int am = ti.m0 + row_half, bn = ti.n0 + row_half;
+        const int k0 = ti.k0, g = ti.g, nk = ti.nk;
+        for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait_bounded(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
           uint64_t* fb = &tail->full[stage];
           const uint32_t fbl = PAIR == 2 ? ptx::mapa(ptx::smem_u32(fb), 0) : 0u;
-          if (rank == 0) ptx::mbar_arrive_expect_tx(fb, pr.tx_bytes * PAIR);
+          if (rank == 0) ptx::mbar_arrive_expect_tx(fb, tx);
           issued_any |= 1u << stage;
           issued_phase_mask = (issued_phase_mask & ~(1u << stage)) | (phase << stage);
           if (MODE == KGROUP) {
-            // A (2 blocks) | B (n_tile / 64 blocks) | lo half of A or of B
-            const int k = ti.k0 + kb * BKK;
+            // A (2 blocks) | B (nblk blocks) | lo half of A or of B
+            const int k = k0 + kb * BKK;
             uint8_t* st = smem + stage * KG_STAGE_BYTES;
-            const int nblk = pr.n_tile / 64;
-            const CUtensorMap* mB = &P.maps[pr.map_b];
             uint8_t* lo = st + KG_A_BYTES + KG_B_BYTES;
-            if (pr.blk3d) {
+            if (blk3d) {
               // one instruction per operand (a TMA load's issue cost barely
               // depends on its size)
-              ptx::tma_load_3d(st, mA, fb, 0, k, ti.m0 / 64);
-              ptx::tma_load_3d(st + KG_A_BYTES, mB, fb, 0, k, ti.n0 / 64);
-              if (pr.map_a_lo >= 0) ptx::tma_load_3d(lo, &P.maps[pr.map_a_lo], fb, 0, k, ti.m0 / 64);
-              else if (pr.map_b_lo >= 0) ptx::tma_load_3d(lo, &P.maps[pr.map_b_lo], fb, 0, k, ti.n0 / 64);
+              ptx::tma_load_3d(st, mA, fb, 0, k, am / 64);
+              ptx::tma_load_3d(st + KG_A_BYTES, mB, fb, 0, k, bn / 64);
+              if (SPLIT == SPLIT_A) ptx::tma_load_3d(lo, mAlo, fb, 0, k, am / 64);
+              if (SPLIT == SPLIT_B) ptx::tma_load_3d(lo, mBlo, fb, 0, k, bn / 64);
             } else {
-              ptx::tma_load_2d(st, mA, fb, ti.m0, k);
-              ptx::tma_load_2d(st + KG_BLOCK_BYTES, mA, fb, ti.m0 + 64, k);
-              for (int j = 0; j < nblk; ++j)
-                ptx::tma_load_2d(st + KG_A_BYTES + j * KG_BLOCK_BYTES, mB, fb, ti.n0 + 64 * j, k);
-              if (pr.map_a_lo >= 0) {
-                ptx::tma_load_2d(lo, &P.maps[pr.map_a_lo], fb, ti.m0, k);
-                ptx::tma_load_2d(lo + KG_BLOCK_BYTES, &P.maps[pr.map_a_lo], fb, ti.m0 + 64, k);
-              } else if (pr.map_b_lo >= 0) {
-                for (int j = 0; j < nblk; ++j)
-                  ptx::tma_load_2d(lo + j * KG_BLOCK_BYTES, &P.maps[pr.map_b_lo], fb, ti.n0 + 64 * j, k);
+              ptx::tma_load_2d(st, mA, fb, am, k);
+              ptx::tma_load_2d(st + KG_BLOCK_BYTES, mA, fb, am + 64, k);
+              for (int j = 0; j < nblk; ++j) ptx::tma_load_2d(st + KG_A_BYTES + j * KG_BLOCK_BYTES, mB, fb, bn + 64 * j, k);
+              if (SPLIT == SPLIT_A) {
+                ptx::tma_load_2d(lo, mAlo, fb, am, k);
+                ptx::tma_load_2d(lo + KG_BLOCK_BYTES, mAlo, fb, am + 64, k);
+              } else if (SPLIT == SPLIT_B) {
+                for (int j = 0; j < nblk; ++j) ptx::tma_load_2d(lo + j * KG_BLOCK_BYTES, mBlo, fb, bn + 64 * j, k);
               }
             }
           } else {
-            const int part = pr.nsplit == 2 ? (kb & 1) : 0;
-            const int k = ti.k0 + (pr.nsplit == 2 ? (kb >> 1) : kb) * BK;
+            const int part = nsplit == 2 ? (kb & 1) : 0;
+            const int k = k0 + (nsplit == 2 ? (kb >> 1) : kb) * BK;
             uint8_t* a_dst = sA + stage * A_BYTES;
             uint8_t* b_dst = sB + stage * B_BYTES;
-            const CUtensorMap* mAk = (part && pr.map_a_lo >= 0) ? &P.maps[pr.map_a_lo] : mA;
-            const int am = ti.m0 + row_half;
+            const CUtensorMap* mAk = (part && mAlo) ? mAlo : mA;
             if (AMN == 0) {
               load_2d<PAIR>(a_dst, mAk, fb, fbl, k, am);
             } else {
@@ -530,23 +541,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
               // B tile = [128 rows of W_g ; 128 rows of W_u]; with a CTA pair
               // each CTA holds one of the two halves
               if (PAIR == 1) {
-                load_3d<PAIR>(b_dst, &P.maps[pr.map_b], fb, fbl, k, ti.n0, ti.g);
-                load_3d<PAIR>(b_dst + (B_BYTES / 2), &P.maps[pr.map_b2], fb, fbl, k, ti.n0, ti.g);
+                load_3d<PAIR>(b_dst, mB, fb, fbl, k, ti.n0, g);
+                load_3d<PAIR>(b_dst + (B_BYTES / 2), mB2, fb, fbl, k, ti.n0, g);
               } else {
-                load_3d<PAIR>(b_dst, &P.maps[rank == 0 ? pr.map_b : pr.map_b2], fb, fbl, k, ti.n0, ti.g);
+                load_3d<PAIR>(b_dst, rank == 0 ? mB : mB2, fb, fbl, k, ti.n0, g);
               }
             } else if (BMN == 0) {
-              load_3d<PAIR>(b_dst, &P.maps[pr.map_b], fb, fbl, k, ti.n0 + row_half, ti.g);
+              load_3d<PAIR>(b_dst, mB, fb, fbl, k, bn, g);
             } else {
-              const int nblk = pr.n_tile / 64 / PAIR;
-              const int bn = ti.n0 + row_half;
-              const CUtensorMap* mB = &P.maps[pr.map_b];
-              int kk = k;
-              if (pr.ksplit > 0 && k >= pr.ksplit) {
-                mB = &P.maps[pr.map_b2];
-                kk = k - pr.ksplit;
-              }
-              for (int j = 0; j < nblk; ++j) load_3d<PAIR>(b_dst + j * MN_BLOCK_BYTES, mB, fb, fbl, bn + 64 * j, kk, ti.g);
+              const bool second = ksplit > 0 && k >= ksplit;
+              const CUtensorMap* mBk = second ? mB2 : mB;
+              const int kk = second ? k - ksplit : k;
+              for (int j = 0; j < nblk; ++j) load_3d<PAIR>(b_dst + j * MN_BLOCK_BYTES, mBk, fb, fbl, bn + 64 * j, kk, g);
             }
           }
           if (++stage == STAGES) {
@@ -592,26 +598,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
+      // per-tile values in registers (see the producer)
       const uint32_t idesc = ptx::idesc_bf16(TILE_M, pr.mma_n, AMN, BMN);
-      for (int kb = 0; kb < ti.nk; ++kb) {
+      const int nk = ti.nk, k_left = ti.k1 - ti.k0;
+      const int nblk_k = pr.n_tile / 64;
+      constexpr bool a_lo = SPLIT == SPLIT_A, b_lo = SPLIT == SPLIT_B;
+      for (int kb = 0; kb < nk; ++kb) {
         if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        if (MODE == KGROUP) {
-          // 32 K rows: per 16-row sub-step one MMA, plus one with the lo half
-          // of the split operand
+        if (MODE == KGROUP && (kb + 1) * BKK <= k_left) {
+          // full 32-row step: straight-line issue, two 16-row sub-steps
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t sa = ptx::smem_u32(smem + stage * KG_STAGE_BYTES), sb = sa + KG_A_BYTES,
+                           sl = sb + KG_B_BYTES;
+            const uint64_t a0 = ptx::smem_desc(sa, KG_BLOCK_BYTES, 1024), a1 = ptx::smem_desc(sa + 2048, KG_BLOCK_BYTES, 1024);
+            const uint64_t b0 = ptx::smem_desc(sb, KG_BLOCK_BYTES, 1024), b1 = ptx::smem_desc(sb + 2048, KG_BLOCK_BYTES, 1024);
+            const uint64_t l0 = ptx::smem_desc(sl, KG_BLOCK_BYTES, 1024), l1 = ptx::smem_desc(sl + 2048, KG_BLOCK_BYTES, 1024);
+            const uint32_t acc0 = kb != 0 ? 1u : 0u;
+            if (SPLIT == SPLIT_A) {
+              ptx::mma_bf16(d_tmem, a0, b0, idesc, acc0);
+              ptx::mma_bf16(d_tmem, l0, b0, idesc, 1u);
+              ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
+              ptx::mma_bf16(d_tmem, l1, b1, idesc, 1u);
+            } else if (SPLIT == SPLIT_B) {
+              ptx::mma_bf16(d_tmem, a0, b0, idesc, acc0);
+              ptx::mma_bf16(d_tmem, a0, l0, idesc, 1u);
+              ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
+              ptx::mma_bf16(d_tmem, a1, l1, idesc, 1u);
+            } else {
+              ptx::mma_bf16(d_tmem, a0, b0, idesc, acc0);
+              ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
+            }
+            ptx::mma_commit(&tail->empty[stage]);
+          }
+          __syncwarp();
+        } else if (MODE == KGROUP) {
+          // the group's last step: rows past its end are zeroed first
           uint8_t* st = smem + stage * KG_STAGE_BYTES;
-          const int valid = min(BKK, ti.k1 - (ti.k0 + kb * BKK));
+          const int valid = min(BKK, k_left - kb * BKK);
           const int nsub = (valid + UMMA_K - 1) / UMMA_K;
-          const int nblk = pr.n_tile / 64;
-          const bool a_lo = pr.map_a_lo >= 0, b_lo = !a_lo && pr.map_b_lo >= 0;
           if (valid < nsub * UMMA_K) {
             const int nrows = nsub * UMMA_K - valid;
             zero_box_rows(st, 2, valid, nrows, lane);
-            zero_box_rows(st + KG_A_BYTES, nblk, valid, nrows, lane);
-            zero_box_rows(st + KG_A_BYTES + KG_B_BYTES, a_lo ? 2 : (b_lo ? nblk : 0), valid, nrows, lane);
+            zero_box_rows(st + KG_A_BYTES, nblk_k, valid, nrows, lane);
+            zero_box_rows(st + KG_A_BYTES + KG_B_BYTES, a_lo ? 2 : (b_lo ? nblk_k : 0), valid, nrows, lane);
             ptx::fence_proxy_async_smem();
           }
           __syncwarp();
@@ -629,12 +663,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           __syncwarp();
         } else {
           const int nsub = BK / UMMA_K;
-          uint8_t* a_st = sA + stage * A_BYTES;
-          uint8_t* b_st = sB + stage * B_BYTES;
           __syncwarp();
           if (lane == 0) {
-            const uint32_t a_addr = ptx::smem_u32(a_st);
-            const uint32_t b_addr = ptx::smem_u32(b_st);
+            const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);
+            const uint32_t b_addr = ptx::smem_u32(sB + stage * B_BYTES);
             for (int s = 0; s < nsub; ++s) {
               const uint64_t ad = AMN ? ptx::smem_desc(a_addr + s * 2048, MN_BLOCK_BYTES, 1024)
                                       : ptx::smem_desc(a_addr + s * 32, 16, 1024);
@@ -655,7 +687,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       }
       if (!ok) break;
       if (lane == 0) {
-        if (ti.nk > 0) {
+        if (nk > 0) {
           if (PAIR == 1) ptx::mma_commit(&tail->tmem_full[acc]);
           else ptx::mma_commit_pair(&tail->tmem_full[acc], 0x3);
         } else {

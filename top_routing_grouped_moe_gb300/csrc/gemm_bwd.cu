@@ -156,7 +156,12 @@ cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* ti
     P.num_problems = i + 1;
   }
   P.tile_counter = tile_counter;
-  return launch<1, 1, KGROUP, EPI_BF16, 1>(P, bound, s);  // ragged K: single CTAs
+  // ragged K: single CTAs; both problems split the same operand
+  if (shared && (!shared->A_lo != !routed.A_lo || !shared->B_lo != !routed.B_lo)) return cudaErrorInvalidValue;
+  if (routed.A_lo && routed.B_lo) return cudaErrorInvalidValue;
+  if (routed.A_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_A>(P, bound, s);
+  if (routed.B_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_B>(P, bound, s);
+  return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_NONE>(P, bound, s);
 }
 
 }  // namespace moe

@@ -95,9 +95,9 @@ inline Problem blank_problem() {
 // Launch a persistent grid for `tile_bound` tiles at most: one CTA per SM
 // (PAIR = 1), or clusters of two CTAs sized by the number of clusters that can
 // be resident at once (PAIR = 2).
-template <int AMN, int BMN, int MODE, int EPI, int PAIR>
+template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT = SPLIT_NONE>
 cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR>;
+  auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR, SPLIT>;
   constexpr size_t smem = smem_bytes<MODE, PAIR>();
   static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   int dev = 0;

@@ -67,7 +67,7 @@ cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const v
   pr.ldo = d;
   pr.gstride = (long long)E * d;
   P.num_problems = 1;
-  return launch<1, 1, KGROUP, EPI_F32, 1>(P, (long long)S * cdiv_h(E, BM) * cdiv_h(d, 256), s);
+  return launch<1, 1, KGROUP, EPI_F32, 1, SPLIT_A>(P, (long long)S * cdiv_h(E, BM) * cdiv_h(d, 256), s);
 }
 
 cudaError_t gemm_router_dx_reduce(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, const float* dx_perm,
