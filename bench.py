@@ -212,11 +212,12 @@ def run_oracle_step(w, f64, n_tokens):
 
 def cpu_baseline(w, inp, n_tokens, steps=1):
     from oracle import moe_oracle as orc
+    n_tokens = min(n_tokens, w.T)
     f64 = orc.inputs_to_f64(oracle_sample(w, inp, n_tokens))
     times = [run_oracle_step(w, f64, n_tokens) for _ in range(steps)]
     t = statistics.median(times)
     return {"value": n_tokens / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"first {n_tokens} of {w.T} tokens of {w.name}, forward+backward, float64 numpy "
+            "sample": f"{n_tokens} of {w.T} tokens of {w.name} (the first), forward+backward, float64 numpy "
                       f"(BLAS on all {os.cpu_count()} host cores), median of {steps}",
             "seconds": t}
 
@@ -230,7 +231,7 @@ def main_reference(args):
                          zipf_bias=w.zipf_bias, capacity_factor=w.capacity_factor, backward=True)
     inp = workloads.make_inputs(w)
     from oracle import moe_oracle as orc
-    n = args.cpu_sample_tokens
+    n = min(args.cpu_sample_tokens, w.T)
     f64 = orc.inputs_to_f64(oracle_sample(w, inp, n))
     for _ in range(args.warmup):
         run_oracle_step(w, f64, n)
@@ -246,7 +247,7 @@ def main_reference(args):
                    "routing": w.routing, "capacity": w.capacity, "pass": "forward+backward",
                    "sample_tokens": n},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"first {n} of {w.T} tokens per step, forward+backward, float64 numpy"},
+                         "sample": f"{n} of {w.T} tokens per step (the first), forward+backward, float64 numpy"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
