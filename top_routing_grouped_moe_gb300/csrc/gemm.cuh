@@ -107,6 +107,7 @@ struct Problem {
   void* gh_lo;
   float* dgp;              // per-row partials of the gate gradient, [rows, ld_dgp] (nullable)
   int ld_dgp;
+  int map_aux;             // tensor map of au (fp32, 32 x 32 boxes): a | u staged by TMA
 };
 
 struct Params {
@@ -142,6 +143,7 @@ struct SmemTailT {
   uint64_t empty[STG];     // stage consumed by the MMAs (both CTAs, PAIR = 2)
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
+  uint64_t au_full[4][2];     // SwiGLU backward: a | u chunk landed (per epilogue warp, 2 buffers)
   uint64_t ring_full[RING];   // dynamic schedule: tile index published
   uint64_t ring_empty[RING];  // ... and read by the MMA warp and the four epilogue warps
   int ring[RING];
@@ -150,16 +152,22 @@ struct SmemTailT {
   Sched sched;
 };
 
-template <int MODE, int PAIR>
+// SwiGLU backward: per epilogue warp, two buffers of one 32-row x 32-column
+// chunk of a and of u (fp32), filled by TMA; the main loop gives up two
+// stages for them (it is not what bounds that launch)
+constexpr int AU_CHUNK_BYTES = 2 * 32 * 32 * 4;
+
+template <int MODE, int EPI, int PAIR>
 struct StageCfg {
-  static constexpr int STAGES = MODE == KGROUP ? KG_STAGES : PairCfg<PAIR>::STAGES;
+  static constexpr int STAGES = MODE == KGROUP ? KG_STAGES : (EPI == EPI_SWIGLU_BWD ? 4 : PairCfg<PAIR>::STAGES);
   static constexpr int BYTES = MODE == KGROUP ? KG_STAGE_BYTES : A_BYTES + PairCfg<PAIR>::B_BYTES;
+  static constexpr int EPI_BYTES = EPI == EPI_SWIGLU_BWD ? 4 * 2 * AU_CHUNK_BYTES : 0;
 };
 
-template <int MODE, int PAIR>
+template <int MODE, int EPI, int PAIR>
 constexpr size_t smem_bytes() {
-  return 1024 + StageCfg<MODE, PAIR>::STAGES * StageCfg<MODE, PAIR>::BYTES +
-         sizeof(SmemTailT<StageCfg<MODE, PAIR>::STAGES>);
+  using C = StageCfg<MODE, EPI, PAIR>;
+  return 1024 + C::STAGES * C::BYTES + C::EPI_BYTES + sizeof(SmemTailT<C::STAGES>);
 }
 
 struct TileInfo {
@@ -381,7 +389,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
   static_assert(MODE == MGROUP || (AMN == 1 && BMN == 1), "ragged-K operands are MN-major");
   static_assert(MODE == KGROUP || SPLIT == SPLIT_NONE, "ragged-M split operands use consecutive stages");
   using Cfg = PairCfg<PAIR>;
-  constexpr int STAGES = StageCfg<MODE, PAIR>::STAGES;
+  using SC = StageCfg<MODE, EPI, PAIR>;
+  constexpr int STAGES = SC::STAGES;
   constexpr int B_BYTES = Cfg::B_BYTES;
   constexpr int TILE_M = Cfg::TILE_M;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -390,7 +399,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   using Tail = SmemTailT<STAGES>;
-  Tail* tail = reinterpret_cast<Tail*>(smem + STAGES * StageCfg<MODE, PAIR>::BYTES);
+  uint8_t* au_buf = smem + STAGES * SC::BYTES;  // SwiGLU backward only
+  Tail* tail = reinterpret_cast<Tail*>(au_buf + SC::EPI_BYTES);
   Sched& S = tail->sched;
   volatile int* abort_flag = &tail->abort_flag;
 
@@ -410,6 +420,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tail->tmem_full[a], 1);
       ptx::mbar_init(&tail->tmem_empty[a], 4 * PAIR);  // one arrival per epilogue warp of each CTA
+    }
+    for (int w = 0; w < 4; ++w) {
+      ptx::mbar_init(&tail->au_full[w][0], 1);
+      ptx::mbar_init(&tail->au_full[w][1], 1);
     }
     for (int r = 0; r < RING; ++r) {
       ptx::mbar_init(&tail->ring_full[r], 1);
@@ -713,6 +727,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     const unsigned FULL = 0xffffffffu;
     const int rs = lane >> 3;         // row within each group of four
     const int cq = (lane & 7) * 4;    // first of this lane's four columns
+    // SwiGLU backward: a | u chunks of this warp's 32 rows arrive by TMA in a
+    // two-buffer ring; au_next counts chunks issued, au_done chunks consumed
+    uint32_t au_next = 0, au_done = 0;
+    uint8_t* au_mine = au_buf + q * 2 * AU_CHUNK_BYTES;
     for (int it = 0;; ++it) {
       int t;
       if (!take_tile(it, t)) {
@@ -725,6 +743,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       const Problem& pr = P.prob[ti.p];
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
+      const int m_cta = ti.m0 + row_half;  // first row (KGROUP: first M index) of this CTA
+      const int row0 = m_cta + q * 32;
+      // SwiGLU backward: chunk c of a | u (columns n0 + 32c of a and of u)
+      const CUtensorMap* m_au = EPI == EPI_SWIGLU_BWD ? &P.maps[pr.map_aux] : nullptr;
+      const int au_H = pr.H;
+      const int au_chunks = EPI == EPI_SWIGLU_BWD ? min(pr.n_tile, pr.N - ti.n0) / 32 : 0;
+      auto au_issue = [&](int c) {
+        const int buf = au_next & 1;
+        if (lane == 0) {
+          uint64_t* bar = &tail->au_full[q][buf];
+          uint8_t* dst = au_mine + buf * AU_CHUNK_BYTES;
+          ptx::mbar_arrive_expect_tx(bar, AU_CHUNK_BYTES);
+          ptx::tma_load_2d(dst, m_au, bar, ti.n0 + 32 * c, row0);
+          ptx::tma_load_2d(dst + AU_CHUNK_BYTES / 2, m_au, bar, au_H + ti.n0 + 32 * c, row0);
+        }
+        ++au_next;
+      };
+      if (EPI == EPI_SWIGLU_BWD) {
+        // the first two chunks load while the main loop still runs
+        for (int c = 0; c < 2 && c < au_chunks; ++c) au_issue(c);
+      }
       if (!ptx::mbar_wait_cluster_bounded(&tail->tmem_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
         *abort_flag = 1;
         record_status(P.status, MOE_ERR_TIMEOUT);
@@ -732,8 +771,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       }
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-      const int m_cta = ti.m0 + row_half;  // first row (KGROUP: first M index) of this CTA
-      const int row0 = m_cta + q * 32;
       const int nrows = max(0, min(32, ti.rows_end - row0));
       const bool has_acc = ti.nk > 0;
 
@@ -812,44 +849,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           gj[j] = __shfl_sync(FULL, g_mine, 4 * j + rs);
           part[j] = 0.0f;
         }
-        const float* aup = reinterpret_cast<const float*>(pr.aux) + (long long)row0 * pr.ld_aux + ti.n0;
-        const long long ro = (long long)row0 * pr.ldo + ti.n0;  // into [rows, 2H]
-        const long long rh = (long long)row0 * pr.H + ti.n0;    // into [rows, H]
+        const int H = au_H;
+        const long long ldo = pr.ldo;
+        const long long ro = (long long)row0 * ldo + ti.n0;  // into [rows, 2H]
+        const long long rh = (long long)row0 * H + ti.n0;    // into [rows, H]
         __nv_bfloat16* dhi = reinterpret_cast<__nv_bfloat16*>(pr.out) + ro;
         __nv_bfloat16* dlo = reinterpret_cast<__nv_bfloat16*>(pr.out_lo) + ro;
         __nv_bfloat16* ghh = reinterpret_cast<__nv_bfloat16*>(pr.gh_hi) + rh;
         __nv_bfloat16* ghl = reinterpret_cast<__nv_bfloat16*>(pr.gh_lo) + rh;
-        const int ncols = min(pr.n_tile, pr.N - ti.n0);
-        // a, u of the next chunk are loaded while the current one is processed
-        float4 na[8], nu[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = 4 * j + rs;
-          if (r < nrows) {
-            na[j] = __ldg(reinterpret_cast<const float4*>(aup + (long long)r * pr.ld_aux + cq));
-            nu[j] = __ldg(reinterpret_cast<const float4*>(aup + (long long)r * pr.ld_aux + pr.H + cq));
+        bool au_ok = true;
+        for (int c = 0; c < au_chunks; ++c) {
+          const int buf = au_done & 1;
+          if (!ptx::mbar_wait_bounded(&tail->au_full[q][buf], (au_done >> 1) & 1, abort_flag, kWaitLimitNs)) {
+            au_ok = false;
+            break;
           }
-        }
-        for (int c0 = 0; c0 < ncols; c0 += 32) {
+          ++au_done;
+          // a, u of this chunk: [32 rows][32 columns] fp32 each, quad layout
+          const float* sa = reinterpret_cast<const float*>(au_mine + buf * AU_CHUNK_BYTES);
+          const float* su = sa + 32 * 32;
           float4 ca[8], cu[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            ca[j] = na[j];
-            cu[j] = nu[j];
+            ca[j] = *reinterpret_cast<const float4*>(sa + (4 * j + rs) * 32 + cq);
+            cu[j] = *reinterpret_cast<const float4*>(su + (4 * j + rs) * 32 + cq);
           }
-          if (c0 + 32 < ncols) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int r = 4 * j + rs;
-              if (r < nrows) {
-                na[j] = __ldg(reinterpret_cast<const float4*>(aup + (long long)r * pr.ld_aux + c0 + 32 + cq));
-                nu[j] = __ldg(reinterpret_cast<const float4*>(aup + (long long)r * pr.ld_aux + pr.H + c0 + 32 + cq));
-              }
-            }
-          }
+          // the buffer is read: chunk c + 2 may overwrite it
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (c + 2 < au_chunks) au_issue(c + 2);
           float4 vd[8];
-          tmem_chunk_quad(taddr + c0, tb, lane, vd);
-          const int c = c0 + cq;
+          tmem_chunk_quad(taddr + 32 * c, tb, lane, vd);
+          const int col = 32 * c + cq;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int r = 4 * j + rs;
@@ -868,13 +899,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
                 du[e] = dh * si;
                 gh[e] = gj[j] * h;
               }
-              const long long o2 = (long long)r * pr.ldo + c;
-              const long long o1 = (long long)r * pr.H + c;
+              const long long o2 = (long long)r * ldo + col;
+              const long long o1 = (long long)r * H + col;
               split_store4(dhi + o2, dlo + o2, make_float4(da[0], da[1], da[2], da[3]));
-              split_store4(dhi + o2 + pr.H, dlo + o2 + pr.H, make_float4(du[0], du[1], du[2], du[3]));
+              split_store4(dhi + o2 + H, dlo + o2 + H, make_float4(du[0], du[1], du[2], du[3]));
               split_store4(ghh + o1, ghl + o1, make_float4(gh[0], gh[1], gh[2], gh[3]));
             }
           }
+        }
+        if (!au_ok) {
+          *abort_flag = 1;
+          record_status(P.status, MOE_ERR_TIMEOUT);
+          break;
         }
         if (pr.dgp) {
           // sum each row's partials over its eight lanes
@@ -955,6 +991,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         if (PAIR == 1 || rank == 0) ptx::mbar_arrive(&tail->tmem_empty[acc]);
         else ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&tail->tmem_empty[acc]), 0));
       }
+    }
+    // after an abort: let a | u copies still in flight land before the CTA's
+    // shared memory goes away
+    if (EPI == EPI_SWIGLU_BWD) {
+      volatile int never = 0;
+      for (; au_done < au_next; ++au_done)
+        ptx::mbar_wait_bounded(&tail->au_full[q][au_done & 1], (au_done >> 1) & 1, &never, 100000000ull);
     }
   }
 

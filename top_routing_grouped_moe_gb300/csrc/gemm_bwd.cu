@@ -42,6 +42,10 @@ bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
   pr.gate_slots = a.gate_slots;
   pr.dgp = a.dgp;
   pr.ld_dgp = cdiv_h(a.H, 256);
+  // a | u come into shared memory by TMA, one 32-row x 32-column box each
+  pr.map_aux = P.num_maps++;
+  if (!encode_2d_f32(&P.maps[pr.map_aux], a.au, 2 * (uint64_t)a.H, a.rows_total, 2 * (uint64_t)a.H * 4, 32, 32))
+    return false;
   return true;
 }
 

@@ -66,6 +66,21 @@ inline bool encode_blocks(CUtensorMap* m, const void* ptr, uint64_t cols, uint64
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 map over a row-major [outer, inner] tensor, no swizzle (rows of a
+// box land contiguously), out-of-bounds elements read as zero.
+inline bool encode_2d_f32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                          uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D bf16 map over [d2, d1, d0] (d0 contiguous); box = b0 x b1 x 1.
 inline bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
                       uint32_t b1) {
@@ -98,7 +113,7 @@ inline Problem blank_problem() {
 template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT = SPLIT_NONE>
 cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR, SPLIT>;
-  constexpr size_t smem = smem_bytes<MODE, PAIR>();
+  constexpr size_t smem = smem_bytes<MODE, EPI, PAIR>();
   static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
