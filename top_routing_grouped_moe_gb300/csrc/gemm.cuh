@@ -617,7 +617,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       const int nk = ti.nk, k_left = ti.k1 - ti.k0;
       const int nblk_k = pr.n_tile / 64;
       constexpr bool a_lo = SPLIT == SPLIT_A, b_lo = SPLIT == SPLIT_B;
-      for (int kb = 0; kb < nk; ++kb) {
+      if (MODE == MGROUP) {
+        // Ragged M has nothing for the other lanes to do in a stage: lane 0
+        // runs the whole stage loop (a warp-wide wait and sync per stage
+        // would sit between the tensor core's MMA groups).
+        if (lane == 0) {
+          for (int kb = 0; kb < nk; ++kb) {
+            if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);
+            const uint32_t b_addr = ptx::smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+            for (int s = 0; s < BK / UMMA_K; ++s) {
+              const uint64_t ad = AMN ? ptx::smem_desc(a_addr + s * 2048, MN_BLOCK_BYTES, 1024)
+                                      : ptx::smem_desc(a_addr + s * 32, 16, 1024);
+              const uint64_t bd = BMN ? ptx::smem_desc(b_addr + s * 2048, MN_BLOCK_BYTES, 1024)
+                                      : ptx::smem_desc(b_addr + s * 32, 16, 1024);
+              if (PAIR == 1) ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+              else ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+            }
+            if (PAIR == 1) ptx::mma_commit(&tail->empty[stage]);
+            else ptx::mma_commit_pair(&tail->empty[stage], 0x3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        stage = __shfl_sync(0xffffffffu, stage, 0);
+        phase = __shfl_sync(0xffffffffu, phase, 0);
+      }
+      for (int kb = 0; MODE == KGROUP && kb < nk; ++kb) {
         if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
@@ -673,24 +708,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
               if (b_lo) ptx::mma_bf16(d_tmem, ad, ptx::smem_desc(sl + s * 2048, KG_BLOCK_BYTES, 1024), idesc, 1u);
             }
             ptx::mma_commit(&tail->empty[stage]);
-          }
-          __syncwarp();
-        } else {
-          const int nsub = BK / UMMA_K;
-          __syncwarp();
-          if (lane == 0) {
-            const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);
-            const uint32_t b_addr = ptx::smem_u32(sB + stage * B_BYTES);
-            for (int s = 0; s < nsub; ++s) {
-              const uint64_t ad = AMN ? ptx::smem_desc(a_addr + s * 2048, MN_BLOCK_BYTES, 1024)
-                                      : ptx::smem_desc(a_addr + s * 32, 16, 1024);
-              const uint64_t bd = BMN ? ptx::smem_desc(b_addr + s * 2048, MN_BLOCK_BYTES, 1024)
-                                      : ptx::smem_desc(b_addr + s * 32, 16, 1024);
-              if (PAIR == 1) ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
-              else ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
-            }
-            if (PAIR == 1) ptx::mma_commit(&tail->empty[stage]);
-            else ptx::mma_commit_pair(&tail->empty[stage], 0x3);
           }
           __syncwarp();
         }
