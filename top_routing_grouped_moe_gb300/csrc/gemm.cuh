@@ -294,7 +294,10 @@ __device__ void build_schedule(const Params& P, Sched& S) {
   __syncthreads();
 }
 
-__device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + __expf(-a)); }
+// sigmoid with CUDA's fast exponential and fast division (about 2 ulp; an
+// IEEE-exact division here was most of the SwiGLU epilogues' time).  For
+// a < -87 the denominator overflows and the result is 0, the right limit.
+__device__ __forceinline__ float sigmoidf_(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
 
 template <int EPI>
 struct OutSel {
