@@ -372,14 +372,15 @@ __device__ __forceinline__ void load_3d(void* dst, const CUtensorMap* m, uint64_
 
 // Ragged K: rows [valid, valid + nrows) of `nblk` consecutive 64 x 32 boxes
 // at `base` belong to the next group (or lie past the end); zero them, whole
-// 128-byte rows (the swizzle permutes within a row only).  One full warp.
-__device__ __forceinline__ void zero_box_rows(uint8_t* base, int nblk, int valid, int nrows, int lane) {
-  const int per_blk = nrows * 8;  // 16-byte chunks
-  for (int c = lane; c < per_blk * nblk; c += 32) {
-    const int blk = c / per_blk;
-    const int w = c - blk * per_blk;
-    *reinterpret_cast<uint4*>(base + blk * KG_BLOCK_BYTES + (valid + (w >> 3)) * 128 + (w & 7) * 16) =
-        make_uint4(0, 0, 0, 0);
+// 128-byte rows (the swizzle permutes within a row only).  One thread.
+__device__ __forceinline__ void zero_box_rows(uint8_t* base, int nblk, int valid, int nrows) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int b = 0; b < nblk; ++b) {
+    uint4* row = reinterpret_cast<uint4*>(base + b * KG_BLOCK_BYTES + valid * 128);
+    for (int r = 0; r < nrows; ++r, row += 8) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) row[c] = z;
+    }
   }
 }
 
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     }
     for (int r = 0; r < RING; ++r) {
       ptx::mbar_init(&tail->ring_full[r], 1);
-      ptx::mbar_init(&tail->ring_empty[r], 5);  // the MMA warp and the four epilogue warps
+      ptx::mbar_init(&tail->ring_empty[r], 5);  // the MMA thread and the four epilogue warps
     }
     tail->abort_flag = 0;
     ptx::fence_mbarrier_init();
@@ -592,46 +593,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // PAIR = 1: this CTA issues.  PAIR = 2: only the leader issues; its full
-    // barriers count both CTAs' bytes, and its commits arrive on the barriers
-    // of both CTAs.
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int it = 0; ok && rank == 0; ++it) {
-      int t;
-      if (!take_tile(it, t)) {
-        ok = false;
-        break;
-      }
-      if (t >= total) break;
-      TileInfo ti = decode<MODE, TILE_M>(P, S, t);
-      const Problem& pr = P.prob[ti.p];
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
-      if (!ptx::mbar_wait_cluster_bounded(&tail->tmem_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      // per-tile values in registers (see the producer)
-      const uint32_t idesc = ptx::idesc_bf16(TILE_M, pr.mma_n, AMN, BMN);
-      const int nk = ti.nk, k_left = ti.k1 - ti.k0;
-      const int nblk_k = pr.n_tile / 64;
-      constexpr bool a_lo = SPLIT == SPLIT_A, b_lo = SPLIT == SPLIT_B;
-      if (MODE == MGROUP) {
-        // Ragged M has nothing for the other lanes to do in a stage: lane 0
-        // runs the whole stage loop (a warp-wide wait and sync per stage
-        // would sit between the tensor core's MMA groups).
-        if (lane == 0) {
-          for (int kb = 0; kb < nk; ++kb) {
-            if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
-              *abort_flag = 1;
-              ok = false;
-              break;
+    // One thread issues everything: lane 0 of the CTA (PAIR = 2: of the
+    // leader, whose full barriers count both CTAs' bytes and whose commits
+    // arrive on the barriers of both CTAs).  The other lanes take part in the
+    // TMEM allocation only: a warp-wide wait or sync inside this loop makes the
+    // warp reconverge, which costs hundreds of cycles between MMA groups.
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        int t;
+        if (dyn) {
+          const int slot = it & (RING - 1);
+          if (!ptx::mbar_wait_bounded(&tail->ring_full[slot], (it / RING) & 1, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          t = *reinterpret_cast<volatile int*>(&tail->ring[slot]);
+          ptx::mbar_arrive(&tail->ring_empty[slot]);
+        } else {
+          t = tile0 + it * tile_step;
+        }
+        if (t >= total) break;
+        TileInfo ti = decode<MODE, TILE_M>(P, S, t);
+        const Problem& pr = P.prob[ti.p];
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!ptx::mbar_wait_cluster_bounded(&tail->tmem_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        // per-tile values in registers (see the producer)
+        const uint32_t idesc = ptx::idesc_bf16(TILE_M, pr.mma_n, AMN, BMN);
+        const int nk = ti.nk, k_left = ti.k1 - ti.k0;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const bool tail_step = MODE == KGROUP && (kb + 1) * BKK > k_left;
+          if (tail_step) {
+            // The group's last step reads rows that belong to the next group
+            // (or lie past the end).  Rows [valid, 16 * ceil(valid / 16)) of A
+            // (and of A's lo half) are zeroed: their products with B then
+            // vanish, as B's rows there are finite data or TMA zero fill.
+            const int valid = k_left - kb * BKK;
+            const int nrows = ((valid + UMMA_K - 1) / UMMA_K) * UMMA_K - valid;
+            if (nrows > 0) {
+              uint8_t* st = smem + stage * KG_STAGE_BYTES;
+              zero_box_rows(st, 2, valid, nrows);
+              if (SPLIT == SPLIT_A) zero_box_rows(st + KG_A_BYTES + KG_B_BYTES, 2, valid, nrows);
+              ptx::fence_proxy_async_smem();
             }
-            ptx::tc_fence_after();
+          }
+          ptx::tc_fence_after();
+          if (MODE == MGROUP) {
             const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);
             const uint32_t b_addr = ptx::smem_u32(sB + stage * B_BYTES);
 #pragma unroll
@@ -645,82 +664,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             }
             if (PAIR == 1) ptx::mma_commit(&tail->empty[stage]);
             else ptx::mma_commit_pair(&tail->empty[stage], 0x3);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        stage = __shfl_sync(0xffffffffu, stage, 0);
-        phase = __shfl_sync(0xffffffffu, phase, 0);
-      }
-      for (int kb = 0; MODE == KGROUP && kb < nk; ++kb) {
-        if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        if (MODE == KGROUP && (kb + 1) * BKK <= k_left) {
-          // full 32-row step: straight-line issue, two 16-row sub-steps
-          __syncwarp();
-          if (lane == 0) {
+          } else {
+            // 32 K rows: per 16-row sub-step one MMA, plus one with the lo half
+            // of the split operand; a full step is one straight-line sequence
             const uint32_t sa = ptx::smem_u32(smem + stage * KG_STAGE_BYTES), sb = sa + KG_A_BYTES,
                            sl = sb + KG_B_BYTES;
             const uint64_t a0 = ptx::smem_desc(sa, KG_BLOCK_BYTES, 1024), a1 = ptx::smem_desc(sa + 2048, KG_BLOCK_BYTES, 1024);
             const uint64_t b0 = ptx::smem_desc(sb, KG_BLOCK_BYTES, 1024), b1 = ptx::smem_desc(sb + 2048, KG_BLOCK_BYTES, 1024);
             const uint64_t l0 = ptx::smem_desc(sl, KG_BLOCK_BYTES, 1024), l1 = ptx::smem_desc(sl + 2048, KG_BLOCK_BYTES, 1024);
             const uint32_t acc0 = kb != 0 ? 1u : 0u;
+            const int nsub = tail_step ? (k_left - kb * BKK + UMMA_K - 1) / UMMA_K : 2;
             if (SPLIT == SPLIT_A) {
               ptx::mma_bf16(d_tmem, a0, b0, idesc, acc0);
               ptx::mma_bf16(d_tmem, l0, b0, idesc, 1u);
-              ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
-              ptx::mma_bf16(d_tmem, l1, b1, idesc, 1u);
+              if (nsub == 2) {
+                ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
+                ptx::mma_bf16(d_tmem, l1, b1, idesc, 1u);
+              }
             } else if (SPLIT == SPLIT_B) {
               ptx::mma_bf16(d_tmem, a0, b0, idesc, acc0);
               ptx::mma_bf16(d_tmem, a0, l0, idesc, 1u);
-              ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
-              ptx::mma_bf16(d_tmem, a1, l1, idesc, 1u);
+              if (nsub == 2) {
+                ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
+                ptx::mma_bf16(d_tmem, a1, l1, idesc, 1u);
+              }
             } else {
               ptx::mma_bf16(d_tmem, a0, b0, idesc, acc0);
-              ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
+              if (nsub == 2) ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
             }
             ptx::mma_commit(&tail->empty[stage]);
           }
-          __syncwarp();
-        } else if (MODE == KGROUP) {
-          // the group's last step: rows past its end are zeroed first
-          uint8_t* st = smem + stage * KG_STAGE_BYTES;
-          const int valid = min(BKK, k_left - kb * BKK);
-          const int nsub = (valid + UMMA_K - 1) / UMMA_K;
-          if (valid < nsub * UMMA_K) {
-            const int nrows = nsub * UMMA_K - valid;
-            zero_box_rows(st, 2, valid, nrows, lane);
-            zero_box_rows(st + KG_A_BYTES, nblk_k, valid, nrows, lane);
-            zero_box_rows(st + KG_A_BYTES + KG_B_BYTES, a_lo ? 2 : (b_lo ? nblk_k : 0), valid, nrows, lane);
-            ptx::fence_proxy_async_smem();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
-          __syncwarp();
-          if (lane == 0) {
-            const uint32_t sa = ptx::smem_u32(st), sb = sa + KG_A_BYTES, sl = sb + KG_B_BYTES;
-            for (int s = 0; s < nsub; ++s) {
-              const uint64_t ad = ptx::smem_desc(sa + s * 2048, KG_BLOCK_BYTES, 1024);
-              const uint64_t bd = ptx::smem_desc(sb + s * 2048, KG_BLOCK_BYTES, 1024);
-              ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
-              if (a_lo) ptx::mma_bf16(d_tmem, ptx::smem_desc(sl + s * 2048, KG_BLOCK_BYTES, 1024), bd, idesc, 1u);
-              if (b_lo) ptx::mma_bf16(d_tmem, ad, ptx::smem_desc(sl + s * 2048, KG_BLOCK_BYTES, 1024), idesc, 1u);
-            }
-            ptx::mma_commit(&tail->empty[stage]);
-          }
-          __syncwarp();
         }
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!ok) break;
-      if (lane == 0) {
+        if (!ok) break;
         if (nk > 0) {
           if (PAIR == 1) ptx::mma_commit(&tail->tmem_full[acc]);
           else ptx::mma_commit_pair(&tail->tmem_full[acc], 0x3);
@@ -729,11 +708,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           if (PAIR == 2) ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&tail->tmem_full[acc]), 1));
         }
       }
-      __syncwarp();
-    }
-    if (!ok) {
-      *abort_flag = 1;
-      record_status(P.status, MOE_ERR_TIMEOUT);
+      if (!ok) {
+        *abort_flag = 1;
+        record_status(P.status, MOE_ERR_TIMEOUT);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
