@@ -331,6 +331,40 @@ def layer_backward(inp: dict, fwd: dict, dY=None):
 
 
 # --------------------------------------------------------------------------
+# router balance loss (auxiliary load-balancing loss)
+# --------------------------------------------------------------------------
+# The pages name load-balancing-loss runs with loss weights 0.02 ... 0.5
+# ("Olmo-core DDP MoE examples", "Other experiments in the report") and give
+# no formula.  Reading taken: the usual auxiliary loss of top-k routing,
+#   L = alpha * E * sum_e f_e P_e,
+#   f_e = #{(t, s): idx[t,s] = e} / (T k)   (router assignments, before any
+#                                            capacity drop),
+#   P_e = (1/T) sum_t softmax(l[t, :])_e    (full softmax over the E experts
+#                                            of the logits used for routing).
+# f is piecewise constant in the logits, so the gradient flows through P:
+#   dL/dl[t,j] = alpha E / T * p[t,j] * (f_j - sum_e f_e p[t,e]).
+def router_probs(logits: np.ndarray) -> np.ndarray:
+    """Full softmax over the E experts of every token (a -inf logit gives 0)."""
+    l = np.asarray(logits, dtype=np.float64)
+    m = l.max(axis=1, keepdims=True)
+    e = np.exp(l - m)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def balance_loss(logits: np.ndarray, idx: np.ndarray, E: int, alpha: float):
+    """Returns (L, f, P, dl): the loss, the assignment fractions, the mean
+    router probabilities and dL/dlogits with f held fixed."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    f = np.bincount(idx.ravel().astype(np.int64), minlength=E)[:E] / float(T * k)
+    p = router_probs(logits)
+    P = p.mean(axis=0)
+    L = alpha * E * float(f @ P)
+    dl = (alpha * E / T) * p * (f[None, :] - (p @ f)[:, None])
+    return L, f, P, dl
+
+
+# --------------------------------------------------------------------------
 # one token / one expert at a time (for sampled checks at full sizes)
 # --------------------------------------------------------------------------
 def token_output(x_t: np.ndarray, experts: list, gates_t: np.ndarray, kept_t: np.ndarray,

@@ -301,3 +301,52 @@ def test_capacity_formula():
     assert orc.capacity_of(8192, 4, 64) == 640          # 1.25 * 8192 * 4 / 64 exactly
     assert orc.capacity_of(10, 1, 3) == math.ceil(1.25 * 10 / 3)
     assert workloads.WORKLOADS["tiny64e_zipf_cap125"].capacity == 640
+
+
+# ---------------------------------------------------------------- balance loss
+BALANCE_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "balance_loss_hand.json")
+
+
+def test_golden_balance_loss_cases():
+    for c in json.load(open(BALANCE_GOLDEN))["cases"]:
+        l = np.array([[_f(v) for v in row] for row in c["logits"]], dtype=np.float64)
+        L, f, P, dl = orc.balance_loss(l, np.array(c["idx"]), c["E"], c["alpha"])
+        assert abs(L - c["loss"]) < 1e-12, c["name"]
+        np.testing.assert_allclose(f, c["f"], rtol=0, atol=1e-15, err_msg=c["name"])
+        np.testing.assert_allclose(P, c["P"], rtol=0, atol=1e-12, err_msg=c["name"])
+        np.testing.assert_allclose(dl, np.array(c["dl"], dtype=np.float64), rtol=0, atol=1e-12, err_msg=c["name"])
+
+
+@pytest.mark.parametrize("E,k", [(5, 2), (8, 3), (64, 4)])
+def test_balance_loss_gradient_matches_finite_differences(E, k):
+    """The assignments are held fixed (they are piecewise constant in the
+    logits); a central difference of the loss itself checks dL/dl."""
+    rng = np.random.default_rng(E * 10 + k)
+    T = 7
+    l = rng.normal(size=(T, E))
+    idx, _ = orc.route_topk(l.astype(np.float32), k)
+    alpha = 0.05
+    L0, f, P, dl = orc.balance_loss(l, idx, E, alpha)
+    eps = 1e-6
+    for t, j in [(0, 0), (3, E - 1), (6, E // 2), (2, 1)]:
+        lp, lm = l.copy(), l.copy()
+        lp[t, j] += eps
+        lm[t, j] -= eps
+        num = (orc.balance_loss(lp, idx, E, alpha)[0] - orc.balance_loss(lm, idx, E, alpha)[0]) / (2 * eps)
+        assert abs(num - dl[t, j]) <= 1e-8 + 1e-6 * abs(dl[t, j]), (t, j, num, dl[t, j])
+
+
+def test_balance_loss_invariants():
+    """f and P are distributions; the gradient of every token sums to zero
+    (softmax); perfect balance gives alpha; the loss is linear in alpha."""
+    rng = np.random.default_rng(3)
+    T, E, k = 50, 16, 4
+    l = rng.normal(size=(T, E)) * 2.0
+    idx, _ = orc.route_topk(l.astype(np.float32), k)
+    L, f, P, dl = orc.balance_loss(l, idx, E, 0.2)
+    assert abs(f.sum() - 1) < 1e-12 and abs(P.sum() - 1) < 1e-12
+    np.testing.assert_allclose(dl.sum(axis=1), 0.0, atol=1e-15)
+    assert abs(orc.balance_loss(l, idx, E, 0.5)[0] - 2.5 * L) < 1e-12
+    # balanced assignments and equal logits: L = alpha exactly
+    idx_b = np.array([[(t * k + s) % E for s in range(k)] for t in range(E)])
+    assert abs(orc.balance_loss(np.zeros((E, E)), idx_b, E, 0.3)[0] - 0.3) < 1e-12
