@@ -40,10 +40,20 @@ def B():
     return _binding
 
 
-def run_layer(w, inp):
+def run_layer(w, inp, poison=False):
     from top_routing_grouped_moe_gb300.layer import MoELayer
     dev = upload(inp)
     layer = MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity)
+    if poison:
+        # every floating-point buffer the path writes, and the workspace
+        # (all bytes 0xFF: NaN as fp32 and bf16), starts as NaN, so a read of a
+        # row that no kernel wrote (e.g. past the kept rows under a capacity
+        # drop) shows up in the results.  Index buffers are left as allocated;
+        # the workspace's index scratch is written before it is read.
+        for v in vars(layer).values():
+            if isinstance(v, torch.Tensor) and v.is_floating_point():
+                v.fill_(float("nan"))
+        layer.ws.fill_(0xFF)
     layer.forward(dev["x"], dev, logits_in=dev.get("logits_in"))
     layer.backward(dev["x"], dev["dY"], dev, learned_router=w.routing == "learned")
     torch.cuda.synchronize()
@@ -58,6 +68,23 @@ def test_layer_forward_backward_parity(B, name):
                              zipf_bias=w.zipf_bias, capacity_factor=w.capacity_factor, backward=True)
     inp = workloads.make_inputs(w)
     layer = run_layer(w, inp)
+    assert B.moe_device_status() == 0
+    f64 = orc.inputs_to_f64(inp)
+    ref = orc.layer_forward(f64, w.k, w.capacity)
+    refb = orc.layer_backward(f64, ref)
+    compare_layer(w, inp, layer, ref, refb)
+
+
+@pytest.mark.parametrize("name", ["zipf_capacity", "partial_tiles"])
+def test_unwritten_rows_never_leak(B, name):
+    """All output and scratch buffers filled with NaN before the step: rows
+    past the kept ones (capacity drop) and past each tile's valid rows are
+    read by the tensor-core loads but must never reach a result."""
+    w = CASES[name]
+    w = workloads.custom(w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, Hs=w.Hs, routing=w.routing,
+                         zipf_bias=w.zipf_bias, capacity_factor=w.capacity_factor, backward=True)
+    inp = workloads.make_inputs(w)
+    layer = run_layer(w, inp, poison=True)
     assert B.moe_device_status() == 0
     f64 = orc.inputs_to_f64(inp)
     ref = orc.layer_forward(f64, w.k, w.capacity)

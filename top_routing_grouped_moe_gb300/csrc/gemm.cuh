@@ -629,6 +629,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         // per-tile values in registers (see the producer)
         const uint32_t idesc = ptx::idesc_bf16(TILE_M, pr.mma_n, AMN, BMN);
         const int nk = ti.nk, k_left = ti.k1 - ti.k0;
+        // Rows from the last group's end up to `extent` are inside the
+        // caller's buffers but were never written (a capacity drop leaves
+        // them untouched): they may hold NaN, and 0 * NaN is NaN.  A tail step
+        // whose 16-row MMAs reach past that end (the last group's, or an
+        // earlier one's when the groups after it are short) zeroes B's tail
+        // rows too.  Past `extent` TMA fills zeros.
+        const int data_end = MODE == KGROUP ? min(S.off[ti.p][pr.G], pr.extent) : 0;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
             ok = false;
@@ -636,16 +643,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           }
           const bool tail_step = MODE == KGROUP && (kb + 1) * BKK > k_left;
           if (tail_step) {
-            // The group's last step reads rows that belong to the next group
+            // The group's last step reads rows that belong to the next groups
             // (or lie past the end).  Rows [valid, 16 * ceil(valid / 16)) of A
             // (and of A's lo half) are zeroed: their products with B then
-            // vanish, as B's rows there are finite data or TMA zero fill.
+            // vanish where B's rows are later groups' (finite) data.
             const int valid = k_left - kb * BKK;
             const int nrows = ((valid + UMMA_K - 1) / UMMA_K) * UMMA_K - valid;
             if (nrows > 0) {
               uint8_t* st = smem + stage * KG_STAGE_BYTES;
               zero_box_rows(st, 2, valid, nrows);
               if (SPLIT == SPLIT_A) zero_box_rows(st + KG_A_BYTES + KG_B_BYTES, 2, valid, nrows);
+              if (ti.k0 + kb * BKK + valid + nrows > data_end) {
+                zero_box_rows(st + KG_A_BYTES, 4, valid, nrows);
+                if (SPLIT == SPLIT_B) zero_box_rows(st + KG_A_BYTES + KG_B_BYTES, 4, valid, nrows);
+              }
               ptx::fence_proxy_async_smem();
             }
           }
