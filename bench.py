@@ -390,6 +390,22 @@ def main_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    # the router balance loss (a further row of the hot path, not part of the
+    # configured step): loss, mean probabilities and the logits gradient
+    lbl_logits = dev["logits_in"] if "logits_in" in dev else layer.logits
+    lbl_out = torch.empty(1 + w.E + w.T * w.E, dtype=torch.float32, device="cuda")
+    lev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps + 3):
+        if i >= 3:
+            flush.fill_(1)
+            lev[i - 3][0].record()
+        B.moe_router_balance_loss(lbl_logits, layer.counts_raw, w.T, w.E, w.k, 0.02, lbl_out[:1],
+                                  lbl_out[1:1 + w.E], lbl_out[1 + w.E:], layer.ws, layer.ws_bytes)
+        if i >= 3:
+            lev[i - 3][1].record()
+    torch.cuda.synchronize()
+    lbl_ms = statistics.mean(a.elapsed_time(b) for a, b in lev)
+    lbl_bytes = 3 * w.T * w.E * 4 + w.E * 8  # logits read twice, gradient written, counts and P
     clocks = sampler.stop()
     graph_ms = max_over_ranks([sum(a.elapsed_time(b) for a, b in gev)], "cuda")[0]
     value = tokens_per_s(w.T, args.steps, world, graph_ms)
@@ -484,6 +500,10 @@ def main_ours(args):
                          "traffic_unit": "bytes per call (ncu dram read + write)",
                          "peak_source": f"{peak_src} bf16 dense (sustained)"},
             "calls": calls_out,
+            "extra_calls": {"moe_router_balance_loss": {
+                "ms": round(lbl_ms, 4), "gbs": round(lbl_bytes / (lbl_ms / 1000.0) / 1e9, 1),
+                "frac_hbm": round(lbl_bytes / (lbl_ms / 1000.0) / 1e9 / hbm_peak, 3),
+                "note": "3 launches, latency-bound at this size; timed alone, not part of the step"}},
             "clocks": clocks,
             "gpu_launches": launches_per_step(w) * args.steps,
             "e2e": e2e,

@@ -243,15 +243,38 @@ MOE_API int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const fl
 
 /* Backward of the top-k softmax gating and of the router product:
  *   dlogits[t,e] = g_s (dgates[t,s] - sum_j g_j dgates[t,j]) if e = topk_idx[t,s],
- *                  0 for experts not selected by t             [T,E] fp32
+ *                  0 for experts not selected by t
+ *                  + dlogits_add[t,e] if dlogits_add != NULL   [T,E] fp32
  *   dW_r[e,c]    = sum_t dlogits[t,e] x[t,c]                   [E,d] fp32
  * (dropped slots have dgates = 0 but stay in the renormalisation set).  x may
- * be NULL only together with dW_r == NULL (given-logits routing).  dW_r uses
- * the tensor cores with dlogits as a bf16 hi + lo pair and fp32
- * accumulation. */
+ * be NULL only together with dW_r == NULL (given-logits routing).
+ * dlogits_add (nullable, [T,E] fp32, device) is a further gradient of the
+ * logits to include, e.g. that of moe_router_balance_loss, so that dW_r and
+ * (through moe_permute_bwd) dx carry it.  dW_r uses the tensor cores with
+ * dlogits as a bf16 hi + lo pair and fp32 accumulation. */
 MOE_API int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
                        const void* x, int T, int d, int E, int k,
-                       float* dlogits, float* dW_r, void* ws, size_t ws_bytes, void* stream);
+                       float* dlogits, float* dW_r, const float* dlogits_add,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Auxiliary load-balancing loss of the router ("Olmo-core DDP MoE examples"
+ * README, "Other experiments in the report": the load-balancing-loss weight
+ * runs, weights 0.02 to 0.5; the pages give no formula, the usual loss of
+ * top-k routing is taken):
+ *   f_e  = counts_raw[e] / (T k)        share of the router assignments of
+ *                                       expert e, before any capacity drop
+ *   P_e  = (1/T) sum_t softmax(logits[t,:])_e   mean full-softmax probability
+ *   loss = alpha E sum_e f_e P_e                device fp32 scalar
+ *   dlogits_lbl[t,j] = alpha E / T p[t,j] (f_j - sum_e f_e p[t,e])
+ *                      (f is piecewise constant in the logits)  [T,E] fp32
+ * logits [T,E] fp32 are the logits the top-k ran on (bias included; -inf
+ * allowed); counts_raw [E] int32 from moe_permute.  P_mean [E] and
+ * dlogits_lbl may be NULL.  Pass dlogits_lbl to moe_route_topk_bwd as
+ * dlogits_add to back-propagate the loss.  Fixed-order reductions:
+ * deterministic.  ws >= moe_workspace_size() bytes. */
+MOE_API int moe_router_balance_loss(const float* logits, const int32_t* counts_raw, int T, int E, int k,
+                                    float alpha, float* loss, float* P_mean, float* dlogits_lbl,
+                                    void* ws, size_t ws_bytes, void* stream);
 
 /* Backward of the permutation (gather-reduce) plus the router's input
  * gradient:

@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) >= 13
+    assert len(names) >= 14
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
@@ -89,6 +89,12 @@ P = 1 << 12  # stand-in device addresses (16-byte aligned); never dereferenced
     (lambda L: L.moe_route_topk_bwd(P, P, P, P, 16, 128, 8, 2, P, None, P, 1 << 20, 0), 1),
     # permute backward: dlogits without W_r
     (lambda L: L.moe_permute_bwd(P, None, P, P, None, 16, 128, 8, 2, P, P, 1 << 20, 0), 1),
+    # balance loss: no loss output
+    (lambda L: L.moe_router_balance_loss(P, P, 16, 8, 2, 0.02, None, None, None, P, 1 << 20, 0), 1),
+    # balance loss: E not a multiple of 8
+    (lambda L: L.moe_router_balance_loss(P, P, 16, 12, 2, 0.02, P, None, None, P, 1 << 20, 0), 2),
+    # balance loss: workspace too small
+    (lambda L: L.moe_router_balance_loss(P, P, 4096, 64, 2, 0.02, P, None, None, P, 16, 0), 3),
 ])
 def test_argument_errors_are_reported_on_the_host(lib, call, expect):
     with pytest.raises(lib.MoEError) as e:

@@ -41,7 +41,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
 
-# name -> argument kinds ('p' pointer/tensor, 'i' int, 'z' size_t, 's' stream)
+# name -> argument kinds ('p' pointer/tensor, 'i' int, 'f' float, 'z' size_t, 's' stream)
 SIGNATURES = {
     "moe_route_topk": "pppp" + "iiii" + "ppp" + "pz" + "s",
     "moe_permute": "pp" + "iiiii" + "pppppp" + "pz" + "s",
@@ -50,11 +50,12 @@ SIGNATURES = {
     "moe_unpermute_combine": "pppp" + "iii" + "p" + "s",
     "moe_unpermute_combine_bwd": "pp" + "iii" + "p" + "s",
     "moe_grouped_swiglu_bwd": "pppppppppp" + "iiiiii" + "pppppp" + "pp" + "pppppp" + "p" + "pz" + "s",
-    "moe_route_topk_bwd": "pppp" + "iiii" + "pp" + "pz" + "s",
+    "moe_route_topk_bwd": "pppp" + "iiii" + "ppp" + "pz" + "s",
+    "moe_router_balance_loss": "pp" + "iii" + "f" + "ppp" + "pz" + "s",
     "moe_permute_bwd": "ppppp" + "iiii" + "p" + "pz" + "s",
 }
 
-_CT = {"p": _P, "i": _I, "z": _SZ, "s": _P}
+_CT = {"p": _P, "i": _I, "f": ctypes.c_float, "z": _SZ, "s": _P}
 
 for _name, _sig in SIGNATURES.items():
     _f = getattr(_lib, _name)
@@ -103,6 +104,8 @@ def _call(name: str, *args):
             conv.append(_ptr(a))
         elif kind == "s":
             conv.append(_stream(a))
+        elif kind == "f":
+            conv.append(float(a))
         else:
             conv.append(int(a))
     rc = getattr(_lib, name)(*conv)
@@ -173,8 +176,15 @@ def moe_grouped_swiglu_bwd(dY_perm, dY, gates, row_of_slot, slot_of_row, offsets
                  dWs_u, dWs_d, dgates, ws, ws_bytes, stream)
 
 
-def moe_route_topk_bwd(dgates, gates, topk_idx, x, T, d, E, k, dlogits, dW_r, ws, ws_bytes, stream=None):
-    return _call("moe_route_topk_bwd", dgates, gates, topk_idx, x, T, d, E, k, dlogits, dW_r, ws, ws_bytes, stream)
+def moe_route_topk_bwd(dgates, gates, topk_idx, x, T, d, E, k, dlogits, dW_r, ws, ws_bytes, stream=None,
+                       dlogits_add=None):
+    return _call("moe_route_topk_bwd", dgates, gates, topk_idx, x, T, d, E, k, dlogits, dW_r, dlogits_add, ws,
+                 ws_bytes, stream)
+
+
+def moe_router_balance_loss(logits, counts_raw, T, E, k, alpha, loss, P_mean, dlogits_lbl, ws, ws_bytes, stream=None):
+    return _call("moe_router_balance_loss", logits, counts_raw, T, E, k, alpha, loss, P_mean, dlogits_lbl, ws,
+                 ws_bytes, stream)
 
 
 def moe_permute_bwd(dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream=None):

@@ -30,9 +30,14 @@ cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_
 // dx_perm, dx_s fp32; dx bf16
 cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, int T, int d,
                                     int k, void* dx, int* status, cudaStream_t s);
-// dlogits [T,E] fp32 (dense) and, if dl_hi != NULL, its bf16 hi + lo halves [T,E]
+// dlogits [T,E] fp32 (dense, + add[T,E] if add != NULL) and, if dl_hi != NULL,
+// its bf16 hi + lo halves [T,E]
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
-                                 float* dlogits, uint16_t* dl_hi, uint16_t* dl_lo, cudaStream_t s);
+                                 const float* add, float* dlogits, uint16_t* dl_hi, uint16_t* dl_lo, cudaStream_t s);
+// router balance loss: loss, P_mean [E] (nullable), dl [T,E] (nullable)
+size_t balance_loss_ws_bytes(int T, int E);
+cudaError_t launch_balance_loss(const float* logits, const int32_t* counts_raw, int T, int E, int k, float alpha,
+                                float* loss, float* P_mean, float* dl, void* ws, cudaStream_t s);
 // v -> bf16 hi + lo halves
 cudaError_t launch_f32_to_bf16_split(const float* src, uint16_t* hi, uint16_t* lo, long long n, cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float* out, cudaStream_t s);

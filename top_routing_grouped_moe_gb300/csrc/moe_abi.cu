@@ -149,6 +149,8 @@ int moe_workspace_size(int T, int d, int E, int k, int H, int Hs, size_t* bytes)
   if (v > b) b = v;
   v = ws_swiglu_bwd(T, k, H, Hs);
   if (v > b) b = v;
+  v = balance_loss_ws_bytes(T, E);
+  if (v > b) b = v;
   *bytes = b;
   return MOE_OK;
 }
@@ -300,13 +302,15 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
 }
 
 int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* topk_idx, const void* x, int T, int d,
-                       int E, int k, float* dlogits, float* dW_r, void* ws, size_t ws_bytes, void* stream) {
+                       int E, int k, float* dlogits, float* dW_r, const float* dlogits_add, void* ws, size_t ws_bytes,
+                       void* stream) {
   if (T < 1 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
   if (k > kMaxK || k > E || E > kMaxE || (E % 8) != 0) return MOE_ERR_UNSUPPORTED;
   if (!dgates || !gates || !topk_idx || !dlogits) return MOE_ERR_INVALID_ARG;
   if ((x == nullptr) != (dW_r == nullptr)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (!x) return check(launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits, nullptr, nullptr, st));
+  if (!x)
+    return check(launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits_add, dlogits, nullptr, nullptr, st));
   int rc = check_dims(T, d, E, k);
   if (rc) return rc;
   if (!al16(x) || !al16(dW_r)) return MOE_ERR_INVALID_ARG;
@@ -314,7 +318,7 @@ int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* t
   char* w = static_cast<char*>(ws);
   uint16_t* dl_hi = reinterpret_cast<uint16_t*>(w);
   uint16_t* dl_lo = reinterpret_cast<uint16_t*>(w + align256((size_t)T * E * 2));
-  cudaError_t e = launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits, dl_hi, dl_lo, st);
+  cudaError_t e = launch_router_bwd_dl(dgates, gates, topk_idx, T, E, k, dlogits_add, dlogits, dl_hi, dl_lo, st);
   if (e != cudaSuccess) return fail_cuda(e);
   const int S = router_dw_splits(T, d, E);
   float* part = S > 1 ? reinterpret_cast<float*>(w + 2 * align256((size_t)T * E * 2)) : dW_r;
@@ -322,6 +326,16 @@ int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* t
   if (e != cudaSuccess) return fail_cuda(e);
   if (S > 1) return check(launch_splitk_reduce(part, S, (long long)E * d, dW_r, st));
   return MOE_OK;
+}
+
+int moe_router_balance_loss(const float* logits, const int32_t* counts_raw, int T, int E, int k, float alpha,
+                            float* loss, float* P_mean, float* dlogits_lbl, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 1 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || k > E || E > kMaxE || (E % 8) != 0) return MOE_ERR_UNSUPPORTED;
+  if (!logits || !counts_raw || !loss) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < balance_loss_ws_bytes(T, E)) return MOE_ERR_WORKSPACE;
+  return check(launch_balance_loss(logits, counts_raw, T, E, k, alpha, loss, P_mean, dlogits_lbl, ws,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 int moe_permute_bwd(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, const float* dlogits,

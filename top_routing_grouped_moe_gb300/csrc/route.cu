@@ -386,7 +386,8 @@ __global__ void unpermute_reduce_kernel(const float4* __restrict__ dx_perm, cons
 // One warp per token: dl_s = g_s (dg_s - sum_j g_j dg_j) scattered into a dense
 // [T,E] row (zeros elsewhere), plus optional bf16 hi + lo halves for the GEMMs.
 __global__ void router_bwd_dl_kernel(const float* __restrict__ dgates, const float* __restrict__ gates,
-                                     const int32_t* __restrict__ idx, int T, int E, int k, float* __restrict__ dl,
+                                     const int32_t* __restrict__ idx, int T, int E, int k,
+                                     const float* __restrict__ add, float* __restrict__ dl,
                                      uint16_t* __restrict__ dl_hi, uint16_t* __restrict__ dl_lo) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -414,6 +415,7 @@ __global__ void router_bwd_dl_kernel(const float* __restrict__ dgates, const flo
 #pragma unroll
     for (int s = 0; s < kMaxK; ++s)
       if (s < k && es[s] == c) v = vs[s];
+    if (add) v += add[(long long)t * E + c];  // e.g. the balance-loss gradient
     dl[(long long)t * E + c] = v;
     if (dl_hi) {
       __nv_bfloat16 hi = __float2bfloat16_rn(v);
@@ -444,6 +446,114 @@ __global__ void splitk_reduce_kernel(const float4* __restrict__ part, int S, lon
       a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
     }
     out[i] = a;
+  }
+}
+
+// ------------------------------------------------------------ router balance loss
+// Full softmax of one token's logits, held by the warp as kNJ values per lane
+// (expert c = lane + 32 j); a row of -inf logits gives all zeros.
+template <int NJ>
+__device__ __forceinline__ void token_softmax(const float* __restrict__ row, int E, int lane, float (&p)[NJ]) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int c = lane + 32 * j;
+    p[j] = c < E ? row[c] : -INFINITY;
+    m = fmaxf(m, p[j]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float sum = 0.0f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    p[j] = (m == -INFINITY || p[j] == -INFINITY) ? 0.0f : expf(p[j] - m);
+    sum += p[j];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) p[j] *= inv;
+}
+
+constexpr int kLblTokensPerWarp = 8;
+
+// partial[b][c] = sum of softmax(l[t])_c over block b's tokens, in a fixed
+// order (each warp over its tokens in order, then the warps in order)
+template <int NJ>
+__global__ void lbl_prob_partials_kernel(const float* __restrict__ logits, int T, int E, float* __restrict__ partial) {
+  __shared__ float acc_s[kWarpsPerBlock][32 * NJ];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) acc[j] = 0.0f;
+  const int t0 = (blockIdx.x * kWarpsPerBlock + warp) * kLblTokensPerWarp;
+  for (int i = 0; i < kLblTokensPerWarp; ++i) {
+    const int t = t0 + i;
+    if (t >= T) break;
+    float p[NJ];
+    token_softmax<NJ>(logits + (long long)t * E, E, lane, p);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) acc[j] += p[j];
+  }
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) acc_s[warp][lane + 32 * j] = acc[j];
+  __syncthreads();
+  for (int c = threadIdx.x; c < E; c += blockDim.x) {
+    float v = 0.0f;
+    for (int w = 0; w < kWarpsPerBlock; ++w) v += acc_s[w][c];
+    partial[(long long)blockIdx.x * E + c] = v;
+  }
+}
+
+// P_c = sum_b partial[b][c] / T; f_c = counts_raw[c] / (T k);
+// loss = alpha E sum_c f_c P_c (fixed-order reduction); coef[c] = f_c
+__global__ void lbl_finish_kernel(const float* __restrict__ partial, int nblk, const int32_t* __restrict__ counts_raw,
+                                  int T, int E, int k, float alpha, float* __restrict__ loss,
+                                  float* __restrict__ P_mean, float* __restrict__ f_out) {
+  __shared__ float red[256];
+  const int c = threadIdx.x;
+  float term = 0.0f;
+  if (c < E) {
+    float P = 0.0f;
+    for (int b = 0; b < nblk; ++b) P += partial[(long long)b * E + c];
+    P /= (float)T;
+    const float f = (float)counts_raw[c] / ((float)T * (float)k);
+    if (P_mean) P_mean[c] = P;
+    f_out[c] = f;
+    term = f * P;
+  }
+  red[c] = term;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (c < w) red[c] += red[c + w];
+    __syncthreads();
+  }
+  if (c == 0) *loss = alpha * (float)E * red[0];
+}
+
+// dl[t,c] = alpha E / T p[t,c] (f_c - sum_e f_e p[t,e])
+template <int NJ>
+__global__ void lbl_grad_kernel(const float* __restrict__ logits, const float* __restrict__ f, int T, int E,
+                                float scale, float* __restrict__ dl) {
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  float p[NJ], fj[NJ];
+  token_softmax<NJ>(logits + (long long)t * E, E, lane, p);
+  float sfp = 0.0f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int c = lane + 32 * j;
+    fj[j] = c < E ? f[c] : 0.0f;
+    sfp += fj[j] * p[j];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sfp += __shfl_xor_sync(0xffffffffu, sfp, off);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int c = lane + 32 * j;
+    if (c < E) dl[(long long)t * E + c] = scale * p[j] * (fj[j] - sfp);
   }
 }
 
@@ -530,9 +640,9 @@ cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, con
 }
 
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
-                                 float* dlogits, uint16_t* dl_hi, uint16_t* dl_lo, cudaStream_t s) {
-  router_bwd_dl_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(dgates, gates, idx, T, E, k, dlogits, dl_hi,
-                                                                       dl_lo);
+                                 const float* add, float* dlogits, uint16_t* dl_hi, uint16_t* dl_lo, cudaStream_t s) {
+  router_bwd_dl_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(dgates, gates, idx, T, E, k, add, dlogits,
+                                                                       dl_hi, dl_lo);
   return cudaGetLastError();
 }
 
@@ -545,6 +655,42 @@ cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float
   const long long n4 = n / 4;
   splitk_reduce_kernel<<<flat_blocks(n4, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(partial), S, n4,
                                                             reinterpret_cast<float4*>(out));
+  return cudaGetLastError();
+}
+
+size_t balance_loss_ws_bytes(int T, int E) {
+  const size_t nblk = (T + kWarpsPerBlock * kLblTokensPerWarp - 1) / (kWarpsPerBlock * kLblTokensPerWarp);
+  return align256(nblk * E * sizeof(float)) + align256((size_t)E * sizeof(float));
+}
+
+cudaError_t launch_balance_loss(const float* logits, const int32_t* counts_raw, int T, int E, int k, float alpha,
+                                float* loss, float* P_mean, float* dl, void* ws, cudaStream_t s) {
+  const int tpb = kWarpsPerBlock * kLblTokensPerWarp;
+  const int nblk = (T + tpb - 1) / tpb;
+  float* partial = static_cast<float*>(ws);
+  float* f = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)nblk * E * sizeof(float)));
+  const int nj = (E + 31) / 32;
+  const unsigned threads = 32 * kWarpsPerBlock;
+  switch (nj) {
+    case 1: lbl_prob_partials_kernel<1><<<nblk, threads, 0, s>>>(logits, T, E, partial); break;
+    case 2: lbl_prob_partials_kernel<2><<<nblk, threads, 0, s>>>(logits, T, E, partial); break;
+    case 3:
+    case 4: lbl_prob_partials_kernel<4><<<nblk, threads, 0, s>>>(logits, T, E, partial); break;
+    default: lbl_prob_partials_kernel<8><<<nblk, threads, 0, s>>>(logits, T, E, partial); break;
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  lbl_finish_kernel<<<1, 256, 0, s>>>(partial, nblk, counts_raw, T, E, k, alpha, loss, P_mean, f);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !dl) return e;
+  const float scale = alpha * (float)E / (float)T;
+  switch (nj) {
+    case 1: lbl_grad_kernel<1><<<warp_blocks(T), threads, 0, s>>>(logits, f, T, E, scale, dl); break;
+    case 2: lbl_grad_kernel<2><<<warp_blocks(T), threads, 0, s>>>(logits, f, T, E, scale, dl); break;
+    case 3:
+    case 4: lbl_grad_kernel<4><<<warp_blocks(T), threads, 0, s>>>(logits, f, T, E, scale, dl); break;
+    default: lbl_grad_kernel<8><<<warp_blocks(T), threads, 0, s>>>(logits, f, T, E, scale, dl); break;
+  }
   return cudaGetLastError();
 }
 

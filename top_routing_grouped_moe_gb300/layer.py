@@ -19,8 +19,9 @@ class MoELayer:
     T tokens, d model width, E experts, k experts per token, H routed hidden
     width, Hs shared hidden width (0 = none), capacity (<= 0: dropless)."""
 
-    def __init__(self, T, d, E, k, H, Hs, capacity=0, device="cuda", backward=True):
+    def __init__(self, T, d, E, k, H, Hs, capacity=0, device="cuda", backward=True, balance_alpha=0.0):
         self.T, self.d, self.E, self.k, self.H, self.Hs, self.capacity = T, d, E, k, H, Hs, capacity
+        self.balance_alpha = float(balance_alpha)
         dev = torch.device(device)
         R = T * k
         e = lambda *shape, dt=BF16: torch.empty(*shape, dtype=dt, device=dev)  # noqa: E731
@@ -40,6 +41,12 @@ class MoELayer:
         self.h_s = e(T, Hs) if Hs else None
         self.s = e(T, d, dt=torch.float32) if Hs else None
         self.y = e(T, d)
+        if self.balance_alpha > 0:
+            # auxiliary load-balancing loss (device scalar), mean router
+            # probabilities and the loss gradient of the logits
+            self.lbl_loss = e(1, dt=torch.float32)
+            self.lbl_P = e(E, dt=torch.float32)
+            self.dlogits_lbl = e(T, E, dt=torch.float32) if backward else None
         self.ws_bytes = B.moe_workspace_size(T, d, E, k, H, Hs)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         if backward:
@@ -67,6 +74,10 @@ class MoELayer:
                          self.ws, self.ws_bytes, stream)
         B.moe_permute(x, self.idx, T, d, E, k, self.capacity, self.counts_raw, self.counts, self.offsets,
                       self.row_of_slot, self.slot_of_row, self.x_perm, self.ws, self.ws_bytes, stream)
+        if self.balance_alpha > 0:
+            B.moe_router_balance_loss(logits_in if logits_in is not None else self.logits, self.counts_raw, T, E, k,
+                                      self.balance_alpha, self.lbl_loss, self.lbl_P, self.dlogits_lbl, self.ws,
+                                      self.ws_bytes, stream)
         B.moe_grouped_swiglu(self.x_perm, self.offsets, x, T, d, E, k, H, Hs, p["W_g"], p["W_u"], p["W_d"],
                              p.get("Ws_g"), p.get("Ws_u"), p.get("Ws_d"), self.au, self.h, self.o_perm,
                              self.au_s, self.h_s, self.s, self.ws, self.ws_bytes, stream)
@@ -75,7 +86,9 @@ class MoELayer:
 
     def backward(self, x, dY, p, learned_router=True, stream=None):
         """Backward of the last forward for upstream dY [T,d] bf16.  Fills
-        dx, dW_g/u/d, dWs_*, dgates, dlogits and (learned router) dW_r."""
+        dx, dW_g/u/d, dWs_*, dgates, dlogits and (learned router) dW_r; with
+        balance_alpha > 0 the load-balancing loss's gradient is included in
+        dlogits, dW_r and dx."""
         T, d, E, k, H, Hs = self.T, self.d, self.E, self.k, self.H, self.Hs
         B.moe_unpermute_combine_bwd(dY, self.row_of_slot, T, d, k, self.dY_perm, stream)
         B.moe_grouped_swiglu_bwd(self.dY_perm, dY, self.gates, self.row_of_slot, self.slot_of_row, self.offsets,
@@ -85,7 +98,8 @@ class MoELayer:
                                  self.ws, self.ws_bytes, stream)
         lr = learned_router and p.get("W_r") is not None
         B.moe_route_topk_bwd(self.dgates, self.gates, self.idx, x if lr else None, T, d, E, k, self.dlogits,
-                             self.dW_r if lr else None, self.ws, self.ws_bytes, stream)
+                             self.dW_r if lr else None, self.ws, self.ws_bytes, stream,
+                             dlogits_add=self.dlogits_lbl if self.balance_alpha > 0 else None)
         B.moe_permute_bwd(self.dx_perm, self.dx_s, self.row_of_slot, self.dlogits if lr else None,
                           p.get("W_r") if lr else None, T, d, E, k, self.dx, self.ws, self.ws_bytes, stream)
         return self.dx
