@@ -390,22 +390,37 @@ def main_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    # the router balance loss (a further row of the hot path, not part of the
-    # configured step): loss, mean probabilities and the logits gradient
+    def time_alone(fn):
+        """mean ms of fn over args.steps calls after 3 warm-up calls, L2 flushed before each"""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps + 3):
+            if i >= 3:
+                flush.fill_(1)
+                ev[i - 3][0].record()
+            fn()
+            if i >= 3:
+                ev[i - 3][1].record()
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # calls of further rows of the hot path, timed alone (not part of the
+    # configured step).  The router balance loss: loss, mean probabilities and
+    # the logits gradient.
     lbl_logits = dev["logits_in"] if "logits_in" in dev else layer.logits
     lbl_out = torch.empty(1 + w.E + w.T * w.E, dtype=torch.float32, device="cuda")
-    lev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps + 3):
-        if i >= 3:
-            flush.fill_(1)
-            lev[i - 3][0].record()
-        B.moe_router_balance_loss(lbl_logits, layer.counts_raw, w.T, w.E, w.k, 0.02, lbl_out[:1],
-                                  lbl_out[1:1 + w.E], lbl_out[1 + w.E:], layer.ws, layer.ws_bytes)
-        if i >= 3:
-            lev[i - 3][1].record()
-    torch.cuda.synchronize()
-    lbl_ms = statistics.mean(a.elapsed_time(b) for a, b in lev)
-    lbl_bytes = 3 * w.T * w.E * 4 + w.E * 8  # logits read twice, gradient written, counts and P
+    lbl_ms = time_alone(lambda: B.moe_router_balance_loss(
+        lbl_logits, layer.counts_raw, w.T, w.E, w.k, 0.02, lbl_out[:1], lbl_out[1:1 + w.E], lbl_out[1 + w.E:],
+        layer.ws, layer.ws_bytes))
+    lbl_bytes = 2 * w.T * w.E * 4 + w.E * 8  # logits read, gradient written, counts and P
+    # Activation recompute: the fp32 a|u rebuilt for the backward (gate/up GEMM
+    # without the h store), written over the layer's saved copy (same values)
+    rec_ms = time_alone(lambda: B.moe_grouped_swiglu_recompute(
+        layer.x_perm, layer.offsets, dev["x"], w.T, w.d, w.E, w.k, w.H, w.Hs, dev["W_g"], dev["W_u"],
+        dev.get("Ws_g"), dev.get("Ws_u"), layer.au, layer.au_s))
+    rows = int(layer.offsets[-1])
+    rec_flops = 2.0 * w.d * 2 * (rows * w.H + w.T * w.Hs)
+    rec_bytes = (rows * w.d * 2 + w.E * 2 * w.H * w.d * 2 + rows * 2 * w.H * 4
+                 + (w.T * w.d * 2 + 2 * w.Hs * w.d * 2 + w.T * 2 * w.Hs * 4 if w.Hs else 0))
     clocks = sampler.stop()
     graph_ms = max_over_ranks([sum(a.elapsed_time(b) for a, b in gev)], "cuda")[0]
     value = tokens_per_s(w.T, args.steps, world, graph_ms)
@@ -503,7 +518,13 @@ def main_ours(args):
             "extra_calls": {"moe_router_balance_loss": {
                 "ms": round(lbl_ms, 4), "gbs": round(lbl_bytes / (lbl_ms / 1000.0) / 1e9, 1),
                 "frac_hbm": round(lbl_bytes / (lbl_ms / 1000.0) / 1e9 / hbm_peak, 3),
-                "note": "3 launches, latency-bound at this size; timed alone, not part of the step"}},
+                "note": "one kernel after a 4-byte memset; timed alone, not part of the step"},
+                "moe_grouped_swiglu_recompute": {
+                "ms": round(rec_ms, 4), "tflops": round(rec_flops / (rec_ms / 1000.0) / 1e12, 1),
+                "frac_bf16": round(rec_flops / (rec_ms / 1000.0) / 1e12 / bf16_peak, 3),
+                "gbs": round(rec_bytes / (rec_ms / 1000.0) / 1e9, 1),
+                "frac_hbm": round(rec_bytes / (rec_ms / 1000.0) / 1e9 / hbm_peak, 3),
+                "note": "one GEMM launch; timed alone, not part of the step"}},
             "clocks": clocks,
             "gpu_launches": launches_per_step(w) * args.steps,
             "e2e": e2e,

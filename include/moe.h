@@ -186,6 +186,24 @@ MOE_API int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const
                        float* au_s, void* h_s, float* s,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* Activation recompute for the backward ("Olmo-core DDP MoE examples"
+ * README: the per-layer recompute of the largest "Production throughput
+ * runs" and the per-block recompute benchmark of "Other experiments in the
+ * report"; the pages name the option only): a forward run with au = au_s =
+ * NULL keeps no fp32 a | u, and this call rebuilds them, just before
+ * moe_grouped_swiglu_bwd, from the same inputs:
+ *   au[r, 0:H]  = x_perm[r] W_g[e]^T,  au[r, H:2H] = x_perm[r] W_u[e]^T
+ *   au_s        = the same for x and Ws_g, Ws_u (when Hs > 0)
+ * It is the forward's gate/up GEMM with h left unstored, so the values are
+ * bit-identical to the ones moe_grouped_swiglu would have saved.  au
+ * [T*k, 2H] and au_s [T, 2Hs] fp32 are outputs (scratch that only has to
+ * live until the backward call has consumed it); other arguments as for
+ * moe_grouped_swiglu.  Rows past offsets[E] are not written. */
+MOE_API int moe_grouped_swiglu_recompute(const void* x_perm, const int32_t* offsets, const void* x,
+                                 int T, int d, int E, int k, int H, int Hs,
+                                 const void* W_g, const void* W_u, const void* Ws_g, const void* Ws_u,
+                                 float* au, float* au_s, void* stream);
+
 /* Gate-weighted unpermute and combine:
  *   y[t,:] = s[t,:] + sum_{s kept} gates[t,s] * o_perm[row_of_slot[t*k+s], :]
  * o_perm [T*k,d] and s [T,d] fp32 (s may be NULL: no shared expert); fp32
@@ -270,8 +288,9 @@ MOE_API int moe_route_topk_bwd(const float* dgates, const float* gates, const in
  * logits [T,E] fp32 are the logits the top-k ran on (bias included; -inf
  * allowed); counts_raw [E] int32 from moe_permute.  P_mean [E] and
  * dlogits_lbl may be NULL.  Pass dlogits_lbl to moe_route_topk_bwd as
- * dlogits_add to back-propagate the loss.  Fixed-order reductions:
- * deterministic.  ws >= moe_workspace_size() bytes. */
+ * dlogits_add to back-propagate the loss.  One pass over the logits (one
+ * kernel after a 4-byte memset); fixed-order reductions: deterministic.
+ * ws >= moe_workspace_size() bytes. */
 MOE_API int moe_router_balance_loss(const float* logits, const int32_t* counts_raw, int T, int E, int k,
                                     float alpha, float* loss, float* P_mean, float* dlogits_lbl,
                                     void* ws, size_t ws_bytes, void* stream);

@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) >= 14
+    assert len(names) >= 15
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
@@ -80,6 +80,13 @@ P = 1 << 12  # stand-in device addresses (16-byte aligned); never dereferenced
     # shared expert without its buffers
     (lambda L: L.moe_grouped_swiglu(P, P, None, 16, 128, 8, 2, 128, 128, P, P, P, None, None, None,
                                     P, P, P, None, None, None, None, 0, 0), 1),
+    # recompute: no a|u output
+    (lambda L: L.moe_grouped_swiglu_recompute(P, P, None, 16, 128, 8, 2, 128, 0, P, P, None, None, None, None, 0),
+     1),
+    # recompute: shared expert without its a|u output
+    (lambda L: L.moe_grouped_swiglu_recompute(P, P, P, 16, 128, 8, 2, 128, 128, P, P, P, P, P, None, 0), 1),
+    # recompute: hidden width not a multiple of 128
+    (lambda L: L.moe_grouped_swiglu_recompute(P, P, None, 16, 128, 8, 2, 96, 0, P, P, None, None, P, None, 0), 2),
     # combine: null y
     (lambda L: L.moe_unpermute_combine(P, None, P, P, 16, 128, 2, None, 0), 1),
     # backward workspace too small

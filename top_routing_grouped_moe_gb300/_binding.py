@@ -47,6 +47,7 @@ SIGNATURES = {
     "moe_permute": "pp" + "iiiii" + "pppppp" + "pz" + "s",
     "moe_permute_static": "pp" + "iiiii" + "pppppp" + "s",
     "moe_grouped_swiglu": "ppp" + "iiiiii" + "pppppp" + "pppppp" + "pz" + "s",
+    "moe_grouped_swiglu_recompute": "ppp" + "iiiiii" + "pppp" + "pp" + "s",
     "moe_unpermute_combine": "pppp" + "iii" + "p" + "s",
     "moe_unpermute_combine_bwd": "pp" + "iii" + "p" + "s",
     "moe_grouped_swiglu_bwd": "pppppppppp" + "iiiiii" + "pppppp" + "pp" + "pppppp" + "p" + "pz" + "s",
@@ -158,6 +159,12 @@ def moe_grouped_swiglu(x_perm, offsets, x, T, d, E, k, H, Hs, W_g, W_u, W_d, Ws_
                        au_s, h_s, s, ws, ws_bytes, stream=None):
     return _call("moe_grouped_swiglu", x_perm, offsets, x, T, d, E, k, H, Hs, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, au,
                  h, o_perm, au_s, h_s, s, ws, ws_bytes, stream)
+
+
+def moe_grouped_swiglu_recompute(x_perm, offsets, x, T, d, E, k, H, Hs, W_g, W_u, Ws_g, Ws_u, au, au_s,
+                                 stream=None):
+    return _call("moe_grouped_swiglu_recompute", x_perm, offsets, x, T, d, E, k, H, Hs, W_g, W_u, Ws_g, Ws_u, au,
+                 au_s, stream)
 
 
 def moe_unpermute_combine(o_perm, s, gates, row_of_slot, T, d, k, y, stream=None):

@@ -812,8 +812,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         }
       } else if (EPI == EPI_SWIGLU_FWD) {
         // accumulator columns [0,128) = a (gate), [128,256) = u (up); h goes
-        // out in bf16 (down-projection input), a and u in fp32 (backward)
-        __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row0 * pr.ldo + ti.n0;
+        // out in bf16 (down-projection input; not stored when `out` is NULL,
+        // the recompute of a and u for the backward), a and u in fp32
+        __nv_bfloat16* hp = pr.out ? reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row0 * pr.ldo + ti.n0
+                                   : nullptr;
         float* ap = pr.aux ? reinterpret_cast<float*>(pr.aux) + (long long)row0 * pr.ld_aux + ti.n0 : nullptr;
         for (int c0 = 0; c0 < 128; c0 += 32) {
           float4 va[8], vu[8];
@@ -827,7 +829,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
               const float4 a = va[j], u = vu[j];
               const float4 h = make_float4(a.x * sigmoidf_(a.x) * u.x, a.y * sigmoidf_(a.y) * u.y,
                                            a.z * sigmoidf_(a.z) * u.z, a.w * sigmoidf_(a.w) * u.w);
-              store4(hp + (long long)r * pr.ldo + c, h);
+              if (hp) store4(hp + (long long)r * pr.ldo + c, h);
               if (ap) {
                 store4(ap + (long long)r * pr.ld_aux + c, a);
                 store4(ap + (long long)r * pr.ld_aux + pr.H + c, u);

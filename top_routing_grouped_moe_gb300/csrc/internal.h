@@ -53,7 +53,7 @@ struct SwigluFwdArgs {
   const void* Wg;       // [G, H, d]
   const void* Wu;
   float* au;            // [rows, 2H] fp32 (a | u) or NULL
-  void* h;              // [rows, H]
+  void* h;              // [rows, H], or NULL (a | u only: the backward's recompute)
 };
 struct DownFwdArgs {
   const void* h;        // [rows, H]

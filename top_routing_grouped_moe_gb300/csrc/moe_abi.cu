@@ -219,6 +219,24 @@ int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const void* x
   return check(gemm_down_fwd(rd, Hs > 0 ? &sd : nullptr, status, st));
 }
 
+int moe_grouped_swiglu_recompute(const void* x_perm, const int32_t* offsets, const void* x, int T, int d, int E,
+                                 int k, int H, int Hs, const void* W_g, const void* W_u, const void* Ws_g,
+                                 const void* Ws_u, float* au, float* au_s, void* stream) {
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  rc = check_hidden(H, Hs);
+  if (rc) return rc;
+  if (!x_perm || !offsets || !W_g || !W_u || !au) return MOE_ERR_INVALID_ARG;
+  if (!al16(x_perm) || !al16(W_g) || !al16(W_u) || !al16(au)) return MOE_ERR_INVALID_ARG;
+  if (Hs > 0) {
+    if (!x || !Ws_g || !Ws_u || !au_s) return MOE_ERR_INVALID_ARG;
+    if (!al16(x) || !al16(Ws_g) || !al16(Ws_u) || !al16(au_s)) return MOE_ERR_INVALID_ARG;
+  }
+  SwigluFwdArgs r{x_perm, T * k, offsets, E, d, H, W_g, W_u, au, nullptr};
+  SwigluFwdArgs sh{x, T, nullptr, 1, d, Hs, Ws_g, Ws_u, au_s, nullptr};
+  return check(gemm_swiglu_fwd(r, Hs > 0 ? &sh : nullptr, device_status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
 int moe_unpermute_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
                           int T, int d, int k, void* y, void* stream) {
   if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;

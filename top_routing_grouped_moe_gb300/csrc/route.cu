@@ -450,17 +450,13 @@ __global__ void splitk_reduce_kernel(const float4* __restrict__ part, int S, lon
 }
 
 // ------------------------------------------------------------ router balance loss
-// Full softmax of one token's logits, held by the warp as kNJ values per lane
-// (expert c = lane + 32 j); a row of -inf logits gives all zeros.
+// Full softmax of one token's logits held by the warp as NJ values per lane
+// (expert c = lane + 32 j; -inf where c >= E); a row of -inf gives all zeros.
 template <int NJ>
-__device__ __forceinline__ void token_softmax(const float* __restrict__ row, int E, int lane, float (&p)[NJ]) {
+__device__ __forceinline__ void token_softmax(float (&p)[NJ]) {
   float m = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    const int c = lane + 32 * j;
-    p[j] = c < E ? row[c] : -INFINITY;
-    m = fmaxf(m, p[j]);
-  }
+  for (int j = 0; j < NJ; ++j) m = fmaxf(m, p[j]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   float sum = 0.0f;
@@ -476,85 +472,96 @@ __device__ __forceinline__ void token_softmax(const float* __restrict__ row, int
   for (int j = 0; j < NJ; ++j) p[j] *= inv;
 }
 
-constexpr int kLblTokensPerWarp = 8;
+constexpr int kLblTokensPerWarp = 4;
+constexpr int kLblTokensPerBlock = kWarpsPerBlock * kLblTokensPerWarp;
 
-// partial[b][c] = sum of softmax(l[t])_c over block b's tokens, in a fixed
-// order (each warp over its tokens in order, then the warps in order)
+// One pass over the logits.  With f_c = counts_raw[c] / (T k) known up
+// front, every warp writes the gradient of its tokens,
+//   dl[t,c] = alpha E / T p[t,c] (f_c - sum_e f_e p[t,e]),
+// and each block writes the sum of its tokens' probabilities (warps in
+// order).  The last block to finish (a ticket counter, zeroed by the host
+// before the launch) adds the block partials in block order, so P_mean and
+//   loss = alpha E sum_c f_c P_c
+// do not depend on which block finishes last.
 template <int NJ>
-__global__ void lbl_prob_partials_kernel(const float* __restrict__ logits, int T, int E, float* __restrict__ partial) {
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+lbl_kernel(const float* __restrict__ logits, const int32_t* __restrict__ counts_raw, int T, int E, int k, float alpha,
+           float* __restrict__ loss, float* __restrict__ P_mean, float* __restrict__ dl, float* __restrict__ partial,
+           unsigned* __restrict__ ticket) {
   __shared__ float acc_s[kWarpsPerBlock][32 * NJ];
+  __shared__ float red[32 * kWarpsPerBlock];
+  __shared__ bool last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float acc[NJ];
+  const float inv_tk = 1.0f / ((float)T * (float)k);
+  float fj[NJ], acc[NJ];
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) acc[j] = 0.0f;
-  const int t0 = (blockIdx.x * kWarpsPerBlock + warp) * kLblTokensPerWarp;
+  for (int j = 0; j < NJ; ++j) {
+    const int c = lane + 32 * j;
+    fj[j] = c < E ? (float)counts_raw[c] * inv_tk : 0.0f;
+    acc[j] = 0.0f;
+  }
+  const int t0 = blockIdx.x * kLblTokensPerBlock + warp * kLblTokensPerWarp;
+  float v[kLblTokensPerWarp][NJ];  // all of the warp's rows in flight at once
+#pragma unroll
+  for (int i = 0; i < kLblTokensPerWarp; ++i)
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int c = lane + 32 * j;
+      v[i][j] = (t0 + i < T && c < E) ? __ldg(logits + (long long)(t0 + i) * E + c) : -INFINITY;
+    }
+  const float scale = alpha * (float)E / (float)T;
+#pragma unroll
   for (int i = 0; i < kLblTokensPerWarp; ++i) {
     const int t = t0 + i;
     if (t >= T) break;
-    float p[NJ];
-    token_softmax<NJ>(logits + (long long)t * E, E, lane, p);
+    token_softmax<NJ>(v[i]);
+    float sfp = 0.0f;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) acc[j] += p[j];
+    for (int j = 0; j < NJ; ++j) {
+      acc[j] += v[i][j];
+      sfp += fj[j] * v[i][j];
+    }
+    if (dl) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sfp += __shfl_xor_sync(0xffffffffu, sfp, off);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int c = lane + 32 * j;
+        if (c < E) dl[(long long)t * E + c] = scale * v[i][j] * (fj[j] - sfp);
+      }
+    }
   }
 #pragma unroll
   for (int j = 0; j < NJ; ++j) acc_s[warp][lane + 32 * j] = acc[j];
   __syncthreads();
   for (int c = threadIdx.x; c < E; c += blockDim.x) {
-    float v = 0.0f;
-    for (int w = 0; w < kWarpsPerBlock; ++w) v += acc_s[w][c];
-    partial[(long long)blockIdx.x * E + c] = v;
+    float s = 0.0f;
+    for (int w = 0; w < kWarpsPerBlock; ++w) s += acc_s[w][c];
+    partial[(long long)blockIdx.x * E + c] = s;
   }
-}
-
-// P_c = sum_b partial[b][c] / T; f_c = counts_raw[c] / (T k);
-// loss = alpha E sum_c f_c P_c (fixed-order reduction); coef[c] = f_c
-__global__ void lbl_finish_kernel(const float* __restrict__ partial, int nblk, const int32_t* __restrict__ counts_raw,
-                                  int T, int E, int k, float alpha, float* __restrict__ loss,
-                                  float* __restrict__ P_mean, float* __restrict__ f_out) {
-  __shared__ float red[256];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // E <= blockDim.x (checked on the host)
   const int c = threadIdx.x;
   float term = 0.0f;
   if (c < E) {
     float P = 0.0f;
-    for (int b = 0; b < nblk; ++b) P += partial[(long long)b * E + c];
+    for (unsigned b = 0; b < gridDim.x; ++b) P += __ldcg(partial + (long long)b * E + c);
     P /= (float)T;
-    const float f = (float)counts_raw[c] / ((float)T * (float)k);
     if (P_mean) P_mean[c] = P;
-    f_out[c] = f;
-    term = f * P;
+    term = (float)counts_raw[c] * inv_tk * P;
   }
   red[c] = term;
   __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
+  for (int w = blockDim.x >> 1; w > 0; w >>= 1) {
     if (c < w) red[c] += red[c + w];
     __syncthreads();
   }
   if (c == 0) *loss = alpha * (float)E * red[0];
-}
-
-// dl[t,c] = alpha E / T p[t,c] (f_c - sum_e f_e p[t,e])
-template <int NJ>
-__global__ void lbl_grad_kernel(const float* __restrict__ logits, const float* __restrict__ f, int T, int E,
-                                float scale, float* __restrict__ dl) {
-  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  float p[NJ], fj[NJ];
-  token_softmax<NJ>(logits + (long long)t * E, E, lane, p);
-  float sfp = 0.0f;
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    const int c = lane + 32 * j;
-    fj[j] = c < E ? f[c] : 0.0f;
-    sfp += fj[j] * p[j];
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sfp += __shfl_xor_sync(0xffffffffu, sfp, off);
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    const int c = lane + 32 * j;
-    if (c < E) dl[(long long)t * E + c] = scale * p[j] * (fj[j] - sfp);
-  }
 }
 
 inline unsigned warp_blocks(long long n) { return static_cast<unsigned>((n + kWarpsPerBlock - 1) / kWarpsPerBlock); }
@@ -659,37 +666,25 @@ cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float
 }
 
 size_t balance_loss_ws_bytes(int T, int E) {
-  const size_t nblk = (T + kWarpsPerBlock * kLblTokensPerWarp - 1) / (kWarpsPerBlock * kLblTokensPerWarp);
-  return align256(nblk * E * sizeof(float)) + align256((size_t)E * sizeof(float));
+  const size_t nblk = (T + kLblTokensPerBlock - 1) / kLblTokensPerBlock;
+  return align256(nblk * E * sizeof(float)) + 256;
 }
 
 cudaError_t launch_balance_loss(const float* logits, const int32_t* counts_raw, int T, int E, int k, float alpha,
                                 float* loss, float* P_mean, float* dl, void* ws, cudaStream_t s) {
-  const int tpb = kWarpsPerBlock * kLblTokensPerWarp;
-  const int nblk = (T + tpb - 1) / tpb;
+  if (E > 32 * kWarpsPerBlock) return cudaErrorInvalidValue;
+  const int nblk = (T + kLblTokensPerBlock - 1) / kLblTokensPerBlock;
   float* partial = static_cast<float*>(ws);
-  float* f = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)nblk * E * sizeof(float)));
-  const int nj = (E + 31) / 32;
-  const unsigned threads = 32 * kWarpsPerBlock;
-  switch (nj) {
-    case 1: lbl_prob_partials_kernel<1><<<nblk, threads, 0, s>>>(logits, T, E, partial); break;
-    case 2: lbl_prob_partials_kernel<2><<<nblk, threads, 0, s>>>(logits, T, E, partial); break;
-    case 3:
-    case 4: lbl_prob_partials_kernel<4><<<nblk, threads, 0, s>>>(logits, T, E, partial); break;
-    default: lbl_prob_partials_kernel<8><<<nblk, threads, 0, s>>>(logits, T, E, partial); break;
-  }
-  cudaError_t e = cudaGetLastError();
+  unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + align256((size_t)nblk * E * sizeof(float)));
+  cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return e;
-  lbl_finish_kernel<<<1, 256, 0, s>>>(partial, nblk, counts_raw, T, E, k, alpha, loss, P_mean, f);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || !dl) return e;
-  const float scale = alpha * (float)E / (float)T;
-  switch (nj) {
-    case 1: lbl_grad_kernel<1><<<warp_blocks(T), threads, 0, s>>>(logits, f, T, E, scale, dl); break;
-    case 2: lbl_grad_kernel<2><<<warp_blocks(T), threads, 0, s>>>(logits, f, T, E, scale, dl); break;
+  const unsigned threads = 32 * kWarpsPerBlock;
+  switch ((E + 31) / 32) {
+    case 1: lbl_kernel<1><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
+    case 2: lbl_kernel<2><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
     case 3:
-    case 4: lbl_grad_kernel<4><<<warp_blocks(T), threads, 0, s>>>(logits, f, T, E, scale, dl); break;
-    default: lbl_grad_kernel<8><<<warp_blocks(T), threads, 0, s>>>(logits, f, T, E, scale, dl); break;
+    case 4: lbl_kernel<4><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
+    default: lbl_kernel<8><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
   }
   return cudaGetLastError();
 }

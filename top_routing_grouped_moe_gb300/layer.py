@@ -19,9 +19,14 @@ class MoELayer:
     T tokens, d model width, E experts, k experts per token, H routed hidden
     width, Hs shared hidden width (0 = none), capacity (<= 0: dropless)."""
 
-    def __init__(self, T, d, E, k, H, Hs, capacity=0, device="cuda", backward=True, balance_alpha=0.0):
+    def __init__(self, T, d, E, k, H, Hs, capacity=0, device="cuda", backward=True, balance_alpha=0.0,
+                 recompute=False):
         self.T, self.d, self.E, self.k, self.H, self.Hs, self.capacity = T, d, E, k, H, Hs, capacity
         self.balance_alpha = float(balance_alpha)
+        # recompute: the forward saves no fp32 a|u; the backward rebuilds them
+        # (moe_grouped_swiglu_recompute) into au / au_s, which then only have
+        # to live through the backward call (scratch that layers can share)
+        self.recompute = bool(recompute)
         dev = torch.device(device)
         R = T * k
         e = lambda *shape, dt=BF16: torch.empty(*shape, dtype=dt, device=dev)  # noqa: E731
@@ -78,9 +83,11 @@ class MoELayer:
             B.moe_router_balance_loss(logits_in if logits_in is not None else self.logits, self.counts_raw, T, E, k,
                                       self.balance_alpha, self.lbl_loss, self.lbl_P, self.dlogits_lbl, self.ws,
                                       self.ws_bytes, stream)
+        save = not self.recompute
         B.moe_grouped_swiglu(self.x_perm, self.offsets, x, T, d, E, k, H, Hs, p["W_g"], p["W_u"], p["W_d"],
-                             p.get("Ws_g"), p.get("Ws_u"), p.get("Ws_d"), self.au, self.h, self.o_perm,
-                             self.au_s, self.h_s, self.s, self.ws, self.ws_bytes, stream)
+                             p.get("Ws_g"), p.get("Ws_u"), p.get("Ws_d"), self.au if save else None, self.h,
+                             self.o_perm, self.au_s if save else None, self.h_s, self.s, self.ws, self.ws_bytes,
+                             stream)
         B.moe_unpermute_combine(self.o_perm, self.s, self.gates, self.row_of_slot, T, d, k, self.y, stream)
         return self.y
 
@@ -90,6 +97,9 @@ class MoELayer:
         balance_alpha > 0 the load-balancing loss's gradient is included in
         dlogits, dW_r and dx."""
         T, d, E, k, H, Hs = self.T, self.d, self.E, self.k, self.H, self.Hs
+        if self.recompute:
+            B.moe_grouped_swiglu_recompute(self.x_perm, self.offsets, x, T, d, E, k, H, Hs, p["W_g"], p["W_u"],
+                                           p.get("Ws_g"), p.get("Ws_u"), self.au, self.au_s, stream)
         B.moe_unpermute_combine_bwd(dY, self.row_of_slot, T, d, k, self.dY_perm, stream)
         B.moe_grouped_swiglu_bwd(self.dY_perm, dY, self.gates, self.row_of_slot, self.slot_of_row, self.offsets,
                                  self.x_perm, x, self.au, self.au_s, T, d, E, k, H, Hs, p["W_g"], p["W_u"],
