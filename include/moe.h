@@ -212,6 +212,15 @@ MOE_API int moe_unpermute_combine(const float* o_perm, const float* s, const flo
                           const int32_t* row_of_slot, int T, int d, int k,
                           void* y, void* stream);
 
+/* Self-check of the device-side tensor-map patching that the weight-gradient
+ * GEMMs use (each expert's rows are read through maps re-based on the device
+ * from the offsets): builds the per-group maps of two operands for an offsets
+ * table with empty, one-row and ragged groups and compares each map byte for
+ * byte with the map the driver's encoder gives for the same sub-matrix.  No
+ * tensor copy runs.  Returns MOE_OK, or MOE_ERR_UNSUPPORTED if a map differs.
+ * Allocates and frees its own scratch and synchronizes the device. */
+MOE_API int moe_selftest_group_maps(void);
+
 /* --------------------------------------------------------------- backward */
 
 /* Backward of moe_unpermute_combine, first half: the upstream gradient of

@@ -54,6 +54,7 @@ SIGNATURES = {
     "moe_route_topk_bwd": "pppp" + "iiii" + "ppp" + "pz" + "s",
     "moe_router_balance_loss": "pp" + "iii" + "f" + "ppp" + "pz" + "s",
     "moe_permute_bwd": "ppppp" + "iiii" + "p" + "pz" + "s",
+    "moe_selftest_group_maps": "",
 }
 
 _CT = {"p": _P, "i": _I, "f": ctypes.c_float, "z": _SZ, "s": _P}
@@ -196,3 +197,7 @@ def moe_router_balance_loss(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl
 
 def moe_permute_bwd(dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream=None):
     return _call("moe_permute_bwd", dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream)
+
+
+def moe_selftest_group_maps():
+    return _call("moe_selftest_group_maps")

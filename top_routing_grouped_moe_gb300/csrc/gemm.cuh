@@ -17,8 +17,9 @@
 //           Forward expert GEMMs and activation-gradient (dgrad) GEMMs.
 //   KGROUP  ragged K: group g contracts over rows [off[g], off[g+1]) of A and
 //           B (both stored with K as the row index) into its own output slab.
-//           Weight-gradient (wgrad) GEMMs; tail rows of the last K step that
-//           belong to the next group are zeroed in shared memory.
+//           Weight-gradient (wgrad) GEMMs.  Each group is read through its
+//           own tensor maps (built on the device from the offsets), so the
+//           rows of its last K step past its end arrive as zeros.
 //
 // Split precision (nsplit = 2): one operand is given as a pair of bf16
 // tensors hi + lo (hi = bf16(v), lo = bf16(v - hi), together ~16 mantissa
@@ -64,6 +65,7 @@ constexpr int KG_B_BYTES = 4 * KG_BLOCK_BYTES;
 constexpr int KG_STAGE_BYTES = KG_A_BYTES + 2 * KG_B_BYTES;  // 40 KB
 constexpr int KG_STAGES = 5;
 constexpr int RING = 4;  // tile indices in flight from the producer to the other roles
+constexpr int KG_MAPS_PER_GROUP = 3;  // ragged K, per-group maps: A, B, lo half
 
 enum Mode : int { MGROUP = 0, KGROUP = 1 };
 // Ragged K: which operand comes as hi + lo halves (a compile-time choice, so
@@ -83,6 +85,11 @@ struct Problem {
   int map_a_lo, map_b_lo;  // lo halves of a split operand (-1 = none)
   int nsplit;          // 1, or 2 = every K step issued with the hi and the lo half
   int blk3d;           // ragged K: A, B (and lo) maps are 64-column block views, one box per operand
+  // ragged K with offsets: per-group block-view maps [G][KG_MAPS_PER_GROUP]
+  // (A, B, lo half) on the device, each over its group's rows only, so that
+  // reads past a group's end come back as zeros; K coordinates are then
+  // relative to the group's first row
+  const CUtensorMap* gmaps;
   uint32_t tx_bytes;   // bytes landing per stage
   // epilogue
   void* out;
@@ -370,25 +377,8 @@ __device__ __forceinline__ void load_3d(void* dst, const CUtensorMap* m, uint64_
   else ptx::tma_load_3d_pair(dst, m, bar_leader, c0, c1, c2);
 }
 
-// Ragged K: rows [valid, valid + nrows) of `nblk` consecutive 64 x 32 boxes
-// at `base` belong to the next group (or lie past the end); zero them, whole
-// 128-byte rows (the swizzle permutes within a row only).  One thread.
-__device__ __forceinline__ void zero_box_rows(uint8_t* base, int nblk, int valid, int nrows) {
-  const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int b = 0; b < nblk; ++b) {
-    uint4* row = reinterpret_cast<uint4*>(base + b * KG_BLOCK_BYTES + valid * 128);
-    for (int r = 0; r < nrows; ++r, row += 8) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) row[c] = z;
-    }
-  }
-}
-
 template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params P) {
-  // ragged-K problems zero tail rows in shared memory before the MMAs, which
-  // a CTA pair cannot do for the peer's rows without a round trip, so they
-  // run on single CTAs
   static_assert(!(MODE == KGROUP && PAIR == 2), "ragged-K GEMMs run on single CTAs");
   static_assert(MODE == MGROUP || (AMN == 1 && BMN == 1), "ragged-K operands are MN-major");
   static_assert(MODE == KGROUP || SPLIT == SPLIT_NONE, "ragged-M split operands use consecutive stages");
@@ -509,7 +499,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         const CUtensorMap* mAlo = pr.map_a_lo >= 0 ? &P.maps[pr.map_a_lo] : nullptr;
         const CUtensorMap* mBlo = pr.map_b_lo >= 0 ? &P.maps[pr.map_b_lo] : nullptr;
         const int am = ti.m0 + row_half, bn = ti.n0 + row_half;
-        const int k0 = ti.k0, g = ti.g, nk = ti.nk;
+        int k0 = ti.k0;
+        const int g = ti.g, nk = ti.nk;
+        if (MODE == KGROUP && pr.gmaps != nullptr && nk > 0) {
+          // this group's own maps (written by an earlier launch: acquire them
+          // for the tensor-map proxy); K rows counted from the group's start
+          const CUtensorMap* gm = pr.gmaps + (long long)g * KG_MAPS_PER_GROUP;
+          mA = gm;
+          mB = gm + 1;
+          if (SPLIT == SPLIT_A) mAlo = gm + 2;
+          if (SPLIT == SPLIT_B) mBlo = gm + 2;
+          ptx::tmap_acquire(mA);
+          ptx::tmap_acquire(mB);
+          if (SPLIT != SPLIT_NONE) ptx::tmap_acquire(gm + 2);
+          k0 = 0;
+        }
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait_bounded(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
@@ -629,37 +633,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         // per-tile values in registers (see the producer)
         const uint32_t idesc = ptx::idesc_bf16(TILE_M, pr.mma_n, AMN, BMN);
         const int nk = ti.nk, k_left = ti.k1 - ti.k0;
-        // Rows from the last group's end up to `extent` are inside the
-        // caller's buffers but were never written (a capacity drop leaves
-        // them untouched): they may hold NaN, and 0 * NaN is NaN.  A tail step
-        // whose 16-row MMAs reach past that end (the last group's, or an
-        // earlier one's when the groups after it are short) zeroes B's tail
-        // rows too.  Past `extent` TMA fills zeros.
-        const int data_end = MODE == KGROUP ? min(S.off[ti.p][pr.G], pr.extent) : 0;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
+          // Ragged K: the rows of a group's last step past its end are zeros
+          // (per-group maps, or TMA's fill past `extent`), and a 16-row
+          // sub-step entirely past the end is not issued.
           const bool tail_step = MODE == KGROUP && (kb + 1) * BKK > k_left;
-          if (tail_step) {
-            // The group's last step reads rows that belong to the next groups
-            // (or lie past the end).  Rows [valid, 16 * ceil(valid / 16)) of A
-            // (and of A's lo half) are zeroed: their products with B then
-            // vanish where B's rows are later groups' (finite) data.
-            const int valid = k_left - kb * BKK;
-            const int nrows = ((valid + UMMA_K - 1) / UMMA_K) * UMMA_K - valid;
-            if (nrows > 0) {
-              uint8_t* st = smem + stage * KG_STAGE_BYTES;
-              zero_box_rows(st, 2, valid, nrows);
-              if (SPLIT == SPLIT_A) zero_box_rows(st + KG_A_BYTES + KG_B_BYTES, 2, valid, nrows);
-              if (ti.k0 + kb * BKK + valid + nrows > data_end) {
-                zero_box_rows(st + KG_A_BYTES, 4, valid, nrows);
-                if (SPLIT == SPLIT_B) zero_box_rows(st + KG_A_BYTES + KG_B_BYTES, 4, valid, nrows);
-              }
-              ptx::fence_proxy_async_smem();
-            }
-          }
           ptx::tc_fence_after();
           if (MODE == MGROUP) {
             const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);

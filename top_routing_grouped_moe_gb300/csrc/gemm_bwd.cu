@@ -145,8 +145,10 @@ cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, 
   return launch<0, 1, MGROUP, EPI_F32, kPair>(P, bound, s);
 }
 
-cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* tile_counter, int* status,
-                       cudaStream_t s) {
+size_t group_maps_bytes(int G) { return (size_t)G * KG_MAPS_PER_GROUP * sizeof(CUtensorMap); }
+
+cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* tile_counter, void* group_maps,
+                       int* status, cudaStream_t s) {
   (void)status;
   Params P;
   std::memset(&P, 0, sizeof(P));
@@ -154,10 +156,36 @@ cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* ti
   // dynamic schedule starts the heaviest tiles first
   const WgradArgs* order[2] = {shared ? shared : &routed, shared ? &routed : nullptr};
   long long bound = 0;
+  int with_offsets = 0;
   for (int i = 0; i < 2 && order[i]; ++i) {
-    if (!fill_wgrad(P, P.prob[i], *order[i])) return cudaErrorInvalidValue;
-    bound += (long long)order[i]->G * cdiv_h(order[i]->M, BM) * cdiv_h(order[i]->N, 256);
+    const WgradArgs& a = *order[i];
+    Problem& pr = P.prob[i];
+    if (!fill_wgrad(P, pr, a)) return cudaErrorInvalidValue;
+    bound += (long long)a.G * cdiv_h(a.M, BM) * cdiv_h(a.N, 256);
     P.num_problems = i + 1;
+    if (a.offsets) {
+      // per-group maps of A, B and the lo half, built on the device before
+      // the GEMM (one scratch area: at most one problem has offsets)
+      if (!group_maps || with_offsets++ > 0) return cudaErrorInvalidValue;
+      const void* lo = a.A_lo ? a.A_lo : a.B_lo;
+      const int nmaps = lo ? 3 : 2;
+      CUtensorMap whole[KG_MAPS_PER_GROUP] = {P.maps[pr.map_a], P.maps[pr.map_b]};
+      if (lo) whole[2] = P.maps[a.A_lo ? pr.map_a_lo : pr.map_b_lo];
+      const void* base[KG_MAPS_PER_GROUP] = {a.A, a.B, lo};
+      const uint64_t cols[KG_MAPS_PER_GROUP] = {(uint64_t)a.M, (uint64_t)a.N, (uint64_t)(a.A_lo ? a.M : a.N)};
+      const uint32_t nblk[KG_MAPS_PER_GROUP] = {2, 4, a.A_lo ? 2u : 4u};
+      CUtensorMap whole_1row[KG_MAPS_PER_GROUP];
+      uint64_t rb[KG_MAPS_PER_GROUP];
+      for (int m = 0; m < nmaps; ++m) {
+        rb[m] = cols[m] * 2;
+        if (!encode_blocks(&whole_1row[m], base[m], cols[m], 1, BKK, nblk[m])) return cudaErrorInvalidValue;
+      }
+      CUtensorMap* gm = static_cast<CUtensorMap*>(group_maps);
+      cudaError_t e =
+          launch_group_maps(whole, whole_1row, base, rb, nmaps, a.offsets, a.G, a.rows_total, gm, s);
+      if (e != cudaSuccess) return e;
+      pr.gmaps = gm;
+    }
   }
   P.tile_counter = tile_counter;
   // ragged K: single CTAs; both problems split the same operand

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace moe {
@@ -110,9 +111,19 @@ struct WgradArgs {        // out[g] = A_g^T B_g over rows [off[g], off[g+1])
 };
 cudaError_t gemm_dgrad_down(const DgradDownArgs& routed, const DgradDownArgs* shared, int* status, cudaStream_t s);
 cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, int* status, cudaStream_t s);
-// `tile_counter`: one device int, zeroed by the launch (dynamic tile schedule)
-cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* tile_counter, int* status,
-                       cudaStream_t s);
+// `tile_counter`: one device int, zeroed by the launch (dynamic tile schedule);
+// `group_maps`: device scratch of group_maps_bytes(G) bytes (128-byte
+// aligned) for the per-group tensor maps of a problem with offsets
+cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* tile_counter, void* group_maps,
+                       int* status, cudaStream_t s);
+size_t group_maps_bytes(int G);
+// Per-group maps: for each group g and operand m, a block view of the whole
+// [extent, cols] buffer at base[m] re-based at row off[g] with off[g+1] -
+// off[g] rows; out[g * 3 + m] in device memory.  `whole` is encoded with the
+// buffer's rows, `whole_1row` with one row (same box).
+cudaError_t launch_group_maps(const CUtensorMap* whole, const CUtensorMap* whole_1row, const void* const* base,
+                              const uint64_t* row_bytes, int nmaps, const int32_t* offsets, int G, int extent,
+                              CUtensorMap* out, cudaStream_t s);
 // dW_r partials: part[S, E, d] = split-K pieces of (dl_hi + dl_lo)^T x; dl halves [T, E] bf16
 cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* x, int T, int d, int E, int S,
                            float* part, int* status, cudaStream_t s);

@@ -52,7 +52,7 @@ size_t ws_permute_bwd(int T, int E) { return 2 * align256((size_t)T * E * 2); }
 // gate-gradient partials [rows, ceil(H/256)], for the routed rows (T*k) and the
 // shared expert (T rows).
 struct SwigluBwdWs {
-  size_t dau_hi, dau_lo, gh_hi, gh_lo, dgp, s_dau_hi, s_dau_lo, s_gh_hi, s_gh_lo, tile_counter, total;
+  size_t dau_hi, dau_lo, gh_hi, gh_lo, dgp, s_dau_hi, s_dau_lo, s_gh_hi, s_gh_lo, tile_counter, group_maps, total;
 };
 SwigluBwdWs swiglu_bwd_ws(int T, int k, int H, int Hs) {
   SwigluBwdWs w;
@@ -69,6 +69,7 @@ SwigluBwdWs swiglu_bwd_ws(int T, int k, int H, int Hs) {
   w.s_gh_hi = take((size_t)T * Hs * 2);
   w.s_gh_lo = take((size_t)T * Hs * 2);
   w.tile_counter = take(sizeof(int));  // dynamic tile schedule of the weight-gradient GEMMs
+  w.group_maps = take(group_maps_bytes(kMaxE));  // their per-expert tensor maps
   w.total = off;
   return w;
 }
@@ -302,7 +303,8 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   WgradArgs r2{dY_perm, nullptr, w + L.gh_hi, w + L.gh_lo, R, offsets, E, d, H, dW_d, nullptr, 0};
   WgradArgs s2{dY, nullptr, w + L.s_gh_hi, w + L.s_gh_lo, T, nullptr, 1, d, Hs, dWs_d, nullptr, 0};
   int* tile_counter = reinterpret_cast<int*>(w + L.tile_counter);
-  e = gemm_wgrad(r2, Hs > 0 ? &s2 : nullptr, tile_counter, status, st);
+  void* group_maps = w + L.group_maps;
+  e = gemm_wgrad(r2, Hs > 0 ? &s2 : nullptr, tile_counter, group_maps, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
 
   // 3. dx_perm = [da|du] [W_g; W_u]
@@ -316,7 +318,7 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   // 4. [dW_g; dW_u] = [da|du]^T x_perm, [da|du] split into bf16 hi + lo
   WgradArgs r4{w + L.dau_hi, w + L.dau_lo, x_perm, nullptr, R, offsets, E, 2 * H, d, dW_g, dW_u, H};
   WgradArgs s4{w + L.s_dau_hi, w + L.s_dau_lo, x, nullptr, T, nullptr, 1, 2 * Hs, d, dWs_g, dWs_u, Hs};
-  return check(gemm_wgrad(r4, Hs > 0 ? &s4 : nullptr, tile_counter, status, st));
+  return check(gemm_wgrad(r4, Hs > 0 ? &s4 : nullptr, tile_counter, group_maps, status, st));
 }
 
 int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* topk_idx, const void* x, int T, int d,

@@ -104,6 +104,27 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
 }
 
 // ------------------------------------------------------------------ TMA
+// Tensor maps patched on the device: a copy in shared memory (128-byte
+// aligned) gets a new global address and a new extent of one dimension, then
+// goes out to global memory with a release of the tensor-map proxy (the whole
+// warp executes the copy); a kernel using such a map acquires it first.
+__device__ __forceinline__ void tmap_set_address(CUtensorMap* smem_map, const void* gaddr) {
+  asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;"
+               ::"r"(smem_u32(smem_map)), "l"(reinterpret_cast<uint64_t>(gaddr)) : "memory");
+}
+template <int ORD>
+__device__ __forceinline__ void tmap_set_dim(CUtensorMap* smem_map, uint32_t extent) {
+  asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], %1, %2;"
+               ::"r"(smem_u32(smem_map)), "n"(ORD), "r"(extent) : "memory");
+}
+__device__ __forceinline__ void tmap_publish(CUtensorMap* gdst, const CUtensorMap* smem_src) {
+  asm volatile("tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], 128;"
+               ::"l"(reinterpret_cast<uint64_t>(gdst)), "r"(smem_u32(smem_src)) : "memory");
+}
+__device__ __forceinline__ void tmap_acquire(const CUtensorMap* gmap) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(gmap))
+               : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
