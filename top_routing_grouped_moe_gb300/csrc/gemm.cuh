@@ -62,8 +62,6 @@ constexpr int BKK = 32;
 constexpr int KG_BLOCK_BYTES = 64 * BKK * 2;
 constexpr int KG_A_BYTES = 2 * KG_BLOCK_BYTES;
 constexpr int KG_B_BYTES = 4 * KG_BLOCK_BYTES;
-constexpr int KG_STAGE_BYTES = KG_A_BYTES + 2 * KG_B_BYTES;  // 40 KB
-constexpr int KG_STAGES = 5;
 constexpr int RING = 4;  // tile indices in flight from the producer to the other roles
 constexpr int KG_MAPS_PER_GROUP = 3;  // ragged K, per-group maps: A, B, lo half
 
@@ -71,6 +69,16 @@ enum Mode : int { MGROUP = 0, KGROUP = 1 };
 // Ragged K: which operand comes as hi + lo halves (a compile-time choice, so
 // that each kernel issues its MMAs from one straight-line sequence)
 enum Split : int { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2 };
+
+// Ragged-K stage: A (2 blocks) | B (4 blocks) | the lo half of the split
+// operand (A's 2 blocks or B's 4), sized for that split so that as many
+// stages as fit in ~200 KB are in flight: 24 KB x 8, 32 KB x 6, 40 KB x 5
+template <int SPLIT>
+struct KgCfg {
+  static constexpr int STAGE_BYTES =
+      KG_A_BYTES + KG_B_BYTES + (SPLIT == SPLIT_A ? KG_A_BYTES : SPLIT == SPLIT_B ? KG_B_BYTES : 0);
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
+};
 enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3, EPI_REDUCE_DX = 4 };
 
 struct Problem {
@@ -164,16 +172,17 @@ struct SmemTailT {
 // stages for them (it is not what bounds that launch)
 constexpr int AU_CHUNK_BYTES = 2 * 32 * 32 * 4;
 
-template <int MODE, int EPI, int PAIR>
+template <int MODE, int EPI, int PAIR, int SPLIT>
 struct StageCfg {
-  static constexpr int STAGES = MODE == KGROUP ? KG_STAGES : (EPI == EPI_SWIGLU_BWD ? 4 : PairCfg<PAIR>::STAGES);
-  static constexpr int BYTES = MODE == KGROUP ? KG_STAGE_BYTES : A_BYTES + PairCfg<PAIR>::B_BYTES;
+  static constexpr int STAGES =
+      MODE == KGROUP ? KgCfg<SPLIT>::STAGES : (EPI == EPI_SWIGLU_BWD ? 4 : PairCfg<PAIR>::STAGES);
+  static constexpr int BYTES = MODE == KGROUP ? KgCfg<SPLIT>::STAGE_BYTES : A_BYTES + PairCfg<PAIR>::B_BYTES;
   static constexpr int EPI_BYTES = EPI == EPI_SWIGLU_BWD ? 4 * 2 * AU_CHUNK_BYTES : 0;
 };
 
-template <int MODE, int EPI, int PAIR>
+template <int MODE, int EPI, int PAIR, int SPLIT>
 constexpr size_t smem_bytes() {
-  using C = StageCfg<MODE, EPI, PAIR>;
+  using C = StageCfg<MODE, EPI, PAIR, SPLIT>;
   return 1024 + C::STAGES * C::BYTES + C::EPI_BYTES + sizeof(SmemTailT<C::STAGES>);
 }
 
@@ -383,13 +392,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
   static_assert(MODE == MGROUP || (AMN == 1 && BMN == 1), "ragged-K operands are MN-major");
   static_assert(MODE == KGROUP || SPLIT == SPLIT_NONE, "ragged-M split operands use consecutive stages");
   using Cfg = PairCfg<PAIR>;
-  using SC = StageCfg<MODE, EPI, PAIR>;
+  using SC = StageCfg<MODE, EPI, PAIR, SPLIT>;
   constexpr int STAGES = SC::STAGES;
   constexpr int B_BYTES = Cfg::B_BYTES;
   constexpr int TILE_M = Cfg::TILE_M;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // ragged M: A ring then B ring; ragged K: stage s at smem + s * KG_STAGE_BYTES
+  // ragged M: A ring then B ring; ragged K: stage s at smem + s * SC::BYTES
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   using Tail = SmemTailT<STAGES>;
@@ -527,7 +536,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           if (MODE == KGROUP) {
             // A (2 blocks) | B (nblk blocks) | lo half of A or of B
             const int k = k0 + kb * BKK;
-            uint8_t* st = smem + stage * KG_STAGE_BYTES;
+            uint8_t* st = smem + stage * SC::BYTES;
             uint8_t* lo = st + KG_A_BYTES + KG_B_BYTES;
             if (blk3d) {
               // one instruction per operand (a TMA load's issue cost barely
@@ -660,7 +669,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           } else {
             // 32 K rows: per 16-row sub-step one MMA, plus one with the lo half
             // of the split operand; a full step is one straight-line sequence
-            const uint32_t sa = ptx::smem_u32(smem + stage * KG_STAGE_BYTES), sb = sa + KG_A_BYTES,
+            const uint32_t sa = ptx::smem_u32(smem + stage * SC::BYTES), sb = sa + KG_A_BYTES,
                            sl = sb + KG_B_BYTES;
             const uint64_t a0 = ptx::smem_desc(sa, KG_BLOCK_BYTES, 1024), a1 = ptx::smem_desc(sa + 2048, KG_BLOCK_BYTES, 1024);
             const uint64_t b0 = ptx::smem_desc(sb, KG_BLOCK_BYTES, 1024), b1 = ptx::smem_desc(sb + 2048, KG_BLOCK_BYTES, 1024);

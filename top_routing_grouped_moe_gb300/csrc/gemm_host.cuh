@@ -113,7 +113,7 @@ inline Problem blank_problem() {
 template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT = SPLIT_NONE>
 cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR, SPLIT>;
-  constexpr size_t smem = smem_bytes<MODE, EPI, PAIR>();
+  constexpr size_t smem = smem_bytes<MODE, EPI, PAIR, SPLIT>();
   static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
