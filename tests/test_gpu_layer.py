@@ -29,6 +29,11 @@ CASES = {
     "random_many_experts": workloads.custom("random_many_experts", T=512, d=256, E=64, k=4, H=128, Hs=128,
                                             routing="random"),
     "partial_tiles": workloads.custom("partial_tiles", T=300, d=384, E=8, k=2, H=384, Hs=384),
+    # every buffer below 128 KiB: all per-expert tensor maps from the one-row class
+    "micro_small_maps": workloads.custom("micro_small_maps", T=24, d=256, E=8, k=2, H=128, Hs=128),
+    # the largest E and k: most experts hold 0-6 rows
+    "e256_k8": workloads.custom("e256_k8", T=64, d=256, E=256, k=8, H=128, Hs=0),
+    "single_token": workloads.custom("single_token", T=1, d=256, E=8, k=2, H=128, Hs=128),
 }
 
 
