@@ -94,7 +94,8 @@ def launches_per_step(w):
     n += 2                                                 # grouped swiglu: gate/up, down
     n += 1                                                 # combine
     n += 1                                                 # combine bwd (gather)
-    n += 5                                                 # swiglu bwd: dgrad-down, dgates, wgrad-down, dgrad-gu, wgrad-gu
+    n += 5 + 2                                             # swiglu bwd: dgrad-down, dgates, wgrad-down, dgrad-gu,
+    #                                                        wgrad-gu, and the per-expert map kernel before each wgrad
     if w.routing == "learned":
         S = max(1, min(64, w.T // 512))
         n += 2 + (1 if S > 1 else 0)                       # router bwd: dl, dW_r GEMM, split-K reduce
