@@ -27,6 +27,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -152,8 +153,14 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu_index = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "",
-                                 f"clocks_rank{gpu_index}.csv")
+        # the raw samples go to MOE_BENCH_CLOCKS_CSV (kept) or a temporary
+        # file (removed once summarised)
+        self.keep = os.environ.get("MOE_BENCH_CLOCKS_CSV")
+        if self.keep:
+            self.path = self.keep.replace("{rank}", str(gpu_index))
+        else:
+            fd, self.path = tempfile.mkstemp(prefix=f"moe_clocks_{gpu_index}_", suffix=".csv")
+            os.close(fd)
 
     def start(self):
         try:
@@ -164,8 +171,16 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def _discard(self):
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
+
     def stop(self):
         if self.proc is None:
+            self._discard()
             return None
         self.proc.terminate()
         try:
@@ -187,6 +202,7 @@ class ClockSampler:
                                parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(name)
+        self._discard()
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
