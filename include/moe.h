@@ -221,6 +221,15 @@ MOE_API int moe_unpermute_combine(const float* o_perm, const float* s, const flo
  * Allocates and frees its own scratch and synchronizes the device. */
 MOE_API int moe_selftest_group_maps(void);
 
+/* Self-check of the failure detection: one warp waits, through the bounded
+ * wait every GEMM uses, on an mbarrier phase that nothing completes, for
+ * limit_us microseconds (1 .. 2,000,000).  The wait then gives up and the
+ * kernel records MOE_ERR_TIMEOUT in the device status word (read and cleared
+ * by moe_device_status()) and returns: no trap, no fault, the context stays
+ * usable.  Asynchronous on `stream`; returns MOE_ERR_INVALID_ARG for a limit
+ * out of range. */
+MOE_API int moe_selftest_wait_timeout(int limit_us, void* stream);
+
 /* --------------------------------------------------------------- backward */
 
 /* Backward of moe_unpermute_combine, first half: the upstream gradient of

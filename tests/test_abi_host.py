@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) >= 15
+    assert len(names) >= 17
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
@@ -87,6 +87,9 @@ P = 1 << 12  # stand-in device addresses (16-byte aligned); never dereferenced
     (lambda L: L.moe_grouped_swiglu_recompute(P, P, P, 16, 128, 8, 2, 128, 128, P, P, P, P, P, None, 0), 1),
     # recompute: hidden width not a multiple of 128
     (lambda L: L.moe_grouped_swiglu_recompute(P, P, None, 16, 128, 8, 2, 96, 0, P, P, None, None, P, None, 0), 2),
+    # failure self-check: limit out of range
+    (lambda L: L.moe_selftest_wait_timeout(0, 0), 1),
+    (lambda L: L.moe_selftest_wait_timeout(3_000_000, 0), 1),
     # combine: null y
     (lambda L: L.moe_unpermute_combine(P, None, P, P, 16, 128, 2, None, 0), 1),
     # backward workspace too small

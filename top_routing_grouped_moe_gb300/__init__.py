@@ -8,7 +8,7 @@ ImportError (there is no CPU fallback)."""
 _BINDING_NAMES = {
     "moe_route_topk", "moe_permute", "moe_permute_static", "moe_grouped_swiglu", "moe_unpermute_combine",
     "moe_unpermute_combine_bwd", "moe_grouped_swiglu_bwd", "moe_route_topk_bwd", "moe_permute_bwd",
-    "moe_router_balance_loss", "moe_grouped_swiglu_recompute", "moe_selftest_group_maps",
+    "moe_router_balance_loss", "moe_grouped_swiglu_recompute", "moe_selftest_group_maps", "moe_selftest_wait_timeout",
     "moe_workspace_size", "moe_version", "moe_device_status", "MoEError", "status_string",
 }
 

@@ -55,6 +55,7 @@ SIGNATURES = {
     "moe_router_balance_loss": "pp" + "iii" + "f" + "ppp" + "pz" + "s",
     "moe_permute_bwd": "ppppp" + "iiii" + "p" + "pz" + "s",
     "moe_selftest_group_maps": "",
+    "moe_selftest_wait_timeout": "i" + "s",
 }
 
 _CT = {"p": _P, "i": _I, "f": ctypes.c_float, "z": _SZ, "s": _P}
@@ -201,3 +202,7 @@ def moe_permute_bwd(dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws
 
 def moe_selftest_group_maps():
     return _call("moe_selftest_group_maps")
+
+
+def moe_selftest_wait_timeout(limit_us, stream=None):
+    return _call("moe_selftest_wait_timeout", limit_us, stream)
