@@ -362,19 +362,3 @@ def balance_loss(logits: np.ndarray, idx: np.ndarray, E: int, alpha: float):
     L = alpha * E * float(f @ P)
     dl = (alpha * E / T) * p * (f[None, :] - (p @ f)[:, None])
     return L, f, P, dl
-
-
-# --------------------------------------------------------------------------
-# one token / one expert at a time (for sampled checks at full sizes)
-# --------------------------------------------------------------------------
-def token_output(x_t: np.ndarray, experts: list, gates_t: np.ndarray, kept_t: np.ndarray,
-                 shared=None):
-    """y[t] for one token from its own expert weights.  experts: list of
-    (Wg, Wu, Wd) float64 for its k slots; shared: (Wsg, Wsu, Wsd) or None."""
-    y = np.zeros(x_t.shape[-1])
-    if shared is not None:
-        y += swiglu_fwd(x_t[None, :], *shared)[3][0]
-    for s_, (Wg, Wu, Wd) in enumerate(experts):
-        if kept_t[s_]:
-            y += gates_t[s_] * swiglu_fwd(x_t[None, :], Wg, Wu, Wd)[3][0]
-    return y

@@ -350,3 +350,113 @@ def test_balance_loss_invariants():
     # balanced assignments and equal logits: L = alpha exactly
     idx_b = np.array([[(t * k + s) % E for s in range(k)] for t in range(E)])
     assert abs(orc.balance_loss(np.zeros((E, E)), idx_b, E, 0.3)[0] - 0.3) < 1e-12
+
+
+# ---------------------------------------------------------------- bf16 decode
+# Hand-written bf16 bit patterns and the values the format definition gives
+# them (sign | 8-bit exponent, bias 127 | 7-bit mantissa; exponent 0 =
+# subnormal with scale 2^-126).
+BF16_KNOWN = [
+    (0x0000, 0.0), (0x8000, -0.0), (0x3F80, 1.0), (0xC040, -3.0), (0x4049, 3.140625),
+    (0x3C00, 2.0 ** -7), (0x0001, 2.0 ** -133), (0x007F, 127 * 2.0 ** -133), (0x0080, 2.0 ** -126),
+    (0x7F7F, 255 * 2.0 ** 120), (0xFF7F, -255 * 2.0 ** 120), (0x7F80, math.inf), (0xFF80, -math.inf),
+]
+
+
+def test_bf16_to_f64_known_values():
+    bits = np.array([b for b, _ in BF16_KNOWN], dtype=np.uint16)
+    got = orc.bf16_to_f64(bits)
+    assert got.dtype == np.float64
+    for (b, want), g in zip(BF16_KNOWN, got):
+        assert g == want and math.copysign(1.0, g) == math.copysign(1.0, want), (hex(b), g, want)
+    # a 2-D array keeps its shape
+    assert orc.bf16_to_f64(bits[:12].reshape(3, 4)).shape == (3, 4)
+
+
+# ---------------------------------------------------------------- router bias
+BIAS_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "router_bias_hand.json")
+
+
+def _bias_case(c):
+    x = orc.bf16_to_f64(np.array([[int(h, 16) for h in c["x_bits"]]], dtype=np.uint16))
+    W_r = orc.bf16_to_f64(np.array([[int(h, 16) for h in row] for row in c["W_r_bits"]], dtype=np.uint16))
+    bias = np.array(c["bias"], dtype=np.float32)
+    return x, W_r, bias
+
+
+def _k2_gates(c):
+    if "gates" in c["k2"]:
+        return np.array([c["k2"]["gates"]])
+    z = math.exp(-1.0 / 8.0)  # the closed form the second case states
+    return np.array([[1.0 / (1.0 + z), z / (1.0 + z)]])
+
+
+def check_router_bias_golden(layer_forward=None, router_logits=None):
+    """The golden cases through the oracle's router and through its whole
+    forward (identity experts), so that the bias is pinned where the layer
+    applies it: in the fp32 logits that both the selection and the gates
+    use."""
+    layer_forward = layer_forward or orc.layer_forward
+    router_logits = router_logits or orc.router_logits
+    for c in json.load(open(BIAS_GOLDEN))["cases"]:
+        x, W_r, bias = _bias_case(c)
+        l = router_logits(x, W_r, bias)
+        assert l.dtype == np.float32, c["name"]
+        assert l[0].tolist() == c["logits"], (c["name"], l[0].tolist())
+        for k, key in ((1, "k1"), (2, "k2")):
+            f = layer_forward({"x": x, "W_r": W_r, "bias": bias}, k, 0, expert_fn=lambda e, xr: xr)
+            assert f["idx"].tolist() == [c[key]["idx"]], (c["name"], k, f["idx"].tolist())
+            want = np.array([c[key]["gates"]]) if k == 1 else _k2_gates(c)
+            np.testing.assert_allclose(f["gates"], want, rtol=0, atol=1e-15, err_msg=f"{c['name']} k={k}")
+
+
+def test_router_bias_golden():
+    check_router_bias_golden()
+
+
+def test_router_bias_moves_selection_and_gates():
+    """A large bias on one expert puts it first for every token, and the gates
+    are the softmax of the biased logits over the selection."""
+    T, d, E, k = 64, 32, 8, 2
+    x = orc.bf16_to_f64(gen.normal_bf16(501, (T, d)))
+    W_r = orc.bf16_to_f64(gen.normal_bf16(502, (E, d), std=0.02))
+    bias = np.zeros(E, dtype=np.float32)
+    bias[5] = 30.0
+    f = orc.layer_forward({"x": x, "W_r": W_r, "bias": bias}, k, 0, expert_fn=lambda e, xr: xr)
+    assert np.all(f["idx"][:, 0] == 5)
+    l = (x @ W_r.T).astype(np.float32) + bias  # fp32 product, then the fp32 add
+    sel = np.take_along_axis(l.astype(np.float64), f["idx"].astype(np.int64), axis=1)
+    g = np.exp(sel - sel[:, :1])
+    np.testing.assert_allclose(f["gates"], g / g.sum(axis=1, keepdims=True), rtol=1e-12)
+    assert np.all(f["gates"][:, 0] > 0.999)  # the gap of ~30 is in the gates too
+
+
+def test_router_bias_pins_catch_planted_mistakes():
+    """Each plausible mistake in the bias branch, planted in a copy of the
+    oracle's router on the CPU, fails the golden check."""
+    def fp64_add(x, W_r, bias=None):  # bias added before the fp32 rounding
+        return (x @ W_r.T + np.asarray(bias, dtype=np.float64)[None, :]).astype(np.float32)
+
+    def sign_flip(x, W_r, bias=None):
+        return (x @ W_r.T).astype(np.float32) - np.asarray(bias, dtype=np.float32)[None, :]
+
+    def no_bias(x, W_r, bias=None):
+        return (x @ W_r.T).astype(np.float32)
+
+    def selection_only(inp, k, cap, expert_fn=None):  # gates from the unbiased logits
+        f = orc.layer_forward(inp, k, cap, expert_fn=expert_fn)
+        l0 = (inp["x"] @ inp["W_r"].T).astype(np.float32).astype(np.float64)
+        sel = np.take_along_axis(l0, f["idx"].astype(np.int64), axis=1)
+        g = np.exp(sel - sel.max(axis=1, keepdims=True))
+        return orc.layer_forward(inp, k, cap, expert_fn=expert_fn, gates=g / g.sum(axis=1, keepdims=True))
+
+    for bad in (fp64_add, sign_flip, no_bias):
+        saved = orc.router_logits
+        orc.router_logits = bad
+        try:
+            with pytest.raises(AssertionError):
+                check_router_bias_golden()
+        finally:
+            orc.router_logits = saved
+    with pytest.raises(AssertionError):
+        check_router_bias_golden(layer_forward=selection_only)
