@@ -7,10 +7,19 @@
 
 namespace moe {
 
+// argument checks shared by every entry point (MOE_OK or the ABI's error code)
+int check_dims(int T, int d, int E, int k);  // limits of T, d, E, k
+int check_hidden(int H, int Hs);             // limits of H and Hs
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 // per-device facts and the device status word
 int device_sm_count();
 int* device_status_ptr();  // device address of the status word of the current device
 void record_cuda_error(cudaError_t e);  // what moe_last_cuda_error() reports in this thread
+// Launch timing (moe_timing_begin): records the caller's next event on `s`
+// and notes `name` (a string literal) when timing is on in this thread; called
+// just before every kernel launch or memset the library issues.
+void timing_mark(cudaStream_t s, const char* name);
 
 // ------------------------------------------------------------ SIMT kernels
 cudaError_t launch_topk_gating(const float* logits, int T, int E, int k, int32_t* idx, float* gates,
@@ -115,7 +124,7 @@ cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, 
 // `group_maps`: device scratch of group_maps_bytes(G) bytes (128-byte
 // aligned) for the per-group tensor maps of a problem with offsets
 cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* tile_counter, void* group_maps,
-                       int* status, cudaStream_t s);
+                       int* status, cudaStream_t s, const char* name);
 size_t group_maps_bytes(int G);
 // Per-group maps: for each group g and operand m, a block view of the whole
 // [extent, cols] buffer at base[m] re-based at row off[g] with off[g+1] -

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "../../include/moe.h"
 #include "common.cuh"
@@ -13,6 +14,8 @@ namespace moe {
 
 // Device status word: kernels record the first device-side error here.
 __device__ int g_moe_status = 0;
+// Where moe_device_status() puts the value it exchanged out of the word.
+__device__ int g_moe_status_out = 0;
 
 namespace {
 thread_local int t_last_cuda_error = 0;
@@ -20,26 +23,23 @@ std::mutex g_dev_mu;
 int g_sm_count[64] = {0};
 int* g_status_ptr[64] = {nullptr};
 
+// launch timing of the calling thread (moe_timing_begin / _end)
+struct LaunchTiming {
+  bool on = false;
+  void* const* events = nullptr;
+  int capacity = 0;
+  int n = 0;
+  std::vector<const char*> names;
+};
+thread_local LaunchTiming t_timing;
+
 inline int fail_cuda(cudaError_t e) {
   t_last_cuda_error = static_cast<int>(e);
   return MOE_ERR_CUDA;
 }
 inline int check(cudaError_t e) { return e == cudaSuccess ? MOE_OK : fail_cuda(e); }
 
-inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
-
-int check_dims(int T, int d, int E, int k) {
-  if (T < 1 || d < 1 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
-  if (k > kMaxK || k > E || E > kMaxE || (E % 8) != 0 || (d % 64) != 0) return MOE_ERR_UNSUPPORTED;
-  if ((long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
-  return MOE_OK;
-}
-int check_hidden(int H, int Hs) {
-  if (H < 128 || (H % 128) != 0) return MOE_ERR_UNSUPPORTED;
-  if (Hs < 0 || (Hs % 128) != 0) return MOE_ERR_UNSUPPORTED;
-  return MOE_OK;
-}
 
 // workspace of each call
 size_t ws_route_topk_bwd(int T, int d, int E) {
@@ -75,9 +75,36 @@ SwigluBwdWs swiglu_bwd_ws(int T, int k, int H, int Hs) {
 }
 size_t ws_swiglu_bwd(int T, int k, int H, int Hs) { return swiglu_bwd_ws(T, k, H, Hs).total; }
 
+// Reads the status word and sets it to zero in one atomic step, so a code
+// recorded by a kernel still running cannot fall between the read and the
+// clear.
+__global__ void status_exchange_kernel(int* status, int* out) { *out = atomicExch(status, 0); }
+
 }  // namespace
 
+int check_dims(int T, int d, int E, int k) {
+  if (T < 1 || d < 1 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || k > E || E > kMaxE || (E % 8) != 0 || (d % 64) != 0) return MOE_ERR_UNSUPPORTED;
+  if ((long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+int check_hidden(int H, int Hs) {
+  if (H < 128 || (H % 128) != 0) return MOE_ERR_UNSUPPORTED;
+  if (Hs < 0 || (Hs % 128) != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
 void record_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
+
+void timing_mark(cudaStream_t s, const char* name) {
+  LaunchTiming& lt = t_timing;
+  if (!lt.on) return;
+  if (lt.n < lt.capacity) {
+    cudaEventRecord(static_cast<cudaEvent_t>(lt.events[lt.n]), s);
+    lt.names.push_back(name);
+  }
+  ++lt.n;
+}
 
 int device_sm_count() {
   int dev = 0;
@@ -127,14 +154,50 @@ int moe_last_cuda_error(void) { return t_last_cuda_error; }
 
 int moe_device_status(int* status_out) {
   if (!status_out) return MOE_ERR_INVALID_ARG;
-  int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_moe_status, sizeof(int));
+  int* st = device_status_ptr();
+  if (!st) return fail_cuda(cudaErrorInvalidSymbol);
+  // one thread swaps the word for 0 and leaves the old value in
+  // g_moe_status_out, which is copied back once that kernel has run
+  int* out = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&out), g_moe_status_out);
   if (e != cudaSuccess) return fail_cuda(e);
-  const int zero = 0;
-  e = cudaMemcpyToSymbol(g_moe_status, &zero, sizeof(int));
+  status_exchange_kernel<<<1, 1>>>(st, out);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e);
+  int v = 0;
+  e = cudaMemcpy(&v, out, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return fail_cuda(e);
   *status_out = v;
   return MOE_OK;
+}
+
+int moe_timing_begin(void* const* events, int capacity) {
+  if (capacity < 0 || (capacity > 0 && !events)) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < capacity; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  LaunchTiming& lt = t_timing;
+  lt.on = true;
+  lt.events = events;
+  lt.capacity = capacity;
+  lt.n = 0;
+  lt.names.clear();
+  lt.names.reserve(capacity);
+  return MOE_OK;
+}
+
+int moe_timing_end(int* n_launches) {
+  LaunchTiming& lt = t_timing;
+  if (!lt.on) return MOE_ERR_INVALID_ARG;
+  lt.on = false;
+  lt.events = nullptr;
+  if (n_launches) *n_launches = lt.n;
+  return MOE_OK;
+}
+
+const char* moe_timing_name(int i) {
+  const LaunchTiming& lt = t_timing;
+  if (i < 0 || i >= static_cast<int>(lt.names.size())) return "";
+  return lt.names[i];
 }
 
 int moe_workspace_size(int T, int d, int E, int k, int H, int Hs, size_t* bytes) {
@@ -304,7 +367,7 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   WgradArgs s2{dY, nullptr, w + L.s_gh_hi, w + L.s_gh_lo, T, nullptr, 1, d, Hs, dWs_d, nullptr, 0};
   int* tile_counter = reinterpret_cast<int*>(w + L.tile_counter);
   void* group_maps = w + L.group_maps;
-  e = gemm_wgrad(r2, Hs > 0 ? &s2 : nullptr, tile_counter, group_maps, status, st);
+  e = gemm_wgrad(r2, Hs > 0 ? &s2 : nullptr, tile_counter, group_maps, status, st, "gemm_wgrad_down");
   if (e != cudaSuccess) return fail_cuda(e);
 
   // 3. dx_perm = [da|du] [W_g; W_u]
@@ -318,7 +381,7 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   // 4. [dW_g; dW_u] = [da|du]^T x_perm, [da|du] split into bf16 hi + lo
   WgradArgs r4{w + L.dau_hi, w + L.dau_lo, x_perm, nullptr, R, offsets, E, 2 * H, d, dW_g, dW_u, H};
   WgradArgs s4{w + L.s_dau_hi, w + L.s_dau_lo, x, nullptr, T, nullptr, 1, 2 * Hs, d, dWs_g, dWs_u, Hs};
-  return check(gemm_wgrad(r4, Hs > 0 ? &s4 : nullptr, tile_counter, group_maps, status, st));
+  return check(gemm_wgrad(r4, Hs > 0 ? &s4 : nullptr, tile_counter, group_maps, status, st, "gemm_wgrad_gate_up"));
 }
 
 int moe_route_topk_bwd(const float* dgates, const float* gates, const int32_t* topk_idx, const void* x, int T, int d,

@@ -62,13 +62,12 @@ using namespace moe;
 extern "C" int moe_permute_static(const void* x, const int32_t* topk_idx, int T, int d, int E, int k, int capacity,
                                   int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
                                   int32_t* slot_of_row, void* x_perm, void* stream) {
-  if (T < 1 || d < 1 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
-  if (k > kMaxK || k > E || E > kMaxE || (E % 8) != 0 || (d % 64) != 0 || (long long)T * k >= (1LL << 31))
-    return MOE_ERR_UNSUPPORTED;
+  // the same checks as moe_permute (one validation path for both)
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
   if (!x || !topk_idx || !counts_raw || !counts || !offsets || !row_of_slot || !slot_of_row || !x_perm)
     return MOE_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_perm) & 15u))
-    return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(x_perm)) return MOE_ERR_INVALID_ARG;
   if (permute_ws_bytes(T, E, k) > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch
   void* scratch = nullptr;
   cudaError_t e = scratch_ptr(&scratch);
