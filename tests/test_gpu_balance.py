@@ -9,7 +9,7 @@ import torch
 
 from oracle import moe_oracle as orc
 from synth import gen, workloads
-from tests.gpu_util import compare_layer, upload
+from tests.gpu_util import compare_layer, oracle_reference, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -82,9 +82,7 @@ def test_balance_loss_in_the_layer(B, routing):
     assert B.moe_device_status() == 0
     layer = layers[alpha]
 
-    f64 = orc.inputs_to_f64(inp)
-    ref = orc.layer_forward(f64, w.k, w.capacity)
-    refb = orc.layer_backward(f64, ref)
+    f64, ref, refb, _ = oracle_reference(w, inp, layer)
     Lr, fr, Pr, dlr = orc.balance_loss(ref["logits"], ref["idx"], w.E, alpha)
     assert abs(float(layer.lbl_loss.item()) - Lr) <= 1e-4 * abs(Lr)
     np.testing.assert_allclose(layer.lbl_P.cpu().numpy(), Pr, rtol=1e-4, atol=1e-6)

@@ -15,7 +15,7 @@ import torch
 
 from oracle import moe_oracle as orc
 from synth import workloads
-from tests.gpu_util import assert_close, compare_layer, host_f64, upload
+from tests.gpu_util import assert_close, compare_layer, host_f64, oracle_reference, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -74,9 +74,7 @@ def test_layer_forward_backward_parity(B, name):
     inp = workloads.make_inputs(w)
     layer = run_layer(w, inp)
     assert B.moe_device_status() == 0
-    f64 = orc.inputs_to_f64(inp)
-    ref = orc.layer_forward(f64, w.k, w.capacity)
-    refb = orc.layer_backward(f64, ref)
+    _, ref, refb, _ = oracle_reference(w, inp, layer)
     compare_layer(w, inp, layer, ref, refb)
 
 
@@ -91,9 +89,7 @@ def test_unwritten_rows_never_leak(B, name):
     inp = workloads.make_inputs(w)
     layer = run_layer(w, inp, poison=True)
     assert B.moe_device_status() == 0
-    f64 = orc.inputs_to_f64(inp)
-    ref = orc.layer_forward(f64, w.k, w.capacity)
-    refb = orc.layer_backward(f64, ref)
+    _, ref, refb, _ = oracle_reference(w, inp, layer)
     compare_layer(w, inp, layer, ref, refb)
 
 

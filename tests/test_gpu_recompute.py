@@ -8,7 +8,7 @@ import torch
 
 from oracle import moe_oracle as orc
 from synth import workloads
-from tests.gpu_util import compare_layer, upload
+from tests.gpu_util import compare_layer, oracle_reference, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -85,7 +85,5 @@ def test_layer_with_recompute(B, name):
             continue
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b), n
-    f64 = orc.inputs_to_f64(inp)
-    ref = orc.layer_forward(f64, w.k, w.capacity)
-    refb = orc.layer_backward(f64, ref)
+    _, ref, refb, _ = oracle_reference(w, inp, rec)
     compare_layer(w, inp, rec, ref, refb)
