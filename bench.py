@@ -6,12 +6,18 @@
 One step = one full forward + backward of the layer (router, top-k gating,
 permutation, grouped SwiGLU experts + shared expert, combine, and every
 backward step) over one batch of seeded synthetic input, through the C ABI.
-Default workload: the 64-expert layer with random routing (T=8192, d=2048,
-E=64, top-4, H=Hs=1024).  Inputs are resident in HBM when the timed region
-starts; L2 (129 MB) is flushed by writing a 256 MB buffer before every step.
+Default workload: the largest layer of the workload table, forward +
+backward (T=8192, d=4096, E=128, top-4, H=Hs=1536, learned router).  Inputs
+are resident in HBM when the timed region starts; L2 (129 MB) is flushed by
+writing a 256 MB buffer before every step.
+
 `value` times the step's calls captured once in a CUDA graph and replayed
-(the calls are asynchronous and allocate nothing); `eager` and the per-call
-breakdown time the same calls launched one by one.
+(the calls are asynchronous and allocate nothing); `fwd_tokens_per_s` does
+the same for the forward calls alone.  `kernels` times every kernel launch
+of the step with CUDA events that the library records just before each of
+its launches (moe_timing_begin), over eager steps; `roofline` is the kernel
+with the largest share of the step, against the binding roof (tensor or HBM)
+of its algorithmic work, with the measured burst peaks.
 
 Prints ONE JSON line (rank 0).  With --gpus N > 1 (torchrun) every rank runs an
 independent replica of the layer on its own tokens (weak scaling; the layer
@@ -27,8 +33,8 @@ import json
 import os
 import statistics
 import subprocess
-import tempfile
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -41,6 +47,7 @@ from synth import workloads  # noqa: E402
 
 METRIC = "MoE layer tokens/s fwd & fwd+bwd on 1 GB300; grouped-GEMM % BF16 peak"
 L2_FLUSH_BYTES = 256 << 20
+REFERENCE_BUDGET_S = 150.0  # CPU seconds the whole --impl reference run aims at
 
 
 def parse():
@@ -49,11 +56,19 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="tiny64e_random", choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    ap.add_argument("--workload", default="large_E128", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--cpu-sample-tokens", type=int, default=0,
+                    help="oracle tokens per step (0: sized for ~20 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
+
+
+def backward_workload(name):
+    base = workloads.WORKLOADS[name]
+    return workloads.custom(base.name, T=base.T, d=base.d, E=base.E, k=base.k, H=base.H, Hs=base.Hs,
+                            routing=base.routing, zipf_bias=base.zipf_bias, capacity_factor=base.capacity_factor,
+                            backward=True)
 
 
 # ------------------------------------------------------------------ accounting
@@ -67,66 +82,75 @@ def gemm_flops(w, R):
     return fwd, bwd
 
 
-def call_flops(w, R):
-    """Algorithmic FLOPs of the tensor-core C-ABI calls."""
+def kernel_work(w, R):
+    """Algorithmic work of one launch of each kernel of the step: (FLOPs,
+    bytes).  FLOPs count the method's products once (the second MMA of a
+    hi + lo split operand is not counted).  Bytes count every operand read
+    once and every output written once, with activations in bf16 (the
+    method's own dtype) and weights and weight gradients in bf16."""
+    T, d, E, k, H, Hs = w.T, w.d, w.E, w.k, w.H, w.Hs
+    sh = 1 if Hs else 0
+    rows = R + T * sh                                # routed rows + shared-expert rows
+    wgu = 2 * (E * H * d + Hs * d) * 2               # W_g and W_u (routed + shared)
+    wdn = (E * H * d + Hs * d) * 2                   # W_d
+    gu = 4.0 * d * (R * H + T * Hs)
+    dn = 2.0 * d * (R * H + T * Hs)
+    hid = R * H + T * Hs                             # hidden elements (routed + shared)
     return {
-        "moe_grouped_swiglu": 6.0 * R * w.d * w.H + 6.0 * w.T * w.d * w.Hs,
-        "moe_grouped_swiglu_bwd": 12.0 * R * w.d * w.H + 12.0 * w.T * w.d * w.Hs,
+        "gemm_gate_up_swiglu": (gu, R * d * 2 + T * d * 2 * sh + wgu + hid * 2 + 2 * hid * 2),
+        "gemm_gate_up_recompute": (gu, R * d * 2 + T * d * 2 * sh + wgu + 2 * hid * 2),
+        "gemm_down": (dn, hid * 2 + wdn + rows * d * 2),
+        "gemm_dgrad_down_swiglu_bwd": (dn, rows * d * 2 + wdn + 2 * hid * 2 + 2 * hid * 2 + hid * 2),
+        "gemm_wgrad_down": (dn, rows * d * 2 + hid * 2 + wdn),
+        "gemm_dgrad_gate_up": (gu, 2 * hid * 2 + wgu + rows * d * 2),
+        "gemm_wgrad_gate_up": (gu, 2 * hid * 2 + rows * d * 2 + wgu),
+        "gemm_router": (2.0 * T * d * E, T * d * 2 + E * d * 2 + T * E * 4),
+        "gemm_router_dw": (2.0 * T * d * E, T * E * 2 + T * d * 2 + E * d * 4),
+        "gemm_router_dx_reduce": (2.0 * T * d * E, T * E * 2 + E * d * 2 + R * d * 2 + T * d * 2 * sh
+                                  + T * d * 2 + T * k * 4),
+        "perm_scatter": (0.0, T * d * 2 + R * d * 2 + T * k * 12 + R * 4),
+        "combine": (0.0, R * d * 2 + T * d * 2 * sh + T * d * 2 + T * k * 8),
+        "gather_rows": (0.0, T * d * 2 + R * d * 2 + T * k * 4),
+        "unpermute_reduce": (0.0, R * d * 2 + T * d * 2 * sh + T * d * 2 + T * k * 4),
+        "topk_gating": (0.0, T * E * 4 + T * k * 8),
     }
 
 
-def call_bytes(w, R):
-    """Algorithmic HBM bytes of the bandwidth-bound C-ABI calls."""
-    T, d, E, k = w.T, w.d, w.E, w.k
-    route = T * E * 4 + T * k * 8 + (T * d * 2 + E * d * 2 + T * E * 4 if w.routing == "learned" else 0)
-    return {
-        "moe_route_topk": route,
-        "moe_permute": T * d * 2 + R * d * 2 + T * k * 4 * 4 + R * 4,
-        "moe_unpermute_combine": R * d * 4 + (T * d * 4 if w.Hs else 0) + T * d * 2 + T * k * 8,
-        "moe_unpermute_combine_bwd": T * d * 2 + R * d * 2 + T * k * 4,
-        "moe_permute_bwd": R * d * 4 + (T * d * 4 if w.Hs else 0) + T * d * 2 + T * k * 4,
-    }
+def kernel_roofline(work, ms, tensor_peak, hbm_peak):
+    """Binding roof of one launch: its algorithmic FLOPs at the tensor peak
+    against its algorithmic bytes at the HBM peak; `frac` = the binding roof's
+    time over the measured time (= achieved / peak on that roof)."""
+    flops, nbytes = work
+    s = ms / 1000.0
+    t_tensor = flops / (tensor_peak * 1e12)
+    t_hbm = nbytes / (hbm_peak * 1e9)
+    if t_tensor >= t_hbm:
+        return {"bound": "tensor", "achieved": round(flops / s / 1e12, 1), "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": round(t_tensor / s, 4), "hbm_frac": round(t_hbm / s, 4),
+                "algorithmic_flops": flops, "algorithmic_bytes": nbytes}
+    return {"bound": "hbm", "achieved": round(nbytes / s / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(t_hbm / s, 4), "tensor_frac": round(t_tensor / s, 4),
+            "algorithmic_flops": flops, "algorithmic_bytes": nbytes}
 
 
-def launches_per_step(w):
-    n = 0
-    n += 1 + (1 if w.routing == "learned" else 0)          # route: [router GEMM] + top-k
-    n += 3                                                 # permute: hist, scan, scatter
-    n += 2                                                 # grouped swiglu: gate/up, down
-    n += 1                                                 # combine
-    n += 1                                                 # combine bwd (gather)
-    n += 5 + 2                                             # swiglu bwd: dgrad-down, dgates, wgrad-down, dgrad-gu,
-    #                                                        wgrad-gu, and the per-expert map kernel before each wgrad
-    if w.routing == "learned":
-        S = max(1, min(64, w.T // 512))
-        n += 2 + (1 if S > 1 else 0)                       # router bwd: dl, dW_r GEMM, split-K reduce
-        n += 2                                             # permute bwd: dl->bf16, router-dx GEMM + reduce
-    else:
-        n += 1 + 1                                         # router bwd dl; unpermute reduce
-    return n
-
-
-# ------------------------------------------------------------------ ranks
-def profiled_traffic(workload_name, call):
-    """DRAM bytes per call of `call` from the committed ncu summaries under
-    profiles/, or None when no summary covers this workload or the kernels
-    have changed since it was taken (its source fingerprint differs)."""
+def profiled_traffic(workload_name, kernel):
+    """DRAM bytes per launch of `kernel` on this workload from the committed ncu
+    summaries under profiles/ (lines `traffic <kernel> <workload> <bytes per
+    launch> <source fingerprint>`), or None when no summary covers it or the
+    sources that kernel compiles from have changed since it was taken."""
     import glob
     from top_routing_grouped_moe_gb300 import build
-    fp = build._fingerprint()
+    fp = build.kernel_fingerprint(kernel)
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
-        kv, traffic = {}, {}
         for line in open(path):
             parts = line.split()
-            if len(parts) == 2 and parts[0] in ("traffic_fingerprint", "traffic_workload"):
-                kv[parts[0]] = parts[1]
-            elif len(parts) == 3 and parts[0] == "traffic_bytes":
-                traffic[parts[1]] = int(parts[2])
-        if kv.get("traffic_fingerprint") == fp and kv.get("traffic_workload") == workload_name and call in traffic:
-            return traffic[call]
+            if (len(parts) == 5 and parts[0] == "traffic" and parts[1] == kernel and parts[2] == workload_name
+                    and parts[4] == fp):
+                return int(parts[3])
     return None
 
 
+# ------------------------------------------------------------------ ranks
 def max_over_ranks(values, device):
     """Element-wise max of a list of floats over all ranks (identity with one
     rank).  The timed region of every rank is compared, the slowest counts."""
@@ -188,7 +212,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
@@ -196,6 +220,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1].split()[0]))
                 smax.append(float(parts[2].split()[0]))
+                power.append(float(parts[3].split()[0]))
             except ValueError:
                 continue
             for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
@@ -206,11 +231,11 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
-# ------------------------------------------------------------------ reference arm
-def oracle_sample(w, inp, n_tokens):
+# ------------------------------------------------------------------ reference arm (the oracle)
+def oracle_sample(inp, n_tokens):
     """Inputs restricted to the first n_tokens tokens (weights unchanged)."""
     sub = dict(inp)
     for key in ("x", "dY", "logits_in"):
@@ -221,41 +246,47 @@ def oracle_sample(w, inp, n_tokens):
 
 def run_oracle_step(w, f64, n_tokens):
     from oracle import moe_oracle as orc
-    cap = 0
-    if w.capacity > 0:
-        cap = orc.capacity_of(n_tokens, w.k, w.E)
+    cap = orc.capacity_of(n_tokens, w.k, w.E) if w.capacity > 0 else 0
     t0 = time.perf_counter()
     fwd = orc.layer_forward(f64, w.k, cap)
     orc.layer_backward(f64, fwd)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, inp, n_tokens, steps=1):
+def oracle_tokens(w, inp_f64, budget_s):
+    """Tokens per oracle step so that one step costs about budget_s of CPU
+    time: a 64-token calibration step, then proportional sizing (multiples of
+    64, at least 64, at most T)."""
+    t = run_oracle_step(w, oracle_sample(inp_f64, 64), 64)
+    n = int(budget_s / max(t, 1e-6) * 64) // 64 * 64
+    return max(64, min(w.T, n))
+
+
+def cpu_baseline(w, inp, n_tokens=0, budget_s=20.0):
     from oracle import moe_oracle as orc
-    n_tokens = min(n_tokens, w.T)
-    f64 = orc.inputs_to_f64(oracle_sample(w, inp, n_tokens))
-    times = [run_oracle_step(w, f64, n_tokens) for _ in range(steps)]
-    t = statistics.median(times)
-    return {"value": n_tokens / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n_tokens} of {w.T} tokens of {w.name} (the first), forward+backward, float64 numpy "
-                      f"(BLAS on all {os.cpu_count()} host cores), median of {steps}",
-            "seconds": t}
+    f64 = orc.inputs_to_f64(inp)
+    n = min(n_tokens, w.T) if n_tokens > 0 else oracle_tokens(w, f64, budget_s)
+    t = run_oracle_step(w, oracle_sample(f64, n), n)
+    return {"value": n / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of {w.name} (the first), forward+backward, float64 numpy "
+                      f"(BLAS on all {os.cpu_count()} host cores), one step of {t:.1f} s"}
 
 
 def main_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    w = workloads.WORKLOADS[args.workload]
-    w = workloads.custom(w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, Hs=w.Hs, routing=w.routing,
-                         zipf_bias=w.zipf_bias, capacity_factor=w.capacity_factor, backward=True)
+    w = backward_workload(args.workload)
     inp = workloads.make_inputs(w)
     from oracle import moe_oracle as orc
-    n = min(args.cpu_sample_tokens, w.T)
-    f64 = orc.inputs_to_f64(oracle_sample(w, inp, n))
+    f64 = orc.inputs_to_f64(inp)
+    nsteps = args.steps + args.warmup
+    n = min(args.cpu_sample_tokens, w.T) if args.cpu_sample_tokens > 0 else \
+        oracle_tokens(w, f64, REFERENCE_BUDGET_S / max(1, nsteps))
+    sub = oracle_sample(f64, n)
     for _ in range(args.warmup):
-        run_oracle_step(w, f64, n)
-    times = [run_oracle_step(w, f64, n) for _ in range(args.steps)]
+        run_oracle_step(w, sub, n)
+    times = [run_oracle_step(w, sub, n) for _ in range(args.steps)]
     total = sum(times)
     value = n * args.steps / total
     line = {
@@ -291,10 +322,7 @@ def main_ours(args):
     from top_routing_grouped_moe_gb300 import _binding as B
     from top_routing_grouped_moe_gb300.layer import MoELayer
 
-    base = workloads.WORKLOADS[args.workload]
-    w = workloads.custom(base.name, T=base.T, d=base.d, E=base.E, k=base.k, H=base.H, Hs=base.Hs,
-                         routing=base.routing, zipf_bias=base.zipf_bias, capacity_factor=base.capacity_factor,
-                         backward=True)
+    w = backward_workload(args.workload)
     # every rank draws its own tokens (weak scaling); weights are the same
     seed = 20261202 + 7919 * rank
     inp = workloads.make_inputs(w, base=seed)
@@ -307,106 +335,112 @@ def main_ours(args):
     learned = w.routing == "learned"
     layer = MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.current_stream()
+    main_stream = torch.cuda.current_stream()
+    T, d, E, k, H, Hs = w.T, w.d, w.E, w.k, w.H, w.Hs
+    L = layer
 
-    calls = ["moe_route_topk", "moe_permute", "moe_grouped_swiglu", "moe_unpermute_combine",
-             "moe_unpermute_combine_bwd", "moe_grouped_swiglu_bwd", "moe_route_topk_bwd", "moe_permute_bwd"]
-
-    def step(evs=None, stream=stream):
+    def forward(stream):
         x = dev["x"]
-        T, d, E, k, H, Hs = w.T, w.d, w.E, w.k, w.H, w.Hs
-        L = layer
-
-        def mark(i):
-            if evs is not None:
-                evs[i].record(stream)
-
-        mark(0)
         B.moe_route_topk(x, dev.get("W_r"), dev.get("bias"), dev.get("logits_in"), T, d, E, k,
                          L.logits if learned else None, L.idx, L.gates, L.ws, L.ws_bytes, stream)
-        mark(1)
         B.moe_permute(x, L.idx, T, d, E, k, L.capacity, L.counts_raw, L.counts, L.offsets, L.row_of_slot,
                       L.slot_of_row, L.x_perm, L.ws, L.ws_bytes, stream)
-        mark(2)
         B.moe_grouped_swiglu(L.x_perm, L.offsets, x, T, d, E, k, H, Hs, dev["W_g"], dev["W_u"], dev["W_d"],
                              dev.get("Ws_g"), dev.get("Ws_u"), dev.get("Ws_d"), L.au, L.h, L.o_perm, L.au_s,
                              L.h_s, L.s, L.ws, L.ws_bytes, stream)
-        mark(3)
         B.moe_unpermute_combine(L.o_perm, L.s, L.gates, L.row_of_slot, T, d, k, L.y, stream)
-        mark(4)
+
+    def backward(stream):
+        x = dev["x"]
         B.moe_unpermute_combine_bwd(dev["dY"], L.row_of_slot, T, d, k, L.dY_perm, stream)
-        mark(5)
         B.moe_grouped_swiglu_bwd(L.dY_perm, dev["dY"], L.gates, L.row_of_slot, L.slot_of_row, L.offsets, L.x_perm,
                                  x, L.au, L.au_s, T, d, E, k, H, Hs, dev["W_g"], dev["W_u"], dev["W_d"],
                                  dev.get("Ws_g"), dev.get("Ws_u"), dev.get("Ws_d"), L.dx_perm, L.dx_s, L.dW_g,
                                  L.dW_u, L.dW_d, L.dWs_g, L.dWs_u, L.dWs_d, L.dgates, L.ws, L.ws_bytes, stream)
-        mark(6)
         B.moe_route_topk_bwd(L.dgates, L.gates, L.idx, x if learned else None, T, d, E, k, L.dlogits,
                              L.dW_r if learned else None, L.ws, L.ws_bytes, stream)
-        mark(7)
         B.moe_permute_bwd(L.dx_perm, L.dx_s, L.row_of_slot, L.dlogits if learned else None,
                           dev.get("W_r") if learned else None, T, d, E, k, L.dx, L.ws, L.ws_bytes, stream)
-        mark(8)
+
+    def step(stream):
+        forward(stream)
+        backward(stream)
 
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
-        step()
+        step(main_stream)
     torch.cuda.synchronize()
     st = B.moe_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st}: {B.status_string(st)}")
     R = int(layer.offsets[-1].item())
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
+    # ---- every kernel launch of the step, timed by the library's own event
+    # marks (eager steps, L2 flushed before each)
+    per_kernel = {}
+    eager_ms = []
+    n_kernels = 0
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
-        step(evs[i])
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    if world > 1:
-        dist.barrier()
-    step_ms = [evs[i][0].elapsed_time(evs[i][8]) for i in range(args.steps)]
-    per_call = {c: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)] for j, c in enumerate(calls)}
-    fwd_ms = [evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)]
-    total_ms, fwd_total = max_over_ranks([sum(step_ms), sum(fwd_ms)], "cuda")
-    eager_value = tokens_per_s(w.T, args.steps, world, total_ms)
-    fwd_value = tokens_per_s(w.T, args.steps, world, fwd_total)
+        with B.LaunchTimer(capacity=64, stream=main_stream) as tm:
+            step(main_stream)
+        torch.cuda.synchronize()
+        lst = tm.launches()
+        eager_ms.append(sum(ms for _, ms in lst))
+        n_kernels = sum(1 for name, _ in lst if not name.startswith("memset"))
+        seen = {}
+        for name, ms in lst:
+            seen.setdefault(name, []).append(ms)
+        for name, v in seen.items():
+            e = per_kernel.setdefault(name, {"launches_per_step": len(v), "ms": []})
+            e["ms"].extend(v)
+    eager_total = max_over_ranks([sum(eager_ms)], "cuda")[0]
 
-    # The same step replayed as one CUDA graph (every call is asynchronous and
-    # allocates nothing, so the 15+ launches capture as they are); the L2
-    # flush stays outside the graph, before every replay.
+    # ---- the step (and the forward alone) as CUDA-graph replays
     gstream = torch.cuda.Stream()
-    gstream.wait_stream(torch.cuda.current_stream())
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=gstream):
-        step(stream=gstream)
-    torch.cuda.current_stream().wait_stream(gstream)
-    for _ in range(3):
-        flush.fill_(1)
-        graph.replay()
+    graphs = {}
+    for gname, fn in (("step", step), ("forward", forward)):
+        gstream.wait_stream(main_stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gstream):
+            fn(gstream)
+        main_stream.wait_stream(gstream)
+        graphs[gname] = g
+    for g in graphs.values():
+        for _ in range(3):
+            flush.fill_(1)
+            g.replay()
     torch.cuda.synchronize()
     st = B.moe_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} after graph replay: {B.status_string(st)}")
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.fill_(1)
-        gev[i][0].record()
-        graph.replay()
-        gev[i][1].record()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+
+    def replay_ms(g):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(1)
+            ev[i][0].record()
+            g.replay()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        return max_over_ranks([sum(a.elapsed_time(b) for a, b in ev)], "cuda")[0]
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    graph_ms = replay_ms(graphs["step"])
+    wall = time.perf_counter() - wall0
+    fwd_ms = replay_ms(graphs["forward"])
+    clocks = sampler.stop()
+    value = tokens_per_s(T, args.steps, world, graph_ms)
+    fwd_value = tokens_per_s(T, args.steps, world, fwd_ms)
+
     def time_alone(fn):
         """mean ms of fn over args.steps calls after 3 warm-up calls, L2 flushed before each"""
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -424,50 +458,46 @@ def main_ours(args):
     # configured step).  The router balance loss: loss, mean probabilities and
     # the logits gradient.
     lbl_logits = dev["logits_in"] if "logits_in" in dev else layer.logits
-    lbl_out = torch.empty(1 + w.E + w.T * w.E, dtype=torch.float32, device="cuda")
+    lbl_out = torch.empty(1 + E + T * E, dtype=torch.float32, device="cuda")
     lbl_ms = time_alone(lambda: B.moe_router_balance_loss(
-        lbl_logits, layer.counts_raw, w.T, w.E, w.k, 0.02, lbl_out[:1], lbl_out[1:1 + w.E], lbl_out[1 + w.E:],
+        lbl_logits, layer.counts_raw, T, E, k, 0.02, lbl_out[:1], lbl_out[1:1 + E], lbl_out[1 + E:],
         layer.ws, layer.ws_bytes))
-    lbl_bytes = 2 * w.T * w.E * 4 + w.E * 8  # logits read, gradient written, counts and P
+    lbl_bytes = 2 * T * E * 4 + E * 8  # logits read, gradient written, counts and P
     # Activation recompute: the fp32 a|u rebuilt for the backward (gate/up GEMM
     # without the h store), written over the layer's saved copy (same values)
     rec_ms = time_alone(lambda: B.moe_grouped_swiglu_recompute(
-        layer.x_perm, layer.offsets, dev["x"], w.T, w.d, w.E, w.k, w.H, w.Hs, dev["W_g"], dev["W_u"],
+        layer.x_perm, layer.offsets, dev["x"], T, d, E, k, H, Hs, dev["W_g"], dev["W_u"],
         dev.get("Ws_g"), dev.get("Ws_u"), layer.au, layer.au_s))
-    rows = int(layer.offsets[-1])
-    rec_flops = 2.0 * w.d * 2 * (rows * w.H + w.T * w.Hs)
-    rec_bytes = (rows * w.d * 2 + w.E * 2 * w.H * w.d * 2 + rows * 2 * w.H * 4
-                 + (w.T * w.d * 2 + 2 * w.Hs * w.d * 2 + w.T * 2 * w.Hs * 4 if w.Hs else 0))
-    clocks = sampler.stop()
-    graph_ms = max_over_ranks([sum(a.elapsed_time(b) for a, b in gev)], "cuda")[0]
-    value = tokens_per_s(w.T, args.steps, world, graph_ms)
 
-    # roofline of the dominant call (the grouped GEMMs, tensor bound)
+    # ---- rooflines: measured burst peaks (kernels timed inside a step of a
+    # few milliseconds)
     peaks = {}
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk):
         peaks = json.load(open(pk))
-    bf16_peak = peaks.get("bf16_tflops_sustained") or 1700.0
+    tensor_peak = peaks.get("bf16_tflops") or 1900.0
     hbm_peak = peaks.get("hbm_gbs") or 6800.0
     peak_src = "measured" if peaks else "fallback"
-    cf = call_flops(w, R)
-    cb = call_bytes(w, R)
-    avg = {c: statistics.mean(v) for c, v in per_call.items()}
-    dom = max(cf, key=lambda c: avg[c])
-    achieved = cf[dom] / (avg[dom] / 1000.0) / 1e12
-    calls_out = {}
-    for c in calls:
-        e = {"ms": round(avg[c], 4), "share": round(avg[c] / (total_ms / args.steps), 4)}
-        if c in cf:
-            e["tflops"] = round(cf[c] / (avg[c] / 1000.0) / 1e12, 1)
-            e["frac_bf16"] = round(e["tflops"] / bf16_peak, 3)
-        if c in cb:
-            e["gbs"] = round(cb[c] / (avg[c] / 1000.0) / 1e9, 1)
-            e["frac_hbm"] = round(e["gbs"] / hbm_peak, 3)
-        calls_out[c] = e
+    work = kernel_work(w, R)
+    step_eager = eager_total / args.steps
+    kernels = {}
+    for name, e in per_kernel.items():
+        mean = statistics.mean(e["ms"])
+        row = {"launches_per_step": e["launches_per_step"], "ms_per_launch": round(mean, 4),
+               "share": round(mean * e["launches_per_step"] / step_eager, 4)}
+        if name in work:
+            row.update(kernel_roofline(work[name], mean, tensor_peak, hbm_peak))
+        kernels[name] = row
+    dom = max((n for n in kernels if n in work), key=lambda n: kernels[n]["share"])
+    roof = dict(kernel_roofline(work[dom], kernels[dom]["ms_per_launch"], tensor_peak, hbm_peak))
+    roof.update({"kernel": dom, "share_of_step": kernels[dom]["share"],
+                 "traffic": profiled_traffic(w.name, dom),
+                 "traffic_unit": "bytes per launch (ncu dram read + write)",
+                 "peak_source": f"{peak_src} burst ({'bf16 cuBLAS' if roof['bound'] == 'tensor' else 'copy'})"})
     ffl, bfl = gemm_flops(w, R)
+    rec_work = work["gemm_gate_up_recompute"]
 
-    # e2e through the public layer API with host buffers
+    # ---- e2e through the public layer API with host buffers
     e2e = None
     if not args.no_e2e:
         pin = {}
@@ -475,13 +505,13 @@ def main_ours(args):
             pin[key] = torch.from_numpy(inp[key].view(np.int16)).view(torch.bfloat16).pin_memory()
         if "logits_in" in inp:
             pin["logits_in"] = torch.from_numpy(inp["logits_in"]).pin_memory()
-        y_host = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
-        dx_host = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
+        y_host = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+        dx_host = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
         xin = torch.empty_like(dev["x"])
         dyin = torch.empty_like(dev["dY"])
         lin = torch.empty_like(dev["logits_in"]) if "logits_in" in dev else None
         h2d = pin["x"].numel() * 2 + pin["dY"].numel() * 2 + (pin["logits_in"].numel() * 4 if lin is not None else 0)
-        d2h = 2 * w.T * w.d * 2
+        d2h = 2 * T * d * 2
 
         def e2e_step():
             xin.copy_(pin["x"], non_blocking=True)
@@ -503,14 +533,12 @@ def main_ours(args):
         for _ in range(args.steps):
             e2e_step()
         el = max_over_ranks([time.perf_counter() - t0], "cuda")[0]
-        e2e = {"value": tokens_per_s(w.T, args.steps, world, el * 1000.0), "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+        e2e = {"value": tokens_per_s(T, args.steps, world, el * 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, inp, args.cpu_sample_tokens)
-        cpu.pop("seconds", None)
 
     if rank == 0:
         line = {
@@ -518,32 +546,29 @@ def main_ours(args):
             "warmup": max(3, args.warmup), "ms_per_step": graph_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded SplitMix64/Box-Muller generator)",
-            "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "H": w.H, "Hs": w.Hs,
+            "config": {"workload": w.name, "T": T, "d": d, "E": E, "k": k, "H": H, "Hs": Hs,
                        "routing": w.routing, "capacity": w.capacity, "pass": "forward+backward",
                        "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}",
-                       "timing": "value: the step's C-ABI calls captured once in a CUDA graph and replayed; "
-                                 "eager: the same calls launched one by one, timed per call"},
-            "eager": {"value": eager_value, "ms_per_step": total_ms / args.steps},
+                       "timing": "value / fwd_tokens_per_s: the C-ABI calls of the step / of the forward "
+                                 "captured once in a CUDA graph and replayed; kernels: every launch of eager "
+                                 "steps, timed by events the library records before each launch"},
             "fwd_tokens_per_s": fwd_value,
+            "fwd_ms_per_step": fwd_ms / args.steps,
+            "eager": {"value": tokens_per_s(T, args.steps, world, eager_total), "ms_per_step": step_eager},
             "gemm_tflops_fwd_bwd": (ffl + bfl) / (graph_ms / args.steps / 1000.0) / 1e12,
-            "roofline": {"bound": "tensor", "kernel": f"{dom} (tcgen05 grouped GEMM launches)",
-                         "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / bf16_peak, 4), "traffic": profiled_traffic(w.name, dom),
-                         "traffic_unit": "bytes per call (ncu dram read + write)",
-                         "peak_source": f"{peak_src} bf16 dense (sustained)"},
-            "calls": calls_out,
-            "extra_calls": {"moe_router_balance_loss": {
-                "ms": round(lbl_ms, 4), "gbs": round(lbl_bytes / (lbl_ms / 1000.0) / 1e9, 1),
-                "frac_hbm": round(lbl_bytes / (lbl_ms / 1000.0) / 1e9 / hbm_peak, 3),
-                "note": "one kernel after a 4-byte memset; timed alone, not part of the step"},
-                "moe_grouped_swiglu_recompute": {
-                "ms": round(rec_ms, 4), "tflops": round(rec_flops / (rec_ms / 1000.0) / 1e12, 1),
-                "frac_bf16": round(rec_flops / (rec_ms / 1000.0) / 1e12 / bf16_peak, 3),
-                "gbs": round(rec_bytes / (rec_ms / 1000.0) / 1e9, 1),
-                "frac_hbm": round(rec_bytes / (rec_ms / 1000.0) / 1e9 / hbm_peak, 3),
-                "note": "one GEMM launch; timed alone, not part of the step"}},
+            "gemm_frac_bf16_fwd_bwd": round((ffl + bfl) / (graph_ms / args.steps / 1000.0) / 1e12 / tensor_peak, 4),
+            "roofline": roof,
+            "kernels": dict(sorted(kernels.items(), key=lambda kv: -kv[1]["share"])),
+            "extra_calls": {
+                "moe_router_balance_loss": {
+                    "ms": round(lbl_ms, 4), "gbs": round(lbl_bytes / (lbl_ms / 1000.0) / 1e9, 1),
+                    "frac_hbm": round(lbl_bytes / (lbl_ms / 1000.0) / 1e9 / hbm_peak, 3),
+                    "note": "one kernel after a 4-byte memset; timed alone, not part of the step"},
+                "moe_grouped_swiglu_recompute": dict(
+                    kernel_roofline(rec_work, rec_ms, tensor_peak, hbm_peak), ms=round(rec_ms, 4),
+                    note="one GEMM launch; timed alone, not part of the step")},
             "clocks": clocks,
-            "gpu_launches": launches_per_step(w) * args.steps,
+            "gpu_launches": n_kernels * args.steps,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "wall_s_timed_region": wall,

@@ -90,6 +90,24 @@ MOE_API int moe_last_cuda_error(void);
  * first device-side error recorded since the last call. */
 MOE_API int moe_device_status(int* status_out);
 
+/* Launch timing, for benchmarks and profiling (no counterpart in the pages).
+ * moe_timing_begin: from now on, in the calling thread only, every kernel
+ * launch or memset that a call of this library issues is preceded by
+ * cudaEventRecord(events[i], stream) for its index i = 0, 1, ... on the
+ * launch's own stream; launches past `capacity` are counted, not recorded.
+ * events: `capacity` cudaEvent_t handles (passed as void*) created by the
+ * caller with timing enabled, owned by the caller, not retained after
+ * moe_timing_end.  The caller records one more event after its last call, so
+ * launch i took elapsed(events[i], events[i+1]) (queue gaps included).
+ * moe_timing_end stops recording and returns the number of launches seen;
+ * moe_timing_name(i) is the i-th launch's kernel name (a static string, ""
+ * out of range), valid until the next moe_timing_begin in this thread.  Use
+ * outside stream capture.  MOE_ERR_INVALID_ARG: NULL events, a negative
+ * capacity, or moe_timing_end without a begin. */
+MOE_API int moe_timing_begin(void* const* events, int capacity);
+MOE_API int moe_timing_end(int* n_launches);
+MOE_API const char* moe_timing_name(int i);
+
 /* Workspace bytes needed by every call below for this shape (the maximum
  * over the calls; a single buffer can serve all of them in sequence on one
  * stream).  Host only.  Returns MOE_ERR_UNSUPPORTED for shapes outside the

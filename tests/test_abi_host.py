@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
     # and the binding covers every compute entry point
     for n in names:
         if n not in ("moe_version", "moe_status_string", "moe_last_cuda_error", "moe_device_status",
-                     "moe_workspace_size"):
+                     "moe_workspace_size", "moe_timing_begin", "moe_timing_end", "moe_timing_name"):
             assert n in lib.SIGNATURES, n
 
 
@@ -110,3 +110,18 @@ def test_argument_errors_are_reported_on_the_host(lib, call, expect):
     with pytest.raises(lib.MoEError) as e:
         call(lib)
     assert e.value.status == expect
+
+
+def test_launch_timing_host_side(lib):
+    """The timing hook's host-side contract (no launch is made): argument
+    errors, end without begin, an empty session, names out of range."""
+    L = lib._lib
+    assert L.moe_timing_begin(None, 4) == lib.MOE_ERR_INVALID_ARG
+    assert L.moe_timing_begin(None, -1) == lib.MOE_ERR_INVALID_ARG
+    arr = (ctypes.c_void_p * 2)(None, None)
+    assert L.moe_timing_begin(arr, 2) == lib.MOE_ERR_INVALID_ARG  # NULL event handles
+    n = ctypes.c_int(-1)
+    assert L.moe_timing_end(ctypes.byref(n)) == lib.MOE_ERR_INVALID_ARG  # no session open
+    assert L.moe_timing_begin(None, 0) == lib.MOE_OK
+    assert L.moe_timing_end(ctypes.byref(n)) == lib.MOE_OK and n.value == 0
+    assert L.moe_timing_name(0) == b"" and L.moe_timing_name(-1) == b""

@@ -75,6 +75,12 @@ _lib.moe_device_status.restype = _I
 _lib.moe_device_status.argtypes = [ctypes.POINTER(_I)]
 _lib.moe_workspace_size.restype = _I
 _lib.moe_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
+_lib.moe_timing_begin.restype = _I
+_lib.moe_timing_begin.argtypes = [ctypes.POINTER(_P), _I]
+_lib.moe_timing_end.restype = _I
+_lib.moe_timing_end.argtypes = [ctypes.POINTER(_I)]
+_lib.moe_timing_name.restype = ctypes.c_char_p
+_lib.moe_timing_name.argtypes = [_I]
 
 
 def _ptr(v):
@@ -138,6 +144,43 @@ def moe_workspace_size(T, d, E, k, H, Hs) -> int:
     if rc != MOE_OK:
         raise MoEError("moe_workspace_size", rc, status_string(rc))
     return b.value
+
+
+class LaunchTimer:
+    """Times every kernel launch of the library's calls made inside a `with`
+    block in this thread (moe_timing_begin / moe_timing_end), with CUDA
+    events recorded on each launch's own stream.  After the block and a
+    synchronize, `launches()` gives [(kernel name, ms)].  Use outside stream
+    capture."""
+
+    def __init__(self, capacity=256, stream=None):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(capacity + 1)]
+        self.stream = stream
+        self._arr = (_P * capacity)(*[ctypes.c_void_p(e.cuda_event) for e in self.events[:capacity]])
+        self.n = 0
+        self.names = []
+
+    def __enter__(self):
+        rc = _lib.moe_timing_begin(self._arr, len(self._arr))
+        if rc != MOE_OK:
+            raise MoEError("moe_timing_begin", rc, status_string(rc))
+        return self
+
+    def __exit__(self, *exc):
+        n = _I(0)
+        rc = _lib.moe_timing_end(ctypes.byref(n))
+        if rc != MOE_OK:
+            raise MoEError("moe_timing_end", rc, status_string(rc))
+        self.n = n.value
+        if self.n > len(self._arr):
+            raise RuntimeError(f"LaunchTimer: {self.n} launches, capacity {len(self._arr)}")
+        self.names = [_lib.moe_timing_name(i).decode() for i in range(self.n)]
+        # the end of the last launch
+        self.events[self.n].record(self.stream if self.stream is not None else torch.cuda.current_stream())
+        return False
+
+    def launches(self):
+        return [(self.names[i], self.events[i].elapsed_time(self.events[i + 1])) for i in range(self.n)]
 
 
 def moe_route_topk(x, W_r, bias, logits_in, T, d, E, k, logits, topk_idx, gates, ws, ws_bytes, stream=None):

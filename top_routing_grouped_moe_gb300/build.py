@@ -8,6 +8,7 @@ from __future__ import annotations
 import glob
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -53,6 +54,42 @@ def _fingerprint() -> str:
             h.update(f.read())
     h.update(" ".join(ARCH + NVCC_FLAGS).encode())
     return h.hexdigest()
+
+
+_GEMM_COMMON = ["gemm.cuh", "gemm_host.cuh", "ptx.cuh", "common.cuh", "internal.h"]
+
+
+def _kernel_sources(kernel: str):
+    """csrc files the named kernel (a launch name of moe_timing_name) is
+    compiled and launched from."""
+    if kernel.startswith("gemm_router"):
+        files = _GEMM_COMMON + ["gemm_router.cu"]
+    elif kernel.startswith(("gemm_gate_up", "gemm_down")):
+        files = _GEMM_COMMON + ["gemm_fwd.cu"]
+    elif kernel.startswith(("gemm_dgrad", "gemm_wgrad")):
+        files = _GEMM_COMMON + ["gemm_bwd.cu", "group_maps.cu"]
+    else:
+        files = ["route.cu", "common.cuh", "internal.h"]
+    return [os.path.join(CSRC, f) for f in files]
+
+
+def _strip_comments(src: str) -> str:
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return " ".join(src.split())
+
+
+def kernel_fingerprint(kernel: str) -> str:
+    """Hash of the code (comments and layout removed) of the sources one kernel
+    is built and launched from, plus the compiler flags: a profile of that
+    kernel stays valid across edits elsewhere in the library."""
+    h = hashlib.sha256()
+    for p in _kernel_sources(kernel):
+        h.update(os.path.basename(p).encode())
+        with open(p) as f:
+            h.update(_strip_comments(f.read()).encode())
+    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    return h.hexdigest()[:32]
 
 
 def up_to_date() -> bool:

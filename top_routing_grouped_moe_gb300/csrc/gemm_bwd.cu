@@ -127,7 +127,7 @@ cudaError_t gemm_dgrad_down(const DgradDownArgs& routed, const DgradDownArgs* sh
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->H, 256);
     P.num_problems = 2;
   }
-  return launch<0, 1, MGROUP, EPI_SWIGLU_BWD, kPair>(P, bound, s);
+  return launch<0, 1, MGROUP, EPI_SWIGLU_BWD, kPair>(P, bound, s, "gemm_dgrad_down_swiglu_bwd");
 }
 
 cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, int* status, cudaStream_t s) {
@@ -142,13 +142,13 @@ cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, 
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->d, 256);
     P.num_problems = 2;
   }
-  return launch<0, 1, MGROUP, EPI_F32, kPair>(P, bound, s);
+  return launch<0, 1, MGROUP, EPI_F32, kPair>(P, bound, s, "gemm_dgrad_gate_up");
 }
 
 size_t group_maps_bytes(int G) { return (size_t)G * KG_MAPS_PER_GROUP * sizeof(CUtensorMap); }
 
 cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* tile_counter, void* group_maps,
-                       int* status, cudaStream_t s) {
+                       int* status, cudaStream_t s, const char* name) {
   (void)status;
   Params P;
   std::memset(&P, 0, sizeof(P));
@@ -191,9 +191,9 @@ cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* ti
   // ragged K: single CTAs; both problems split the same operand
   if (shared && (!shared->A_lo != !routed.A_lo || !shared->B_lo != !routed.B_lo)) return cudaErrorInvalidValue;
   if (routed.A_lo && routed.B_lo) return cudaErrorInvalidValue;
-  if (routed.A_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_A>(P, bound, s);
-  if (routed.B_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_B>(P, bound, s);
-  return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_NONE>(P, bound, s);
+  if (routed.A_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_A>(P, bound, s, name);
+  if (routed.B_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_B>(P, bound, s, name);
+  return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_NONE>(P, bound, s, name);
 }
 
 }  // namespace moe

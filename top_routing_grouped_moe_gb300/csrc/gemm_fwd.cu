@@ -71,7 +71,8 @@ cudaError_t gemm_swiglu_fwd(const SwigluFwdArgs& routed, const SwigluFwdArgs* sh
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->H, 128);
     P.num_problems = 2;
   }
-  return launch<0, 0, MGROUP, EPI_SWIGLU_FWD, kPair>(P, bound, s);
+  return launch<0, 0, MGROUP, EPI_SWIGLU_FWD, kPair>(P, bound, s,
+                                                    routed.h ? "gemm_gate_up_swiglu" : "gemm_gate_up_recompute");
 }
 
 cudaError_t gemm_down_fwd(const DownFwdArgs& routed, const DownFwdArgs* shared, int* status, cudaStream_t s) {
@@ -86,7 +87,7 @@ cudaError_t gemm_down_fwd(const DownFwdArgs& routed, const DownFwdArgs* shared, 
     bound += mgroup_tile_bound(shared->rows_total, shared->G, shared->d, 256);
     P.num_problems = 2;
   }
-  return launch<0, 0, MGROUP, EPI_F32, kPair>(P, bound, s);
+  return launch<0, 0, MGROUP, EPI_F32, kPair>(P, bound, s, "gemm_down");
 }
 
 }  // namespace moe

@@ -111,7 +111,7 @@ inline Problem blank_problem() {
 // (PAIR = 1), or clusters of two CTAs sized by the number of clusters that can
 // be resident at once (PAIR = 2).
 template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT = SPLIT_NONE>
-cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s) {
+cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s, const char* name) {
   auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR, SPLIT>;
   constexpr size_t smem = smem_bytes<MODE, EPI, PAIR, SPLIT>();
   static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
@@ -150,9 +150,11 @@ cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s) {
   if (tile_bound <= 0) return cudaSuccess;
   P.status = device_status_ptr();
   if (P.tile_counter) {
+    timing_mark(s, "memset_tile_counter");
     e = cudaMemsetAsync(P.tile_counter, 0, sizeof(int), s);
     if (e != cudaSuccess) return e;
   }
+  timing_mark(s, name);
   if (PAIR == 1) {
     int grid = device_sm_count();
     if (tile_bound < grid) grid = static_cast<int>(tile_bound);

@@ -29,7 +29,7 @@ cudaError_t gemm_router_fwd(const void* x, const void* W_r, const float* bias, i
   pr.ldo = E;
   pr.bias = bias;
   P.num_problems = 1;
-  return launch<0, 0, MGROUP, EPI_F32, 1>(P, cdiv_h(T, BM), s);
+  return launch<0, 0, MGROUP, EPI_F32, 1>(P, cdiv_h(T, BM), s, "gemm_router");
 }
 
 int router_dw_splits(int T, int d, int E) {
@@ -67,7 +67,8 @@ cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const v
   pr.ldo = d;
   pr.gstride = (long long)E * d;
   P.num_problems = 1;
-  return launch<1, 1, KGROUP, EPI_F32, 1, SPLIT_A>(P, (long long)S * cdiv_h(E, BM) * cdiv_h(d, 256), s);
+  return launch<1, 1, KGROUP, EPI_F32, 1, SPLIT_A>(P, (long long)S * cdiv_h(E, BM) * cdiv_h(d, 256), s,
+                                                  "gemm_router_dw");
 }
 
 cudaError_t gemm_router_dx_reduce(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, const float* dx_perm,
@@ -102,7 +103,8 @@ cudaError_t gemm_router_dx_reduce(const uint16_t* dl_hi, const uint16_t* dl_lo, 
   pr.topk = k;
   pr.aux_rows = T * k;
   P.num_problems = 1;
-  return launch<0, 1, MGROUP, EPI_REDUCE_DX, 1>(P, (long long)cdiv_h(T, BM) * cdiv_h(d, 256), s);
+  return launch<0, 1, MGROUP, EPI_REDUCE_DX, 1>(P, (long long)cdiv_h(T, BM) * cdiv_h(d, 256), s,
+                                              "gemm_router_dx_reduce");
 }
 
 }  // namespace moe

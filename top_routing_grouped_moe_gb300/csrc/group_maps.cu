@@ -85,6 +85,7 @@ cudaError_t launch_group_maps(const CUtensorMap* whole, const CUtensorMap* whole
   a.G = G;
   a.extent = extent;
   a.out = out;
+  timing_mark(s, "group_maps");
   group_maps_kernel<<<G, 32, 0, s>>>(a);
   return cudaGetLastError();
 }

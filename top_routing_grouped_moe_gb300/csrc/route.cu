@@ -578,6 +578,7 @@ cudaError_t launch_topk_gating(const float* logits, int T, int E, int k, int32_t
   (void)status;
   const unsigned grid = warp_blocks(T);
   const int nj = (E + 31) / 32;
+  timing_mark(s, "topk_gating");
   switch (nj) {
     case 1: topk_gating_kernel<1><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
     case 2: topk_gating_kernel<2><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
@@ -603,12 +604,15 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
   int32_t* tile_counts = reinterpret_cast<int32_t*>(w);
   int32_t* tile_base = reinterpret_cast<int32_t*>(w + align256((size_t)ntile * E * 4));
   int32_t* inrank = reinterpret_cast<int32_t*>(w + 2 * align256((size_t)ntile * E * 4));
+  timing_mark(s, "perm_tile_hist");
   perm_tile_hist_kernel<<<ntile, kRouteTile, 0, s>>>(idx, T, E, k, tile_counts, inrank, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  timing_mark(s, "perm_scan");
   perm_scan_kernel<<<1, 1024, 0, s>>>(tile_counts, ntile, E, capacity, tile_base, counts_raw, counts, offsets);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  timing_mark(s, "perm_scatter");
   perm_scatter_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
       static_cast<const uint4*>(x), idx, inrank, tile_base, offsets, T, d, E, k, capacity, row_of_slot, slot_of_row,
       static_cast<uint4*>(x_perm));
@@ -617,6 +621,7 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
 
 cudaError_t launch_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
                            int T, int d, int k, void* y, int* status, cudaStream_t s) {
+  timing_mark(s, "combine");
   combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
       reinterpret_cast<const float4*>(o_perm), reinterpret_cast<const float4*>(s_out), gates, row_of_slot, T, d, k,
       (long long)T * k, static_cast<uint4*>(y), status);
@@ -625,6 +630,7 @@ cudaError_t launch_combine(const float* o_perm, const float* s_out, const float*
 
 cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
                                int* status, cudaStream_t s) {
+  timing_mark(s, "gather_rows");
   gather_rows_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
       static_cast<const uint4*>(dY), row_of_slot, T, d, k, (long long)T * k, static_cast<uint4*>(dY_perm), status);
   return cudaGetLastError();
@@ -633,12 +639,14 @@ cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T
 cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_slot, int T, int k, float* dgates,
                                  cudaStream_t s) {
   const long long n = (long long)T * k;
+  timing_mark(s, "dgates_reduce");
   dgates_reduce_kernel<<<flat_blocks(n, 256), 256, 0, s>>>(dgp, P, row_of_slot, n, dgates);
   return cudaGetLastError();
 }
 
 cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, int T, int d,
                                     int k, void* dx, int* status, cudaStream_t s) {
+  timing_mark(s, "unpermute_reduce");
   unpermute_reduce_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
       reinterpret_cast<const float4*>(dx_perm), reinterpret_cast<const float4*>(dx_s), row_of_slot, T, d, k,
       (long long)T * k,
@@ -648,18 +656,21 @@ cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, con
 
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
                                  const float* add, float* dlogits, uint16_t* dl_hi, uint16_t* dl_lo, cudaStream_t s) {
+  timing_mark(s, "router_bwd_dl");
   router_bwd_dl_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(dgates, gates, idx, T, E, k, add, dlogits,
                                                                        dl_hi, dl_lo);
   return cudaGetLastError();
 }
 
 cudaError_t launch_f32_to_bf16_split(const float* src, uint16_t* hi, uint16_t* lo, long long n, cudaStream_t s) {
+  timing_mark(s, "f32_to_bf16_split");
   f32_to_bf16_split_kernel<<<flat_blocks(n, 256), 256, 0, s>>>(src, hi, lo, n);
   return cudaGetLastError();
 }
 
 cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float* out, cudaStream_t s) {
   const long long n4 = n / 4;
+  timing_mark(s, "splitk_reduce");
   splitk_reduce_kernel<<<flat_blocks(n4, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(partial), S, n4,
                                                             reinterpret_cast<float4*>(out));
   return cudaGetLastError();
@@ -676,9 +687,11 @@ cudaError_t launch_balance_loss(const float* logits, const int32_t* counts_raw, 
   const int nblk = (T + kLblTokensPerBlock - 1) / kLblTokensPerBlock;
   float* partial = static_cast<float*>(ws);
   unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + align256((size_t)nblk * E * sizeof(float)));
+  timing_mark(s, "memset_ticket");
   cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return e;
   const unsigned threads = 32 * kWarpsPerBlock;
+  timing_mark(s, "balance_loss");
   switch ((E + 31) / 32) {
     case 1: lbl_kernel<1><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
     case 2: lbl_kernel<2><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
