@@ -12,6 +12,8 @@ FSDP comparison"):
   tiny64e_zipf_cap125  same, capacity factor 1.25
   scale_E{8,32,64,128} T=16384 d=2048 k=4 H=768 Hs=768, learned, fwd+bwd
   large_E128      T=8192  d=4096 E=128 k=4 H=1536 Hs=1536, learned, fwd+bwd
+  large_E16_slice T=1024  d=4096 E=16  k=4 H=1536 Hs=1536 (large_E128's per-expert
+                  shapes with 16 experts: a small case for profiling)
 
 Values: x, dY ~ N(0,1) bf16; every weight ~ N(0, 0.02^2) bf16 (std 0.02).
 
@@ -64,6 +66,10 @@ WORKLOADS = {
     "scale_E64": Workload("scale_E64", 16384, 2048, 64, 4, 768, 768, "learned", backward=True),
     "scale_E128": Workload("scale_E128", 16384, 2048, 128, 4, 768, 768, "learned", backward=True),
     "large_E128": Workload("large_E128", 8192, 4096, 128, 4, 1536, 1536, "learned", backward=True),
+    # the per-expert shapes of large_E128 (256 rows per expert, d=4096,
+    # H=Hs=1536) with 16 experts and 1024 tokens: a case of a few GB for
+    # profiling the same tiles with many counters
+    "large_E16_slice": Workload("large_E16_slice", 1024, 4096, 16, 4, 1536, 1536, "learned", backward=True),
 }
 
 

@@ -156,6 +156,10 @@ class LaunchTimer:
     def __init__(self, capacity=256, stream=None):
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(capacity + 1)]
         self.stream = stream
+        # torch creates the CUDA event at its first record: record each once so
+        # that every handle exists before the library records it
+        for e in self.events:
+            e.record(stream if stream is not None else torch.cuda.current_stream())
         self._arr = (_P * capacity)(*[ctypes.c_void_p(e.cuda_event) for e in self.events[:capacity]])
         self.n = 0
         self.names = []

@@ -51,7 +51,7 @@ constexpr int UMMA_K = 16;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB: this CTA's A tile per stage
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_PROBLEMS = 2;
-constexpr int MAX_MAPS = 8;
+constexpr int MAX_MAPS = 12;
 constexpr int MAX_G = kMaxE + 1;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) MN-major box: 8 KB
@@ -105,6 +105,7 @@ struct Problem {
   long long gstride;   // elements between groups' output slabs (KGROUP)
   void* out2;          // rows >= row_split go to out2 (KGROUP; 0 = off)
   int row_split;
+  int map_out, map_out2;   // EPI_BF16 (ragged K): TMA-store maps of out / out2, [G][rows][N], 32 x 32 boxes
   void* aux;           // SWIGLU_FWD: au out; SWIGLU_BWD: au in; REDUCE_DX: dx_perm in
   long long ld_aux;
   const void* aux2;    // REDUCE_DX: dx_s in (nullable)
@@ -339,7 +340,7 @@ constexpr int TB_STRIDE = 36;  // floats per row of the staging buffer (16-byte 
 __device__ __forceinline__ void tmem_chunk_quad(uint32_t taddr, float* tb, int lane, float4 (&v)[8]) {
   uint32_t r[32];
   ptx::tmem_ld32(taddr, r);
-  ptx::tmem_ld_wait();
+  ptx::tmem_ld_wait(r);
   __syncwarp();
 #pragma unroll
   for (int m = 0; m < 8; ++m)
@@ -730,6 +731,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     // SwiGLU backward: a | u chunks of this warp's 32 rows arrive by TMA in a
     // two-buffer ring; au_next counts chunks issued, au_done chunks consumed
     uint32_t au_next = 0, au_done = 0;
+    uint32_t n_stores = 0;  // EPI_BF16: TMA stores issued by this warp (staging boxes alternate)
     uint8_t* au_mine = au_buf + q * 2 * AU_CHUNK_BYTES;
     for (int it = 0;; ++it) {
       int t;
@@ -774,7 +776,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       const int nrows = max(0, min(32, ti.rows_end - row0));
       const bool has_acc = ti.nk > 0;
 
-      if (EPI == EPI_BF16 || EPI == EPI_F32) {
+      if (EPI == EPI_BF16) {
+        // Ragged K, bf16 out: each 32-column chunk goes TMEM -> registers (one
+        // row per thread) -> bf16 -> this warp's staging box in shared memory
+        // (64-byte swizzle, two boxes in turn) -> TMA store of the 32 x 32 box.
+        // The next chunk's TMEM load is in flight while a chunk is stored.
+        static_assert(EPI != EPI_BF16 || MODE == KGROUP, "bf16 output: ragged-K GEMMs");
+        const bool second = pr.row_split > 0 && m_cta >= pr.row_split;
+        const CUtensorMap* mo = &P.maps[second ? pr.map_out2 : pr.map_out];
+        const int orow = row0 - (second ? pr.row_split : 0);
+        const int nch = min(pr.n_tile, pr.N - ti.n0) / 32;
+        uint8_t* stage_box = reinterpret_cast<uint8_t*>(tb);
+        if (row0 < ti.rows_end) {
+          uint32_t r[2][32];
+          if (has_acc) {
+            ptx::tmem_ld32(taddr, r[0]);
+            ptx::tmem_ld_wait(r[0]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[0][e] = 0u;
+          }
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            if (c >= nch) break;
+            uint32_t(&cur)[32] = r[c & 1];
+            uint32_t(&nxt)[32] = r[(c + 1) & 1];
+            if (c + 1 < nch) {
+              if (has_acc) {
+                ptx::tmem_ld32(taddr + 32 * (c + 1), nxt);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) nxt[e] = 0u;
+              }
+            }
+            // the box written two stores ago has been read by its TMA store
+            uint8_t* box = stage_box + (n_stores & 1) * 2048;
+            if (n_stores >= 2) {
+              if (lane == 0) ptx::bulk_wait_read<1>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 v = make_uint4(
+                  pack_bf16(__uint_as_float(cur[8 * j]), __uint_as_float(cur[8 * j + 1])),
+                  pack_bf16(__uint_as_float(cur[8 * j + 2]), __uint_as_float(cur[8 * j + 3])),
+                  pack_bf16(__uint_as_float(cur[8 * j + 4]), __uint_as_float(cur[8 * j + 5])),
+                  pack_bf16(__uint_as_float(cur[8 * j + 6]), __uint_as_float(cur[8 * j + 7])));
+              // row `lane` of the box, 16-byte piece j at its 64-byte-swizzle slot
+              *reinterpret_cast<uint4*>(box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(mo, box, ti.n0 + 32 * c, orow, ti.g);
+              ptx::bulk_commit();
+            }
+            ++n_stores;
+            if (has_acc && c + 1 < nch) ptx::tmem_ld_wait(nxt);
+          }
+        }
+      } else if (EPI == EPI_F32) {
         long long base;  // element offset of (row0, 0)
         OutT<EPI>* outp;
         if (MODE == KGROUP && pr.row_split > 0 && m_cta >= pr.row_split) {
@@ -994,6 +1055,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         else ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&tail->tmem_empty[acc]), 0));
       }
     }
+    // TMA stores still reading their staging box (or in flight) complete
+    // before the CTA's shared memory goes away
+    if (EPI == EPI_BF16 && lane == 0) ptx::bulk_wait_all();
     // after an abort: let a | u copies still in flight land before the CTA's
     // shared memory goes away
     if (EPI == EPI_SWIGLU_BWD) {

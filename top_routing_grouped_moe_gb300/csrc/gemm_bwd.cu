@@ -14,7 +14,8 @@ long long mgroup_tile_bound(int rows_total, int G, int N, int n_tile) {
 }
 
 bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
-  const int ia = P.num_maps++, ib = P.num_maps++;
+  const int ia = new_map(P), ib = new_map(P);
+  if (ia < 0 || ib < 0) return false;
   if (!encode_2d(&P.maps[ia], a.dY, a.d, a.rows_total, (uint64_t)a.d * 2, 64, BM)) return false;
   // B[n = j in H, k = c in d] = W_d[g][c][j]: MN-major, stored [G][K=d][N=H]
   if (!encode_3d(&P.maps[ib], a.Wd, a.H, a.d, a.G, 64, 64)) return false;
@@ -43,21 +44,24 @@ bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
   pr.dgp = a.dgp;
   pr.ld_dgp = cdiv_h(a.H, 256);
   // a | u come into shared memory by TMA, one 32-row x 32-column box each
-  pr.map_aux = P.num_maps++;
+  pr.map_aux = new_map(P);
+  if (pr.map_aux < 0) return false;
   if (!encode_2d_f32(&P.maps[pr.map_aux], a.au, 2 * (uint64_t)a.H, a.rows_total, 2 * (uint64_t)a.H * 4, 32, 32))
     return false;
   return true;
 }
 
 bool fill_dgrad_gu(Params& P, Problem& pr, const DgradGuArgs& a) {
-  const int ia = P.num_maps++, ig = P.num_maps++, iu = P.num_maps++;
+  const int ia = new_map(P), ig = new_map(P), iu = new_map(P);
+  if (ia < 0 || ig < 0 || iu < 0) return false;
   if (!encode_2d(&P.maps[ia], a.dau, 2 * a.H, a.rows_total, (uint64_t)a.H * 4, 64, BM)) return false;
   // B[n = c in d, k = j in 2H]: W_g[g][j][c] for j < H, W_u[g][j-H][c] after
   if (!encode_3d(&P.maps[ig], a.Wg, a.d, a.H, a.G, 64, 64)) return false;
   if (!encode_3d(&P.maps[iu], a.Wu, a.d, a.H, a.G, 64, 64)) return false;
   pr = blank_problem();
   if (a.dau_lo) {
-    pr.map_a_lo = P.num_maps++;
+    pr.map_a_lo = new_map(P);
+    if (pr.map_a_lo < 0) return false;
     if (!encode_2d(&P.maps[pr.map_a_lo], a.dau_lo, 2 * a.H, a.rows_total, (uint64_t)a.H * 4, 64, BM)) return false;
     pr.nsplit = 2;
   }
@@ -79,17 +83,20 @@ bool fill_dgrad_gu(Params& P, Problem& pr, const DgradGuArgs& a) {
 }
 
 bool fill_wgrad(Params& P, Problem& pr, const WgradArgs& a) {
-  const int ia = P.num_maps++, ib = P.num_maps++;
+  const int ia = new_map(P), ib = new_map(P);
+  if (ia < 0 || ib < 0) return false;
   // 64-column block views: one TMA box per operand and stage (A: 2 blocks, B: 4)
   if (!encode_blocks(&P.maps[ia], a.A, a.M, a.rows_total, BKK, 2)) return false;
   if (!encode_blocks(&P.maps[ib], a.B, a.N, a.rows_total, BKK, 4)) return false;
   pr = blank_problem();
   if (a.A_lo) {
-    pr.map_a_lo = P.num_maps++;
+    pr.map_a_lo = new_map(P);
+    if (pr.map_a_lo < 0) return false;
     if (!encode_blocks(&P.maps[pr.map_a_lo], a.A_lo, a.M, a.rows_total, BKK, 2)) return false;
   }
   if (a.B_lo) {
-    pr.map_b_lo = P.num_maps++;
+    pr.map_b_lo = new_map(P);
+    if (pr.map_b_lo < 0) return false;
     if (!encode_blocks(&P.maps[pr.map_b_lo], a.B_lo, a.N, a.rows_total, BKK, 4)) return false;
   }
   pr.nsplit = (a.A_lo || a.B_lo) ? 2 : 1;
@@ -110,6 +117,16 @@ bool fill_wgrad(Params& P, Problem& pr, const WgradArgs& a) {
   pr.row_split = a.out2 ? a.row_split : 0;
   pr.ldo = a.N;
   pr.gstride = (long long)(a.out2 ? a.row_split : a.M) * a.N;
+  // the epilogue's TMA stores: out [G][rows < row_split][N], out2 [G][the rest][N]
+  const int rows1 = a.out2 ? a.row_split : a.M;
+  pr.map_out = new_map(P);
+  if (pr.map_out < 0) return false;
+  if (!encode_store_3d(&P.maps[pr.map_out], a.out, a.N, rows1, a.G)) return false;
+  if (a.out2) {
+    pr.map_out2 = new_map(P);
+    if (pr.map_out2 < 0) return false;
+    if (!encode_store_3d(&P.maps[pr.map_out2], a.out2, a.N, a.M - a.row_split, a.G)) return false;
+  }
   return true;
 }
 

@@ -9,7 +9,8 @@ namespace {
 constexpr int kPair = 2;  // expert GEMMs run on CTA pairs
 
 bool fill_swiglu_fwd(Params& P, Problem& pr, const SwigluFwdArgs& a) {
-  const int ia = P.num_maps++, ig = P.num_maps++, iu = P.num_maps++;
+  const int ia = new_map(P), ig = new_map(P), iu = new_map(P);
+  if (ia < 0 || ig < 0 || iu < 0) return false;
   if (!encode_2d(&P.maps[ia], a.a, a.d, a.rows_total, (uint64_t)a.d * 2, 64, BM)) return false;
   if (!encode_3d(&P.maps[ig], a.Wg, a.d, a.H, a.G, 64, 128)) return false;
   if (!encode_3d(&P.maps[iu], a.Wu, a.d, a.H, a.G, 64, 128)) return false;
@@ -34,7 +35,8 @@ bool fill_swiglu_fwd(Params& P, Problem& pr, const SwigluFwdArgs& a) {
 }
 
 bool fill_down_fwd(Params& P, Problem& pr, const DownFwdArgs& a) {
-  const int ia = P.num_maps++, ib = P.num_maps++;
+  const int ia = new_map(P), ib = new_map(P);
+  if (ia < 0 || ib < 0) return false;
   if (!encode_2d(&P.maps[ia], a.h, a.H, a.rows_total, (uint64_t)a.H * 2, 64, BM)) return false;
   if (!encode_3d(&P.maps[ib], a.Wd, a.H, a.d, a.G, 64, 256 / kPair)) return false;
   pr = blank_problem();

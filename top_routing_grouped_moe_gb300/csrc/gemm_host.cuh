@@ -95,6 +95,24 @@ inline bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map for TMA stores of 32 x 32 boxes into [d2][d1][d0] (d0
+// contiguous), 64-byte swizzle (the epilogue's staging layout).
+inline bool encode_store_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Next free tensor-map slot of P, or -1 when all MAX_MAPS are taken (the
+// caller then reports an invalid launch instead of writing past the array).
+inline int new_map(Params& P) { return P.num_maps < MAX_MAPS ? P.num_maps++ : -1; }
+
 inline int cdiv_h(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 inline Problem blank_problem() {
@@ -103,6 +121,8 @@ inline Problem blank_problem() {
   p.map_b2 = -1;
   p.map_a_lo = -1;
   p.map_b_lo = -1;
+  p.map_out = -1;
+  p.map_out2 = -1;
   p.nsplit = 1;
   return p;
 }
