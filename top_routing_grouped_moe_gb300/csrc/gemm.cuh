@@ -56,12 +56,6 @@ constexpr int MAX_G = kMaxE + 1;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) MN-major box: 8 KB
 
-// Ragged-K stage: 32 K rows of A (128 M) | B (256 N) | the lo half of the
-// split operand.  MN-major boxes of 64 (MN) x 32 (K): 4 KB each.
-constexpr int BKK = 32;
-constexpr int KG_BLOCK_BYTES = 64 * BKK * 2;
-constexpr int KG_A_BYTES = 2 * KG_BLOCK_BYTES;
-constexpr int KG_B_BYTES = 4 * KG_BLOCK_BYTES;
 constexpr int RING = 4;  // tile indices in flight from the producer to the other roles
 constexpr int KG_MAPS_PER_GROUP = 3;  // ragged K, per-group maps: A, B, lo half
 
@@ -70,13 +64,23 @@ enum Mode : int { MGROUP = 0, KGROUP = 1 };
 // that each kernel issues its MMAs from one straight-line sequence)
 enum Split : int { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2 };
 
-// Ragged-K stage: A (2 blocks) | B (4 blocks) | the lo half of the split
-// operand (A's 2 blocks or B's 4), sized for that split so that as many
-// stages as fit in ~200 KB are in flight: 24 KB x 8, 32 KB x 6, 40 KB x 5
+// K rows per ragged-K stage: 64 (four 16-row MMA sub-steps) when A or
+// nothing is split, 32 when B (256 columns) is split, so that a stage stays
+// small enough for several of them to be in flight.  Host code sizes the TMA
+// boxes with the same function.
+__host__ __device__ constexpr int kg_rows(int split) { return split == SPLIT_B ? 32 : 64; }
+
+// Ragged-K stage: BKK K rows of A (2 MN-major blocks of 64 columns) | B (4
+// blocks) | the lo half of the split operand (A's 2 blocks or B's 4), as many
+// stages as fit in ~200 KB: 48 KB x 4 (no split), 64 KB x 3 (A split),
+// 40 KB x 5 (B split, 32 rows).
 template <int SPLIT>
 struct KgCfg {
-  static constexpr int STAGE_BYTES =
-      KG_A_BYTES + KG_B_BYTES + (SPLIT == SPLIT_A ? KG_A_BYTES : SPLIT == SPLIT_B ? KG_B_BYTES : 0);
+  static constexpr int BKK = kg_rows(SPLIT);
+  static constexpr int BLOCK_BYTES = 64 * BKK * 2;  // one 64 (MN) x BKK (K) block
+  static constexpr int A_BYTES = 2 * BLOCK_BYTES;
+  static constexpr int B_BYTES = 4 * BLOCK_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + (SPLIT == SPLIT_A ? A_BYTES : SPLIT == SPLIT_B ? B_BYTES : 0);
   static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
 };
 enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3, EPI_REDUCE_DX = 4 };
@@ -193,7 +197,7 @@ struct TileInfo {
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-template <int MODE, int TILE_M>
+template <int MODE, int TILE_M, int KBK>
 __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int t) {
   TileInfo ti;
   int p = (P.num_problems > 1 && t >= S.tile_start[1]) ? 1 : 0;
@@ -232,7 +236,7 @@ __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int 
     ti.n0 = n_idx * pr.n_tile;
     ti.k0 = S.off[p][g];
     ti.k1 = S.off[p][g + 1];
-    ti.nk = cdiv(ti.k1 - ti.k0, BKK);
+    ti.nk = cdiv(ti.k1 - ti.k0, KBK);
   }
   return ti;
 }
@@ -397,6 +401,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
   constexpr int STAGES = SC::STAGES;
   constexpr int B_BYTES = Cfg::B_BYTES;
   constexpr int TILE_M = Cfg::TILE_M;
+  // ragged K: rows per stage and the stage's blocks
+  constexpr int KBK = KgCfg<SPLIT>::BKK;
+  constexpr int KG_BLOCK_BYTES = KgCfg<SPLIT>::BLOCK_BYTES;
+  constexpr int KG_A_BYTES = KgCfg<SPLIT>::A_BYTES;
+  constexpr int KG_B_BYTES = KgCfg<SPLIT>::B_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // ragged M: A ring then B ring; ragged K: stage s at smem + s * SC::BYTES
@@ -475,7 +484,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       uint32_t issued_phase_mask = 0;  // bit s: parity of the last load issued into stage s
       uint32_t issued_any = 0;
       bool ok = true;
-      int fetched = 0;
+      int fetched = 0;   // raw value of the last tile-counter atomic
+      int acquired = -1;  // (problem, group) whose per-group maps this thread last acquired
       for (int i = 0; ok; ++i) {
         int t;
         if (dyn) {
@@ -486,16 +496,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             ok = false;
             break;
           }
-          t = i == 0 ? tile0 : fetched;
+          t = i == 0 ? tile0 : fetched + tile_step;
           *reinterpret_cast<volatile int*>(&tail->ring[slot]) = t;
           ptx::mbar_arrive(&tail->ring_full[slot]);
           if (t >= total) break;
-          fetched = atomicAdd(P.tile_counter, 1) + tile_step;
+          // used at the next tile only: no instruction here waits for the
+          // atomic's round trip
+          fetched = atomicAdd(P.tile_counter, 1);
         } else {
           t = tile0 + i * tile_step;
           if (t >= total) break;
         }
-        TileInfo ti = decode<MODE, TILE_M>(P, S, t);
+        TileInfo ti = decode<MODE, TILE_M, KBK>(P, S, t);
         // Everything the stage loop needs, read once per tile: a parameter
         // read inside the loop would be repeated after every asm statement
         // (they all clobber memory), which cost as much as the MMAs.
@@ -512,16 +524,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         int k0 = ti.k0;
         const int g = ti.g, nk = ti.nk;
         if (MODE == KGROUP && pr.gmaps != nullptr && nk > 0) {
-          // this group's own maps (written by an earlier launch: acquire them
-          // for the tensor-map proxy); K rows counted from the group's start
+          // this group's own maps (written by an earlier launch: acquired for
+          // the tensor-map proxy once per group this thread loads from); K rows
+          // counted from the group's start
           const CUtensorMap* gm = pr.gmaps + (long long)g * KG_MAPS_PER_GROUP;
           mA = gm;
           mB = gm + 1;
           if (SPLIT == SPLIT_A) mAlo = gm + 2;
           if (SPLIT == SPLIT_B) mBlo = gm + 2;
-          ptx::tmap_acquire(mA);
-          ptx::tmap_acquire(mB);
-          if (SPLIT != SPLIT_NONE) ptx::tmap_acquire(gm + 2);
+          const int key = ti.p * MAX_G + g;
+          if (key != acquired) {
+            ptx::tmap_acquire(mA);
+            ptx::tmap_acquire(mB);
+            if (SPLIT != SPLIT_NONE) ptx::tmap_acquire(gm + 2);
+            acquired = key;
+          }
           k0 = 0;
         }
         for (int kb = 0; kb < nk; ++kb) {
@@ -536,7 +553,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           issued_phase_mask = (issued_phase_mask & ~(1u << stage)) | (phase << stage);
           if (MODE == KGROUP) {
             // A (2 blocks) | B (nblk blocks) | lo half of A or of B
-            const int k = k0 + kb * BKK;
+            const int k = k0 + kb * KBK;
             uint8_t* st = smem + stage * SC::BYTES;
             uint8_t* lo = st + KG_A_BYTES + KG_B_BYTES;
             if (blk3d) {
@@ -630,7 +647,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           t = tile0 + it * tile_step;
         }
         if (t >= total) break;
-        TileInfo ti = decode<MODE, TILE_M>(P, S, t);
+        TileInfo ti = decode<MODE, TILE_M, KBK>(P, S, t);
         const Problem& pr = P.prob[ti.p];
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
@@ -651,7 +668,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           // Ragged K: the rows of a group's last step past its end are zeros
           // (per-group maps, or TMA's fill past `extent`), and a 16-row
           // sub-step entirely past the end is not issued.
-          const bool tail_step = MODE == KGROUP && (kb + 1) * BKK > k_left;
+          const bool tail_step = MODE == KGROUP && (kb + 1) * KBK > k_left;
           ptx::tc_fence_after();
           if (MODE == MGROUP) {
             const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);
@@ -668,32 +685,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             if (PAIR == 1) ptx::mma_commit(&tail->empty[stage]);
             else ptx::mma_commit_pair(&tail->empty[stage], 0x3);
           } else {
-            // 32 K rows: per 16-row sub-step one MMA, plus one with the lo half
+            // KBK K rows: per 16-row sub-step one MMA, plus one with the lo half
             // of the split operand; a full step is one straight-line sequence
             const uint32_t sa = ptx::smem_u32(smem + stage * SC::BYTES), sb = sa + KG_A_BYTES,
                            sl = sb + KG_B_BYTES;
-            const uint64_t a0 = ptx::smem_desc(sa, KG_BLOCK_BYTES, 1024), a1 = ptx::smem_desc(sa + 2048, KG_BLOCK_BYTES, 1024);
-            const uint64_t b0 = ptx::smem_desc(sb, KG_BLOCK_BYTES, 1024), b1 = ptx::smem_desc(sb + 2048, KG_BLOCK_BYTES, 1024);
-            const uint64_t l0 = ptx::smem_desc(sl, KG_BLOCK_BYTES, 1024), l1 = ptx::smem_desc(sl + 2048, KG_BLOCK_BYTES, 1024);
-            const uint32_t acc0 = kb != 0 ? 1u : 0u;
-            const int nsub = tail_step ? (k_left - kb * BKK + UMMA_K - 1) / UMMA_K : 2;
-            if (SPLIT == SPLIT_A) {
-              ptx::mma_bf16(d_tmem, a0, b0, idesc, acc0);
-              ptx::mma_bf16(d_tmem, l0, b0, idesc, 1u);
-              if (nsub == 2) {
-                ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
-                ptx::mma_bf16(d_tmem, l1, b1, idesc, 1u);
-              }
-            } else if (SPLIT == SPLIT_B) {
-              ptx::mma_bf16(d_tmem, a0, b0, idesc, acc0);
-              ptx::mma_bf16(d_tmem, a0, l0, idesc, 1u);
-              if (nsub == 2) {
-                ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
-                ptx::mma_bf16(d_tmem, a1, l1, idesc, 1u);
-              }
+            constexpr int NSUB = KBK / UMMA_K;
+            const int nsub = tail_step ? (k_left - kb * KBK + UMMA_K - 1) / UMMA_K : NSUB;
+            auto sub_step = [&](int s) {
+              const uint64_t as = ptx::smem_desc(sa + s * 2048, KG_BLOCK_BYTES, 1024);
+              const uint64_t bs = ptx::smem_desc(sb + s * 2048, KG_BLOCK_BYTES, 1024);
+              const uint32_t acc0 = (kb | s) != 0 ? 1u : 0u;
+              ptx::mma_bf16(d_tmem, as, bs, idesc, acc0);
+              if (SPLIT == SPLIT_A) ptx::mma_bf16(d_tmem, ptx::smem_desc(sl + s * 2048, KG_BLOCK_BYTES, 1024), bs, idesc, 1u);
+              if (SPLIT == SPLIT_B) ptx::mma_bf16(d_tmem, as, ptx::smem_desc(sl + s * 2048, KG_BLOCK_BYTES, 1024), idesc, 1u);
+            };
+            if (nsub == NSUB) {
+#pragma unroll
+              for (int s = 0; s < NSUB; ++s) sub_step(s);
             } else {
-              ptx::mma_bf16(d_tmem, a0, b0, idesc, acc0);
-              if (nsub == 2) ptx::mma_bf16(d_tmem, a1, b1, idesc, 1u);
+              for (int s = 0; s < nsub; ++s) sub_step(s);
             }
             ptx::mma_commit(&tail->empty[stage]);
           }
@@ -741,7 +751,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         break;
       }
       if (t >= total) break;
-      TileInfo ti = decode<MODE, TILE_M>(P, S, t);
+      TileInfo ti = decode<MODE, TILE_M, KBK>(P, S, t);
       const Problem& pr = P.prob[ti.p];
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;

@@ -86,18 +86,19 @@ bool fill_wgrad(Params& P, Problem& pr, const WgradArgs& a) {
   const int ia = new_map(P), ib = new_map(P);
   if (ia < 0 || ib < 0) return false;
   // 64-column block views: one TMA box per operand and stage (A: 2 blocks, B: 4)
-  if (!encode_blocks(&P.maps[ia], a.A, a.M, a.rows_total, BKK, 2)) return false;
-  if (!encode_blocks(&P.maps[ib], a.B, a.N, a.rows_total, BKK, 4)) return false;
+  const int bkk = kg_rows(a.A_lo ? SPLIT_A : a.B_lo ? SPLIT_B : SPLIT_NONE);
+  if (!encode_blocks(&P.maps[ia], a.A, a.M, a.rows_total, bkk, 2)) return false;
+  if (!encode_blocks(&P.maps[ib], a.B, a.N, a.rows_total, bkk, 4)) return false;
   pr = blank_problem();
   if (a.A_lo) {
     pr.map_a_lo = new_map(P);
     if (pr.map_a_lo < 0) return false;
-    if (!encode_blocks(&P.maps[pr.map_a_lo], a.A_lo, a.M, a.rows_total, BKK, 2)) return false;
+    if (!encode_blocks(&P.maps[pr.map_a_lo], a.A_lo, a.M, a.rows_total, bkk, 2)) return false;
   }
   if (a.B_lo) {
     pr.map_b_lo = new_map(P);
     if (pr.map_b_lo < 0) return false;
-    if (!encode_blocks(&P.maps[pr.map_b_lo], a.B_lo, a.N, a.rows_total, BKK, 4)) return false;
+    if (!encode_blocks(&P.maps[pr.map_b_lo], a.B_lo, a.N, a.rows_total, bkk, 4)) return false;
   }
   pr.nsplit = (a.A_lo || a.B_lo) ? 2 : 1;
   pr.blk3d = 1;
@@ -111,7 +112,7 @@ bool fill_wgrad(Params& P, Problem& pr, const WgradArgs& a) {
   pr.map_a = ia;
   pr.map_b = ib;
   // one ragged-K stage: A (2 blocks), B (4), and the lo half of A (2) or of B (4)
-  pr.tx_bytes = (2 + 4 + (a.A_lo ? 2 : a.B_lo ? 4 : 0)) * KG_BLOCK_BYTES;
+  pr.tx_bytes = (2 + 4 + (a.A_lo ? 2 : a.B_lo ? 4 : 0)) * 64 * bkk * 2;
   pr.out = a.out;
   pr.out2 = a.out2;
   pr.row_split = a.out2 ? a.row_split : 0;
@@ -193,9 +194,10 @@ cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* ti
       const uint32_t nblk[KG_MAPS_PER_GROUP] = {2, 4, a.A_lo ? 2u : 4u};
       CUtensorMap whole_1row[KG_MAPS_PER_GROUP];
       uint64_t rb[KG_MAPS_PER_GROUP];
+      const int bkk = kg_rows(a.A_lo ? SPLIT_A : a.B_lo ? SPLIT_B : SPLIT_NONE);
       for (int m = 0; m < nmaps; ++m) {
         rb[m] = cols[m] * 2;
-        if (!encode_blocks(&whole_1row[m], base[m], cols[m], 1, BKK, nblk[m])) return cudaErrorInvalidValue;
+        if (!encode_blocks(&whole_1row[m], base[m], cols[m], 1, bkk, nblk[m])) return cudaErrorInvalidValue;
       }
       CUtensorMap* gm = static_cast<CUtensorMap*>(group_maps);
       cudaError_t e =

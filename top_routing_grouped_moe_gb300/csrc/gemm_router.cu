@@ -47,9 +47,10 @@ cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const v
   Params P;
   std::memset(&P, 0, sizeof(P));
   P.num_maps = 3;
-  if (!encode_2d(&P.maps[0], dl_hi, E, T, (uint64_t)E * 2, 64, BKK)) return cudaErrorInvalidValue;
-  if (!encode_2d(&P.maps[1], x, d, T, (uint64_t)d * 2, 64, BKK)) return cudaErrorInvalidValue;
-  if (!encode_2d(&P.maps[2], dl_lo, E, T, (uint64_t)E * 2, 64, BKK)) return cudaErrorInvalidValue;
+  constexpr int bkk = kg_rows(SPLIT_A);  // K rows (tokens) per stage
+  if (!encode_2d(&P.maps[0], dl_hi, E, T, (uint64_t)E * 2, 64, bkk)) return cudaErrorInvalidValue;
+  if (!encode_2d(&P.maps[1], x, d, T, (uint64_t)d * 2, 64, bkk)) return cudaErrorInvalidValue;
+  if (!encode_2d(&P.maps[2], dl_lo, E, T, (uint64_t)E * 2, 64, bkk)) return cudaErrorInvalidValue;
   Problem& pr = P.prob[0];
   pr = blank_problem();
   pr.map_a_lo = 2;
@@ -62,7 +63,7 @@ cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const v
   pr.n_tile = 256;
   pr.map_a = 0;
   pr.map_b = 1;
-  pr.tx_bytes = (2 + 4 + 2) * KG_BLOCK_BYTES;  // A, B, lo half of A
+  pr.tx_bytes = (2 + 4 + 2) * 64 * bkk * 2;  // A, B, lo half of A
   pr.out = part;
   pr.ldo = d;
   pr.gstride = (long long)E * d;

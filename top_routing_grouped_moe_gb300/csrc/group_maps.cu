@@ -108,6 +108,8 @@ extern "C" MOE_API int moe_selftest_group_maps(void) {
   cudaError_t e = cudaMalloc(&buf, (size_t)rows * 4096 * 2);
   if (e == cudaSuccess) e = cudaMalloc(&d_off, (kMaxGroups + 1) * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&d_maps, (size_t)kMaxGroups * kMapsPerGroup * sizeof(CUtensorMap));
+  // both box heights the weight-gradient GEMMs use (32 and 64 rows per stage)
+  for (int bkk : {kg_rows(SPLIT_B), kg_rows(SPLIT_A)})
   for (uint64_t cols : widths) {
     if (e != cudaSuccess || rc != MOE_OK) break;
     // groups laid end to end: sizes around n* (the first size at 128 KiB)
@@ -129,8 +131,8 @@ extern "C" MOE_API int moe_selftest_group_maps(void) {
     const void* base[2] = {buf, buf};
     const uint64_t row_bytes[2] = {cols * 2, cols * 2};
     for (int m = 0; m < 2; ++m)
-      if (!encode_blocks(&whole[m], buf, cols, rows, BKK, blocks[m]) ||
-          !encode_blocks(&whole_1row[m], buf, cols, 1, BKK, blocks[m]))
+      if (!encode_blocks(&whole[m], buf, cols, rows, bkk, blocks[m]) ||
+          !encode_blocks(&whole_1row[m], buf, cols, 1, bkk, blocks[m]))
         rc = MOE_ERR_UNSUPPORTED;
     if (rc != MOE_OK) break;
     e = cudaMemcpy(d_off, h_off, (G + 1) * sizeof(int32_t), cudaMemcpyHostToDevice);
@@ -146,7 +148,7 @@ extern "C" MOE_API int moe_selftest_group_maps(void) {
       }
       for (int m = 0; m < 2; ++m) {
         CUtensorMap want;
-        if (!encode_blocks(&want, static_cast<const char*>(buf) + (uint64_t)r0 * row_bytes[m], cols, n, BKK,
+        if (!encode_blocks(&want, static_cast<const char*>(buf) + (uint64_t)r0 * row_bytes[m], cols, n, bkk,
                            blocks[m]) ||
             std::memcmp(&want, &got[g * kMapsPerGroup + m], sizeof(CUtensorMap)) != 0)
           rc = MOE_ERR_UNSUPPORTED;
