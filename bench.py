@@ -106,8 +106,7 @@ def kernel_work(w, R):
         "gemm_wgrad_gate_up": (gu, 2 * hid * 2 + rows * d * 2 + wgu),
         "gemm_router": (2.0 * T * d * E, T * d * 2 + E * d * 2 + T * E * 4),
         "gemm_router_dw": (2.0 * T * d * E, T * E * 2 + T * d * 2 + E * d * 4),
-        "gemm_router_dx_reduce": (2.0 * T * d * E, T * E * 2 + E * d * 2 + R * d * 2 + T * d * 2 * sh
-                                  + T * d * 2 + T * k * 4),
+        "gemm_router_dx": (2.0 * T * d * E, T * E * 4 + E * d * 2 + T * d * 2),
         "perm_scatter": (0.0, T * d * 2 + R * d * 2 + T * k * 12 + R * 4),
         "combine": (0.0, R * d * 2 + T * d * 2 * sh + T * d * 2 + T * k * 8),
         "gather_rows": (0.0, T * d * 2 + R * d * 2 + T * k * 4),

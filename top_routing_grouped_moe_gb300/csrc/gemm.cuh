@@ -83,7 +83,7 @@ struct KgCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + (SPLIT == SPLIT_A ? A_BYTES : SPLIT == SPLIT_B ? B_BYTES : 0);
   static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
 };
-enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3, EPI_REDUCE_DX = 4 };
+enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3 };
 
 struct Problem {
   const int* offsets;  // [G+1] device; NULL: `extent` split evenly into G chunks
@@ -110,13 +110,9 @@ struct Problem {
   void* out2;          // rows >= row_split go to out2 (KGROUP; 0 = off)
   int row_split;
   int map_out, map_out2;   // EPI_BF16 (ragged K): TMA-store maps of out / out2, [G][rows][N], 32 x 32 boxes
-  void* aux;           // SWIGLU_FWD: au out; SWIGLU_BWD: au in; REDUCE_DX: dx_perm in
+  void* aux;           // SWIGLU_FWD: au out; SWIGLU_BWD: au in
   long long ld_aux;
-  const void* aux2;    // REDUCE_DX: dx_s in (nullable)
   const float* bias;   // EPI_F32 (nullable)
-  const int* row_of_slot;  // REDUCE_DX
-  int topk;
-  int aux_rows;        // REDUCE_DX: rows of the dx_perm buffer (bounds check)
   int H;               // SWIGLU: column offset of u within au
   // EPI_SWIGLU_BWD
   const float* gates;      // per-slot gate (nullable: g = 1)
@@ -996,66 +992,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             const int r = 4 * j + rs;
             if ((lane & 7) == 0 && r < nrows) pr.dgp[(long long)(row0 + r) * pr.ld_dgp + ti.n0 / pr.n_tile] = v;
           }
-        }
-      } else if (EPI == EPI_REDUCE_DX) {
-        // dx[t] = acc (router term) + dx_s[t] + sum_s dx_perm[row(t,s)]
-        const int kk = pr.topk;
-        int my_rows[kMaxK];
-#pragma unroll
-        for (int s = 0; s < kMaxK; ++s) {
-          my_rows[s] = -1;
-          if (s < kk && lane < nrows) {
-            int rr = __ldg(pr.row_of_slot + (long long)(row0 + lane) * kk + s);
-            if (rr >= pr.aux_rows) {
-              record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
-              rr = -1;
-            }
-            my_rows[s] = rr;
-          }
-        }
-        int rows_j[8][kMaxK];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int s = 0; s < kMaxK; ++s) rows_j[j][s] = __shfl_sync(FULL, my_rows[s], 4 * j + rs);
-        __nv_bfloat16* dxp = reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row0 * pr.ldo;
-        const float* xs = pr.aux2 ? reinterpret_cast<const float*>(pr.aux2) + (long long)row0 * pr.ldo : nullptr;
-        const float* xp = reinterpret_cast<const float*>(pr.aux);
-        for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
-          if (ti.n0 + c0 >= pr.N) break;
-          float4 v[8];
-          if (has_acc) tmem_chunk_quad(taddr + c0, tb, lane, v);
-          else zero_quad(v);
-          const int col = ti.n0 + c0 + cq;
-          // one term at a time for all eight rows, so eight loads are in flight
-          if (xs) {
-            float4 b[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (4 * j + rs < nrows) b[j] = __ldg(reinterpret_cast<const float4*>(xs + (long long)(4 * j + rs) * pr.ldo + col));
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (4 * j + rs < nrows) {
-                v[j].x += b[j].x; v[j].y += b[j].y; v[j].z += b[j].z; v[j].w += b[j].w;
-              }
-          }
-#pragma unroll
-          for (int s = 0; s < kMaxK; ++s) {
-            if (s >= kk) break;
-            float4 b[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (4 * j + rs < nrows && rows_j[j][s] >= 0)
-                b[j] = __ldg(reinterpret_cast<const float4*>(xp + (long long)rows_j[j][s] * pr.ld_aux + col));
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (4 * j + rs < nrows && rows_j[j][s] >= 0) {
-                v[j].x += b[j].x; v[j].y += b[j].y; v[j].z += b[j].z; v[j].w += b[j].w;
-              }
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (4 * j + rs < nrows) store4(dxp + (long long)(4 * j + rs) * pr.ldo + col, v[j]);
         }
       }
       ptx::tc_fence_before();

@@ -1,5 +1,5 @@
 // Router GEMMs: logits = x W_r^T + b (forward), dW_r split-K partials and the
-// router's input gradient fused with the unpermute reduction (backward).
+// router's input gradient (backward).
 #include "gemm_host.cuh"
 
 namespace moe {
@@ -72,9 +72,8 @@ cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const v
                                                   "gemm_router_dw");
 }
 
-cudaError_t gemm_router_dx_reduce(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, const float* dx_perm,
-                                  const float* dx_s, const int32_t* row_of_slot, int T, int d, int E, int k, void* dx,
-                                  int* status, cudaStream_t s) {
+cudaError_t gemm_router_dx(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, int T, int d, int E,
+                           float* dx_r, int* status, cudaStream_t s) {
   (void)status;
   Params P;
   std::memset(&P, 0, sizeof(P));
@@ -95,17 +94,10 @@ cudaError_t gemm_router_dx_reduce(const uint16_t* dl_hi, const uint16_t* dl_lo, 
   pr.map_a = 0;
   pr.map_b = 1;
   pr.tx_bytes = A_BYTES + 4 * MN_BLOCK_BYTES;
-  pr.out = dx;
+  pr.out = dx_r;
   pr.ldo = d;
-  pr.aux = const_cast<float*>(dx_perm);
-  pr.ld_aux = d;
-  pr.aux2 = dx_s;
-  pr.row_of_slot = row_of_slot;
-  pr.topk = k;
-  pr.aux_rows = T * k;
   P.num_problems = 1;
-  return launch<0, 1, MGROUP, EPI_REDUCE_DX, 1>(P, (long long)cdiv_h(T, BM) * cdiv_h(d, 256), s,
-                                              "gemm_router_dx_reduce");
+  return launch<0, 1, MGROUP, EPI_F32, 1>(P, (long long)cdiv_h(T, BM) * cdiv_h(d, 256), s, "gemm_router_dx");
 }
 
 }  // namespace moe

@@ -37,9 +37,11 @@ cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T
 // dgates[t,s] = sum_p dgp[row_of_slot[t*k+s], p] (0 for dropped slots)
 cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_slot, int T, int k, float* dgates,
                                  cudaStream_t s);
-// dx_perm, dx_s fp32; dx bf16
-cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, int T, int d,
-                                    int k, void* dx, int* status, cudaStream_t s);
+// dx[t] = sum_s dx_perm[row(t,s)] + dx_s[t] + dx_r[t]   (fp32 terms, dx_s and dx_r
+// nullable; dx bf16)
+cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const float* dx_r,
+                                    const int32_t* row_of_slot, int T, int d, int k, void* dx, int* status,
+                                    cudaStream_t s);
 // dlogits [T,E] fp32 (dense, + add[T,E] if add != NULL) and, if dl_hi != NULL,
 // its bf16 hi + lo halves [T,E]
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
@@ -136,11 +138,9 @@ cudaError_t launch_group_maps(const CUtensorMap* whole, const CUtensorMap* whole
 // dW_r partials: part[S, E, d] = split-K pieces of (dl_hi + dl_lo)^T x; dl halves [T, E] bf16
 cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* x, int T, int d, int E, int S,
                            float* part, int* status, cudaStream_t s);
-// dx = (dl_hi + dl_lo) W_r + dx_s + sum_s dx_perm[row(t,s)]   (dx_perm, dx_s fp32)
-cudaError_t gemm_router_dx_reduce(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, const float* dx_perm,
-                                  const float* dx_s,
-                                  const int32_t* row_of_slot, int T, int d, int E, int k, void* dx, int* status,
-                                  cudaStream_t s);
+// dx_r [T, d] fp32 = (dl_hi + dl_lo) W_r, the router's term of the input gradient
+cudaError_t gemm_router_dx(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, int T, int d, int E,
+                           float* dx_r, int* status, cudaStream_t s);
 
 // split-K factor used for dW_r
 int router_dw_splits(int T, int d, int E);

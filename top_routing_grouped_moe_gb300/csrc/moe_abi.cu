@@ -46,7 +46,8 @@ size_t ws_route_topk_bwd(int T, int d, int E) {
   const int S = router_dw_splits(T, d, E);
   return 2 * align256((size_t)T * E * 2) + (S > 1 ? align256((size_t)S * E * d * 4) : 0);
 }
-size_t ws_permute_bwd(int T, int E) { return 2 * align256((size_t)T * E * 2); }
+// dlogits as bf16 hi + lo [T,E] x2, the router's fp32 term of dx [T,d]
+size_t ws_permute_bwd(int T, int d, int E) { return 2 * align256((size_t)T * E * 2) + align256((size_t)T * d * 4); }
 
 // grouped SwiGLU backward scratch: da|du hi+lo [rows,2H] x2, g*h hi+lo [rows,H] x2,
 // gate-gradient partials [rows, ceil(H/256)], for the routed rows (T*k) and the
@@ -209,7 +210,7 @@ int moe_workspace_size(int T, int d, int E, int k, int H, int Hs, size_t* bytes)
   size_t b = permute_ws_bytes(T, E, k);
   size_t v = ws_route_topk_bwd(T, d, E);
   if (v > b) b = v;
-  v = ws_permute_bwd(T, E);
+  v = ws_permute_bwd(T, d, E);
   if (v > b) b = v;
   v = ws_swiglu_bwd(T, k, H, Hs);
   if (v > b) b = v;
@@ -429,17 +430,20 @@ int moe_permute_bwd(const float* dx_perm, const float* dx_s, const int32_t* row_
   if (!al16(dx_perm) || !al16(dx) || (dx_s && !al16(dx_s))) return MOE_ERR_INVALID_ARG;
   if ((dlogits == nullptr) != (W_r == nullptr)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (!W_r) return check(launch_unpermute_reduce(dx_perm, dx_s, row_of_slot, T, d, k, dx, device_status_ptr(), st));
+  if (!W_r)
+    return check(launch_unpermute_reduce(dx_perm, dx_s, nullptr, row_of_slot, T, d, k, dx, device_status_ptr(), st));
   int rc = check_dims(T, d, E, k);
   if (rc) return rc;
   if (!al16(W_r)) return MOE_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < ws_permute_bwd(T, E)) return MOE_ERR_WORKSPACE;
+  if (!ws || ws_bytes < ws_permute_bwd(T, d, E)) return MOE_ERR_WORKSPACE;
   uint16_t* dl_hi = static_cast<uint16_t*>(ws);
   uint16_t* dl_lo = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + align256((size_t)T * E * 2));
   cudaError_t e = launch_f32_to_bf16_split(dlogits, dl_hi, dl_lo, (long long)T * E, st);
   if (e != cudaSuccess) return fail_cuda(e);
-  return check(gemm_router_dx_reduce(dl_hi, dl_lo, W_r, dx_perm, dx_s, row_of_slot, T, d, E, k, dx,
-                                     device_status_ptr(), st));
+  float* dx_r = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * align256((size_t)T * E * 2));
+  e = gemm_router_dx(dl_hi, dl_lo, W_r, T, d, E, dx_r, device_status_ptr(), st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return check(launch_unpermute_reduce(dx_perm, dx_s, dx_r, row_of_slot, T, d, k, dx, device_status_ptr(), st));
 }
 
 }  // extern "C"

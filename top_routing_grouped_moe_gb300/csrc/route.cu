@@ -343,8 +343,8 @@ __global__ void dgates_reduce_kernel(const float* __restrict__ dgp, int P, const
 }
 
 __global__ void unpermute_reduce_kernel(const float4* __restrict__ dx_perm, const float4* __restrict__ dx_s,
-                                        const int32_t* __restrict__ row_of_slot, int T, int d, int k,
-                                        long long max_rows, uint4* __restrict__ dx, int* status) {
+                                        const float4* __restrict__ dx_r, const int32_t* __restrict__ row_of_slot,
+                                        int T, int d, int k, long long max_rows, uint4* __restrict__ dx, int* status) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -362,12 +362,17 @@ __global__ void unpermute_reduce_kernel(const float4* __restrict__ dx_perm, cons
   const int vpr = d / 8;
   for (int c = lane; c < vpr; c += 32) {
     float acc[8];
-    if (dx_s) {
-      float4 a = __ldg(dx_s + (long long)t * 2 * vpr + 2 * c), b = __ldg(dx_s + (long long)t * 2 * vpr + 2 * c + 1);
-      acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w; acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
-    } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    // the per-token terms (shared expert, router), then the kept rows
+    const float4* tok_terms[2] = {dx_s, dx_r};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (!tok_terms[i]) continue;
+      const float4* src = tok_terms[i] + (long long)t * 2 * vpr + 2 * c;
+      float4 a = __ldg(src), b = __ldg(src + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
     }
 #pragma unroll
     for (int s = 0; s < kMaxK; ++s) {
@@ -644,11 +649,13 @@ cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, int T, int d,
-                                    int k, void* dx, int* status, cudaStream_t s) {
+cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const float* dx_r,
+                                    const int32_t* row_of_slot, int T, int d, int k, void* dx, int* status,
+                                    cudaStream_t s) {
   timing_mark(s, "unpermute_reduce");
   unpermute_reduce_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-      reinterpret_cast<const float4*>(dx_perm), reinterpret_cast<const float4*>(dx_s), row_of_slot, T, d, k,
+      reinterpret_cast<const float4*>(dx_perm), reinterpret_cast<const float4*>(dx_s),
+      reinterpret_cast<const float4*>(dx_r), row_of_slot, T, d, k,
       (long long)T * k,
       static_cast<uint4*>(dx), status);
   return cudaGetLastError();
