@@ -23,8 +23,9 @@ Prints ONE JSON line (rank 0).  With --gpus N > 1 (torchrun) every rank runs an
 independent replica of the layer on its own tokens (weak scaling; the layer
 has no exchange step, so no collective runs on the data path).
 
---impl reference times the CPU oracle (float64 numpy, the machine's host cores) on
-a bounded token sample of the same workload: rank 0 only.
+--impl reference times the CPU oracle (the C++ fp64 layer of
+oracle/moe_oracle.cpp on all host cores) on a bounded token sample of the same
+workload: rank 0 only.
 """
 from __future__ import annotations
 
@@ -244,7 +245,7 @@ def oracle_sample(inp, n_tokens):
 
 
 def run_oracle_step(w, f64, n_tokens):
-    from oracle import moe_oracle as orc
+    from oracle import moe_oracle_cpp as orc
     cap = orc.capacity_of(n_tokens, w.k, w.E) if w.capacity > 0 else 0
     t0 = time.perf_counter()
     fwd = orc.layer_forward(f64, w.k, cap)
@@ -262,13 +263,13 @@ def oracle_tokens(w, inp_f64, budget_s):
 
 
 def cpu_baseline(w, inp, n_tokens=0, budget_s=20.0):
-    from oracle import moe_oracle as orc
+    from oracle import moe_oracle_cpp as orc
     f64 = orc.inputs_to_f64(inp)
     n = min(n_tokens, w.T) if n_tokens > 0 else oracle_tokens(w, f64, budget_s)
     t = run_oracle_step(w, oracle_sample(f64, n), n)
-    return {"value": n / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} of {w.T} tokens of {w.name} (the first), forward+backward, float64 numpy "
-                      f"(BLAS on all {os.cpu_count()} host cores), one step of {t:.1f} s"}
+    return {"value": n / t, "unit": "tokens/s", "cores": orc.threads(), "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of {w.name} (the first), forward+backward, the C++ fp64 oracle "
+                      f"on {orc.threads()} host threads, one step of {t:.1f} s"}
 
 
 def main_reference(args):
@@ -277,7 +278,7 @@ def main_reference(args):
         return 0
     w = backward_workload(args.workload)
     inp = workloads.make_inputs(w)
-    from oracle import moe_oracle as orc
+    from oracle import moe_oracle_cpp as orc
     f64 = orc.inputs_to_f64(inp)
     nsteps = args.steps + args.warmup
     n = min(args.cpu_sample_tokens, w.T) if args.cpu_sample_tokens > 0 else \
@@ -296,8 +297,9 @@ def main_reference(args):
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "H": w.H, "Hs": w.Hs,
                    "routing": w.routing, "capacity": w.capacity, "pass": "forward+backward",
                    "sample_tokens": n},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{n} of {w.T} tokens per step (the first), forward+backward, float64 numpy"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": orc.threads(), "kind": "oracle",
+                         "sample": f"{n} of {w.T} tokens per step (the first), forward+backward, the C++ fp64 "
+                                   f"oracle on {orc.threads()} host threads"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

@@ -107,7 +107,7 @@ class ParityInfo(UserWarning):
     from the fp64-router oracle at near ties."""
 
 
-def oracle_reference(w, inp, layer, f64=None):
+def oracle_reference(w, inp, layer, f64=None, impl=None):
     """The oracle's forward and backward for a finished GPU layer run.
 
     Learned routing: the GPU's fp32 logits are first checked against the
@@ -117,10 +117,12 @@ def oracle_reference(w, inp, layer, f64=None):
     rounding allowance).  The oracle then runs the whole layer on the GPU's
     logits, so that routing, permutation, gates and every downstream value are
     compared on the same fp32 logits, with no token or expert left out.
-    Returns (f64 inputs, forward dict, backward dict, number of near-tie
-    tokens)."""
+    impl: the oracle module (default the numpy one; oracle.moe_oracle_cpp
+    has the same interface).  Returns (f64 inputs, forward dict, backward
+    dict, number of near-tie tokens)."""
     import warnings
-    from oracle import moe_oracle as orc
+    from oracle import moe_oracle
+    orc = impl or moe_oracle
     if f64 is None:
         f64 = orc.inputs_to_f64(inp)
     flips = 0

@@ -19,6 +19,16 @@ import torch
 from oracle import moe_oracle as orc
 from synth import gen, workloads
 
+
+@pytest.fixture(params=["numpy", "cpp"])
+def impl(request):
+    """The oracle under test: the numpy oracle or the C++ one; both must meet
+    every pin that takes this fixture."""
+    if request.param == "numpy":
+        return orc
+    from oracle import moe_oracle_cpp
+    return moe_oracle_cpp
+
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "routing_hand.json")
 
 
@@ -27,20 +37,20 @@ def _f(v):
 
 
 # ---------------------------------------------------------------- golden
-def test_golden_topk_cases():
+def test_golden_topk_cases(impl):
     cases = json.load(open(GOLDEN))["topk"]
     for c in cases:
         l = np.array([[_f(v) for v in row] for row in c["logits"]], dtype=np.float32)
-        idx, g = orc.route_topk(l, c["k"])
+        idx, g = impl.route_topk(l, c["k"])
         assert idx.tolist() == c["idx"], c["name"]
         np.testing.assert_allclose(g, np.array(c["gates"]), rtol=0, atol=1e-15, err_msg=c["name"])
 
 
-def test_golden_permute_cases():
+def test_golden_permute_cases(impl):
     cases = json.load(open(GOLDEN))["permute"]
     for c in cases:
         idx = np.array(c["idx"], dtype=np.int32)
-        p = orc.permute(idx, c["E"], c["capacity"])
+        p = impl.permute(idx, c["E"], c["capacity"])
         for key in ("counts_raw", "counts", "offsets", "row_of_slot", "slot_of_row"):
             assert p[key].tolist() == c[key], (c["name"], key)
 
@@ -74,16 +84,16 @@ def _adversarial_logits(T, E, seed):
 
 
 @pytest.mark.parametrize("E,k", [(8, 2), (8, 8), (64, 4), (128, 4), (256, 8), (5, 1)])
-def test_topk_matches_brute_force(E, k):
+def test_topk_matches_brute_force(E, k, impl):
     l = _adversarial_logits(12, E, seed=E * 31 + k)
-    idx, g = orc.route_topk(l, k)
+    idx, g = impl.route_topk(l, k)
     assert np.array_equal(idx, brute_force_topk(l, k))
 
 
 @pytest.mark.parametrize("E,k", [(8, 2), (64, 4), (128, 4)])
-def test_gates_closed_form(E, k):
+def test_gates_closed_form(E, k, impl):
     l = gen.random_logits(64, E)
-    idx, g = orc.route_topk(l, k)
+    idx, g = impl.route_topk(l, k)
     # softmax over all E, then renormalise over the selected set
     l64 = l.astype(np.float64)
     p = np.exp(l64 - l64.max(axis=1, keepdims=True))
@@ -94,11 +104,11 @@ def test_gates_closed_form(E, k):
     assert np.all(np.diff(g, axis=1) <= 0)  # slot order = descending gate
 
 
-def test_random_routing_gates_are_softmax_over_the_k_drawn():
+def test_random_routing_gates_are_softmax_over_the_k_drawn(impl):
     T, E, k = 256, 64, 4
     l = gen.random_routing_logits(T, E, k)
     assert np.all(np.isfinite(l).sum(axis=1) == k)
-    idx, g = orc.route_topk(l, k)
+    idx, g = impl.route_topk(l, k)
     for t in range(T):
         fin = np.nonzero(np.isfinite(l[t]))[0]
         assert set(idx[t].tolist()) == set(fin.tolist())
@@ -110,11 +120,11 @@ def test_random_routing_gates_are_softmax_over_the_k_drawn():
 # ---------------------------------------------------------------- permutation
 @pytest.mark.parametrize("T,E,k,cap", [(300, 8, 2, 0), (300, 8, 2, 40), (1000, 64, 4, 0),
                                        (1000, 64, 4, orc.capacity_of(1000, 4, 64)), (7, 4, 4, 1)])
-def test_permutation_invariants(T, E, k, cap):
+def test_permutation_invariants(T, E, k, cap, impl):
     l = gen.random_logits(T, E)
     l[:, 0] += 1.0  # skew the load
-    idx, _ = orc.route_topk(l, k)
-    p = orc.permute(idx, E, cap)
+    idx, _ = impl.route_topk(l, k)
+    p = impl.permute(idx, E, cap)
     R = int(p["offsets"][-1])
     row = p["row_of_slot"]
     kept = row >= 0
@@ -157,11 +167,11 @@ def _tiny_inputs(T, d, E, H, Hs, seed, learned=True):
 
 
 @pytest.mark.parametrize("cap", [0, 3])
-def test_identity_experts_return_x_times_sum_of_kept_gates(cap):
+def test_identity_experts_return_x_times_sum_of_kept_gates(cap, impl):
     w = workloads.WORKLOADS["tiny"]
-    inp = orc.inputs_to_f64(workloads.make_inputs(w))
+    inp = impl.inputs_to_f64(workloads.make_inputs(w))
     inp.pop("Ws_g", None)
-    f = orc.layer_forward(inp, w.k, cap, expert_fn=lambda e, xr: xr)
+    f = impl.layer_forward(inp, w.k, cap, expert_fn=lambda e, xr: xr)
     kept_gate_sum = (f["gates"] * f["kept"]).sum(axis=1)
     np.testing.assert_allclose(f["y"], inp["x"] * kept_gate_sum[:, None], rtol=1e-13, atol=1e-13)
     if cap == 0:
@@ -207,16 +217,16 @@ def dense_masked_layer(inp, k, cap):
 
 
 @pytest.mark.parametrize("cap", [0, 5])
-def test_routed_layer_equals_dense_masked_layer(cap):
+def test_routed_layer_equals_dense_masked_layer(cap, impl):
     inp = _tiny_inputs(T=24, d=16, E=6, H=12, Hs=8, seed=3)
-    f = orc.layer_forward(inp, 2, cap)
+    f = impl.layer_forward(inp, 2, cap)
     yd = dense_masked_layer(inp, 2, cap)
     np.testing.assert_allclose(f["y"], yd, rtol=1e-12, atol=1e-12)
 
 
-def test_single_expert_k1_is_a_dense_swiglu_mlp():
+def test_single_expert_k1_is_a_dense_swiglu_mlp(impl):
     inp = _tiny_inputs(T=10, d=16, E=1, H=24, Hs=8, seed=5)
-    f = orc.layer_forward(inp, 1, 0)
+    f = impl.layer_forward(inp, 1, 0)
     F = torch.nn.functional
     x = torch.tensor(inp["x"])
 
@@ -229,8 +239,8 @@ def test_single_expert_k1_is_a_dense_swiglu_mlp():
 
 
 # ---------------------------------------------------------------- backward
-def _loss(inp, k, cap, **kw):
-    f = orc.layer_forward(inp, k, cap, exact_router=True, **kw)
+def _loss(impl, inp, k, cap, **kw):
+    f = impl.layer_forward(inp, k, cap, exact_router=True, **kw)
     return float((f["y"] * inp["dY"]).sum()), f
 
 
@@ -246,11 +256,11 @@ def _fd_setup(cap, seed0=11):
 
 
 @pytest.mark.parametrize("cap", [0, 3])
-def test_backward_matches_central_finite_differences(cap):
+def test_backward_matches_central_finite_differences(cap, impl):
     k = 2
     inp = _fd_setup(cap)
-    _, f = _loss(inp, k, cap)
-    b = orc.layer_backward(inp, f)
+    _, f = _loss(impl, inp, k, cap)
+    b = impl.layer_backward(inp, f)
     eps = 1e-6
     names = {"x": "dx", "W_r": "dW_r", "W_g": "dW_g", "W_u": "dW_u", "W_d": "dW_d",
              "Ws_g": "dWs_g", "Ws_u": "dWs_u", "Ws_d": "dWs_d"}
@@ -262,9 +272,9 @@ def test_backward_matches_central_finite_differences(cap):
             i = it.multi_index
             old = P[i]
             P[i] = old + eps
-            lp, fp = _loss(inp, k, cap)
+            lp, fp = _loss(impl, inp, k, cap)
             P[i] = old - eps
-            lm, fm = _loss(inp, k, cap)
+            lm, fm = _loss(impl, inp, k, cap)
             P[i] = old
             assert np.array_equal(fp["idx"], f["idx"]) and np.array_equal(fm["idx"], f["idx"])
             num[i] = (lp - lm) / (2 * eps)
@@ -275,7 +285,7 @@ def test_backward_matches_central_finite_differences(cap):
     for i in np.ndindex(G.shape):
         Gp = G.copy(); Gp[i] += eps
         Gm = G.copy(); Gm[i] -= eps
-        num[i] = (_loss(inp, k, cap, gates=Gp)[0] - _loss(inp, k, cap, gates=Gm)[0]) / (2 * eps)
+        num[i] = (_loss(impl, inp, k, cap, gates=Gp)[0] - _loss(impl, inp, k, cap, gates=Gm)[0]) / (2 * eps)
     np.testing.assert_allclose(b["dgates"], num, rtol=1e-6, atol=1e-7)
     # logits treated as inputs
     L = f["logits"].copy()
@@ -283,7 +293,7 @@ def test_backward_matches_central_finite_differences(cap):
     for i in np.ndindex(L.shape):
         Lp = L.copy(); Lp[i] += eps
         Lm = L.copy(); Lm[i] -= eps
-        num[i] = (_loss(inp, k, cap, logits=Lp)[0] - _loss(inp, k, cap, logits=Lm)[0]) / (2 * eps)
+        num[i] = (_loss(impl, inp, k, cap, logits=Lp)[0] - _loss(impl, inp, k, cap, logits=Lm)[0]) / (2 * eps)
     np.testing.assert_allclose(b["dlogits"], num, rtol=1e-6, atol=1e-7)
 
 
@@ -363,14 +373,14 @@ BF16_KNOWN = [
 ]
 
 
-def test_bf16_to_f64_known_values():
+def test_bf16_to_f64_known_values(impl):
     bits = np.array([b for b, _ in BF16_KNOWN], dtype=np.uint16)
-    got = orc.bf16_to_f64(bits)
+    got = impl.bf16_to_f64(bits)
     assert got.dtype == np.float64
     for (b, want), g in zip(BF16_KNOWN, got):
         assert g == want and math.copysign(1.0, g) == math.copysign(1.0, want), (hex(b), g, want)
     # a 2-D array keeps its shape
-    assert orc.bf16_to_f64(bits[:12].reshape(3, 4)).shape == (3, 4)
+    assert impl.bf16_to_f64(bits[:12].reshape(3, 4)).shape == (3, 4)
 
 
 # ---------------------------------------------------------------- router bias
@@ -378,6 +388,8 @@ BIAS_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "router_bias_han
 
 
 def _bias_case(c):
+    # the hand-written bit patterns decoded by the numpy oracle (pinned by
+    # test_bf16_to_f64_known_values)
     x = orc.bf16_to_f64(np.array([[int(h, 16) for h in c["x_bits"]]], dtype=np.uint16))
     W_r = orc.bf16_to_f64(np.array([[int(h, 16) for h in row] for row in c["W_r_bits"]], dtype=np.uint16))
     bias = np.array(c["bias"], dtype=np.float32)
@@ -391,13 +403,13 @@ def _k2_gates(c):
     return np.array([[1.0 / (1.0 + z), z / (1.0 + z)]])
 
 
-def check_router_bias_golden(layer_forward=None, router_logits=None):
+def check_router_bias_golden(layer_forward=None, router_logits=None, impl=orc):
     """The golden cases through the oracle's router and through its whole
     forward (identity experts), so that the bias is pinned where the layer
     applies it: in the fp32 logits that both the selection and the gates
     use."""
-    layer_forward = layer_forward or orc.layer_forward
-    router_logits = router_logits or orc.router_logits
+    layer_forward = layer_forward or impl.layer_forward
+    router_logits = router_logits or impl.router_logits
     for c in json.load(open(BIAS_GOLDEN))["cases"]:
         x, W_r, bias = _bias_case(c)
         l = router_logits(x, W_r, bias)
@@ -410,19 +422,19 @@ def check_router_bias_golden(layer_forward=None, router_logits=None):
             np.testing.assert_allclose(f["gates"], want, rtol=0, atol=1e-15, err_msg=f"{c['name']} k={k}")
 
 
-def test_router_bias_golden():
-    check_router_bias_golden()
+def test_router_bias_golden(impl):
+    check_router_bias_golden(impl=impl)
 
 
-def test_router_bias_moves_selection_and_gates():
+def test_router_bias_moves_selection_and_gates(impl):
     """A large bias on one expert puts it first for every token, and the gates
     are the softmax of the biased logits over the selection."""
     T, d, E, k = 64, 32, 8, 2
-    x = orc.bf16_to_f64(gen.normal_bf16(501, (T, d)))
-    W_r = orc.bf16_to_f64(gen.normal_bf16(502, (E, d), std=0.02))
+    x = impl.bf16_to_f64(gen.normal_bf16(501, (T, d)))
+    W_r = impl.bf16_to_f64(gen.normal_bf16(502, (E, d), std=0.02))
     bias = np.zeros(E, dtype=np.float32)
     bias[5] = 30.0
-    f = orc.layer_forward({"x": x, "W_r": W_r, "bias": bias}, k, 0, expert_fn=lambda e, xr: xr)
+    f = impl.layer_forward({"x": x, "W_r": W_r, "bias": bias}, k, 0, expert_fn=lambda e, xr: xr)
     assert np.all(f["idx"][:, 0] == 5)
     l = (x @ W_r.T).astype(np.float32) + bias  # fp32 product, then the fp32 add
     sel = np.take_along_axis(l.astype(np.float64), f["idx"].astype(np.int64), axis=1)
