@@ -20,7 +20,9 @@ format with FP8 E4M3 elements; the plainest reading of it, written out here:
             largest normal binade, so the block's largest value lands in
             [256, 512); an all-zero block takes the smallest scale 2^-127.
   convert   code_i = E4M3(v_i / X), rounding to nearest, ties to the even
-            mantissa, and saturating to +-448 (v / X can reach up to 512).
+            mantissa, and saturating to +-448 (v / X can reach up to 512);
+            a negative value that rounds to zero gives -0 (code 0x80), as
+            rounding keeps the sign of zero in IEEE arithmetic.
   GEMM      C[m, n] = sum_k (A_code[m,k] X_A[m, k/32]) (B_code[n,k] X_B[n, k/32])
             summed exactly (float64 here; the tensor cores sum in fp32).
   expert    a = MX(x) MX(W_g)^T, u = MX(x) MX(W_u)^T, h = silu(a) u,
@@ -62,16 +64,13 @@ def e4m3_decode_table() -> np.ndarray:
 
 
 _TABLE = e4m3_decode_table()
-# value -> code for the finite values (+0 for zero; the negative codes for
-# negative values)
+# magnitude -> code of the non-negative finite values; the sign bit (0x80) is
+# added for a negative rounded value, -0 included: rounding to nearest keeps
+# the sign of a value that rounds to zero, as in IEEE arithmetic, and E4M3 has
+# a negative zero (0x80)
 _CODE_OF = {}
-for _c in range(256):
-    _v = _TABLE[_c]
-    if np.isnan(_v):
-        continue
-    if _v == 0.0 and _c != 0:
-        continue  # -0 decodes to 0; encode zero as +0
-    _CODE_OF[float(_v)] = _c
+for _c in range(0x7F):
+    _CODE_OF[float(_TABLE[_c])] = _c
 
 
 def e4m3_round(v: np.ndarray) -> np.ndarray:
@@ -89,15 +88,30 @@ def e4m3_round(v: np.ndarray) -> np.ndarray:
     return np.copysign(q, v)
 
 
-def e4m3_encode(v: np.ndarray) -> np.ndarray:
-    """E4M3 codes (uint8) of the rounded values of v."""
+def e4m3_encode_elementwise(v: np.ndarray) -> np.ndarray:
+    """E4M3 codes (uint8) of the rounded values of v, one element at a time
+    through the value -> code dictionary."""
     r = e4m3_round(v)
     flat = r.ravel()
     codes = np.empty(flat.shape, dtype=np.uint8)
     for i, x in enumerate(flat):
         c = _CODE_OF[float(abs(x))]
-        codes[i] = c | (0x80 if (x < 0) else 0)
+        codes[i] = c | (0x80 if np.signbit(x) else 0)
     return codes.reshape(r.shape)
+
+
+# the non-negative finite values in code order (codes 0x00..0x7E increase
+# with the value), for the vectorized lookup
+_POS_VALUES = _TABLE[:0x7F]
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    """E4M3 codes (uint8) of the rounded values of v: the same lookup as
+    e4m3_encode_elementwise, vectorized (a rounded magnitude is one of the
+    table's values exactly, found by binary search)."""
+    r = e4m3_round(v)
+    c = np.searchsorted(_POS_VALUES, np.abs(r)).astype(np.uint8)
+    return np.where(np.signbit(r), c | np.uint8(0x80), c).astype(np.uint8)
 
 
 def mx_scale_exponent(amax: np.ndarray) -> np.ndarray:

@@ -163,3 +163,24 @@ def test_mxfp8_expert_agrees_with_the_unquantized_expert_within_the_quantization
     o_perm = mx.mxfp8_grouped_swiglu_fwd(x, offsets, Wg3, Wu3, Wd3)
     np.testing.assert_array_equal(o_perm[:40], mx.mxfp8_swiglu_fwd(x[:40], Wg, Wu, Wd)[3])
     np.testing.assert_array_equal(o_perm[40:], -mx.mxfp8_swiglu_fwd(x[40:], Wg, Wu, Wd)[3])
+
+
+def test_vectorized_encoder_equals_the_elementwise_lookup():
+    """The vectorized E4M3 encoder returns the element-wise dictionary lookup's
+    code for every finite code value, their midpoints, values past 448 and
+    random values across the format's range."""
+    t = mx.e4m3_decode_table()
+    vals = t[~np.isnan(t)]
+    mids = (np.sort(np.unique(np.abs(vals)))[1:] + np.sort(np.unique(np.abs(vals)))[:-1]) / 2
+    rng = np.random.default_rng(7)
+    rand = rng.standard_normal(4000) * np.exp2(rng.integers(-12, 10, 4000))
+    v = np.concatenate([vals, mids, -mids, [500.0, -1e6, 0.0, -0.0], rand])
+    assert np.array_equal(mx.e4m3_encode(v), mx.e4m3_encode_elementwise(v))
+
+
+def test_rounding_keeps_the_sign_of_zero():
+    """A negative value that rounds to zero encodes as -0 (0x80), a positive
+    one and +0 as +0 (0x00), as round-to-nearest does in IEEE arithmetic."""
+    v = np.array([-1e-9, -0.0, 0.0, 1e-9, -2.0 ** -11, 2.0 ** -11])
+    assert mx.e4m3_encode(v).tolist() == [0x80, 0x80, 0x00, 0x00, 0x80, 0x00]
+    assert np.array_equal(mx.e4m3_encode_elementwise(v), mx.e4m3_encode(v))
