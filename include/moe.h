@@ -344,6 +344,88 @@ MOE_API int moe_permute_bwd(const float* dx_perm, const float* dx_s, const int32
                     int T, int d, int E, int k, void* dx,
                     void* ws, size_t ws_bytes, void* stream);
 
+/* ----------------------------------------------------------------- MXFP8 */
+
+/* MXFP8 expert MLP ("Olmo-core DDP MoE examples" README: the MXFP8 rows of
+ * "Production throughput runs" and the MXFP8 recipe of "Other experiments in
+ * the report"; the pages name the precision only).  Format: the OCP
+ * microscaling format with FP8 E4M3 elements: every 32 consecutive values
+ * along the contraction dimension share one power-of-two scale
+ * X = 2^(floor(log2 max|v|) - 8) (E8M0 byte = exponent + 127; 2^-127 for an
+ * all-zero block), and code = E4M3(v / X) rounded to nearest (ties to even),
+ * saturating at +-448.
+ *
+ * Layouts.  Codes: one byte per element, row-major.  Scales ("tile atoms"):
+ * the scales of rows [128 t, 128 t + 128) and 32-value blocks [4 q, 4 q + 4)
+ * of a [rows, cols] matrix form one 512-byte atom at byte (t * cols/128 + q)
+ * * 512; in it the scale of row 128 t + 32 j + l, block 4 q + b is byte
+ * 16 l + 4 j + b.  moe_mxfp8_scales_bytes gives an array's size (rows rounded
+ * up to 128).  Padded row space: the MX permutation places expert e's rows
+ * from mx_offsets[e], a multiple of 128 (mx_offsets = exclusive prefix sum of
+ * the counts rounded up to 128), in buffers of moe_mxfp8_rows(T, E, k) rows.
+ * Shape limits: those of the bf16 path and d % 128 == 0. */
+
+/* *rows = rows of the padded row space: T*k + 127*E rounded up to 128. */
+MOE_API int moe_mxfp8_rows(int T, int E, int k, long long* rows);
+
+/* *bytes = size of the tile-atom scale array of a [rows, cols] matrix
+ * (cols % 128 == 0). */
+MOE_API int moe_mxfp8_scales_bytes(long long rows, int cols, size_t* bytes);
+
+/* Quantize bf16 rows: src [rows, cols] bf16 -> codes [rows, cols] E4M3 and
+ * scales (tile atoms), blocks of 32 along each row.  For the weights of the
+ * down projection (W_d [E, d, H] as E*d rows of H), of the shared expert and
+ * for x (the shared expert's input, T rows of d).  Asynchronous. */
+MOE_API int moe_mxfp8_quantize(const void* src, long long rows, int cols, void* codes, void* scales,
+                               void* stream);
+
+/* Quantize the gate and up weights W_g, W_u [E, H, d] into one packed matrix
+ * [E, 2H, d] of codes (blocks of 32 along d) and its scales: for every 64
+ * h-columns j (rows [128 j', 128 j' + 128) of expert e's 2H rows) the 64 rows
+ * of W_g, then the 64 rows of W_u of the same h columns, so that one 128-row
+ * tile of the packed matrix yields 64 columns of a and of u.  E = 1 with the
+ * shared weights [Hs, d] packs those. */
+MOE_API int moe_mxfp8_quantize_gate_up(const void* W_g, const void* W_u, int E, int H, int d, void* codes,
+                                       void* scales, void* stream);
+
+/* moe_permute with x_perm in MXFP8 and the rows in the padded row space:
+ * counts_raw, counts, offsets as moe_permute (bit-exact, unpadded); mx_offsets
+ * [E+1] the padded offsets; row_of_slot [T*k] (-1 dropped) and slot_of_row
+ * [moe_mxfp8_rows] in padded rows; x_codes [moe_mxfp8_rows, d] and x_scales
+ * (tile atoms of that many rows): the codes and scales of x[t], quantized once
+ * per token along d, in every kept row of t.  Rows of the padding are not
+ * written.  ws as for moe_permute. */
+MOE_API int moe_permute_mxfp8(const void* x, const int32_t* topk_idx, int T, int d, int E, int k, int capacity,
+                              int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* mx_offsets,
+                              int32_t* row_of_slot, int32_t* slot_of_row, void* x_codes, void* x_scales,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* The expert MLP on MXFP8 operands, plus the shared expert: per kept row r of
+ * expert e (rows [mx_offsets[e], mx_offsets[e] + counts[e]) of the padded
+ * space),
+ *   a = MX(x) MX(W_g[e])^T, u = MX(x) MX(W_u[e])^T   (fp32 accumulate)
+ *   h = silu(a) u, quantized along H (blocks of 32) into h_codes / h_scales
+ *   o = MX(h) MX(W_d[e])^T  -> o_perm [moe_mxfp8_rows, d] fp32
+ * and the same on every token with the shared weights (xs = MX(x) from
+ * moe_mxfp8_quantize, h_s -> hs_codes [T, Hs] / hs_scales, s [T, d] fp32).
+ * Wgu: the packed gate/up codes and scales (moe_mxfp8_quantize_gate_up);
+ * Wd: W_d quantized as E*d rows of H.  The products run on the tensor cores
+ * as block-scaled E4M3 MMAs (tcgen05 kind::mxf8f6f4, E8M0 scales in tensor
+ * memory).  Rows of the padding are not written. */
+MOE_API int moe_grouped_swiglu_mxfp8(const void* x_codes, const void* x_scales, const int32_t* mx_offsets,
+                                     const int32_t* counts, const void* xs_codes, const void* xs_scales, int T,
+                                     int d, int E, int k, int H, int Hs, const void* Wgu_codes,
+                                     const void* Wgu_scales, const void* Wd_codes, const void* Wd_scales,
+                                     const void* Wsgu_codes, const void* Wsgu_scales, const void* Wsd_codes,
+                                     const void* Wsd_scales, void* h_codes, void* h_scales, void* hs_codes,
+                                     void* hs_scales, float* o_perm, float* s, void* stream);
+
+/* moe_unpermute_combine for o_perm in the padded row space of the MXFP8
+ * path (moe_mxfp8_rows(T, E, k) rows; row_of_slot from moe_permute_mxfp8). */
+MOE_API int moe_unpermute_combine_mxfp8(const float* o_perm, const float* s, const float* gates,
+                                        const int32_t* row_of_slot, int T, int d, int E, int k, void* y,
+                                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

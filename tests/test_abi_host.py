@@ -36,7 +36,8 @@ def test_every_declared_symbol_is_exported(lib):
     # and the binding covers every compute entry point
     for n in names:
         if n not in ("moe_version", "moe_status_string", "moe_last_cuda_error", "moe_device_status",
-                     "moe_workspace_size", "moe_timing_begin", "moe_timing_end", "moe_timing_name"):
+                     "moe_workspace_size", "moe_timing_begin", "moe_timing_end", "moe_timing_name",
+                     "moe_mxfp8_rows", "moe_mxfp8_scales_bytes"):
             assert n in lib.SIGNATURES, n
 
 

@@ -54,11 +54,16 @@ SIGNATURES = {
     "moe_route_topk_bwd": "pppp" + "iiii" + "ppp" + "pz" + "s",
     "moe_router_balance_loss": "pp" + "iii" + "f" + "ppp" + "pz" + "s",
     "moe_permute_bwd": "ppppp" + "iiii" + "p" + "pz" + "s",
+    "moe_mxfp8_quantize": "p" + "Li" + "pp" + "s",
+    "moe_mxfp8_quantize_gate_up": "pp" + "iii" + "pp" + "s",
+    "moe_permute_mxfp8": "pp" + "iiiii" + "pppppp" + "pp" + "pz" + "s",
+    "moe_grouped_swiglu_mxfp8": "pppppp" + "iiiiii" + "pppppppp" + "pppp" + "pp" + "s",
+    "moe_unpermute_combine_mxfp8": "pppp" + "iiii" + "p" + "s",
     "moe_selftest_group_maps": "",
     "moe_selftest_wait_timeout": "i" + "s",
 }
 
-_CT = {"p": _P, "i": _I, "f": ctypes.c_float, "z": _SZ, "s": _P}
+_CT = {"p": _P, "i": _I, "L": ctypes.c_longlong, "f": ctypes.c_float, "z": _SZ, "s": _P}
 
 for _name, _sig in SIGNATURES.items():
     _f = getattr(_lib, _name)
@@ -75,6 +80,10 @@ _lib.moe_device_status.restype = _I
 _lib.moe_device_status.argtypes = [ctypes.POINTER(_I)]
 _lib.moe_workspace_size.restype = _I
 _lib.moe_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]
+_lib.moe_mxfp8_rows.restype = _I
+_lib.moe_mxfp8_rows.argtypes = [_I, _I, _I, ctypes.POINTER(ctypes.c_longlong)]
+_lib.moe_mxfp8_scales_bytes.restype = _I
+_lib.moe_mxfp8_scales_bytes.argtypes = [ctypes.c_longlong, _I, ctypes.POINTER(_SZ)]
 _lib.moe_timing_begin.restype = _I
 _lib.moe_timing_begin.argtypes = [ctypes.POINTER(_P), _I]
 _lib.moe_timing_end.restype = _I
@@ -245,6 +254,48 @@ def moe_router_balance_loss(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl
 
 def moe_permute_bwd(dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream=None):
     return _call("moe_permute_bwd", dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream)
+
+
+def moe_mxfp8_rows(T, E, k) -> int:
+    v = ctypes.c_longlong(0)
+    rc = _lib.moe_mxfp8_rows(T, E, k, ctypes.byref(v))
+    if rc != MOE_OK:
+        raise MoEError("moe_mxfp8_rows", rc, status_string(rc))
+    return v.value
+
+
+def moe_mxfp8_scales_bytes(rows, cols) -> int:
+    v = _SZ(0)
+    rc = _lib.moe_mxfp8_scales_bytes(rows, cols, ctypes.byref(v))
+    if rc != MOE_OK:
+        raise MoEError("moe_mxfp8_scales_bytes", rc, status_string(rc))
+    return v.value
+
+
+def moe_mxfp8_quantize(src, rows, cols, codes, scales, stream=None):
+    return _call("moe_mxfp8_quantize", src, rows, cols, codes, scales, stream)
+
+
+def moe_mxfp8_quantize_gate_up(W_g, W_u, E, H, d, codes, scales, stream=None):
+    return _call("moe_mxfp8_quantize_gate_up", W_g, W_u, E, H, d, codes, scales, stream)
+
+
+def moe_permute_mxfp8(x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, mx_offsets, row_of_slot,
+                      slot_of_row, x_codes, x_scales, ws, ws_bytes, stream=None):
+    return _call("moe_permute_mxfp8", x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, mx_offsets,
+                 row_of_slot, slot_of_row, x_codes, x_scales, ws, ws_bytes, stream)
+
+
+def moe_grouped_swiglu_mxfp8(x_codes, x_scales, mx_offsets, counts, xs_codes, xs_scales, T, d, E, k, H, Hs,
+                             Wgu_codes, Wgu_scales, Wd_codes, Wd_scales, Wsgu_codes, Wsgu_scales, Wsd_codes,
+                             Wsd_scales, h_codes, h_scales, hs_codes, hs_scales, o_perm, s, stream=None):
+    return _call("moe_grouped_swiglu_mxfp8", x_codes, x_scales, mx_offsets, counts, xs_codes, xs_scales, T, d, E, k,
+                 H, Hs, Wgu_codes, Wgu_scales, Wd_codes, Wd_scales, Wsgu_codes, Wsgu_scales, Wsd_codes, Wsd_scales,
+                 h_codes, h_scales, hs_codes, hs_scales, o_perm, s, stream)
+
+
+def moe_unpermute_combine_mxfp8(o_perm, s, gates, row_of_slot, T, d, E, k, y, stream=None):
+    return _call("moe_unpermute_combine_mxfp8", o_perm, s, gates, row_of_slot, T, d, E, k, y, stream)
 
 
 def moe_selftest_group_maps():

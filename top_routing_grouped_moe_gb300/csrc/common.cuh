@@ -2,6 +2,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "../../include/moe.h"
@@ -54,6 +55,43 @@ __device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo
   }
   hi = pack8(h);
   lo = pack8(l);
+}
+
+// ------------------------------------------------------------ MXFP8
+// (E4M3 elements, one E8M0 scale 2^(floor(log2 max|v|) - 8) per 32 values along
+// K; scales of rows [128 t, 128 t + 128) x blocks [4 q, 4 q + 4) form one
+// 512-byte "tile atom", row 128 t + 32 j + l, block 4 q + b at byte
+// 16 l + 4 j + b)
+// E8M0 exponent of the block scale for the block maximum |v| = amax (fp32):
+// floor(log2 amax) - 8, clamped to [-127, 127]; -127 for amax == 0.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = (int)((b >> 23) & 0xFF);
+  int e;
+  if (ef != 0) {
+    e = ef - 127;
+  } else {  // subnormal: amax = m 2^-149, floor(log2) = (31 - clz(m)) - 149
+    e = (31 - __clz((int)(b & 0x7FFFFF))) - 149;
+  }
+  return min(max(e - 8, -127), 127);
+}
+
+// 2^-se as an fp32 normal (se in [-127, 126]; bf16 blocks give se <= 120)
+__device__ __forceinline__ float mx_inv_scale(int se) { return __uint_as_float((uint32_t)(127 - se) << 23); }
+
+// 4 values -> 4 E4M3 codes (byte i = code of v[i]), each v[i] scaled by
+// inv = 2^-se (exact: a power-of-two scaling; a result below fp32's normal
+// range is far below E4M3's smallest subnormal and rounds to 0 either way)
+__device__ __forceinline__ uint32_t mx_codes4(float v0, float v1, float v2, float v3, float inv) {
+  const float a0 = v0 * inv, a1 = v1 * inv, a2 = v2 * inv, a3 = v3 * inv;
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a2, a3), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__device__ __forceinline__ long long mx_atom_offset(long long row, int block, int nq) {
+  return ((row >> 7) * nq + (block >> 2)) * 512 + 16 * (row & 31) + 4 * ((row & 127) >> 5) + (block & 3);
 }
 
 }  // namespace moe

@@ -110,6 +110,17 @@ struct Problem {
   void* out2;          // rows >= row_split go to out2 (KGROUP; 0 = off)
   int row_split;
   int map_out, map_out2;   // EPI_BF16 (ragged K): TMA-store maps of out / out2, [G][rows][N], 32 x 32 boxes
+  // MXFP8 operands (MX launches): tile-atom scale arrays of A (rows of the A
+  // buffer) and B (per group, sfb_gstride bytes apart), K / 128 atoms per row
+  // tile; `counts` (nullable) ends group g's rows at off[g] + counts[g]
+  // (the offsets then mark padded segments)
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  long long sfb_gstride;
+  int nkq;
+  const int* counts;
+  uint8_t* out_sf;         // SwiGLU (MX): tile-atom scales of the quantized h
+  int out_sf_nq;           // ... H / 128
   void* aux;           // SWIGLU_FWD: au out; SWIGLU_BWD: au in
   long long ld_aux;
   const float* bias;   // EPI_F32 (nullable)
@@ -139,6 +150,7 @@ struct Sched {
   int tile_start[MAX_PROBLEMS + 1];
   int off[MAX_PROBLEMS][MAX_G];
   int tpre[MAX_PROBLEMS][MAX_G];  // MGROUP: exclusive prefix of tiles per group
+  int end[MAX_PROBLEMS][MAX_G];   // MGROUP: first row past group g's rows
 };
 
 // PAIR = 1: one CTA computes a 128 x 256 tile.  PAIR = 2: a cluster of two
@@ -173,17 +185,31 @@ struct SmemTailT {
 // stages for them (it is not what bounds that launch)
 constexpr int AU_CHUNK_BYTES = 2 * 32 * 32 * 4;
 
-template <int MODE, int EPI, int PAIR, int SPLIT>
+// MXFP8 (MX = 1, ragged M, single CTA): a stage holds 128 K values (128 bytes
+// of E4M3 per row: one 128-byte swizzle row) of A (128 rows) and B (128 rows)
+// and one 512-byte scale atom of each; 6 stages.  The scale atoms go to a
+// ring of tensor-memory columns (MX_SF_COL + 8 * stage) between the two
+// 128-column accumulators.
+constexpr int MX_BK = 128;
+constexpr int MX_B_BYTES = 128 * MX_BK;
+constexpr int MX_SF_BYTES = 1024;
+constexpr int MX_STAGES = 6;
+constexpr int MX_N = 128;      // MMA N of the MX launches
+constexpr int MX_SF_COL = 128;  // first tensor-memory column of the scale ring
+
+template <int MODE, int EPI, int PAIR, int SPLIT, int MX = 0>
 struct StageCfg {
   static constexpr int STAGES =
-      MODE == KGROUP ? KgCfg<SPLIT>::STAGES : (EPI == EPI_SWIGLU_BWD ? 4 : PairCfg<PAIR>::STAGES);
-  static constexpr int BYTES = MODE == KGROUP ? KgCfg<SPLIT>::STAGE_BYTES : A_BYTES + PairCfg<PAIR>::B_BYTES;
+      MX ? MX_STAGES
+         : (MODE == KGROUP ? KgCfg<SPLIT>::STAGES : (EPI == EPI_SWIGLU_BWD ? 4 : PairCfg<PAIR>::STAGES));
+  static constexpr int BYTES = MX ? A_BYTES + MX_B_BYTES + MX_SF_BYTES
+                                  : (MODE == KGROUP ? KgCfg<SPLIT>::STAGE_BYTES : A_BYTES + PairCfg<PAIR>::B_BYTES);
   static constexpr int EPI_BYTES = EPI == EPI_SWIGLU_BWD ? 4 * 2 * AU_CHUNK_BYTES : 0;
 };
 
-template <int MODE, int EPI, int PAIR, int SPLIT>
+template <int MODE, int EPI, int PAIR, int SPLIT, int MX = 0>
 constexpr size_t smem_bytes() {
-  using C = StageCfg<MODE, EPI, PAIR, SPLIT>;
+  using C = StageCfg<MODE, EPI, PAIR, SPLIT, MX>;
   return 1024 + C::STAGES * C::BYTES + C::EPI_BYTES + sizeof(SmemTailT<C::STAGES>);
 }
 
@@ -193,7 +219,7 @@ struct TileInfo {
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-template <int MODE, int TILE_M, int KBK>
+template <int MODE, int TILE_M, int KBK, int MBK>
 __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int t) {
   TileInfo ti;
   int p = (P.num_problems > 1 && t >= S.tile_start[1]) ? 1 : 0;
@@ -215,11 +241,12 @@ __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int 
     int m_idx = within / nt, n_idx = within - m_idx * nt;
     ti.g = g;
     ti.m0 = r0 + m_idx * TILE_M;
-    ti.rows_end = r1;
+    ti.rows_end = S.end[p][g];
+    (void)r1;
     ti.n0 = n_idx * pr.n_tile;
     ti.k0 = 0;
     ti.k1 = pr.K;
-    ti.nk = cdiv(pr.K, BK) * pr.nsplit;
+    ti.nk = cdiv(pr.K, MBK) * pr.nsplit;
   } else {
     int mt = cdiv(pr.M, TILE_M);
     int per = mt * nt;
@@ -266,6 +293,14 @@ __device__ void build_schedule(const Params& P, Sched& S) {
       prev = v;
     }
     if (bad) record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
+  }
+  __syncthreads();
+  for (int p = 0; p < P.num_problems; ++p) {
+    const Problem& pr = P.prob[p];
+    for (int g = threadIdx.x; g < pr.G; g += blockDim.x) {
+      const int r0 = S.off[p][g], r1 = S.off[p][g + 1];
+      S.end[p][g] = pr.counts ? r0 + min(max(__ldg(pr.counts + g), 0), r1 - r0) : r1;
+    }
   }
   __syncthreads();
   if (threadIdx.x < 32) {
@@ -387,15 +422,19 @@ __device__ __forceinline__ void load_3d(void* dst, const CUtensorMap* m, uint64_
   else ptx::tma_load_3d_pair(dst, m, bar_leader, c0, c1, c2);
 }
 
-template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT>
+template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT, int MX = 0>
 __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params P) {
   static_assert(!(MODE == KGROUP && PAIR == 2), "ragged-K GEMMs run on single CTAs");
+  static_assert(!MX || (MODE == MGROUP && PAIR == 1 && AMN == 0 && BMN == 0 && SPLIT == SPLIT_NONE &&
+                        (EPI == EPI_SWIGLU_FWD || EPI == EPI_F32)),
+                "MXFP8: ragged-M, single-CTA, K-major operands, SwiGLU or fp32 epilogue");
   static_assert(MODE == MGROUP || (AMN == 1 && BMN == 1), "ragged-K operands are MN-major");
   static_assert(MODE == KGROUP || SPLIT == SPLIT_NONE, "ragged-M split operands use consecutive stages");
   using Cfg = PairCfg<PAIR>;
-  using SC = StageCfg<MODE, EPI, PAIR, SPLIT>;
+  using SC = StageCfg<MODE, EPI, PAIR, SPLIT, MX>;
   constexpr int STAGES = SC::STAGES;
-  constexpr int B_BYTES = Cfg::B_BYTES;
+  constexpr int B_BYTES = MX ? MX_B_BYTES : Cfg::B_BYTES;
+  constexpr int MBK = MX ? MX_BK : BK;  // K per ragged-M stage
   constexpr int TILE_M = Cfg::TILE_M;
   // ragged K: rows per stage and the stage's blocks
   constexpr int KBK = KgCfg<SPLIT>::BKK;
@@ -407,6 +446,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
   // ragged M: A ring then B ring; ragged K: stage s at smem + s * SC::BYTES
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
+  uint8_t* sSF = sB + STAGES * B_BYTES;  // MX: the stages' scale atoms (A at +0, B at +512)
   using Tail = SmemTailT<STAGES>;
   uint8_t* au_buf = smem + STAGES * SC::BYTES;  // SwiGLU backward only
   Tail* tail = reinterpret_cast<Tail*>(au_buf + SC::EPI_BYTES);
@@ -503,7 +543,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           t = tile0 + i * tile_step;
           if (t >= total) break;
         }
-        TileInfo ti = decode<MODE, TILE_M, KBK>(P, S, t);
+        TileInfo ti = decode<MODE, TILE_M, KBK, MBK>(P, S, t);
         // Everything the stage loop needs, read once per tile: a parameter
         // read inside the loop would be repeated after every asm statement
         // (they all clobber memory), which cost as much as the MMAs.
@@ -517,6 +557,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         const CUtensorMap* mAlo = pr.map_a_lo >= 0 ? &P.maps[pr.map_a_lo] : nullptr;
         const CUtensorMap* mBlo = pr.map_b_lo >= 0 ? &P.maps[pr.map_b_lo] : nullptr;
         const int am = ti.m0 + row_half, bn = ti.n0 + row_half;
+        const uint8_t* mx_sfa = pr.sfa;
+        const uint8_t* mx_sfb = pr.sfb + (long long)ti.g * pr.sfb_gstride;
+        const int mx_nkq = pr.nkq;
         int k0 = ti.k0;
         const int g = ti.g, nk = ti.nk;
         if (MODE == KGROUP && pr.gmaps != nullptr && nk > 0) {
@@ -570,6 +613,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
                 for (int j = 0; j < nblk; ++j) ptx::tma_load_2d(lo + j * KG_BLOCK_BYTES, mBlo, fb, bn + 64 * j, k);
               }
             }
+          } else if constexpr (MX) {
+            // E4M3 A and B tiles (128 K values = 128 bytes per row) and the
+            // two scale atoms of this 128-row x 128-K stage.  B rows: the
+            // packed gate/up matrix holds 64 gate and 64 up rows per 64 h
+            // columns, so the tile of h columns [n0, n0 + 64) starts at row 2 n0
+            const int k = kb * MX_BK;
+            const int brow = EPI == EPI_SWIGLU_FWD ? 2 * ti.n0 : ti.n0;
+            uint8_t* sf = sSF + stage * MX_SF_BYTES;
+            ptx::tma_load_2d(sA + stage * A_BYTES, mA, fb, k, am);
+            ptx::tma_load_3d(sB + stage * B_BYTES, mB, fb, k, brow, g);
+            ptx::bulk_load(sf, mx_sfa + ((long long)(am >> 7) * mx_nkq + kb) * 512, 512, fb);
+            ptx::bulk_load(sf + 512, mx_sfb + ((long long)(brow >> 7) * mx_nkq + kb) * 512, 512, fb);
           } else {
             const int part = nsplit == 2 ? (kb & 1) : 0;
             const int k = k0 + (nsplit == 2 ? (kb >> 1) : kb) * BK;
@@ -643,7 +698,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           t = tile0 + it * tile_step;
         }
         if (t >= total) break;
-        TileInfo ti = decode<MODE, TILE_M, KBK>(P, S, t);
+        TileInfo ti = decode<MODE, TILE_M, KBK, MBK>(P, S, t);
         const Problem& pr = P.prob[ti.p];
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
@@ -666,7 +721,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           // sub-step entirely past the end is not issued.
           const bool tail_step = MODE == KGROUP && (kb + 1) * KBK > k_left;
           ptx::tc_fence_after();
-          if (MODE == MGROUP) {
+          if (MODE == MGROUP && MX) {
+            // the stage's scale atoms into this stage's tensor-memory columns,
+            // then four K = 32 block-scaled MMAs (scale byte = K block)
+            const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);
+            const uint32_t b_addr = ptx::smem_u32(sB + stage * B_BYTES);
+            const uint32_t sf_t = tmem_base + MX_SF_COL + stage * 8;
+            const uint32_t sf_s = ptx::smem_u32(sSF + stage * MX_SF_BYTES);
+            ptx::tmem_cp_scales(sf_t, ptx::smem_desc_plain(sf_s, 128, 128));
+            ptx::tmem_cp_scales(sf_t + 4, ptx::smem_desc_plain(sf_s + 512, 128, 128));
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const uint64_t ad = ptx::smem_desc(a_addr + s * 32, 16, 1024);
+              const uint64_t bd = ptx::smem_desc(b_addr + s * 32, 16, 1024);
+              ptx::mma_mxf8(d_tmem, ad, bd, ptx::idesc_mxf8(BM, MX_N, s), sf_t, sf_t + 4, (kb | s) != 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(&tail->empty[stage]);
+          } else if (MODE == MGROUP) {
             const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);
             const uint32_t b_addr = ptx::smem_u32(sB + stage * B_BYTES);
 #pragma unroll
@@ -747,7 +818,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         break;
       }
       if (t >= total) break;
-      TileInfo ti = decode<MODE, TILE_M, KBK>(P, S, t);
+      TileInfo ti = decode<MODE, TILE_M, KBK, MBK>(P, S, t);
       const Problem& pr = P.prob[ti.p];
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
@@ -866,6 +937,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             if (r < nrows && col_ok)
               store4(outp + base + (long long)r * pr.ldo + col,
                      make_float4(v[j].x + b.x, v[j].y + b.y, v[j].z + b.z, v[j].w + b.w));
+          }
+        }
+      } else if (EPI == EPI_SWIGLU_FWD && MX) {
+        // MXFP8: accumulator columns [0,64) = a (the tile's 64 gate rows),
+        // [64,128) = u; h = silu(a) u in fp32, quantized per row in blocks of
+        // 32 h columns (one chunk: the row's 8 lanes reduce the block maximum
+        // by shuffles) into E4M3 codes [rows, H] and the scale tile atoms
+        uint8_t* hc = reinterpret_cast<uint8_t*>(pr.out);
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          float4 va[8], vu[8];
+          tmem_chunk_quad(taddr + c0, tb, lane, va);
+          tmem_chunk_quad(taddr + 64 + c0, tb, lane, vu);
+          const int col = ti.n0 + c0 + cq;
+          const int block = (ti.n0 + c0) >> 5;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + rs;
+            const float4 a = va[j], u = vu[j];
+            const float h0 = a.x * sigmoidf_(a.x) * u.x, h1 = a.y * sigmoidf_(a.y) * u.y;
+            const float h2 = a.z * sigmoidf_(a.z) * u.z, h3 = a.w * sigmoidf_(a.w) * u.w;
+            float amax = fmaxf(fmaxf(fabsf(h0), fabsf(h1)), fmaxf(fabsf(h2), fabsf(h3)));
+            amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 4));
+            const int se = mx_scale_exp(amax);
+            const uint32_t codes = mx_codes4(h0, h1, h2, h3, mx_inv_scale(se));
+            if (r < nrows) {
+              const long long row = row0 + r;
+              *reinterpret_cast<uint32_t*>(hc + row * pr.ldo + col) = codes;
+              if (cq == 0) pr.out_sf[mx_atom_offset(row, block, pr.out_sf_nq)] = (uint8_t)(se + 127);
+            }
           }
         }
       } else if (EPI == EPI_SWIGLU_FWD) {

@@ -95,6 +95,31 @@ inline bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 (one byte per element) maps with 128-byte swizzle, boxes of 128 K
+// bytes (one swizzle row) x 128 rows: 2-D over [rows, K], 3-D over [G][N][K].
+inline bool encode_u8_2d(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  cuuint64_t dims[2] = {K, rows};
+  cuuint64_t strides[1] = {K};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t es[2] = {1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+inline bool encode_u8_3d(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t N, uint64_t G) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  cuuint64_t dims[3] = {K, N, G};
+  cuuint64_t strides[2] = {K, K * N};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D bf16 map for TMA stores of 32 x 32 boxes into [d2][d1][d0] (d0
 // contiguous), 64-byte swizzle (the epilogue's staging layout).
 inline bool encode_store_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2) {
@@ -130,10 +155,10 @@ inline Problem blank_problem() {
 // Launch a persistent grid for `tile_bound` tiles at most: one CTA per SM
 // (PAIR = 1), or clusters of two CTAs sized by the number of clusters that can
 // be resident at once (PAIR = 2).
-template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT = SPLIT_NONE>
+template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT = SPLIT_NONE, int MX = 0>
 cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s, const char* name) {
-  auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR, SPLIT>;
-  constexpr size_t smem = smem_bytes<MODE, EPI, PAIR, SPLIT>();
+  auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR, SPLIT, MX>;
+  constexpr size_t smem = smem_bytes<MODE, EPI, PAIR, SPLIT, MX>();
   static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

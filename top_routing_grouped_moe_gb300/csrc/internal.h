@@ -28,6 +28,29 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
                            int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
                            int32_t* slot_of_row, void* x_perm, void* ws, int* status, cudaStream_t s);
 size_t permute_ws_bytes(int T, int E, int k);
+// histogram + scan of the permutation (the scatter's inputs: per-tile bases
+// and in-tile ranks, in ws); mx_offsets (nullable) receives the offsets of the
+// padded row space of the MXFP8 path (every expert's rows start at a multiple
+// of 128)
+cudaError_t launch_permute_counts(const int32_t* idx, int T, int E, int k, int capacity, int32_t* counts_raw,
+                                  int32_t* counts, int32_t* offsets, int32_t* mx_offsets, void* ws,
+                                  int32_t** tile_base_out, int32_t** inrank_out, int* status, cudaStream_t s);
+
+// ------------------------------------------------------------ MXFP8
+// rows of the padded row space (each expert's rows rounded up to 128): at most
+// T*k + 127*E, rounded up to a whole 128-row tile
+inline long long mx_rows_max(int T, int E, int k) {
+  return ((long long)T * k + 127LL * E + 127) / 128 * 128;
+}
+// bytes of the tile-atom scale array of a [rows, cols] MXFP8 matrix
+size_t mx_scales_bytes(long long rows, int cols);
+cudaError_t launch_mx_quantize(const void* src, long long rows, int cols, void* codes, void* scales, cudaStream_t s);
+cudaError_t launch_mx_quantize_gate_up(const void* W_g, const void* W_u, int E, int H, int d, void* codes,
+                                       void* scales, cudaStream_t s);
+cudaError_t launch_permute_mx(const void* x, const int32_t* idx, int T, int d, int E, int k, int capacity,
+                              int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* mx_offsets,
+                              int32_t* row_of_slot, int32_t* slot_of_row, void* codes, void* scales, void* ws,
+                              int* status, cudaStream_t s);
 // o_perm, s_out fp32; y bf16
 cudaError_t launch_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
                            int T, int d, int k, void* y, int* status, cudaStream_t s);
@@ -141,6 +164,30 @@ cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const v
 // dx_r [T, d] fp32 = (dl_hi + dl_lo) W_r, the router's term of the input gradient
 cudaError_t gemm_router_dx(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, int T, int d, int E,
                            float* dx_r, int* status, cudaStream_t s);
+
+// MXFP8 expert GEMMs (E4M3 operands, tile-atom E8M0 scales).  A: [rows_total,
+// K] codes; rows of group g start at offsets[g] (a multiple of 128, or dense
+// G = 1 over rows_total when offsets is NULL) and number counts[g] (NULL: up to
+// the next offset).  B: [G][Nb][K] codes, Nb = 2N for the packed gate/up
+// weights (64 gate rows, then the 64 up rows of the same h columns), N for
+// down.  Out: h codes [rows, N] + their scale atoms (SwiGLU), or fp32 [rows, N].
+struct MxGemmArgs {
+  const void* a_codes;
+  const uint8_t* a_scales;
+  int rows_total;
+  const int32_t* offsets;
+  const int32_t* counts;
+  int G, K, N;
+  const void* b_codes;
+  const uint8_t* b_scales;
+  void* out;
+  uint8_t* out_scales;
+};
+cudaError_t gemm_mx_swiglu(const MxGemmArgs& routed, const MxGemmArgs* shared, cudaStream_t s);
+cudaError_t gemm_mx_down(const MxGemmArgs& routed, const MxGemmArgs* shared, cudaStream_t s);
+cudaError_t launch_combine_rows(const float* o_perm, const float* s_out, const float* gates,
+                                const int32_t* row_of_slot, int T, int d, int k, long long o_rows, void* y,
+                                int* status, cudaStream_t s);
 
 // split-K factor used for dW_r
 int router_dw_splits(int T, int d, int E);

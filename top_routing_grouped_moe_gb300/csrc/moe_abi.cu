@@ -422,6 +422,102 @@ int moe_router_balance_loss(const float* logits, const int32_t* counts_raw, int 
                                    static_cast<cudaStream_t>(stream)));
 }
 
+int moe_mxfp8_rows(int T, int E, int k, long long* rows) {
+  if (!rows || T < 1 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || k > E || E > kMaxE || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  *rows = mx_rows_max(T, E, k);
+  return MOE_OK;
+}
+
+int moe_mxfp8_scales_bytes(long long rows, int cols, size_t* bytes) {
+  if (!bytes || rows < 1 || cols < 1) return MOE_ERR_INVALID_ARG;
+  if (cols % 128) return MOE_ERR_UNSUPPORTED;
+  *bytes = mx_scales_bytes(rows, cols);
+  return MOE_OK;
+}
+
+int moe_mxfp8_quantize(const void* src, long long rows, int cols, void* codes, void* scales, void* stream) {
+  if (!src || !codes || !scales || rows < 1 || cols < 1) return MOE_ERR_INVALID_ARG;
+  if (cols % 128 || rows * cols >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  if (!al16(src) || !al16(codes) || !al16(scales)) return MOE_ERR_INVALID_ARG;
+  return check(launch_mx_quantize(src, rows, cols, codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_mxfp8_quantize_gate_up(const void* W_g, const void* W_u, int E, int H, int d, void* codes, void* scales,
+                               void* stream) {
+  if (!W_g || !W_u || !codes || !scales || E < 1 || H < 1 || d < 1) return MOE_ERR_INVALID_ARG;
+  if (d % 128 || H % 128) return MOE_ERR_UNSUPPORTED;
+  if (!al16(W_g) || !al16(W_u) || !al16(codes) || !al16(scales)) return MOE_ERR_INVALID_ARG;
+  return check(launch_mx_quantize_gate_up(W_g, W_u, E, H, d, codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_permute_mxfp8(const void* x, const int32_t* topk_idx, int T, int d, int E, int k, int capacity,
+                      int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* mx_offsets,
+                      int32_t* row_of_slot, int32_t* slot_of_row, void* x_codes, void* x_scales, void* ws,
+                      size_t ws_bytes, void* stream) {
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  if (d % 128) return MOE_ERR_UNSUPPORTED;
+  if (!x || !topk_idx || !counts_raw || !counts || !offsets || !mx_offsets || !row_of_slot || !slot_of_row ||
+      !x_codes || !x_scales)
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(x_codes) || !al16(x_scales)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < permute_ws_bytes(T, E, k)) return MOE_ERR_WORKSPACE;
+  return check(launch_permute_mx(x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, mx_offsets,
+                                 row_of_slot, slot_of_row, x_codes, x_scales, ws, device_status_ptr(),
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_swiglu_mxfp8(const void* x_codes, const void* x_scales, const int32_t* mx_offsets,
+                             const int32_t* counts, const void* xs_codes, const void* xs_scales, int T, int d, int E,
+                             int k, int H, int Hs, const void* Wgu_codes, const void* Wgu_scales,
+                             const void* Wd_codes, const void* Wd_scales, const void* Wsgu_codes,
+                             const void* Wsgu_scales, const void* Wsd_codes, const void* Wsd_scales, void* h_codes,
+                             void* h_scales, void* hs_codes, void* hs_scales, float* o_perm, float* s_out,
+                             void* stream) {
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  rc = check_hidden(H, Hs);
+  if (rc) return rc;
+  if (d % 128) return MOE_ERR_UNSUPPORTED;
+  const void* req[] = {x_codes, x_scales, mx_offsets, counts, Wgu_codes, Wgu_scales, Wd_codes, Wd_scales,
+                       h_codes, h_scales, o_perm};
+  for (const void* p : req)
+    if (!p) return MOE_ERR_INVALID_ARG;
+  const void* req16[] = {x_codes, x_scales, Wgu_codes, Wgu_scales, Wd_codes, Wd_scales, h_codes, h_scales, o_perm};
+  for (const void* p : req16)
+    if (!al16(p)) return MOE_ERR_INVALID_ARG;
+  if (Hs > 0) {
+    const void* req_s[] = {xs_codes, xs_scales, Wsgu_codes, Wsgu_scales, Wsd_codes, Wsd_scales, hs_codes,
+                           hs_scales, s_out};
+    for (const void* p : req_s)
+      if (!p || !al16(p)) return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int rows = static_cast<int>(mx_rows_max(T, E, k));
+  auto U = [](const void* p) { return static_cast<const uint8_t*>(p); };
+  MxGemmArgs r1{x_codes, U(x_scales), rows, mx_offsets, counts, E, d, H, Wgu_codes, U(Wgu_scales), h_codes,
+                static_cast<uint8_t*>(h_scales)};
+  MxGemmArgs s1{xs_codes, U(xs_scales), T, nullptr, nullptr, 1, d, Hs, Wsgu_codes, U(Wsgu_scales), hs_codes,
+                static_cast<uint8_t*>(hs_scales)};
+  cudaError_t e = gemm_mx_swiglu(r1, Hs > 0 ? &s1 : nullptr, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  MxGemmArgs r2{h_codes, U(h_scales), rows, mx_offsets, counts, E, H, d, Wd_codes, U(Wd_scales), o_perm, nullptr};
+  MxGemmArgs s2{hs_codes, U(hs_scales), T, nullptr, nullptr, 1, Hs, d, Wsd_codes, U(Wsd_scales), s_out, nullptr};
+  return check(gemm_mx_down(r2, Hs > 0 ? &s2 : nullptr, st));
+}
+
+int moe_unpermute_combine_mxfp8(const float* o_perm, const float* s_out, const float* gates,
+                                const int32_t* row_of_slot, int T, int d, int E, int k, void* y, void* stream) {
+  if (T < 1 || d < 1 || k < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || k > E || E > kMaxE || (d % 64) != 0 || (long long)T * k >= (1LL << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (!o_perm || !gates || !row_of_slot || !y) return MOE_ERR_INVALID_ARG;
+  if (!al16(o_perm) || !al16(y) || (s_out && !al16(s_out))) return MOE_ERR_INVALID_ARG;
+  return check(launch_combine_rows(o_perm, s_out, gates, row_of_slot, T, d, k, mx_rows_max(T, E, k), y,
+                                   device_status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
 int moe_permute_bwd(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, const float* dlogits,
                     const void* W_r, int T, int d, int E, int k, void* dx, void* ws, size_t ws_bytes, void* stream) {
   if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;

@@ -178,6 +178,14 @@ __device__ __forceinline__ void bulk_wait_read() {
 // Wait until every bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Bulk (non-tensor) copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global to this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Generic-proxy writes to shared memory -> visible to the async proxy
 // (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -302,6 +310,49 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   d |= 1ull << 46;  // descriptor version (tcgen05)
   d |= 2ull << 61;  // swizzle: 128B
   return d;
+}
+
+// Shared-memory descriptor without swizzle (8-row x 16-byte core matrices,
+// SBO bytes between consecutive 8-row groups): the source of tcgen05.cp.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // descriptor version (tcgen05); layout bits 61-63 = 0: no swizzle
+  return d;
+}
+
+// Block scales into tensor memory: a 32-row x 16-byte matrix (one MXFP8 tile
+// atom) copied to 4 columns of all four 32-lane quadrants.
+__device__ __forceinline__ void tmem_cp_scales(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sfa)(B * 2^sfb): kind::mxf8f6f4 with block scales (E4M3
+// operands, one E8M0 scale per 32 K values, read from tensor memory at
+// sfa_tmem / sfb_tmem; the instruction descriptor selects the byte, i.e. the
+// 32-value block within each 4-block atom column).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A and B (K-major), fp32
+// D, UE8M0 scales; sf_id picks the scale byte of both operands.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4)         // B scale byte
+         | (0u << 7)                                 // A format: E4M3
+         | (0u << 10)                                // B format: E4M3
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (1u << 23)                                // scale format: UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)
+         | (static_cast<uint32_t>(sf_id) << 29);     // A scale byte
 }
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.

@@ -138,10 +138,13 @@ __global__ void perm_tile_hist_kernel(const int32_t* __restrict__ idx, int T, in
 }
 
 // (2) one block: per expert, exclusive scan of the tile counts over tiles
-// (tile_base), totals (counts_raw), capacity clamp (counts) and offsets.
+// (tile_base), totals (counts_raw), capacity clamp (counts) and offsets; with
+// mx_offsets, also the offsets of the padded row space in which every
+// expert's rows start at a multiple of 128.
 __global__ void perm_scan_kernel(const int32_t* __restrict__ tile_counts, int ntile, int E, int capacity,
                                  int32_t* __restrict__ tile_base, int32_t* __restrict__ counts_raw,
-                                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+                                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                 int32_t* __restrict__ mx_offsets) {
   __shared__ int seg[1024];
   __shared__ int cnt[kMaxE];
   const int P = blockDim.x / E;  // segments of tiles per expert
@@ -172,28 +175,32 @@ __global__ void perm_scan_kernel(const int32_t* __restrict__ tile_counts, int nt
     }
   }
   __syncthreads();
-  if (tid < 32) {
-    // exclusive scan of cnt[0..E) by one warp
+  // exclusive scan of cnt[0..E) (warp 0) and, with mx_offsets, of the counts
+  // rounded up to 128 (warp 1)
+  const int w = tid >> 5, lane = tid & 31;
+  if (w == 0 || (w == 1 && mx_offsets)) {
+    int32_t* out = w == 0 ? offsets : mx_offsets;
+    const int round = w == 0 ? 1 : 128;
     int per = (E + 31) / 32;
     int loc = 0;
     for (int j = 0; j < per; ++j) {
-      int i = tid * per + j;
-      if (i < E) loc += cnt[i];
+      int i = lane * per + j;
+      if (i < E) loc += (cnt[i] + round - 1) / round * round;
     }
     int incl = loc;
     for (int s = 1; s < 32; s <<= 1) {
       int v = __shfl_up_sync(0xffffffffu, incl, s);
-      if (tid >= s) incl += v;
+      if (lane >= s) incl += v;
     }
     int run = incl - loc;
     for (int j = 0; j < per; ++j) {
-      int i = tid * per + j;
+      int i = lane * per + j;
       if (i < E) {
-        offsets[i] = run;
-        run += cnt[i];
+        out[i] = run;
+        run += (cnt[i] + round - 1) / round * round;
       }
     }
-    if (tid == 31) offsets[E] = incl;
+    if (lane == 31) out[E] = incl;
   }
 }
 
@@ -601,9 +608,9 @@ size_t permute_ws_bytes(int T, int E, int k) {
   return 2 * align256(ntile * E * sizeof(int32_t)) + align256((size_t)T * k * sizeof(int32_t));
 }
 
-cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int E, int k, int capacity,
-                           int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
-                           int32_t* slot_of_row, void* x_perm, void* ws, int* status, cudaStream_t s) {
+cudaError_t launch_permute_counts(const int32_t* idx, int T, int E, int k, int capacity, int32_t* counts_raw,
+                                  int32_t* counts, int32_t* offsets, int32_t* mx_offsets, void* ws,
+                                  int32_t** tile_base_out, int32_t** inrank_out, int* status, cudaStream_t s) {
   const int ntile = (T + kRouteTile - 1) / kRouteTile;
   char* w = static_cast<char*>(ws);
   int32_t* tile_counts = reinterpret_cast<int32_t*>(w);
@@ -614,8 +621,20 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   timing_mark(s, "perm_scan");
-  perm_scan_kernel<<<1, 1024, 0, s>>>(tile_counts, ntile, E, capacity, tile_base, counts_raw, counts, offsets);
-  e = cudaGetLastError();
+  perm_scan_kernel<<<1, 1024, 0, s>>>(tile_counts, ntile, E, capacity, tile_base, counts_raw, counts, offsets,
+                                      mx_offsets);
+  *tile_base_out = tile_base;
+  *inrank_out = inrank;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int E, int k, int capacity,
+                           int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
+                           int32_t* slot_of_row, void* x_perm, void* ws, int* status, cudaStream_t s) {
+  int32_t* tile_base = nullptr;
+  int32_t* inrank = nullptr;
+  cudaError_t e = launch_permute_counts(idx, T, E, k, capacity, counts_raw, counts, offsets, nullptr, ws,
+                                        &tile_base, &inrank, status, s);
   if (e != cudaSuccess) return e;
   timing_mark(s, "perm_scatter");
   perm_scatter_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
@@ -624,13 +643,19 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
-                           int T, int d, int k, void* y, int* status, cudaStream_t s) {
+cudaError_t launch_combine_rows(const float* o_perm, const float* s_out, const float* gates,
+                                const int32_t* row_of_slot, int T, int d, int k, long long o_rows, void* y,
+                                int* status, cudaStream_t s) {
   timing_mark(s, "combine");
   combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
       reinterpret_cast<const float4*>(o_perm), reinterpret_cast<const float4*>(s_out), gates, row_of_slot, T, d, k,
-      (long long)T * k, static_cast<uint4*>(y), status);
+      o_rows, static_cast<uint4*>(y), status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
+                           int T, int d, int k, void* y, int* status, cudaStream_t s) {
+  return launch_combine_rows(o_perm, s_out, gates, row_of_slot, T, d, k, (long long)T * k, y, status, s);
 }
 
 cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
