@@ -113,6 +113,11 @@ def kernel_work(w, R):
         "gather_rows": (0.0, T * d * 2 + R * d * 2 + T * k * 4),
         "unpermute_reduce": (0.0, R * d * 2 + T * d * 2 * sh + T * d * 2 + T * k * 4),
         "topk_gating": (0.0, T * E * 4 + T * k * 8),
+        # MXFP8 forward: E4M3 operands (1 byte) with one scale byte per 32
+        "gemm_mx_gate_up_swiglu": (gu, (R * d + T * d * sh) * 33 // 32 + wgu // 2 * 33 // 32
+                                   + hid * 33 // 32),
+        "gemm_mx_down": (dn, hid * 33 // 32 + wdn // 2 * 33 // 32 + rows * d * 2),
+        "perm_scatter_mx": (0.0, T * d * 2 + R * d * 33 // 32 + T * k * 12 + R * 4),
     }
 
 
@@ -470,6 +475,71 @@ def main_ours(args):
         layer.x_perm, layer.offsets, dev["x"], T, d, E, k, H, Hs, dev["W_g"], dev["W_u"],
         dev.get("Ws_g"), dev.get("Ws_u"), layer.au, layer.au_s))
 
+    # ---- the MXFP8 forward (block-scaled E4M3 expert GEMMs): routing, the MX
+    # permutation, the MX expert MLP and the combine, as a graph replay; the
+    # weights and the shared expert's input are quantized once, before
+    mx_fwd = None
+    if d % 128 == 0 and Hs > 0:
+        u8 = lambda n: torch.empty(n, dtype=torch.uint8, device="cuda")  # noqa: E731
+        i32 = lambda n: torch.empty(n, dtype=torch.int32, device="cuda")  # noqa: E731
+        mrows = B.moe_mxfp8_rows(T, E, k)
+        sb = B.moe_mxfp8_scales_bytes
+        mxb = {"off": i32(E + 1), "row": i32(T * k), "sor": i32(mrows), "cr": i32(E), "c": i32(E), "o0": i32(E + 1),
+               "xc": u8(mrows * d), "xs": u8(sb(mrows, d)), "hc": u8(mrows * H), "hs": u8(sb(mrows, H)),
+               "gu_c": u8(E * 2 * H * d), "gu_s": u8(sb(E * 2 * H, d)), "d_c": u8(E * d * H), "d_s": u8(sb(E * d, H)),
+               "sgu_c": u8(2 * Hs * d), "sgu_s": u8(sb(2 * Hs, d)), "sd_c": u8(d * Hs), "sd_s": u8(sb(d, Hs)),
+               "xsc": u8(T * d), "xss": u8(sb(T, d)), "hsc": u8(T * Hs), "hss": u8(sb(T, Hs)),
+               "o": torch.empty(mrows, d, dtype=torch.float32, device="cuda"),
+               "s": torch.empty(T, d, dtype=torch.float32, device="cuda"),
+               "y": torch.empty(T, d, dtype=torch.bfloat16, device="cuda")}
+        B.moe_mxfp8_quantize_gate_up(dev["W_g"], dev["W_u"], E, H, d, mxb["gu_c"], mxb["gu_s"])
+        B.moe_mxfp8_quantize(dev["W_d"], E * d, H, mxb["d_c"], mxb["d_s"])
+        B.moe_mxfp8_quantize_gate_up(dev["Ws_g"], dev["Ws_u"], 1, Hs, d, mxb["sgu_c"], mxb["sgu_s"])
+        B.moe_mxfp8_quantize(dev["Ws_d"], d, Hs, mxb["sd_c"], mxb["sd_s"])
+
+        def mx_forward(stream):
+            x = dev["x"]
+            B.moe_route_topk(x, dev.get("W_r"), dev.get("bias"), dev.get("logits_in"), T, d, E, k,
+                             L.logits if learned else None, L.idx, L.gates, L.ws, L.ws_bytes, stream)
+            B.moe_permute_mxfp8(x, L.idx, T, d, E, k, L.capacity, mxb["cr"], mxb["c"], mxb["o0"], mxb["off"],
+                                mxb["row"], mxb["sor"], mxb["xc"], mxb["xs"], L.ws, L.ws_bytes, stream)
+            B.moe_mxfp8_quantize(x, T, d, mxb["xsc"], mxb["xss"], stream)
+            B.moe_grouped_swiglu_mxfp8(mxb["xc"], mxb["xs"], mxb["off"], mxb["c"], mxb["xsc"], mxb["xss"], T, d, E,
+                                       k, H, Hs, mxb["gu_c"], mxb["gu_s"], mxb["d_c"], mxb["d_s"], mxb["sgu_c"],
+                                       mxb["sgu_s"], mxb["sd_c"], mxb["sd_s"], mxb["hc"], mxb["hs"], mxb["hsc"],
+                                       mxb["hss"], mxb["o"], mxb["s"], stream)
+            B.moe_unpermute_combine_mxfp8(mxb["o"], mxb["s"], L.gates, mxb["row"], T, d, E, k, mxb["y"], stream)
+
+        for _ in range(3):
+            flush.fill_(1)
+            mx_forward(main_stream)
+        torch.cuda.synchronize()
+        st = B.moe_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} in the MXFP8 forward: {B.status_string(st)}")
+        mx_kernels = {}
+        for i in range(args.steps):
+            flush.fill_(1)
+            with B.LaunchTimer(capacity=64, stream=main_stream) as tm:
+                mx_forward(main_stream)
+            torch.cuda.synchronize()
+            for name, ms in tm.launches():
+                mx_kernels.setdefault(name, []).append(ms)
+        gstream.wait_stream(main_stream)
+        gmx = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gmx, stream=gstream):
+            mx_forward(gstream)
+        main_stream.wait_stream(gstream)
+        for _ in range(3):
+            flush.fill_(1)
+            gmx.replay()
+        mx_ms = replay_ms(gmx)
+        mx_fwd = {"tokens_per_s": tokens_per_s(T, args.steps, world, mx_ms), "ms_per_step": mx_ms / args.steps,
+                  "kernels": {n: round(statistics.mean(v) * len(v) / args.steps, 4) for n, v in mx_kernels.items()},
+                  "note": "forward with MXFP8 (E4M3, E8M0 per 32) expert and shared-expert GEMMs on the tensor "
+                          "cores; routing, x quantized inside the permutation, combine; weights quantized once, "
+                          "outside the timed region; graph replay, L2 flushed before each"}
+
     # ---- rooflines: measured burst peaks (kernels timed inside a step of a
     # few milliseconds)
     peaks = {}
@@ -497,6 +567,14 @@ def main_ours(args):
                  "peak_source": f"{peak_src} burst ({'bf16 cuBLAS' if roof['bound'] == 'tensor' else 'copy'})"})
     ffl, bfl = gemm_flops(w, R)
     rec_work = work["gemm_gate_up_recompute"]
+    if mx_fwd is not None:
+        fp8_peak = 2.0 * tensor_peak  # the fp8 dense tensor rate is twice bf16's (nominal ratio)
+        mx_fwd["rooflines"] = {}
+        for name in ("gemm_mx_gate_up_swiglu", "gemm_mx_down", "perm_scatter_mx"):
+            if name in mx_fwd["kernels"]:
+                mx_fwd["rooflines"][name] = dict(kernel_roofline(work[name], mx_fwd["kernels"][name], fp8_peak,
+                                                                 hbm_peak), ms=mx_fwd["kernels"][name])
+        mx_fwd["fp8_peak_source"] = f"{peak_src} bf16 burst x 2 (nominal fp8 / bf16 ratio)"
 
     # ---- e2e through the public layer API with host buffers
     e2e = None
@@ -554,6 +632,7 @@ def main_ours(args):
                                  "captured once in a CUDA graph and replayed; kernels: every launch of eager "
                                  "steps, timed by events the library records before each launch"},
             "fwd_tokens_per_s": fwd_value,
+            "mxfp8_forward": mx_fwd,
             "fwd_ms_per_step": fwd_ms / args.steps,
             "eager": {"value": tokens_per_s(T, args.steps, world, eager_total), "ms_per_step": step_eager},
             "gemm_tflops_fwd_bwd": (ffl + bfl) / (graph_ms / args.steps / 1000.0) / 1e12,
