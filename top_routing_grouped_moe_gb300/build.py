@@ -64,10 +64,16 @@ def _kernel_sources(kernel: str):
     compiled and launched from."""
     if kernel.startswith("gemm_router"):
         files = _GEMM_COMMON + ["gemm_router.cu"]
+    elif kernel.startswith("gemm_mx"):
+        files = _GEMM_COMMON + ["gemm_mx.cu"]
     elif kernel.startswith(("gemm_gate_up", "gemm_down")):
         files = _GEMM_COMMON + ["gemm_fwd.cu"]
     elif kernel.startswith(("gemm_dgrad", "gemm_wgrad")):
         files = _GEMM_COMMON + ["gemm_bwd.cu", "group_maps.cu"]
+    elif kernel == "group_maps":
+        files = ["group_maps.cu", "gemm_host.cuh", "gemm.cuh", "ptx.cuh", "common.cuh", "internal.h"]
+    elif kernel.startswith("mx_") or kernel.endswith("_mx"):
+        files = ["mxfp8.cu", "route.cu", "common.cuh", "internal.h"]
     else:
         files = ["route.cu", "common.cuh", "internal.h"]
     return [os.path.join(CSRC, f) for f in files]
