@@ -91,6 +91,9 @@ struct Problem {
   int extent;          // rows (MGROUP) or K (KGROUP) covered when offsets == NULL; also an upper clamp
   int M, N, K;         // MGROUP uses N, K (M per group); KGROUP uses M, N (K per group)
   int mma_n;           // instruction N (multiple of 16, <= 256)
+  int half_ok;         // CTA pair, ragged M: a group's last tile with <= 128 rows
+                       // runs as an M = 128 pair MMA (n_tile == mma_n == 256, or
+                       // the SwiGLU forward's interleaved gate/up tile)
   int n_tile;          // output columns per tile (256; 128 h columns for EPI_SWIGLU_FWD)
   int map_a, map_b, map_b2;  // tensor-map indices; map_b2 = second B map or -1
   int ksplit;          // MN-major B: k >= ksplit reads map_b2 at k - ksplit (0 = off)
@@ -215,6 +218,12 @@ constexpr size_t smem_bytes() {
 
 struct TileInfo {
   int p, g, m0, n0, rows_end, k0, k1, nk;
+  // CTA pair, last tile of a group with at most 128 rows left: an M = 128
+  // pair MMA (64 rows from each CTA) at half the MMA work of a 256-row tile.
+  // Its accumulator is folded over the lanes: in each CTA, TMEM lanes 0-63
+  // hold the CTA's 64 rows for accumulator columns [0, N/2) and lanes 64-127
+  // the same rows for columns [N/2, N), both at TMEM columns [0, N/2).
+  bool half;
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -247,6 +256,7 @@ __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int 
     ti.k0 = 0;
     ti.k1 = pr.K;
     ti.nk = cdiv(pr.K, MBK) * pr.nsplit;
+    ti.half = TILE_M == 2 * BM && pr.half_ok && ti.rows_end - ti.m0 <= BM;
   } else {
     int mt = cdiv(pr.M, TILE_M);
     int per = mt * nt;
@@ -260,6 +270,7 @@ __device__ __forceinline__ TileInfo decode(const Params& P, const Sched& S, int 
     ti.k0 = S.off[p][g];
     ti.k1 = S.off[p][g + 1];
     ti.nk = cdiv(ti.k1 - ti.k0, KBK);
+    ti.half = false;
   }
   return ti;
 }
@@ -556,7 +567,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         const CUtensorMap* mB2 = &P.maps[pr.map_b2 >= 0 ? pr.map_b2 : pr.map_b];
         const CUtensorMap* mAlo = pr.map_a_lo >= 0 ? &P.maps[pr.map_a_lo] : nullptr;
         const CUtensorMap* mBlo = pr.map_b_lo >= 0 ? &P.maps[pr.map_b_lo] : nullptr;
-        const int am = ti.m0 + row_half, bn = ti.n0 + row_half;
+        // a half tile takes 64 rows from each CTA: the peer's start 64 rows on
+        const int am = ti.m0 + (ti.half ? rank * (BM / 2) : row_half), bn = ti.n0 + row_half;
         const uint8_t* mx_sfa = pr.sfa;
         const uint8_t* mx_sfb = pr.sfb + (long long)ti.g * pr.sfb_gstride;
         const int mx_nkq = pr.nkq;
@@ -638,13 +650,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
               load_2d<PAIR>(a_dst + MN_BLOCK_BYTES, mAk, fb, fbl, am + 64, k);
             }
             if (EPI == EPI_SWIGLU_FWD) {
-              // B tile = [128 rows of W_g ; 128 rows of W_u]; with a CTA pair
-              // each CTA holds one of the two halves
-              if (PAIR == 1) {
-                load_3d<PAIR>(b_dst, mB, fb, fbl, k, ti.n0, g);
-                load_3d<PAIR>(b_dst + (B_BYTES / 2), mB2, fb, fbl, k, ti.n0, g);
-              } else {
-                load_3d<PAIR>(b_dst, rank == 0 ? mB : mB2, fb, fbl, k, ti.n0, g);
+              // B tile = 128 h columns as two 64-column slices, each [64 rows
+              // of W_g ; 64 rows of W_u] (accumulator columns: a | u | a | u,
+              // 64 each); with a CTA pair each CTA holds one slice, so that a
+              // and u of an h column stay in the same lanes of a folded
+              // (half-tile) accumulator too
+#pragma unroll
+              for (int j = 0; j < 2 / PAIR; ++j) {
+                const int slice = PAIR == 1 ? j : rank;
+                uint8_t* dst = b_dst + j * (2 * MN_BLOCK_BYTES);
+                load_3d<PAIR>(dst, mB, fb, fbl, k, ti.n0 + 64 * slice, g);
+                load_3d<PAIR>(dst + MN_BLOCK_BYTES, mB2, fb, fbl, k, ti.n0 + 64 * slice, g);
               }
             } else if (BMN == 0) {
               load_3d<PAIR>(b_dst, mB, fb, fbl, k, bn, g);
@@ -709,7 +725,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         // per-tile values in registers (see the producer)
-        const uint32_t idesc = ptx::idesc_bf16(TILE_M, pr.mma_n, AMN, BMN);
+        const uint32_t idesc = ptx::idesc_bf16(ti.half ? BM : TILE_M, pr.mma_n, AMN, BMN);
         const int nk = ti.nk, k_left = ti.k1 - ti.k0;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait_bounded(&tail->full[stage], phase, abort_flag, kWaitLimitNs)) {
@@ -822,12 +838,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       const Problem& pr = P.prob[ti.p];
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      const int m_cta = ti.m0 + row_half;  // first row (KGROUP: first M index) of this CTA
-      const int row0 = m_cta + q * 32;
+      // first row (KGROUP: first M index) of this CTA.  A half tile's
+      // accumulator is folded: warps 0-1 take the CTA's 64 rows for the
+      // accumulator columns [0, N/2), warps 2-3 the same rows for [N/2, N),
+      // which sit at TMEM columns [0, N/2) of lanes 64-127.
+      const int m_cta = ti.m0 + (ti.half ? rank * (BM / 2) : row_half);
+      const int ch = ti.half ? (q >> 1) : 0;
+      const int row0 = m_cta + (ti.half ? (q & 1) : q) * 32;
+      const int col_shift = ch * (pr.mma_n / 2);  // accumulator column at this warp's TMEM column 0
       // SwiGLU backward: chunk c of a | u (columns n0 + 32c of a and of u)
       const CUtensorMap* m_au = EPI == EPI_SWIGLU_BWD ? &P.maps[pr.map_aux] : nullptr;
       const int au_H = pr.H;
-      const int au_chunks = EPI == EPI_SWIGLU_BWD ? min(pr.n_tile, pr.N - ti.n0) / 32 : 0;
+      // this warp's chunks [au_c0, au_c1) (a half tile's warp: its half of them)
+      const int au_all = EPI == EPI_SWIGLU_BWD ? min(pr.n_tile, pr.N - ti.n0) / 32 : 0;
+      const int au_c0 = ti.half ? min(au_all, col_shift / 32) : 0;
+      const int au_c1 = ti.half ? min(au_all, au_c0 + pr.mma_n / 64) : au_all;
       auto au_issue = [&](int c) {
         const int buf = au_next & 1;
         if (lane == 0) {
@@ -841,7 +866,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       };
       if (EPI == EPI_SWIGLU_BWD) {
         // the first two chunks load while the main loop still runs
-        for (int c = 0; c < 2 && c < au_chunks; ++c) au_issue(c);
+        for (int c = au_c0; c < au_c0 + 2 && c < au_c1; ++c) au_issue(c);
       }
       if (!ptx::mbar_wait_cluster_bounded(&tail->tmem_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
         *abort_flag = 1;
@@ -922,10 +947,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           outp = reinterpret_cast<OutT<EPI>*>(pr.out);
           base = (MODE == KGROUP ? ti.g * pr.gstride : 0) + (long long)row0 * pr.ldo;
         }
-        for (int c0 = 0; c0 < pr.n_tile; c0 += 32) {
+        const int c_end = ti.half ? col_shift + pr.mma_n / 2 : pr.n_tile;
+        for (int c0 = col_shift; c0 < c_end; c0 += 32) {
           if (ti.n0 + c0 >= pr.N) break;
           float4 v[8];
-          if (has_acc) tmem_chunk_quad(taddr + c0, tb, lane, v);
+          if (has_acc) tmem_chunk_quad(taddr + c0 - col_shift, tb, lane, v);
           else zero_quad(v);
           const int col = ti.n0 + c0 + cq;
           const bool col_ok = col < pr.N;  // N is a multiple of 4
@@ -971,17 +997,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           }
         }
       } else if (EPI == EPI_SWIGLU_FWD) {
-        // accumulator columns [0,128) = a (gate), [128,256) = u (up); h goes
-        // out in bf16 (down-projection input; not stored when `out` is NULL,
-        // the recompute of a and u for the backward), a and u in fp32
+        // accumulator columns a | u | a | u, 64 each: h columns [n0, n0+64)
+        // then [n0+64, n0+128) (a half tile's warp: one of the two slices).
+        // h goes out in bf16 (down-projection input; not stored when `out` is
+        // NULL, the recompute of a and u for the backward), a and u in fp32
         __nv_bfloat16* hp = pr.out ? reinterpret_cast<__nv_bfloat16*>(pr.out) + (long long)row0 * pr.ldo + ti.n0
                                    : nullptr;
         float* ap = pr.aux ? reinterpret_cast<float*>(pr.aux) + (long long)row0 * pr.ld_aux + ti.n0 : nullptr;
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        const int cc0 = ti.half ? 2 * ch : 0, cc1 = ti.half ? 2 * ch + 2 : 4;
+        for (int cc = cc0; cc < cc1; ++cc) {
+          // 32 h columns [32 cc, 32 cc + 32) of the tile: a at accumulator
+          // column la, u at la + 64
+          const int la = 128 * (cc >> 1) + 32 * (cc & 1);
           float4 va[8], vu[8];
-          tmem_chunk_quad(taddr + c0, tb, lane, va);
-          tmem_chunk_quad(taddr + 128 + c0, tb, lane, vu);
-          const int c = c0 + cq;
+          tmem_chunk_quad(taddr + la - col_shift, tb, lane, va);
+          tmem_chunk_quad(taddr + la + 64 - col_shift, tb, lane, vu);
+          const int c = 32 * cc + cq;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int r = 4 * j + rs;
@@ -1029,7 +1060,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         __nv_bfloat16* ghh = reinterpret_cast<__nv_bfloat16*>(pr.gh_hi) + rh;
         __nv_bfloat16* ghl = reinterpret_cast<__nv_bfloat16*>(pr.gh_lo) + rh;
         bool au_ok = true;
-        for (int c = 0; c < au_chunks; ++c) {
+        for (int c = au_c0; c < au_c1; ++c) {
           const int buf = au_done & 1;
           if (!ptx::mbar_wait_bounded(&tail->au_full[q][buf], (au_done >> 1) & 1, abort_flag, kWaitLimitNs)) {
             au_ok = false;
@@ -1048,9 +1079,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           // the buffer is read: chunk c + 2 may overwrite it
           ptx::fence_proxy_async_smem();
           __syncwarp();
-          if (c + 2 < au_chunks) au_issue(c + 2);
+          if (c + 2 < au_c1) au_issue(c + 2);
           float4 vd[8];
-          tmem_chunk_quad(taddr + 32 * c, tb, lane, vd);
+          tmem_chunk_quad(taddr + 32 * c - col_shift, tb, lane, vd);
           const int col = 32 * c + cq;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -1084,7 +1115,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           break;
         }
         if (pr.dgp) {
-          // sum each row's partials over its eight lanes
+          // sum each row's partials over its eight lanes; two slots per
+          // column tile, one per accumulator-column half (a full tile puts
+          // its whole sum in the first and 0 in the second)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             float v = part[j];
@@ -1092,7 +1125,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             v += __shfl_xor_sync(FULL, v, 2);
             v += __shfl_xor_sync(FULL, v, 4);
             const int r = 4 * j + rs;
-            if ((lane & 7) == 0 && r < nrows) pr.dgp[(long long)(row0 + r) * pr.ld_dgp + ti.n0 / pr.n_tile] = v;
+            if ((lane & 7) == 0 && r < nrows) {
+              float* slot = pr.dgp + (long long)(row0 + r) * pr.ld_dgp + 2 * (ti.n0 / pr.n_tile);
+              if (ti.half) {
+                slot[ch] = v;
+              } else {
+                slot[0] = v;
+                slot[1] = 0.0f;
+              }
+            }
           }
         }
       }

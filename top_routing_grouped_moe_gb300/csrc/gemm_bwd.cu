@@ -27,6 +27,7 @@ bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
   pr.K = a.d;
   pr.mma_n = 256;
   pr.n_tile = 256;
+  pr.half_ok = 1;
   pr.map_a = ia;
   pr.map_b = ib;
   pr.tx_bytes = A_BYTES + PairCfg<kPair>::B_BYTES;
@@ -42,7 +43,7 @@ bool fill_dgrad_down(Params& P, Problem& pr, const DgradDownArgs& a) {
   pr.slot_of_row = a.slot_of_row;
   pr.gate_slots = a.gate_slots;
   pr.dgp = a.dgp;
-  pr.ld_dgp = cdiv_h(a.H, 256);
+  pr.ld_dgp = dgp_slots(a.H);
   // a | u come into shared memory by TMA, one 32-row x 32-column box each
   pr.map_aux = new_map(P);
   if (pr.map_aux < 0) return false;
@@ -72,6 +73,7 @@ bool fill_dgrad_gu(Params& P, Problem& pr, const DgradGuArgs& a) {
   pr.K = 2 * a.H;
   pr.mma_n = 256;
   pr.n_tile = 256;
+  pr.half_ok = 1;
   pr.map_a = ia;
   pr.map_b = ig;
   pr.map_b2 = iu;

@@ -12,8 +12,9 @@ bool fill_swiglu_fwd(Params& P, Problem& pr, const SwigluFwdArgs& a) {
   const int ia = new_map(P), ig = new_map(P), iu = new_map(P);
   if (ia < 0 || ig < 0 || iu < 0) return false;
   if (!encode_2d(&P.maps[ia], a.a, a.d, a.rows_total, (uint64_t)a.d * 2, 64, BM)) return false;
-  if (!encode_3d(&P.maps[ig], a.Wg, a.d, a.H, a.G, 64, 128)) return false;
-  if (!encode_3d(&P.maps[iu], a.Wu, a.d, a.H, a.G, 64, 128)) return false;
+  // 64-row boxes: each 64-column h slice takes 64 rows of W_g and 64 of W_u
+  if (!encode_3d(&P.maps[ig], a.Wg, a.d, a.H, a.G, 64, 64)) return false;
+  if (!encode_3d(&P.maps[iu], a.Wu, a.d, a.H, a.G, 64, 64)) return false;
   pr = blank_problem();
   pr.offsets = a.offsets;
   pr.G = a.G;
@@ -22,6 +23,7 @@ bool fill_swiglu_fwd(Params& P, Problem& pr, const SwigluFwdArgs& a) {
   pr.K = a.d;
   pr.mma_n = 256;
   pr.n_tile = 128;  // 128 gate + 128 up accumulator columns -> 128 h columns
+  pr.half_ok = 1;
   pr.map_a = ia;
   pr.map_b = ig;
   pr.map_b2 = iu;
@@ -47,6 +49,7 @@ bool fill_down_fwd(Params& P, Problem& pr, const DownFwdArgs& a) {
   pr.K = a.H;
   pr.mma_n = 256;
   pr.n_tile = 256;
+  pr.half_ok = 1;
   pr.map_a = ia;
   pr.map_b = ib;
   pr.tx_bytes = A_BYTES + PairCfg<kPair>::B_BYTES;

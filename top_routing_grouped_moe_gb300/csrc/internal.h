@@ -57,6 +57,9 @@ cudaError_t launch_combine(const float* o_perm, const float* s_out, const float*
 // dY_perm[row_of_slot[t*k+s]] = dY[t] for every kept slot
 cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
                                int* status, cudaStream_t s);
+// per-row partials of the gate gradient: two per 256-column tile of H (one
+// per accumulator-column half of the tile)
+inline int dgp_slots(int H) { return 2 * ((H + 255) / 256); }
 // dgates[t,s] = sum_p dgp[row_of_slot[t*k+s], p] (0 for dropped slots)
 cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_slot, int T, int k, float* dgates,
                                  cudaStream_t s);
@@ -119,7 +122,7 @@ struct DgradDownArgs {    // dau = swiglu_bwd(g * (dY_perm W_d), au), plus g*h a
   const float* gates;     // per-slot gates or NULL (g = 1)
   const int32_t* slot_of_row;
   int gate_slots;
-  float* dgp;             // [rows, ceil(H/256)] or NULL
+  float* dgp;             // [rows, dgp_slots(H)] or NULL
 };
 struct DgradGuArgs {      // dx = (dau_hi + dau_lo) [W_g; W_u]
   const void* dau;        // [rows, 2H] bf16 hi half

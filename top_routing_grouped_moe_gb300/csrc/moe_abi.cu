@@ -64,7 +64,7 @@ SwigluBwdWs swiglu_bwd_ws(int T, int k, int H, int Hs) {
   w.dau_lo = take(R * 2 * H * 2);
   w.gh_hi = take(R * H * 2);
   w.gh_lo = take(R * H * 2);
-  w.dgp = take(R * ((H + 255) / 256) * 4);
+  w.dgp = take(R * dgp_slots(H) * 4);
   w.s_dau_hi = take((size_t)T * 2 * Hs * 2);
   w.s_dau_lo = take((size_t)T * 2 * Hs * 2);
   w.s_gh_hi = take((size_t)T * Hs * 2);
@@ -360,7 +360,7 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
                    w + L.s_gh_lo, nullptr, nullptr, 0, nullptr};
   cudaError_t e = gemm_dgrad_down(r1, Hs > 0 ? &s1 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
-  e = launch_dgates_reduce(dgp, (H + 255) / 256, row_of_slot, T, k, dgates, st);
+  e = launch_dgates_reduce(dgp, dgp_slots(H), row_of_slot, T, k, dgates, st);
   if (e != cudaSuccess) return fail_cuda(e);
 
   // 2. dW_d = dY_perm^T (g h), g h split into bf16 hi + lo
