@@ -1,7 +1,8 @@
 """Benchmark of the MoE layer hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--cpu-sample-tokens N] [--no-cpu-baseline]
+                    [--workload NAME] [--path fused|unfused] [--cpu-sample-tokens N]
+                    [--no-cpu-baseline]
 
 One step = one full forward + backward of the layer (router, top-k gating,
 permutation, grouped SwiGLU experts + shared expert, combine, and every
@@ -10,6 +11,16 @@ Default workload: the largest layer of the workload table, forward +
 backward (T=8192, d=4096, E=128, top-4, H=Hs=1536, learned router).  Inputs
 are resident in HBM when the timed region starts; L2 (129 MB) is flushed by
 writing a 256 MB buffer before every step.
+
+Two call sequences compute the same step (identical results): "fused", the
+permutation inside the GEMMs' operand loads (TMA row gathers from x and dY)
+and the combine inside the shared expert's down-projection epilogue
+(moe_grouped_swiglu_fused, the gather mode of moe_grouped_swiglu_bwd), and
+"unfused", with x_perm / dY_perm / o_perm / s written and read back
+(moe_permute rows, moe_grouped_swiglu, moe_unpermute_combine and
+moe_unpermute_combine_bwd).  --path picks the one the line reports (default
+unfused, the faster on GB300: the row gathers cannot feed the tensor cores
+at the rate of tiled TMA loads); the other is timed too (`other_path`).
 
 `value` times the step's calls captured once in a CUDA graph and replayed
 (the calls are asynchronous and allocate nothing); `fwd_tokens_per_s` does
@@ -62,6 +73,7 @@ def parse():
                     help="oracle tokens per step (0: sized for ~20 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--path", default="unfused", choices=["fused", "unfused"])
     return ap.parse_args()
 
 
@@ -83,7 +95,7 @@ def gemm_flops(w, R):
     return fwd, bwd
 
 
-def kernel_work(w, R):
+def kernel_work(w, R, fused=False):
     """Algorithmic work of one launch of each kernel of the step: (FLOPs,
     bytes).  FLOPs count the method's products once (the second MMA of a
     hi + lo split operand is not counted).  Bytes count every operand read
@@ -97,14 +109,17 @@ def kernel_work(w, R):
     gu = 4.0 * d * (R * H + T * Hs)
     dn = 2.0 * d * (R * H + T * Hs)
     hid = R * H + T * Hs                             # hidden elements (routed + shared)
+    # the weight gradients' token operand: x_perm / dY_perm rows, or (fused)
+    # the gathered source read once
+    tok = T * d * 2 * (1 + sh) if fused else rows * d * 2
     return {
         "gemm_gate_up_swiglu": (gu, R * d * 2 + T * d * 2 * sh + wgu + hid * 2 + 2 * hid * 2),
         "gemm_gate_up_recompute": (gu, R * d * 2 + T * d * 2 * sh + wgu + 2 * hid * 2),
         "gemm_down": (dn, hid * 2 + wdn + rows * d * 2),
         "gemm_dgrad_down_swiglu_bwd": (dn, rows * d * 2 + wdn + 2 * hid * 2 + 2 * hid * 2 + hid * 2),
-        "gemm_wgrad_down": (dn, rows * d * 2 + hid * 2 + wdn),
+        "gemm_wgrad_down": (dn, tok + hid * 2 + wdn),
         "gemm_dgrad_gate_up": (gu, 2 * hid * 2 + wgu + rows * d * 2),
-        "gemm_wgrad_gate_up": (gu, 2 * hid * 2 + rows * d * 2 + wgu),
+        "gemm_wgrad_gate_up": (gu, 2 * hid * 2 + tok + wgu),
         "gemm_router": (2.0 * T * d * E, T * d * 2 + E * d * 2 + T * E * 4),
         "gemm_router_dw": (2.0 * T * d * E, T * E * 2 + T * d * 2 + E * d * 4),
         "gemm_router_dx": (2.0 * T * d * E, T * E * 4 + E * d * 2 + T * d * 2),
@@ -118,6 +133,15 @@ def kernel_work(w, R):
                                    + hid * 33 // 32),
         "gemm_mx_down": (dn, hid * 33 // 32 + wdn // 2 * 33 // 32 + rows * d * 2),
         "perm_scatter_mx": (0.0, T * d * 2 + R * d * 33 // 32 + T * k * 12 + R * 4),
+        # fused path: a gathered operand's algorithmic bytes are its source
+        # (x or dY, T rows) read once; the expert outputs by slot
+        "perm_maps": (0.0, T * k * 12 + R * 4),
+        "gemm_gate_up_swiglu_gather": (gu, T * d * 2 * (1 + sh) + wgu + hid * 2 + 2 * hid * 2),
+        "gemm_gate_up_recompute_gather": (gu, T * d * 2 * (1 + sh) + wgu + 2 * hid * 2),
+        "gemm_down_slots": (2.0 * d * R * H, R * H * 2 + E * H * d * 2 + R * d * 2),
+        "gemm_down_shared_combine": (2.0 * d * T * Hs, T * Hs * 2 + Hs * d * 2 + R * d * 2 + T * d * 2 + T * k * 8),
+        "combine_slots": (0.0, R * d * 2 + T * d * 2 + T * k * 8),
+        "gemm_dgrad_down_swiglu_bwd_gather": (dn, T * d * 2 * (1 + sh) + wdn + 2 * hid * 2 + 2 * hid * 2 + hid * 2),
     }
 
 
@@ -339,42 +363,38 @@ def main_ours(args):
         else:
             dev[key] = torch.from_numpy(v.view(np.int16)).cuda().view(torch.bfloat16)
     learned = w.routing == "learned"
-    layer = MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity)
+    fused = args.path == "fused"
+    # one layer per call sequence (same inputs, same results); the reported
+    # path's layer is `layer`
+    layers = {p: MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity, fused=(p == "fused"))
+              for p in ("fused", "unfused")}
+    layer = layers[args.path]
+    L = layer
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     main_stream = torch.cuda.current_stream()
     T, d, E, k, H, Hs = w.T, w.d, w.E, w.k, w.H, w.Hs
-    L = layer
+    logits_in = dev.get("logits_in")
 
-    def forward(stream):
-        x = dev["x"]
-        B.moe_route_topk(x, dev.get("W_r"), dev.get("bias"), dev.get("logits_in"), T, d, E, k,
-                         L.logits if learned else None, L.idx, L.gates, L.ws, L.ws_bytes, stream)
-        B.moe_permute(x, L.idx, T, d, E, k, L.capacity, L.counts_raw, L.counts, L.offsets, L.row_of_slot,
-                      L.slot_of_row, L.x_perm, L.ws, L.ws_bytes, stream)
-        B.moe_grouped_swiglu(L.x_perm, L.offsets, x, T, d, E, k, H, Hs, dev["W_g"], dev["W_u"], dev["W_d"],
-                             dev.get("Ws_g"), dev.get("Ws_u"), dev.get("Ws_d"), L.au, L.h, L.o_perm, L.au_s,
-                             L.h_s, L.s, L.ws, L.ws_bytes, stream)
-        B.moe_unpermute_combine(L.o_perm, L.s, L.gates, L.row_of_slot, T, d, k, L.y, stream)
+    def calls(lay):
+        """The forward and the step of one layer: its C-ABI call sequence
+        (MoELayer.forward / backward), on a given stream."""
+        def forward(stream):
+            lay.forward(dev["x"], dev, logits_in=logits_in, stream=stream)
 
-    def backward(stream):
-        x = dev["x"]
-        B.moe_unpermute_combine_bwd(dev["dY"], L.row_of_slot, T, d, k, L.dY_perm, stream)
-        B.moe_grouped_swiglu_bwd(L.dY_perm, dev["dY"], L.gates, L.row_of_slot, L.slot_of_row, L.offsets, L.x_perm,
-                                 x, L.au, L.au_s, T, d, E, k, H, Hs, dev["W_g"], dev["W_u"], dev["W_d"],
-                                 dev.get("Ws_g"), dev.get("Ws_u"), dev.get("Ws_d"), L.dx_perm, L.dx_s, L.dW_g,
-                                 L.dW_u, L.dW_d, L.dWs_g, L.dWs_u, L.dWs_d, L.dgates, L.ws, L.ws_bytes, stream)
-        B.moe_route_topk_bwd(L.dgates, L.gates, L.idx, x if learned else None, T, d, E, k, L.dlogits,
-                             L.dW_r if learned else None, L.ws, L.ws_bytes, stream)
-        B.moe_permute_bwd(L.dx_perm, L.dx_s, L.row_of_slot, L.dlogits if learned else None,
-                          dev.get("W_r") if learned else None, T, d, E, k, L.dx, L.ws, L.ws_bytes, stream)
+        def step(stream):
+            lay.forward(dev["x"], dev, logits_in=logits_in, stream=stream)
+            lay.backward(dev["x"], dev["dY"], dev, learned_router=learned, stream=stream)
+        return forward, step
 
-    def step(stream):
-        forward(stream)
-        backward(stream)
+    forward, step = calls(layer)
+    other = "unfused" if fused else "fused"
+    other_forward, other_step = calls(layers[other])
 
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
         step(main_stream)
+        flush.fill_(1)
+        other_step(main_stream)
     torch.cuda.synchronize()
     st = B.moe_device_status()
     if st != 0:
@@ -405,7 +425,8 @@ def main_ours(args):
     # ---- the step (and the forward alone) as CUDA-graph replays
     gstream = torch.cuda.Stream()
     graphs = {}
-    for gname, fn in (("step", step), ("forward", forward)):
+    for gname, fn in (("step", step), ("forward", forward), ("other_step", other_step),
+                      ("other_forward", other_forward)):
         gstream.wait_stream(main_stream)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=gstream):
@@ -444,6 +465,8 @@ def main_ours(args):
     wall = time.perf_counter() - wall0
     fwd_ms = replay_ms(graphs["forward"])
     clocks = sampler.stop()
+    other_ms = replay_ms(graphs["other_step"])
+    other_fwd_ms = replay_ms(graphs["other_forward"])
     value = tokens_per_s(T, args.steps, world, graph_ms)
     fwd_value = tokens_per_s(T, args.steps, world, fwd_ms)
 
@@ -471,9 +494,14 @@ def main_ours(args):
     lbl_bytes = 2 * T * E * 4 + E * 8  # logits read, gradient written, counts and P
     # Activation recompute: the fp32 a|u rebuilt for the backward (gate/up GEMM
     # without the h store), written over the layer's saved copy (same values)
-    rec_ms = time_alone(lambda: B.moe_grouped_swiglu_recompute(
-        layer.x_perm, layer.offsets, dev["x"], T, d, E, k, H, Hs, dev["W_g"], dev["W_u"],
-        dev.get("Ws_g"), dev.get("Ws_u"), layer.au, layer.au_s))
+    if fused:
+        rec_ms = time_alone(lambda: B.moe_grouped_swiglu_recompute_fused(
+            dev["x"], layer.slot_of_row, layer.offsets, T, d, E, k, H, Hs, dev["W_g"], dev["W_u"],
+            dev.get("Ws_g"), dev.get("Ws_u"), layer.au, layer.au_s))
+    else:
+        rec_ms = time_alone(lambda: B.moe_grouped_swiglu_recompute(
+            layer.x_perm, layer.offsets, dev["x"], T, d, E, k, H, Hs, dev["W_g"], dev["W_u"],
+            dev.get("Ws_g"), dev.get("Ws_u"), layer.au, layer.au_s))
 
     # ---- the MXFP8 forward (block-scaled E4M3 expert GEMMs): routing, the MX
     # permutation, the MX expert MLP and the combine, as a graph replay; the
@@ -549,7 +577,7 @@ def main_ours(args):
     tensor_peak = peaks.get("bf16_tflops") or 1900.0
     hbm_peak = peaks.get("hbm_gbs") or 6800.0
     peak_src = "measured" if peaks else "fallback"
-    work = kernel_work(w, R)
+    work = kernel_work(w, R, fused)
     step_eager = eager_total / args.steps
     kernels = {}
     for name, e in per_kernel.items():
@@ -566,7 +594,7 @@ def main_ours(args):
                  "traffic_unit": "bytes per launch (ncu dram read + write)",
                  "peak_source": f"{peak_src} burst ({'bf16 cuBLAS' if roof['bound'] == 'tensor' else 'copy'})"})
     ffl, bfl = gemm_flops(w, R)
-    rec_work = work["gemm_gate_up_recompute"]
+    rec_work = work["gemm_gate_up_recompute_gather" if fused else "gemm_gate_up_recompute"]
     if mx_fwd is not None:
         fp8_peak = 2.0 * tensor_peak  # the fp8 dense tensor rate is twice bf16's (nominal ratio)
         mx_fwd["rooflines"] = {}
@@ -632,6 +660,13 @@ def main_ours(args):
                                  "captured once in a CUDA graph and replayed; kernels: every launch of eager "
                                  "steps, timed by events the library records before each launch"},
             "fwd_tokens_per_s": fwd_value,
+            "path": args.path,
+            "other_path": {"path": other, "tokens_per_s": tokens_per_s(T, args.steps, world, other_ms),
+                           "ms_per_step": other_ms / args.steps,
+                           "fwd_tokens_per_s": tokens_per_s(T, args.steps, world, other_fwd_ms),
+                           "fwd_ms_per_step": other_fwd_ms / args.steps,
+                           "note": "the same step through the other call sequence (identical results); "
+                                   "graph replay, L2 flushed before each"},
             "mxfp8_forward": mx_fwd,
             "fwd_ms_per_step": fwd_ms / args.steps,
             "eager": {"value": tokens_per_s(T, args.steps, world, eager_total), "ms_per_step": step_eager},

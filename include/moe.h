@@ -149,6 +149,8 @@ MOE_API int moe_route_topk(const void* x, const void* W_r, const float* bias, co
  *   row_of_slot[t*k+s] = offsets[e] + rank(t,s) if kept, else -1   [T*k]
  *   slot_of_row[row]   = t*k+s for every kept pair (rows [0,R))     [T*k]
  *   x_perm[row, :]     = x[t, :]                                  [T*k, d] bf16
+ * x_perm == NULL: the maps only (x may be NULL too), for the fused path
+ * (moe_grouped_swiglu_fused), whose GEMMs gather the rows of x themselves.
  * Deterministic (no order-dependent atomics): the results are bit-exact. */
 MOE_API int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int k, int capacity,
                 int32_t* counts_raw, int32_t* counts, int32_t* offsets,
@@ -222,6 +224,47 @@ MOE_API int moe_grouped_swiglu_recompute(const void* x_perm, const int32_t* offs
                                  const void* W_g, const void* W_u, const void* Ws_g, const void* Ws_u,
                                  float* au, float* au_s, void* stream);
 
+/* The expert MLP with the permutation and the combine fused into the GEMMs
+ * (tokens stay where they are and the experts read them: "Olmo-core 3 Opens
+ * Large MoE Training", "Technical Deep Dive"; the combine of "Production
+ * throughput runs" of the "Olmo-core DDP MoE examples" README).  Same values
+ * as moe_permute (rows) + moe_grouped_swiglu + moe_unpermute_combine, without
+ * x_perm, o_perm or s in memory:
+ *   - the routed gate/up GEMM loads its A rows straight from x: permuted row
+ *     r is token slot_of_row[r] / k, copied 16 bytes per thread (cp.async)
+ *     into the tile's swizzled layout; the gathering GEMMs run on single CTAs
+ *     (128-row tiles);
+ *   - the routed down projection stores row r's fp32 output at its slot:
+ *     o_slot[slot_of_row[r]] ([T*k, d] fp32; rows of dropped slots are not
+ *     written);
+ *   - the shared expert's down projection (a second launch on the stream)
+ *     adds, in its epilogue, the gate-weighted kept slots of each token in
+ *     slot order to its fp32 accumulator s[t] and writes y[t] in bf16 once:
+ *       y[t] = bf16(s[t] + sum_{j kept} gates[t,j] o_slot[t*k+j])
+ *     -- the same operations in the same order as moe_unpermute_combine, so y
+ *     is bit-identical to the unfused path's.  Hs == 0: a combine pass over
+ *     o_slot.
+ * slot_of_row, row_of_slot and offsets come from moe_permute (x_perm may be
+ * NULL there); au, h, au_s, h_s as for moe_grouped_swiglu (h and au in
+ * permuted row order, for the backward).
+ * Speed: on GB300 this path is slower than the unfused one -- per-row
+ * gathers (cp.async, or TMA tile::gather4) do not reach the rate of the
+ * tiled TMA loads that read x_perm -- so the unfused sequence is the fast
+ * one; this call exists for callers that cannot hold x_perm / o_perm. */
+MOE_API int moe_grouped_swiglu_fused(const void* x, const int32_t* slot_of_row, const int32_t* row_of_slot,
+                                     const float* gates, const int32_t* offsets, int T, int d, int E, int k, int H,
+                                     int Hs, const void* W_g, const void* W_u, const void* W_d, const void* Ws_g,
+                                     const void* Ws_u, const void* Ws_d, float* au, void* h, float* o_slot,
+                                     float* au_s, void* h_s, void* y, void* stream);
+
+/* moe_grouped_swiglu_recompute for the fused path: the routed rows are
+ * gathered from x by slot_of_row (no x_perm).  Bit-identical to the a | u
+ * that moe_grouped_swiglu_fused would have saved. */
+MOE_API int moe_grouped_swiglu_recompute_fused(const void* x, const int32_t* slot_of_row, const int32_t* offsets,
+                                               int T, int d, int E, int k, int H, int Hs, const void* W_g,
+                                               const void* W_u, const void* Ws_g, const void* Ws_u, float* au,
+                                               float* au_s, void* stream);
+
 /* Gate-weighted unpermute and combine:
  *   y[t,:] = s[t,:] + sum_{s kept} gates[t,s] * o_perm[row_of_slot[t*k+s], :]
  * o_perm [T*k,d] and s [T,d] fp32 (s may be NULL: no shared expert); fp32
@@ -282,6 +325,12 @@ MOE_API int moe_unpermute_combine_bwd(const void* dY, const int32_t* row_of_slot
  * dW_d [E,d,H] (zero for experts with no rows), dWs_g, dWs_u [Hs,d],
  * dWs_d [d,Hs] (all bf16) and dgates [T,k] fp32 (0 for dropped slots).  Each
  * output element is owned by one tile: no atomics, deterministic.
+ * Fused path: dY_perm == x_perm == NULL (both or neither) -- the dgrad of
+ * the down projection and the two weight gradients then read the rows of dY
+ * and x themselves through slot_of_row (16-byte cp.async row copies; the
+ * permutation fused into their operand loads, no moe_unpermute_combine_bwd
+ * call needed; slower than the permuted copies on GB300);
+ * dY and x are required.  Same results as with the permuted copies.
  * ws >= moe_workspace_size() bytes. */
 MOE_API int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gates,
                            const int32_t* row_of_slot, const int32_t* slot_of_row,

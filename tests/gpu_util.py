@@ -151,7 +151,9 @@ def compare_layer(w, inp, layer, ref, refb):
     (`oracle_reference`: the oracle run on the same fp32 logits).  Top-k
     indices, counts, offsets, both row maps, x_perm and dY_perm bit-exact;
     every floating output and gradient within the layer tolerance, every
-    token and every expert."""
+    token and every expert.  A fused layer (the permutation inside the GEMMs'
+    loads, the combine inside the shared down projection) has no x_perm,
+    dY_perm or s, and holds the expert outputs by slot."""
     import torch
     MARGINS.clear()
     k = w.k
@@ -162,10 +164,12 @@ def compare_layer(w, inp, layer, ref, refb):
         assert np.array_equal(getattr(layer, key).cpu().numpy(), ref[key]), key
     R = int(ref["offsets"][-1])
     assert np.array_equal(layer.slot_of_row.cpu().numpy()[:R], ref["slot_of_row"]), "slot_of_row"
-    xp = layer.x_perm.view(torch.int16).cpu().numpy().view(np.uint16)[:R]
-    assert np.array_equal(xp, inp["x"][ref["slot_of_row"] // k]), "x_perm"
-    dyp = layer.dY_perm.view(torch.int16).cpu().numpy().view(np.uint16)[:R]
-    assert np.array_equal(dyp, inp["dY"][ref["slot_of_row"] // k]), "dY_perm"
+    fused = getattr(layer, "fused", False)
+    if not fused:
+        xp = layer.x_perm.view(torch.int16).cpu().numpy().view(np.uint16)[:R]
+        assert np.array_equal(xp, inp["x"][ref["slot_of_row"] // k]), "x_perm"
+        dyp = layer.dY_perm.view(torch.int16).cpu().numpy().view(np.uint16)[:R]
+        assert np.array_equal(dyp, inp["dY"][ref["slot_of_row"] // k]), "dY_perm"
     # gates: fp32 expf on the GPU against float64
     np.testing.assert_allclose(layer.gates.cpu().numpy(), ref["gates"], rtol=1e-5, atol=1e-6)
 
@@ -174,8 +178,13 @@ def compare_layer(w, inp, layer, ref, refb):
         assert_close("a", host_f64(layer.au[:R, :w.H]), ref["a"])
         assert_close("u", host_f64(layer.au[:R, w.H:]), ref["u"])
     assert_close("h", host_f64(layer.h[:R]), ref["h"])
-    assert_close("o_perm", host_f64(layer.o_perm[:R]), ref["o"])
-    if w.Hs:
+    if fused:
+        # expert outputs stored by slot: row r's output at slot_of_row[r]
+        slots = torch.from_numpy(ref["slot_of_row"].astype(np.int64)).to(layer.o_perm.device)
+        assert_close("o_slot", host_f64(layer.o_perm[slots]), ref["o"])
+    else:
+        assert_close("o_perm", host_f64(layer.o_perm[:R]), ref["o"])
+    if w.Hs and not fused:
         assert_close("s", host_f64(layer.s), ref["s"])
     assert_close("y", host_f64(layer.y), ref["y"])
 

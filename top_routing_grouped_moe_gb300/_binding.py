@@ -48,6 +48,8 @@ SIGNATURES = {
     "moe_permute_static": "pp" + "iiiii" + "pppppp" + "s",
     "moe_grouped_swiglu": "ppp" + "iiiiii" + "pppppp" + "pppppp" + "pz" + "s",
     "moe_grouped_swiglu_recompute": "ppp" + "iiiiii" + "pppp" + "pp" + "s",
+    "moe_grouped_swiglu_fused": "ppppp" + "iiiiii" + "pppppp" + "ppp" + "ppp" + "s",
+    "moe_grouped_swiglu_recompute_fused": "ppp" + "iiiiii" + "pppp" + "pp" + "s",
     "moe_unpermute_combine": "pppp" + "iii" + "p" + "s",
     "moe_unpermute_combine_bwd": "pp" + "iii" + "p" + "s",
     "moe_grouped_swiglu_bwd": "pppppppppp" + "iiiiii" + "pppppp" + "pp" + "pppppp" + "p" + "pz" + "s",
@@ -223,6 +225,18 @@ def moe_grouped_swiglu_recompute(x_perm, offsets, x, T, d, E, k, H, Hs, W_g, W_u
                                  stream=None):
     return _call("moe_grouped_swiglu_recompute", x_perm, offsets, x, T, d, E, k, H, Hs, W_g, W_u, Ws_g, Ws_u, au,
                  au_s, stream)
+
+
+def moe_grouped_swiglu_fused(x, slot_of_row, row_of_slot, gates, offsets, T, d, E, k, H, Hs, W_g, W_u, W_d, Ws_g,
+                             Ws_u, Ws_d, au, h, o_slot, au_s, h_s, y, stream=None):
+    return _call("moe_grouped_swiglu_fused", x, slot_of_row, row_of_slot, gates, offsets, T, d, E, k, H, Hs, W_g,
+                 W_u, W_d, Ws_g, Ws_u, Ws_d, au, h, o_slot, au_s, h_s, y, stream)
+
+
+def moe_grouped_swiglu_recompute_fused(x, slot_of_row, offsets, T, d, E, k, H, Hs, W_g, W_u, Ws_g, Ws_u, au, au_s,
+                                       stream=None):
+    return _call("moe_grouped_swiglu_recompute_fused", x, slot_of_row, offsets, T, d, E, k, H, Hs, W_g, W_u, Ws_g,
+                 Ws_u, au, au_s, stream)
 
 
 def moe_unpermute_combine(o_perm, s, gates, row_of_slot, T, d, k, y, stream=None):

@@ -138,6 +138,34 @@ struct Problem {
   float* dgp;              // per-row partials of the gate gradient, [rows, ld_dgp] (nullable)
   int ld_dgp;
   int map_aux;             // tensor map of au (fp32, 32 x 32 boxes): a | u staged by TMA
+  // Row gather (the permutation fused into the operand loads; GATHER
+  // launches, single CTAs): one operand is read row by row from a
+  // token-indexed source [src rows, cols] (gather_src, gather_pitch bytes per
+  // row) by 16-byte cp.async copies into the stage's 128-byte-swizzled
+  // layout; the stage's barrier expects one more arrival per producer lane.
+  // Permuted row r stands for source row gather_slot[r] / gather_k.  Ragged
+  // M: A row r of the tile.  Ragged K: K row r of the group (the operand
+  // gather_op, 0 = A, 1 = B).  Rows past the group's end read source row 0:
+  // ragged-M rows there are never stored, and on ragged-K rows there the
+  // other operand is zero.
+  const int* gather_slot;  // NULL: no gather
+  const uint8_t* gather_src;
+  long long gather_pitch;
+  int gather_k;
+  int gather_slots;        // valid slot values are [0, gather_slots)
+  int gather_op;
+  // EPI_F32, ragged M: row r of the problem is stored at output row
+  // out_row_map[r] (NULL: row r), which must lie in [0, out_map_rows)
+  const int* out_row_map;
+  int out_map_rows;
+  // EPI_F32, the shared expert's down projection with the combine fused in
+  // (comb_y != NULL): instead of s, y[t] = bf16(s[t] + sum over kept slots
+  // (t,j) of gates[t,j] o_slot[t*k+j]), the sum taken in slot order
+  const float* comb_o;          // [T*k, ldo] fp32 expert outputs in slot order
+  const float* comb_gates;      // [T*k]
+  const int* comb_row_of_slot;  // [T*k]: slot kept iff >= 0
+  int comb_k;
+  void* comb_y;                 // [T, ldo] bf16
 };
 
 struct Params {
@@ -178,6 +206,7 @@ struct SmemTailT {
   uint64_t ring_full[RING];   // dynamic schedule: tile index published
   uint64_t ring_empty[RING];  // ... and read by the MMA warp and the four epilogue warps
   int ring[RING];
+  alignas(16) int gsrc[2][128];  // row gather: source rows of the rows being loaded (two buffers)
   uint32_t tmem_base;
   int abort_flag;
   Sched sched;
@@ -204,7 +233,8 @@ template <int MODE, int EPI, int PAIR, int SPLIT, int MX = 0>
 struct StageCfg {
   static constexpr int STAGES =
       MX ? MX_STAGES
-         : (MODE == KGROUP ? KgCfg<SPLIT>::STAGES : (EPI == EPI_SWIGLU_BWD ? 4 : PairCfg<PAIR>::STAGES));
+         : (MODE == KGROUP ? KgCfg<SPLIT>::STAGES
+                           : (EPI == EPI_SWIGLU_BWD ? (PAIR == 2 ? 4 : 2) : PairCfg<PAIR>::STAGES));
   static constexpr int BYTES = MX ? A_BYTES + MX_B_BYTES + MX_SF_BYTES
                                   : (MODE == KGROUP ? KgCfg<SPLIT>::STAGE_BYTES : A_BYTES + PairCfg<PAIR>::B_BYTES);
   static constexpr int EPI_BYTES = EPI == EPI_SWIGLU_BWD ? 4 * 2 * AU_CHUNK_BYTES : 0;
@@ -214,6 +244,20 @@ template <int MODE, int EPI, int PAIR, int SPLIT, int MX = 0>
 constexpr size_t smem_bytes() {
   using C = StageCfg<MODE, EPI, PAIR, SPLIT, MX>;
   return 1024 + C::STAGES * C::BYTES + C::EPI_BYTES + sizeof(SmemTailT<C::STAGES>);
+}
+
+// Source row of permuted row `row` of a gathered operand (0 for rows at or
+// past `end`, and for an out-of-range slot, which is recorded as a device
+// bounds error).
+__device__ __forceinline__ int gather_source(const int* slot_of_row, int div, int nslots, int row, int end,
+                                             int* status) {
+  if (row >= end) return 0;
+  const int slot = __ldg(slot_of_row + row);
+  if (slot < 0 || slot >= nslots) {
+    record_status(status, MOE_ERR_DEVICE_BOUNDS);
+    return 0;
+  }
+  return slot / div;
 }
 
 struct TileInfo {
@@ -433,8 +477,10 @@ __device__ __forceinline__ void load_3d(void* dst, const CUtensorMap* m, uint64_
   else ptx::tma_load_3d_pair(dst, m, bar_leader, c0, c1, c2);
 }
 
-template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT, int MX = 0>
+template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT, int MX = 0, int GATHER = 0>
 __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params P) {
+  static_assert(!GATHER || (!MX && PAIR == 1 && (MODE == KGROUP || AMN == 0)),
+                "row gather: single CTAs, K-major A (ragged M) or ragged K");
   static_assert(!(MODE == KGROUP && PAIR == 2), "ragged-K GEMMs run on single CTAs");
   static_assert(!MX || (MODE == MGROUP && PAIR == 1 && AMN == 0 && BMN == 0 && SPLIT == SPLIT_NONE &&
                         (EPI == EPI_SWIGLU_FWD || EPI == EPI_F32)),
@@ -474,7 +520,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&tail->full[s], 1);
+      // GATHER: the lead's expect-tx arrival and one cp.async arrival per lane
+      ptx::mbar_init(&tail->full[s], GATHER ? 33 : 1);
       ptx::mbar_init(&tail->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -525,7 +572,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // One thread waits on the barriers and issues the loads.  GATHER: the
+    // whole warp runs the loop; lane 0 waits and issues the tiled loads, and
+    // every lane issues gathers of four rows of the gathered operand.
+    if (GATHER || lane == 0) {
+      const bool lead = lane == 0;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_phase_mask = 0;  // bit s: parity of the last load issued into stage s
@@ -534,22 +585,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
       int fetched = 0;   // raw value of the last tile-counter atomic
       int acquired = -1;  // (problem, group) whose per-group maps this thread last acquired
       for (int i = 0; ok; ++i) {
-        int t;
+        int t = 0;
         if (dyn) {
           // publish this tile's index, then fetch the next one (its latency
           // is hidden behind this tile's loads)
           const int slot = i & (RING - 1);
-          if (!ptx::mbar_wait_bounded(&tail->ring_empty[slot], ((i / RING) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+          bool got = true;
+          if (lead) {
+            got = ptx::mbar_wait_bounded(&tail->ring_empty[slot], ((i / RING) & 1) ^ 1, abort_flag, kWaitLimitNs);
+            if (got) {
+              t = i == 0 ? tile0 : fetched + tile_step;
+              *reinterpret_cast<volatile int*>(&tail->ring[slot]) = t;
+              ptx::mbar_arrive(&tail->ring_full[slot]);
+              // used at the next tile only: no instruction here waits for the
+              // atomic's round trip
+              if (t < total) fetched = atomicAdd(P.tile_counter, 1);
+            }
+          }
+          if (GATHER) {
+            got = __shfl_sync(0xffffffffu, got, 0);
+            t = __shfl_sync(0xffffffffu, t, 0);
+          }
+          if (!got) {
             ok = false;
             break;
           }
-          t = i == 0 ? tile0 : fetched + tile_step;
-          *reinterpret_cast<volatile int*>(&tail->ring[slot]) = t;
-          ptx::mbar_arrive(&tail->ring_full[slot]);
           if (t >= total) break;
-          // used at the next tile only: no instruction here waits for the
-          // atomic's round trip
-          fetched = atomicAdd(P.tile_counter, 1);
         } else {
           t = tile0 + i * tile_step;
           if (t >= total) break;
@@ -574,17 +635,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         const int mx_nkq = pr.nkq;
         int k0 = ti.k0;
         const int g = ti.g, nk = ti.nk;
+        // Row gather: ragged M gathers this CTA's 128 A rows (this lane's four
+        // rows am + 4 lane + 0..3, fixed for the tile); ragged K gathers, per
+        // stage, the quad kq of the stage's K rows into every block of the
+        // gathered operand (lanes past the last (quad, block) pair idle)
+        // Row gather: the lanes look the source rows up (slot_of_row / k)
+        // into shared memory, then copy them 16 bytes at a time (lane: chunk
+        // lane & 7 of rows lane >> 3, +4, +8, ...: four whole 128-byte rows
+        // per instruction).  These copies go through the L1's miss queue, so
+        // fewer bytes are in flight than with a tiled TMA load (TMA's own
+        // four-row gathers take about 60 cycles per instruction): a gathering
+        // GEMM runs at a fraction of the tiled one's rate.
+        const bool gat = GATHER && pr.gather_slot != nullptr;
+        const uint8_t* g_src = pr.gather_src;
+        const long long g_pitch = pr.gather_pitch;
+        const int g_chunk = lane & 7, g_rg = lane >> 3;
+        const int* g_slot = pr.gather_slot;
+        const int g_div = pr.gather_k, g_nslots = pr.gather_slots, g_op = pr.gather_op;
+        constexpr int KNQ = KBK / 4;  // ragged K: row quads per stage (<= 16)
+        int gnext[4] = {0, 0, 0, 0};  // ragged K: source rows of lane's quad of the next stage
+        if (gat) {
+          if (MODE == MGROUP) {
+            // rows am .. am + 127 of this tile, fixed for its stages (the
+            // last tile's gathers were issued before lane 0 reaches this sync)
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              tail->gsrc[0][4 * lane + q] =
+                  gather_source(g_slot, g_div, g_nslots, am + 4 * lane + q, ti.rows_end, P.status);
+            __syncwarp();
+          } else if (nk > 0 && lane < KNQ) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              gnext[q] = gather_source(g_slot, g_div, g_nslots, ti.k0 + 4 * lane + q, ti.k1, P.status);
+          }
+        }
         if (MODE == KGROUP && pr.gmaps != nullptr && nk > 0) {
           // this group's own maps (written by an earlier launch: acquired for
-          // the tensor-map proxy once per group this thread loads from); K rows
-          // counted from the group's start
+          // the tensor-map proxy once per group by the thread that loads from
+          // them); K rows counted from the group's start
           const CUtensorMap* gm = pr.gmaps + (long long)g * KG_MAPS_PER_GROUP;
           mA = gm;
           mB = gm + 1;
           if (SPLIT == SPLIT_A) mAlo = gm + 2;
           if (SPLIT == SPLIT_B) mBlo = gm + 2;
           const int key = ti.p * MAX_G + g;
-          if (key != acquired) {
+          if (lead && key != acquired) {
             ptx::tmap_acquire(mA);
             ptx::tmap_acquire(mB);
             if (SPLIT != SPLIT_NONE) ptx::tmap_acquire(gm + 2);
@@ -593,13 +689,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           k0 = 0;
         }
         for (int kb = 0; kb < nk; ++kb) {
-          if (!ptx::mbar_wait_bounded(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          if (MODE == KGROUP && gat) {
+            // this stage's source rows into buffer kb & 1 (lane 0 reads the
+            // other buffer for the previous stage until this sync); the next
+            // stage's lookups are issued now and complete behind this stage's
+            // wait
+            if (lane < KNQ) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) tail->gsrc[kb & 1][4 * lane + q] = gnext[q];
+              if (kb + 1 < nk) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  gnext[q] = gather_source(g_slot, g_div, g_nslots, ti.k0 + (kb + 1) * KBK + 4 * lane + q, ti.k1,
+                                           P.status);
+              }
+            }
+            __syncwarp();
+          }
+          bool got = true;
+          if (lead) got = ptx::mbar_wait_bounded(&tail->empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs);
+          if (GATHER) got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
             ok = false;
             break;
           }
           uint64_t* fb = &tail->full[stage];
           const uint32_t fbl = PAIR == 2 ? ptx::mapa(ptx::smem_u32(fb), 0) : 0u;
-          if (rank == 0) ptx::mbar_arrive_expect_tx(fb, tx);
+          if (lead && rank == 0) ptx::mbar_arrive_expect_tx(fb, tx);
           issued_any |= 1u << stage;
           issued_phase_mask = (issued_phase_mask & ~(1u << stage)) | (phase << stage);
           if (MODE == KGROUP) {
@@ -610,11 +726,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             if (blk3d) {
               // one instruction per operand (a TMA load's issue cost barely
               // depends on its size)
-              ptx::tma_load_3d(st, mA, fb, 0, k, am / 64);
-              ptx::tma_load_3d(st + KG_A_BYTES, mB, fb, 0, k, bn / 64);
-              if (SPLIT == SPLIT_A) ptx::tma_load_3d(lo, mAlo, fb, 0, k, am / 64);
-              if (SPLIT == SPLIT_B) ptx::tma_load_3d(lo, mBlo, fb, 0, k, bn / 64);
-            } else {
+              if (lead) {
+                if (!(gat && g_op == 0)) ptx::tma_load_3d(st, mA, fb, 0, k, am / 64);
+                if (!(gat && g_op == 1)) ptx::tma_load_3d(st + KG_A_BYTES, mB, fb, 0, k, bn / 64);
+                if (SPLIT == SPLIT_A) ptx::tma_load_3d(lo, mAlo, fb, 0, k, am / 64);
+                if (SPLIT == SPLIT_B) ptx::tma_load_3d(lo, mBlo, fb, 0, k, bn / 64);
+              }
+              if (gat) {
+                // the gathered operand's blocks (A: 2, B: 4) of 64 columns
+                // x KBK rows
+                const int nbg = g_op == 0 ? 2 : 4;
+                uint8_t* gdst = st + (g_op == 0 ? 0 : KG_A_BYTES);
+                const uint8_t* gsrc0 = g_src + (long long)(g_op == 0 ? am : bn) * 2 + g_chunk * 16;
+                const int* rows = tail->gsrc[kb & 1];
+                for (int i = 0; i < KBK / 4; ++i) {
+                  const int r = 4 * i + g_rg;
+                  const uint8_t* src = gsrc0 + (long long)rows[r] * g_pitch;
+                  uint8_t* dst = gdst + r * 128 + ((g_chunk ^ (r & 7)) << 4);
+                  for (int j = 0; j < nbg; ++j) ptx::cp_async_16(dst + j * KG_BLOCK_BYTES, src + j * 128);
+                }
+              }
+            } else if (lead) {
               ptx::tma_load_2d(st, mA, fb, am, k);
               ptx::tma_load_2d(st + KG_BLOCK_BYTES, mA, fb, am + 64, k);
               for (int j = 0; j < nblk; ++j) ptx::tma_load_2d(st + KG_A_BYTES + j * KG_BLOCK_BYTES, mB, fb, bn + 64 * j, k);
@@ -643,41 +775,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             uint8_t* a_dst = sA + stage * A_BYTES;
             uint8_t* b_dst = sB + stage * B_BYTES;
             const CUtensorMap* mAk = (part && mAlo) ? mAlo : mA;
-            if (AMN == 0) {
-              load_2d<PAIR>(a_dst, mAk, fb, fbl, k, am);
-            } else {
-              load_2d<PAIR>(a_dst, mAk, fb, fbl, am, k);
-              load_2d<PAIR>(a_dst + MN_BLOCK_BYTES, mAk, fb, fbl, am + 64, k);
-            }
-            if (EPI == EPI_SWIGLU_FWD) {
-              // B tile = 128 h columns as two 64-column slices, each [64 rows
-              // of W_g ; 64 rows of W_u] (accumulator columns: a | u | a | u,
-              // 64 each); with a CTA pair each CTA holds one slice, so that a
-              // and u of an h column stay in the same lanes of a folded
-              // (half-tile) accumulator too
-#pragma unroll
-              for (int j = 0; j < 2 / PAIR; ++j) {
-                const int slice = PAIR == 1 ? j : rank;
-                uint8_t* dst = b_dst + j * (2 * MN_BLOCK_BYTES);
-                load_3d<PAIR>(dst, mB, fb, fbl, k, ti.n0 + 64 * slice, g);
-                load_3d<PAIR>(dst + MN_BLOCK_BYTES, mB2, fb, fbl, k, ti.n0 + 64 * slice, g);
+            if (gat) {
+              // the tile's 128 A rows, K columns [k, k + 64)
+              const uint8_t* gsrc0 = g_src + (long long)k * 2 + g_chunk * 16;
+              const int* rows = tail->gsrc[0];
+#pragma unroll 8
+              for (int i = 0; i < 32; ++i) {
+                const int r = 4 * i + g_rg;
+                ptx::cp_async_16(a_dst + r * 128 + ((g_chunk ^ (r & 7)) << 4), gsrc0 + (long long)rows[r] * g_pitch);
               }
-            } else if (BMN == 0) {
-              load_3d<PAIR>(b_dst, mB, fb, fbl, k, bn, g);
-            } else {
-              const bool second = ksplit > 0 && k >= ksplit;
-              const CUtensorMap* mBk = second ? mB2 : mB;
-              const int kk = second ? k - ksplit : k;
-              for (int j = 0; j < nblk; ++j) load_3d<PAIR>(b_dst + j * MN_BLOCK_BYTES, mBk, fb, fbl, bn + 64 * j, kk, g);
+            } else if (lead) {
+              if (AMN == 0) {
+                load_2d<PAIR>(a_dst, mAk, fb, fbl, k, am);
+              } else {
+                load_2d<PAIR>(a_dst, mAk, fb, fbl, am, k);
+                load_2d<PAIR>(a_dst + MN_BLOCK_BYTES, mAk, fb, fbl, am + 64, k);
+              }
+            }
+            if (lead) {
+              if (EPI == EPI_SWIGLU_FWD) {
+                // B tile = 128 h columns as two 64-column slices, each [64 rows
+                // of W_g ; 64 rows of W_u] (accumulator columns: a | u | a | u,
+                // 64 each); with a CTA pair each CTA holds one slice, so that a
+                // and u of an h column stay in the same lanes of a folded
+                // (half-tile) accumulator too
+#pragma unroll
+                for (int j = 0; j < 2 / PAIR; ++j) {
+                  const int slice = PAIR == 1 ? j : rank;
+                  uint8_t* dst = b_dst + j * (2 * MN_BLOCK_BYTES);
+                  load_3d<PAIR>(dst, mB, fb, fbl, k, ti.n0 + 64 * slice, g);
+                  load_3d<PAIR>(dst + MN_BLOCK_BYTES, mB2, fb, fbl, k, ti.n0 + 64 * slice, g);
+                }
+              } else if (BMN == 0) {
+                load_3d<PAIR>(b_dst, mB, fb, fbl, k, bn, g);
+              } else {
+                const bool second = ksplit > 0 && k >= ksplit;
+                const CUtensorMap* mBk = second ? mB2 : mB;
+                const int kk = second ? k - ksplit : k;
+                for (int j = 0; j < nblk; ++j) load_3d<PAIR>(b_dst + j * MN_BLOCK_BYTES, mBk, fb, fbl, bn + 64 * j, kk, g);
+              }
             }
           }
+          // GATHER: each lane's arrival fires once its copies have landed
+          // (every stage, gathered or not: the barrier counts 32 of them)
+          if (GATHER) ptx::cp_async_mbar_arrive(fb);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
+      // copies still in flight land before the CTA's shared memory goes away
+      if (GATHER) asm volatile("cp.async.wait_all;" ::: "memory");
+      if (!ok && lead) {
         *abort_flag = 1;
         record_status(P.status, MOE_ERR_TIMEOUT);
         // let copies already in flight land before the CTA's shared memory goes
@@ -732,6 +882,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
             ok = false;
             break;
           }
+          // rows copied by cp.async (generic proxy) are read by the MMAs
+          // (async proxy)
+          if (GATHER) ptx::fence_proxy_async_smem();
           // Ragged K: the rows of a group's last step past its end are zeros
           // (per-group maps, or TMA's fill past `extent`), and a 16-row
           // sub-step entirely past the end is not issued.
@@ -947,6 +1100,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           outp = reinterpret_cast<OutT<EPI>*>(pr.out);
           base = (MODE == KGROUP ? ti.g * pr.gstride : 0) + (long long)row0 * pr.ldo;
         }
+        // ragged M with a row map: this thread's eight rows 4 j + rs go to
+        // output rows orow[j] (-1: not stored)
+        const bool mapped = MODE == MGROUP && pr.out_row_map != nullptr;
+        int orow[8];
+        if (mapped) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + rs;
+            orow[j] = -1;
+            if (r < nrows) {
+              const int v = __ldg(pr.out_row_map + row0 + r);
+              if (v < 0 || v >= pr.out_map_rows) record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
+              else orow[j] = v;
+            }
+          }
+        }
+        const bool comb = MODE == MGROUP && pr.comb_y != nullptr;
+        const int ck = pr.comb_k;
         const int c_end = ti.half ? col_shift + pr.mma_n / 2 : pr.n_tile;
         for (int c0 = col_shift; c0 < c_end; c0 += 32) {
           if (ti.n0 + c0 >= pr.N) break;
@@ -960,9 +1131,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int r = 4 * j + rs;
-            if (r < nrows && col_ok)
-              store4(outp + base + (long long)r * pr.ldo + col,
-                     make_float4(v[j].x + b.x, v[j].y + b.y, v[j].z + b.z, v[j].w + b.w));
+            if (r >= nrows || !col_ok) continue;
+            float4 a = make_float4(v[j].x + b.x, v[j].y + b.y, v[j].z + b.z, v[j].w + b.w);
+            if (comb) {
+              // token t = row0 + r: its kept slots' expert outputs, gate-
+              // weighted, added in slot order (the combine's own order)
+              const long long slot0 = (long long)(row0 + r) * ck;
+              float4 o[kMaxK];
+#pragma unroll
+              for (int q = 0; q < kMaxK; ++q)
+                if (q < ck) o[q] = __ldg(reinterpret_cast<const float4*>(pr.comb_o + (slot0 + q) * pr.ldo + col));
+#pragma unroll
+              for (int q = 0; q < kMaxK; ++q) {
+                if (q >= ck) break;
+                if (__ldg(pr.comb_row_of_slot + slot0 + q) < 0) continue;
+                const float gq = __ldg(pr.comb_gates + slot0 + q);
+                a = make_float4(fmaf(gq, o[q].x, a.x), fmaf(gq, o[q].y, a.y), fmaf(gq, o[q].z, a.z),
+                                fmaf(gq, o[q].w, a.w));
+              }
+              store4(reinterpret_cast<__nv_bfloat16*>(pr.comb_y) + (long long)(row0 + r) * pr.ldo + col, a);
+            } else if (mapped) {
+              if (orow[j] >= 0) store4(outp + (long long)orow[j] * pr.ldo + col, a);
+            } else {
+              store4(outp + base + (long long)r * pr.ldo + col, a);
+            }
           }
         }
       } else if (EPI == EPI_SWIGLU_FWD && MX) {

@@ -140,6 +140,20 @@ inline int new_map(Params& P) { return P.num_maps < MAX_MAPS ? P.num_maps++ : -1
 
 inline int cdiv_h(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
+// Row gather of problem `pr`'s operand `op` (0 = A, 1 = B) from the bf16
+// source [src_rows, cols] by permuted row -> slot (slot / k = source row).
+inline bool set_gather(Problem& pr, int op, const void* src, int cols, const int32_t* slot_of_row, int k,
+                       int nslots) {
+  if (!src || !slot_of_row || k < 1 || (reinterpret_cast<uintptr_t>(src) & 15) || (cols % 64)) return false;
+  pr.gather_src = static_cast<const uint8_t*>(src);
+  pr.gather_pitch = (long long)cols * 2;
+  pr.gather_slot = slot_of_row;
+  pr.gather_k = k;
+  pr.gather_slots = nslots;
+  pr.gather_op = op;
+  return true;
+}
+
 inline Problem blank_problem() {
   Problem p;
   std::memset(&p, 0, sizeof(p));
@@ -155,9 +169,9 @@ inline Problem blank_problem() {
 // Launch a persistent grid for `tile_bound` tiles at most: one CTA per SM
 // (PAIR = 1), or clusters of two CTAs sized by the number of clusters that can
 // be resident at once (PAIR = 2).
-template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT = SPLIT_NONE, int MX = 0>
+template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT = SPLIT_NONE, int MX = 0, int GATHER = 0>
 cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s, const char* name) {
-  auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR, SPLIT, MX>;
+  auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR, SPLIT, MX, GATHER>;
   constexpr size_t smem = smem_bytes<MODE, EPI, PAIR, SPLIT, MX>();
   static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   int dev = 0;

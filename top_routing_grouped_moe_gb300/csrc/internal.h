@@ -83,6 +83,15 @@ cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float
 // ------------------------------------------------------------ tensor-core GEMMs
 // All return cudaSuccess or an error; tensor-map encoding failures map to
 // cudaErrorInvalidValue.
+// Row gather (the permutation fused into an operand's TMA loads): permuted
+// row r of the operand is row slot_of_row[r] / k of src.  src == NULL: none.
+struct RowGather {
+  const void* src;             // [src_rows, cols] bf16 (x or dY)
+  int src_rows;
+  const int32_t* slot_of_row;  // permuted row -> slot t*k+s
+  int k;
+  int nslots;                  // T*k
+};
 struct SwigluFwdArgs {
   const void* a;        // [rows, d] bf16 (x_perm or x)
   int rows_total;       // rows of the A buffer
@@ -92,6 +101,7 @@ struct SwigluFwdArgs {
   const void* Wu;
   float* au;            // [rows, 2H] fp32 (a | u) or NULL
   void* h;              // [rows, H], or NULL (a | u only: the backward's recompute)
+  RowGather gather;     // A rows gathered from gather.src (`a` unused)
 };
 struct DownFwdArgs {
   const void* h;        // [rows, H]
@@ -99,7 +109,16 @@ struct DownFwdArgs {
   const int32_t* offsets;
   int G, d, H;
   const void* Wd;       // [G, d, H]
-  float* o;             // [rows, d] fp32
+  float* o;             // [rows, d] fp32 (unused with comb_y)
+  const int32_t* out_row_map;  // row r stored at row out_row_map[r] of o (NULL: r)
+  int out_map_rows;            // rows of o with a row map
+  // combine fused into this (dense, shared-expert) problem's epilogue:
+  // y[t] = bf16(o[t] + sum_{kept j} gates[t,j] comb_o[t*k+j]), o not stored
+  const float* comb_o;         // [T*k, d] fp32, slot order
+  const float* comb_gates;
+  const int32_t* comb_row_of_slot;
+  int comb_k;
+  void* comb_y;                // [T, d] bf16
 };
 // routed + (optional) shared in one persistent launch
 cudaError_t gemm_swiglu_fwd(const SwigluFwdArgs& routed, const SwigluFwdArgs* shared, int* status, cudaStream_t s);
@@ -123,6 +142,7 @@ struct DgradDownArgs {    // dau = swiglu_bwd(g * (dY_perm W_d), au), plus g*h a
   const int32_t* slot_of_row;
   int gate_slots;
   float* dgp;             // [rows, dgp_slots(H)] or NULL
+  RowGather gather;       // dY rows gathered from gather.src (`dY` unused)
 };
 struct DgradGuArgs {      // dx = (dau_hi + dau_lo) [W_g; W_u]
   const void* dau;        // [rows, 2H] bf16 hi half
@@ -145,6 +165,8 @@ struct WgradArgs {        // out[g] = A_g^T B_g over rows [off[g], off[g+1])
   void* out;              // [G, M, N] (rows < row_split), bf16
   void* out2;             // rows >= row_split go here as [G, M - row_split, N]; NULL = none
   int row_split;
+  RowGather gather;       // rows of operand gather_op (0: A, 1: B) gathered (that pointer unused)
+  int gather_op;
 };
 cudaError_t gemm_dgrad_down(const DgradDownArgs& routed, const DgradDownArgs* shared, int* status, cudaStream_t s);
 cudaError_t gemm_dgrad_gu(const DgradGuArgs& routed, const DgradGuArgs* shared, int* status, cudaStream_t s);
@@ -191,6 +213,11 @@ cudaError_t gemm_mx_down(const MxGemmArgs& routed, const MxGemmArgs* shared, cud
 cudaError_t launch_combine_rows(const float* o_perm, const float* s_out, const float* gates,
                                 const int32_t* row_of_slot, int T, int d, int k, long long o_rows, void* y,
                                 int* status, cudaStream_t s);
+// the same with the expert outputs stored by slot: y[t] = s[t] + sum_{kept j}
+// g[t,j] o_slot[t*k+j]
+cudaError_t launch_combine_slots(const float* o_slot, const float* s_out, const float* gates,
+                                 const int32_t* row_of_slot, int T, int d, int k, void* y, int* status,
+                                 cudaStream_t s);
 
 // split-K factor used for dW_r
 int router_dw_splits(int T, int d, int E);

@@ -246,9 +246,9 @@ int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int
                 size_t ws_bytes, void* stream) {
   int rc = check_dims(T, d, E, k);
   if (rc) return rc;
-  if (!x || !topk_idx || !counts_raw || !counts || !offsets || !row_of_slot || !slot_of_row || !x_perm)
-    return MOE_ERR_INVALID_ARG;
-  if (!al16(x) || !al16(x_perm)) return MOE_ERR_INVALID_ARG;
+  if (!topk_idx || !counts_raw || !counts || !offsets || !row_of_slot || !slot_of_row) return MOE_ERR_INVALID_ARG;
+  // x_perm == NULL: the maps only (x unused)
+  if (x_perm && (!x || !al16(x) || !al16(x_perm))) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < permute_ws_bytes(T, E, k)) return MOE_ERR_WORKSPACE;
   return check(launch_permute(x, topk_idx, T, d, E, k, capacity, counts_raw, counts, offsets, row_of_slot,
                               slot_of_row, x_perm, ws, device_status_ptr(), static_cast<cudaStream_t>(stream)));
@@ -302,6 +302,65 @@ int moe_grouped_swiglu_recompute(const void* x_perm, const int32_t* offsets, con
   return check(gemm_swiglu_fwd(r, Hs > 0 ? &sh : nullptr, device_status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 
+int moe_grouped_swiglu_fused(const void* x, const int32_t* slot_of_row, const int32_t* row_of_slot,
+                             const float* gates, const int32_t* offsets, int T, int d, int E, int k, int H, int Hs,
+                             const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
+                             const void* Ws_d, float* au, void* h, float* o_slot, float* au_s, void* h_s, void* y,
+                             void* stream) {
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  rc = check_hidden(H, Hs);
+  if (rc) return rc;
+  const void* req[] = {x, slot_of_row, row_of_slot, gates, offsets, W_g, W_u, W_d, h, o_slot, y};
+  for (const void* p : req)
+    if (!p) return MOE_ERR_INVALID_ARG;
+  const void* req16[] = {x, W_g, W_u, W_d, h, o_slot, y};
+  for (const void* p : req16)
+    if (!al16(p)) return MOE_ERR_INVALID_ARG;
+  if (au && !al16(au)) return MOE_ERR_INVALID_ARG;
+  if (Hs > 0) {
+    if (!Ws_g || !Ws_u || !Ws_d || !h_s) return MOE_ERR_INVALID_ARG;
+    if (!al16(Ws_g) || !al16(Ws_u) || !al16(Ws_d) || !al16(h_s) || (au_s && !al16(au_s))) return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = device_status_ptr();
+  const int R = T * k;
+  const RowGather gx{x, T, slot_of_row, k, R};
+  // gate/up: routed A rows gathered from x; shared expert on x
+  SwigluFwdArgs r{nullptr, R, offsets, E, d, H, W_g, W_u, au, h, gx};
+  SwigluFwdArgs sh{x, T, nullptr, 1, d, Hs, Ws_g, Ws_u, au_s, h_s};
+  cudaError_t e = gemm_swiglu_fwd(r, Hs > 0 ? &sh : nullptr, status, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  // routed down projection: each row's output stored at its slot
+  DownFwdArgs rd{h, R, offsets, E, d, H, W_d, o_slot, slot_of_row, R};
+  e = gemm_down_fwd(rd, nullptr, status, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (Hs == 0) return check(launch_combine_slots(o_slot, nullptr, gates, row_of_slot, T, d, k, y, status, st));
+  // shared down projection with the combine in its epilogue (after the
+  // routed one on the same stream: every o_slot row is written by then)
+  DownFwdArgs sd{h_s, T, nullptr, 1, d, Hs, Ws_d, nullptr, nullptr, 0, o_slot, gates, row_of_slot, k, y};
+  return check(gemm_down_fwd(sd, nullptr, status, st));
+}
+
+int moe_grouped_swiglu_recompute_fused(const void* x, const int32_t* slot_of_row, const int32_t* offsets, int T,
+                                       int d, int E, int k, int H, int Hs, const void* W_g, const void* W_u,
+                                       const void* Ws_g, const void* Ws_u, float* au, float* au_s, void* stream) {
+  int rc = check_dims(T, d, E, k);
+  if (rc) return rc;
+  rc = check_hidden(H, Hs);
+  if (rc) return rc;
+  if (!x || !slot_of_row || !offsets || !W_g || !W_u || !au) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(W_g) || !al16(W_u) || !al16(au)) return MOE_ERR_INVALID_ARG;
+  if (Hs > 0) {
+    if (!Ws_g || !Ws_u || !au_s) return MOE_ERR_INVALID_ARG;
+    if (!al16(Ws_g) || !al16(Ws_u) || !al16(au_s)) return MOE_ERR_INVALID_ARG;
+  }
+  const int R = T * k;
+  SwigluFwdArgs r{nullptr, R, offsets, E, d, H, W_g, W_u, au, nullptr, RowGather{x, T, slot_of_row, k, R}};
+  SwigluFwdArgs sh{x, T, nullptr, 1, d, Hs, Ws_g, Ws_u, au_s, nullptr};
+  return check(gemm_swiglu_fwd(r, Hs > 0 ? &sh : nullptr, device_status_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
 int moe_unpermute_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
                           int T, int d, int k, void* y, void* stream) {
   if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
@@ -333,13 +392,17 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   if (rc) return rc;
   rc = check_hidden(H, Hs);
   if (rc) return rc;
-  const void* req[] = {dY_perm, gates, row_of_slot, slot_of_row, offsets, x_perm, au, W_g, W_u, W_d,
-                       dx_perm, dW_g, dW_u, dW_d, dgates};
+  // dY_perm == x_perm == NULL: the GEMMs gather the rows of dY and x
+  // themselves (the permutation fused into their loads)
+  const bool gather = dY_perm == nullptr;
+  if ((x_perm == nullptr) != gather) return MOE_ERR_INVALID_ARG;
+  const void* req[] = {gates, row_of_slot, slot_of_row, offsets, au, W_g, W_u, W_d, dx_perm, dW_g, dW_u, dW_d, dgates};
   for (const void* p : req)
     if (!p) return MOE_ERR_INVALID_ARG;
-  const void* req16[] = {dY_perm, x_perm, au, W_g, W_u, W_d, dx_perm, dW_g, dW_u, dW_d};
+  const void* req16[] = {au, W_g, W_u, W_d, dx_perm, dW_g, dW_u, dW_d};
   for (const void* p : req16)
     if (!al16(p)) return MOE_ERR_INVALID_ARG;
+  if (gather ? (!dY || !x || !al16(dY) || !al16(x)) : (!al16(dY_perm) || !al16(x_perm))) return MOE_ERR_INVALID_ARG;
   if (Hs > 0) {
     const void* req_s[] = {dY, x, au_s, Ws_g, Ws_u, Ws_d, dx_s, dWs_g, dWs_u, dWs_d};
     for (const void* p : req_s)
@@ -352,10 +415,12 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   char* w = static_cast<char*>(ws);
   const int R = T * k;
   float* dgp = reinterpret_cast<float*>(w + L.dgp);
+  const RowGather gdy = gather ? RowGather{dY, T, slot_of_row, k, R} : RowGather{};
+  const RowGather gx = gather ? RowGather{x, T, slot_of_row, k, R} : RowGather{};
 
   // 1. dgrad of the down projection with the SwiGLU backward epilogue
   DgradDownArgs r1{dY_perm, R, offsets, E, d, H, W_d, au, w + L.dau_hi, w + L.dau_lo, w + L.gh_hi, w + L.gh_lo,
-                   gates, slot_of_row, R, dgp};
+                   gates, slot_of_row, R, dgp, gdy};
   DgradDownArgs s1{dY, T, nullptr, 1, d, Hs, Ws_d, au_s, w + L.s_dau_hi, w + L.s_dau_lo, w + L.s_gh_hi,
                    w + L.s_gh_lo, nullptr, nullptr, 0, nullptr};
   cudaError_t e = gemm_dgrad_down(r1, Hs > 0 ? &s1 : nullptr, status, st);
@@ -364,7 +429,7 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   if (e != cudaSuccess) return fail_cuda(e);
 
   // 2. dW_d = dY_perm^T (g h), g h split into bf16 hi + lo
-  WgradArgs r2{dY_perm, nullptr, w + L.gh_hi, w + L.gh_lo, R, offsets, E, d, H, dW_d, nullptr, 0};
+  WgradArgs r2{dY_perm, nullptr, w + L.gh_hi, w + L.gh_lo, R, offsets, E, d, H, dW_d, nullptr, 0, gdy, 0};
   WgradArgs s2{dY, nullptr, w + L.s_gh_hi, w + L.s_gh_lo, T, nullptr, 1, d, Hs, dWs_d, nullptr, 0};
   int* tile_counter = reinterpret_cast<int*>(w + L.tile_counter);
   void* group_maps = w + L.group_maps;
@@ -380,7 +445,7 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   if (e != cudaSuccess) return fail_cuda(e);
 
   // 4. [dW_g; dW_u] = [da|du]^T x_perm, [da|du] split into bf16 hi + lo
-  WgradArgs r4{w + L.dau_hi, w + L.dau_lo, x_perm, nullptr, R, offsets, E, 2 * H, d, dW_g, dW_u, H};
+  WgradArgs r4{w + L.dau_hi, w + L.dau_lo, x_perm, nullptr, R, offsets, E, 2 * H, d, dW_g, dW_u, H, gx, 1};
   WgradArgs s4{w + L.s_dau_hi, w + L.s_dau_lo, x, nullptr, T, nullptr, 1, 2 * Hs, d, dWs_g, dWs_u, Hs};
   return check(gemm_wgrad(r4, Hs > 0 ? &s4 : nullptr, tile_counter, group_maps, status, st, "gemm_wgrad_gate_up"));
 }

@@ -160,6 +160,16 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 (cp.async.cg), and
+// the arrive on an mbarrier that fires once every cp.async this thread has
+// issued so far has landed (.noinc: the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // TMA store of one box from this CTA's shared memory (bulk-group completion:
 // bulk_commit after the stores of a group, bulk_wait_read before the source
 // buffer is written again).  Elements of the box outside the tensor's extent

@@ -226,6 +226,8 @@ __global__ void perm_scatter_kernel(const uint4* __restrict__ x, const int32_t* 
     row_of_slot[slot] = row;
     if (row >= 0) slot_of_row[row] = static_cast<int32_t>(slot);
   }
+  // maps only (x_perm == NULL: the GEMMs gather the rows themselves)
+  if (x_perm == nullptr) return;
   int rows[kMaxK];
 #pragma unroll
   for (int s = 0; s < kMaxK; ++s) rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
@@ -250,9 +252,11 @@ __global__ void perm_scatter_kernel(const uint4* __restrict__ x, const int32_t* 
 
 // ------------------------------------------------------------------ combine
 // fp32 expert / shared outputs, fp32 accumulation, one bf16 rounding of y.
+// slot_order: the expert outputs are stored by slot (o[t*k+s]) instead of by
+// permuted row
 __global__ void combine_kernel(const float4* __restrict__ o_perm, const float4* __restrict__ s_out,
                                const float* __restrict__ gates, const int32_t* __restrict__ row_of_slot, int T, int d,
-                               int k, long long max_rows, uint4* __restrict__ y, int* status) {
+                               int k, long long max_rows, int slot_order, uint4* __restrict__ y, int* status) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -261,6 +265,7 @@ __global__ void combine_kernel(const float4* __restrict__ o_perm, const float4* 
   if (lane < k) {
     row = row_of_slot[(long long)t * k + lane];
     g = gates[(long long)t * k + lane];
+    if (slot_order && row >= 0) row = t * k + lane;
     if (row >= max_rows) {
       record_status(status, MOE_ERR_DEVICE_BOUNDS);
       row = -1;
@@ -636,7 +641,7 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
   cudaError_t e = launch_permute_counts(idx, T, E, k, capacity, counts_raw, counts, offsets, nullptr, ws,
                                         &tile_base, &inrank, status, s);
   if (e != cudaSuccess) return e;
-  timing_mark(s, "perm_scatter");
+  timing_mark(s, x_perm ? "perm_scatter" : "perm_maps");
   perm_scatter_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
       static_cast<const uint4*>(x), idx, inrank, tile_base, offsets, T, d, E, k, capacity, row_of_slot, slot_of_row,
       static_cast<uint4*>(x_perm));
@@ -649,7 +654,17 @@ cudaError_t launch_combine_rows(const float* o_perm, const float* s_out, const f
   timing_mark(s, "combine");
   combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
       reinterpret_cast<const float4*>(o_perm), reinterpret_cast<const float4*>(s_out), gates, row_of_slot, T, d, k,
-      o_rows, static_cast<uint4*>(y), status);
+      o_rows, 0, static_cast<uint4*>(y), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_slots(const float* o_slot, const float* s_out, const float* gates,
+                                 const int32_t* row_of_slot, int T, int d, int k, void* y, int* status,
+                                 cudaStream_t s) {
+  timing_mark(s, "combine_slots");
+  combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+      reinterpret_cast<const float4*>(o_slot), reinterpret_cast<const float4*>(s_out), gates, row_of_slot, T, d, k,
+      (long long)T * k, 1, static_cast<uint4*>(y), status);
   return cudaGetLastError();
 }
 

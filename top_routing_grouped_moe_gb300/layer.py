@@ -20,13 +20,18 @@ class MoELayer:
     width, Hs shared hidden width (0 = none), capacity (<= 0: dropless)."""
 
     def __init__(self, T, d, E, k, H, Hs, capacity=0, device="cuda", backward=True, balance_alpha=0.0,
-                 recompute=False):
+                 recompute=False, fused=False):
         self.T, self.d, self.E, self.k, self.H, self.Hs, self.capacity = T, d, E, k, H, Hs, capacity
         self.balance_alpha = float(balance_alpha)
         # recompute: the forward saves no fp32 a|u; the backward rebuilds them
         # (moe_grouped_swiglu_recompute) into au / au_s, which then only have
         # to live through the backward call (scratch that layers can share)
         self.recompute = bool(recompute)
+        # fused: the permutation is fused into the GEMMs' operand loads (row
+        # gathers from x and dY) and the combine into the shared expert's
+        # down-projection epilogue: no x_perm, dY_perm or s; o_perm holds the
+        # expert outputs by slot (moe_grouped_swiglu_fused)
+        self.fused = bool(fused)
         dev = torch.device(device)
         R = T * k
         e = lambda *shape, dt=BF16: torch.empty(*shape, dtype=dt, device=dev)  # noqa: E731
@@ -38,13 +43,13 @@ class MoELayer:
         self.offsets = e(E + 1, dt=torch.int32)
         self.row_of_slot = e(R, dt=torch.int32)
         self.slot_of_row = e(R, dt=torch.int32)
-        self.x_perm = e(R, d)
+        self.x_perm = None if self.fused else e(R, d)
         self.au = e(R, 2 * H, dt=torch.float32) if backward else None
         self.h = e(R, H)
         self.o_perm = e(R, d, dt=torch.float32)
         self.au_s = e(T, 2 * Hs, dt=torch.float32) if (Hs and backward) else None
         self.h_s = e(T, Hs) if Hs else None
-        self.s = e(T, d, dt=torch.float32) if Hs else None
+        self.s = e(T, d, dt=torch.float32) if (Hs and not self.fused) else None
         self.y = e(T, d)
         if self.balance_alpha > 0:
             # auxiliary load-balancing loss (device scalar), mean router
@@ -55,7 +60,7 @@ class MoELayer:
         self.ws_bytes = B.moe_workspace_size(T, d, E, k, H, Hs)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         if backward:
-            self.dY_perm = e(R, d)
+            self.dY_perm = None if self.fused else e(R, d)
             self.dgates = e(T, k, dt=torch.float32)
             self.dx_perm = e(R, d, dt=torch.float32)
             self.dx_s = e(T, d, dt=torch.float32) if Hs else None
@@ -77,13 +82,19 @@ class MoELayer:
         B.moe_route_topk(x, p.get("W_r"), p.get("bias"), logits_in, T, d, E, k,
                          None if logits_in is not None else self.logits, self.idx, self.gates,
                          self.ws, self.ws_bytes, stream)
-        B.moe_permute(x, self.idx, T, d, E, k, self.capacity, self.counts_raw, self.counts, self.offsets,
-                      self.row_of_slot, self.slot_of_row, self.x_perm, self.ws, self.ws_bytes, stream)
+        B.moe_permute(None if self.fused else x, self.idx, T, d, E, k, self.capacity, self.counts_raw, self.counts,
+                      self.offsets, self.row_of_slot, self.slot_of_row, self.x_perm, self.ws, self.ws_bytes, stream)
         if self.balance_alpha > 0:
             B.moe_router_balance_loss(logits_in if logits_in is not None else self.logits, self.counts_raw, T, E, k,
                                       self.balance_alpha, self.lbl_loss, self.lbl_P, self.dlogits_lbl, self.ws,
                                       self.ws_bytes, stream)
         save = not self.recompute
+        if self.fused:
+            B.moe_grouped_swiglu_fused(x, self.slot_of_row, self.row_of_slot, self.gates, self.offsets, T, d, E, k, H,
+                                       Hs, p["W_g"], p["W_u"], p["W_d"], p.get("Ws_g"), p.get("Ws_u"), p.get("Ws_d"),
+                                       self.au if save else None, self.h, self.o_perm,
+                                       self.au_s if save else None, self.h_s, self.y, stream)
+            return self.y
         B.moe_grouped_swiglu(self.x_perm, self.offsets, x, T, d, E, k, H, Hs, p["W_g"], p["W_u"], p["W_d"],
                              p.get("Ws_g"), p.get("Ws_u"), p.get("Ws_d"), self.au if save else None, self.h,
                              self.o_perm, self.au_s if save else None, self.h_s, self.s, self.ws, self.ws_bytes,
@@ -97,10 +108,14 @@ class MoELayer:
         balance_alpha > 0 the load-balancing loss's gradient is included in
         dlogits, dW_r and dx."""
         T, d, E, k, H, Hs = self.T, self.d, self.E, self.k, self.H, self.Hs
-        if self.recompute:
+        if self.recompute and self.fused:
+            B.moe_grouped_swiglu_recompute_fused(x, self.slot_of_row, self.offsets, T, d, E, k, H, Hs, p["W_g"],
+                                                 p["W_u"], p.get("Ws_g"), p.get("Ws_u"), self.au, self.au_s, stream)
+        elif self.recompute:
             B.moe_grouped_swiglu_recompute(self.x_perm, self.offsets, x, T, d, E, k, H, Hs, p["W_g"], p["W_u"],
                                            p.get("Ws_g"), p.get("Ws_u"), self.au, self.au_s, stream)
-        B.moe_unpermute_combine_bwd(dY, self.row_of_slot, T, d, k, self.dY_perm, stream)
+        if not self.fused:
+            B.moe_unpermute_combine_bwd(dY, self.row_of_slot, T, d, k, self.dY_perm, stream)
         B.moe_grouped_swiglu_bwd(self.dY_perm, dY, self.gates, self.row_of_slot, self.slot_of_row, self.offsets,
                                  self.x_perm, x, self.au, self.au_s, T, d, E, k, H, Hs, p["W_g"], p["W_u"],
                                  p["W_d"], p.get("Ws_g"), p.get("Ws_u"), p.get("Ws_d"), self.dx_perm, self.dx_s,
