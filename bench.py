@@ -620,17 +620,29 @@ def main_ours(args):
         h2d = pin["x"].numel() * 2 + pin["dY"].numel() * 2 + (pin["logits_in"].numel() * 4 if lin is not None else 0)
         d2h = 2 * T * d * 2
 
+        # a second stream carries the transfers that need not wait: dY's
+        # upload runs beside the forward, y's download beside the backward
+        side = torch.cuda.Stream()
+
         def e2e_step():
+            main = torch.cuda.current_stream()
             xin.copy_(pin["x"], non_blocking=True)
-            dyin.copy_(pin["dY"], non_blocking=True)
             if lin is not None:
                 lin.copy_(pin["logits_in"], non_blocking=True)
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                dyin.copy_(pin["dY"], non_blocking=True)
             p = dict(dev)
             layer.forward(xin, p, logits_in=lin)
+            fwd_done = main.record_event()
+            main.wait_stream(side)
+            with torch.cuda.stream(side):
+                side.wait_event(fwd_done)
+                y_host.copy_(layer.y, non_blocking=True)
             layer.backward(xin, dyin, p, learned_router=learned)
-            y_host.copy_(layer.y, non_blocking=True)
             dx_host.copy_(layer.dx, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+            main.synchronize()
+            side.synchronize()
 
         for _ in range(3):
             e2e_step()
