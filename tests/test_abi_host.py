@@ -106,6 +106,29 @@ P = 1 << 12  # stand-in device addresses (16-byte aligned); never dereferenced
     (lambda L: L.moe_router_balance_loss(P, P, 16, 12, 2, 0.02, P, None, None, P, 1 << 20, 0), 2),
     # balance loss: workspace too small
     (lambda L: L.moe_router_balance_loss(P, P, 4096, 64, 2, 0.02, P, None, None, P, 16, 0), 3),
+    # fused forward: no x to gather from
+    (lambda L: L.moe_grouped_swiglu_fused(None, P, P, P, P, 16, 128, 8, 2, 128, 128, P, P, P, P, P, P, None, P, P,
+                                          None, P, P, 0), 1),
+    # fused forward: shared expert without its hidden buffer
+    (lambda L: L.moe_grouped_swiglu_fused(P, P, P, P, P, 16, 128, 8, 2, 128, 128, P, P, P, P, P, P, None, P, P,
+                                          None, None, P, 0), 1),
+    # fused forward: misaligned expert-output buffer
+    (lambda L: L.moe_grouped_swiglu_fused(P, P, P, P, P, 16, 128, 8, 2, 128, 0, P, P, P, None, None, None, None,
+                                          P, P + 4, None, None, P, 0), 1),
+    # fused forward: hidden width not a multiple of 128
+    (lambda L: L.moe_grouped_swiglu_fused(P, P, P, P, P, 16, 128, 8, 2, 96, 0, P, P, P, None, None, None, None,
+                                          P, P, None, None, P, 0), 2),
+    # fused recompute: no slot map
+    (lambda L: L.moe_grouped_swiglu_recompute_fused(P, None, P, 16, 128, 8, 2, 128, 0, P, P, None, None, P, None,
+                                                    0), 1),
+    # backward: x_perm given, dY_perm not (neither the copied nor the gather form)
+    (lambda L: L.moe_grouped_swiglu_bwd(None, P, P, P, P, P, P, P, P, P, 16, 128, 8, 2, 128, 128, P, P, P, P, P, P,
+                                        P, P, P, P, P, P, P, P, P, P, 1 << 30, 0), 1),
+    # backward, gather form: no dY to gather from
+    (lambda L: L.moe_grouped_swiglu_bwd(None, None, P, P, P, P, None, P, P, P, 16, 128, 8, 2, 128, 0, P, P, P,
+                                        None, None, None, P, None, P, P, P, None, None, None, P, P, 1 << 30, 0), 1),
+    # permute, maps only: still needs its maps
+    (lambda L: L.moe_permute(None, P, 16, 128, 64, 4, 0, P, P, P, None, P, None, P, 1 << 20, 0), 1),
 ])
 def test_argument_errors_are_reported_on_the_host(lib, call, expect):
     with pytest.raises(lib.MoEError) as e:
