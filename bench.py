@@ -74,6 +74,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--path", default="unfused", choices=["fused", "unfused"])
+    ap.add_argument("--no-other-path", action="store_true", help="do not time the other call sequence")
     return ap.parse_args()
 
 
@@ -393,8 +394,9 @@ def main_ours(args):
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
         step(main_stream)
-        flush.fill_(1)
-        other_step(main_stream)
+        if not args.no_other_path:
+            flush.fill_(1)
+            other_step(main_stream)
     torch.cuda.synchronize()
     st = B.moe_device_status()
     if st != 0:
@@ -425,8 +427,10 @@ def main_ours(args):
     # ---- the step (and the forward alone) as CUDA-graph replays
     gstream = torch.cuda.Stream()
     graphs = {}
-    for gname, fn in (("step", step), ("forward", forward), ("other_step", other_step),
-                      ("other_forward", other_forward)):
+    graph_fns = [("step", step), ("forward", forward)]
+    if not args.no_other_path:
+        graph_fns += [("other_step", other_step), ("other_forward", other_forward)]
+    for gname, fn in graph_fns:
         gstream.wait_stream(main_stream)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=gstream):
@@ -465,8 +469,8 @@ def main_ours(args):
     wall = time.perf_counter() - wall0
     fwd_ms = replay_ms(graphs["forward"])
     clocks = sampler.stop()
-    other_ms = replay_ms(graphs["other_step"])
-    other_fwd_ms = replay_ms(graphs["other_forward"])
+    other_ms = replay_ms(graphs["other_step"]) if "other_step" in graphs else None
+    other_fwd_ms = replay_ms(graphs["other_forward"]) if "other_forward" in graphs else None
     value = tokens_per_s(T, args.steps, world, graph_ms)
     fwd_value = tokens_per_s(T, args.steps, world, fwd_ms)
 
@@ -673,12 +677,13 @@ def main_ours(args):
                                  "steps, timed by events the library records before each launch"},
             "fwd_tokens_per_s": fwd_value,
             "path": args.path,
-            "other_path": {"path": other, "tokens_per_s": tokens_per_s(T, args.steps, world, other_ms),
-                           "ms_per_step": other_ms / args.steps,
-                           "fwd_tokens_per_s": tokens_per_s(T, args.steps, world, other_fwd_ms),
-                           "fwd_ms_per_step": other_fwd_ms / args.steps,
-                           "note": "the same step through the other call sequence (identical results); "
-                                   "graph replay, L2 flushed before each"},
+            "other_path": None if other_ms is None else {
+                "path": other, "tokens_per_s": tokens_per_s(T, args.steps, world, other_ms),
+                "ms_per_step": other_ms / args.steps,
+                "fwd_tokens_per_s": tokens_per_s(T, args.steps, world, other_fwd_ms),
+                "fwd_ms_per_step": other_fwd_ms / args.steps,
+                "note": "the same step through the other call sequence (identical results); "
+                        "graph replay, L2 flushed before each"},
             "mxfp8_forward": mx_fwd,
             "fwd_ms_per_step": fwd_ms / args.steps,
             "eager": {"value": tokens_per_s(T, args.steps, world, eager_total), "ms_per_step": step_eager},
