@@ -72,7 +72,11 @@ enum {
   MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
   MOE_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
   MOE_ERR_TIMEOUT = 5,      /* device status: a bounded wait expired */
-  MOE_ERR_DEVICE_BOUNDS = 6 /* device status: an index was out of range */
+  MOE_ERR_DEVICE_BOUNDS = 6, /* device status: an index was out of range */
+  MOE_ERR_RANGE = 7          /* device status: a per-token sum (combine, input
+                                gradient) was not finite: one of its fp16 terms
+                                was beyond the fp16 range (|v| > 65504, stored
+                                as inf) or a value upstream was inf / NaN */
 };
 
 /* Library version, (major << 16) | minor.  No side effects. */
@@ -191,10 +195,14 @@ MOE_API int moe_permute_static(const void* x, const int32_t* topk_idx, int T, in
  *   au [T*k, 2H] FP32 receives a in columns [0,H) and u in [H,2H), kept for
  *   the backward pass (may be NULL when no backward follows);
  *   h [T*k, H] bf16 (the down projection's input, required);
- *   o_perm [T*k, d] FP32 (kept in fp32 so that the combine adds unrounded
- *   expert outputs).
+ *   o_perm [T*k, d] FP16: the terms of the combine's per-token sum.  fp16
+ *   carries 11 significant bits where bf16 carries 8: with bf16 terms the
+ *   summed y reaches the edge of the parity bound at d = 4096 (their
+ *   rounding adds up where the terms cancel), with fp16 it stays where fp32
+ *   terms leave it.  A term beyond the fp16 range (|v| > 65504) is stored
+ *   as inf; the combine then records MOE_ERR_RANGE in the device status.
  *   Shared expert (Hs > 0): the same on every token of x [T,d] with Ws_*,
- *   writing au_s [T,2Hs] fp32 (nullable), h_s [T,Hs] bf16 and s [T,d] fp32.
+ *   writing au_s [T,2Hs] fp32 (nullable), h_s [T,Hs] bf16 and s [T,d] fp16.
  *   Hs == 0: the shared pointers are ignored.
  * Tensor-core (tcgen05) grouped GEMMs fed by TMA; the per-expert tile
  * schedule is read from `offsets` on the device.  ws is unused (may be NULL). */
@@ -202,8 +210,8 @@ MOE_API int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const
                        int T, int d, int E, int k, int H, int Hs,
                        const void* W_g, const void* W_u, const void* W_d,
                        const void* Ws_g, const void* Ws_u, const void* Ws_d,
-                       float* au, void* h, float* o_perm,
-                       float* au_s, void* h_s, float* s,
+                       float* au, void* h, void* o_perm,
+                       float* au_s, void* h_s, void* s,
                        void* ws, size_t ws_bytes, void* stream);
 
 /* Activation recompute for the backward ("Olmo-core DDP MoE examples"
@@ -234,12 +242,13 @@ MOE_API int moe_grouped_swiglu_recompute(const void* x_perm, const int32_t* offs
  *     r is token slot_of_row[r] / k, copied 16 bytes per thread (cp.async)
  *     into the tile's swizzled layout; the gathering GEMMs run on single CTAs
  *     (128-row tiles);
- *   - the routed down projection stores row r's fp32 output at its slot:
- *     o_slot[slot_of_row[r]] ([T*k, d] fp32; rows of dropped slots are not
+ *   - the routed down projection stores row r's output at its slot:
+ *     o_slot[slot_of_row[r]] ([T*k, d] fp16; rows of dropped slots are not
  *     written);
  *   - the shared expert's down projection (a second launch on the stream)
  *     adds, in its epilogue, the gate-weighted kept slots of each token in
- *     slot order to its fp32 accumulator s[t] and writes y[t] in bf16 once:
+ *     slot order to its accumulator s[t] (rounded through fp16, as the
+ *     unfused path stores s) and writes y[t] in bf16 once:
  *       y[t] = bf16(s[t] + sum_{j kept} gates[t,j] o_slot[t*k+j])
  *     -- the same operations in the same order as moe_unpermute_combine, so y
  *     is bit-identical to the unfused path's.  Hs == 0: a combine pass over
@@ -254,7 +263,7 @@ MOE_API int moe_grouped_swiglu_recompute(const void* x_perm, const int32_t* offs
 MOE_API int moe_grouped_swiglu_fused(const void* x, const int32_t* slot_of_row, const int32_t* row_of_slot,
                                      const float* gates, const int32_t* offsets, int T, int d, int E, int k, int H,
                                      int Hs, const void* W_g, const void* W_u, const void* W_d, const void* Ws_g,
-                                     const void* Ws_u, const void* Ws_d, float* au, void* h, float* o_slot,
+                                     const void* Ws_u, const void* Ws_d, float* au, void* h, void* o_slot,
                                      float* au_s, void* h_s, void* y, void* stream);
 
 /* moe_grouped_swiglu_recompute for the fused path: the routed rows are
@@ -267,9 +276,10 @@ MOE_API int moe_grouped_swiglu_recompute_fused(const void* x, const int32_t* slo
 
 /* Gate-weighted unpermute and combine:
  *   y[t,:] = s[t,:] + sum_{s kept} gates[t,s] * o_perm[row_of_slot[t*k+s], :]
- * o_perm [T*k,d] and s [T,d] fp32 (s may be NULL: no shared expert); fp32
- * accumulation, one bf16 rounding: y [T,d] bf16. */
-MOE_API int moe_unpermute_combine(const float* o_perm, const float* s, const float* gates,
+ * o_perm [T*k,d] and s [T,d] fp16 (s may be NULL: no shared expert); fp32
+ * accumulation in slot order, one bf16 rounding: y [T,d] bf16.  A
+ * non-finite sum records MOE_ERR_RANGE in the device status. */
+MOE_API int moe_unpermute_combine(const void* o_perm, const void* s, const float* gates,
                           const int32_t* row_of_slot, int T, int d, int k,
                           void* y, void* stream);
 
@@ -320,8 +330,10 @@ MOE_API int moe_unpermute_combine_bwd(const void* dY, const int32_t* row_of_slot
  * and the same for the shared expert over all T tokens with g = 1 (no gate
  * gradient).  The products take their derived operand (g h, da | du) as a
  * bf16 hi + lo pair, so the result keeps ~16 bits over sums of thousands of
- * rows (weight gradients) or of 2H products (input gradients).  Outputs: dx_perm [T*k,d] and dx_s [T,d] in fp32 (summed
- * per token by moe_permute_bwd before any rounding), dW_g, dW_u [E,H,d],
+ * rows (weight gradients) or of 2H products (input gradients).  Outputs: dx_perm [T*k,d] and dx_s [T,d] in fp16 (the
+ * terms of moe_permute_bwd's per-token sum, as o_perm for the combine; a
+ * term beyond the fp16 range makes that sum report MOE_ERR_RANGE), dW_g,
+ * dW_u [E,H,d],
  * dW_d [E,d,H] (zero for experts with no rows), dWs_g, dWs_u [Hs,d],
  * dWs_d [d,Hs] (all bf16) and dgates [T,k] fp32 (0 for dropped slots).  Each
  * output element is owned by one tile: no atomics, deterministic.
@@ -339,7 +351,7 @@ MOE_API int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const fl
                            int T, int d, int E, int k, int H, int Hs,
                            const void* W_g, const void* W_u, const void* W_d,
                            const void* Ws_g, const void* Ws_u, const void* Ws_d,
-                           float* dx_perm, float* dx_s,
+                           void* dx_perm, void* dx_s,
                            void* dW_g, void* dW_u, void* dW_d,
                            void* dWs_g, void* dWs_u, void* dWs_d,
                            float* dgates, void* ws, size_t ws_bytes, void* stream);
@@ -384,11 +396,13 @@ MOE_API int moe_router_balance_loss(const float* logits, const int32_t* counts_r
  * gradient:
  *   dx[t,:] = sum_{s kept} dx_perm[row_of_slot[t*k+s], :] + dx_s[t,:]
  *             + sum_e dlogits[t,e] W_r[e,:]
- * dx_perm [T*k,d] and dx_s [T,d] fp32; fp32 accumulation, one bf16 rounding:
- * dx [T,d] bf16.  dx_s may be NULL (no shared expert); dlogits and W_r may
- * both be NULL (given-logits routing).  The router term uses the tensor
- * cores with dlogits as a bf16 hi + lo pair. */
-MOE_API int moe_permute_bwd(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot,
+ * dx_perm [T*k,d] and dx_s [T,d] fp16 (from moe_grouped_swiglu_bwd); fp32
+ * accumulation, one bf16 rounding: dx [T,d] bf16 (a non-finite sum records
+ * MOE_ERR_RANGE).  dx_s may be NULL (no
+ * shared expert); dlogits and W_r may both be NULL (given-logits routing).
+ * The router term uses the tensor cores with dlogits as a bf16 hi + lo pair
+ * and enters the sum as an fp16 term. */
+MOE_API int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot,
                     const float* dlogits, const void* W_r,
                     int T, int d, int E, int k, void* dx,
                     void* ws, size_t ws_bytes, void* stream);

@@ -124,7 +124,7 @@ def test_identity_expert_combine(B, cap):
     idx, g = run_topk(B, l, k)
     x_bits = gen.normal_bf16(305, (T, d))
     p = run_permute(B, x_bits, idx, E, cap)
-    x_perm = dev_bf16(p["x_perm"]).float()   # expert outputs are fp32
+    x_perm = dev_bf16(p["x_perm"]).half()   # expert outputs are fp16 (bf16 values of this size convert exactly)
     y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
     B.moe_unpermute_combine(x_perm, None, dev_f32(g), torch.from_numpy(p["row_of_slot"]).cuda(), T, d, k, y)
     torch.cuda.synchronize()
@@ -146,9 +146,10 @@ def test_combine_bwd_gather_and_reduce(B):
     row = torch.from_numpy(p["row_of_slot"]).cuda()
     dYp = torch.zeros(T * k, d, dtype=torch.bfloat16, device="cuda")
     B.moe_unpermute_combine_bwd(dev_bf16(dY_bits), row, T, d, k, dYp)
-    # reduce: dx = sum_s dx_perm[row] + dx_s, with dx_perm = o, dx_s = dY (fp32 inputs)
+    # reduce: dx = sum_s dx_perm[row] + dx_s, with dx_perm = o, dx_s = dY (fp16 inputs: the bf16 values of
+    # this size convert exactly)
     dx = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
-    B.moe_permute_bwd(dev_bf16(o_bits).float(), dev_bf16(dY_bits).float(), row, None, None, T, d, E, k, dx, None, 0)
+    B.moe_permute_bwd(dev_bf16(o_bits).half(), dev_bf16(dY_bits).half(), row, None, None, T, d, E, k, dx, None, 0)
     torch.cuda.synchronize()
     # the oracle routes the same generator logits on its own
     ridx, rg = orc.route_topk(l, k)
@@ -173,3 +174,33 @@ def test_router_bwd_dlogits(B):
     ridx, rg = orc.route_topk(l, k)
     ref = orc.topk_bwd(rg, ridx, dg.astype(np.float64), E)
     np.testing.assert_allclose(dl.cpu().numpy(), ref, rtol=1e-5, atol=1e-6)
+
+
+def test_sum_terms_out_of_fp16_range_are_reported(B):
+    """The per-token sums read fp16 terms: a term beyond the fp16 range is
+    stored as inf, and the combine and the unpermute reduce then report
+    MOE_ERR_RANGE in the device status (an inf planted here on the host); a
+    finite sum reports nothing."""
+    T, E, k, d = 64, 8, 2, 128
+    l = gen.random_logits(T, E, tensor=310)
+    idx, g = run_topk(B, l, k)
+    x_bits = gen.normal_bf16(311, (T, d))
+    p = run_permute(B, x_bits, idx, E, 0)
+    row = torch.from_numpy(p["row_of_slot"]).cuda()
+    terms = dev_bf16(gen.normal_bf16(312, (T * k, d))).half()
+    y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    assert B.moe_device_status() == 0
+    B.moe_unpermute_combine(terms, None, dev_f32(g), row, T, d, k, y)
+    torch.cuda.synchronize()
+    assert B.moe_device_status() == 0
+    kept_row = int(p["row_of_slot"][0])
+    assert kept_row >= 0
+    terms[kept_row, 5] = float("inf")
+    B.moe_unpermute_combine(terms, None, dev_f32(g), row, T, d, k, y)
+    torch.cuda.synchronize()
+    assert B.moe_device_status() == B.MOE_ERR_RANGE
+    dx = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    B.moe_permute_bwd(terms, None, row, None, None, T, d, E, k, dx, None, 0)
+    torch.cuda.synchronize()
+    assert B.moe_device_status() == B.MOE_ERR_RANGE
+    assert B.moe_device_status() == 0  # read and cleared

@@ -20,6 +20,7 @@ MOE_ERR_WORKSPACE = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_TIMEOUT = 5
 MOE_ERR_DEVICE_BOUNDS = 6
+MOE_ERR_RANGE = 7
 
 
 class MoEError(RuntimeError):

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -42,6 +43,26 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 }
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+}
+
+// fp16 storage of the terms of a per-token sum (expert outputs, the shared
+// output, input-gradient terms): four values rounded to nearest even; one
+// beyond the fp16 range becomes inf, which the kernel that sums the terms
+// finds in its sum and reports.
+__device__ __forceinline__ uint2 f16x4(const float4& v) {
+  const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+// 4 fp16 (one uint2) -> fp32
+__device__ __forceinline__ float4 unpack_f16x4(const uint2& v) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+// 8 fp16 (one uint4) -> fp32
+__device__ __forceinline__ void unpack_f16x8(const uint4& v, float (&f)[8]) {
+  const float4 a = unpack_f16x4(make_uint2(v.x, v.y)), b = unpack_f16x4(make_uint2(v.z, v.w));
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
 // v = hi + lo with hi = bf16(v), lo = bf16(v - hi): about 16 significant bits

@@ -127,6 +127,7 @@ struct Problem {
   void* aux;           // SWIGLU_FWD: au out; SWIGLU_BWD: au in
   long long ld_aux;
   const float* bias;   // EPI_F32 (nullable)
+  int out_f16;         // EPI_F32: out holds fp16 (a value beyond its range records MOE_ERR_RANGE)
   int H;               // SWIGLU: column offset of u within au
   // EPI_SWIGLU_BWD
   const float* gates;      // per-slot gate (nullable: g = 1)
@@ -161,7 +162,7 @@ struct Problem {
   // EPI_F32, the shared expert's down projection with the combine fused in
   // (comb_y != NULL): instead of s, y[t] = bf16(s[t] + sum over kept slots
   // (t,j) of gates[t,j] o_slot[t*k+j]), the sum taken in slot order
-  const float* comb_o;          // [T*k, ldo] fp32 expert outputs in slot order
+  const void* comb_o;           // [T*k, ldo] fp16 expert outputs in slot order
   const float* comb_gates;      // [T*k]
   const int* comb_row_of_slot;  // [T*k]: slot kept iff >= 0
   int comb_k;
@@ -405,17 +406,6 @@ __device__ void build_schedule(const Params& P, Sched& S) {
 // IEEE-exact division here was most of the SwiGLU epilogues' time).  For
 // a < -87 the denominator overflows and the result is 0, the right limit.
 __device__ __forceinline__ float sigmoidf_(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
-
-template <int EPI>
-struct OutSel {
-  using type = __nv_bfloat16;
-};
-template <>
-struct OutSel<EPI_F32> {
-  using type = float;
-};
-template <int EPI>
-using OutT = typename OutSel<EPI>::type;
 
 // Epilogue register layout ("quad layout"): for a warp's 32 rows x 32
 // columns, lane l holds, for j = 0..7, the four consecutive columns
@@ -1092,32 +1082,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
         }
       } else if (EPI == EPI_F32) {
         long long base;  // element offset of (row0, 0)
-        OutT<EPI>* outp;
+        void* outv;
         if (MODE == KGROUP && pr.row_split > 0 && m_cta >= pr.row_split) {
-          outp = reinterpret_cast<OutT<EPI>*>(pr.out2);
+          outv = pr.out2;
           base = ti.g * pr.gstride + (long long)(row0 - pr.row_split) * pr.ldo;
         } else {
-          outp = reinterpret_cast<OutT<EPI>*>(pr.out);
+          outv = pr.out;
           base = (MODE == KGROUP ? ti.g * pr.gstride : 0) + (long long)row0 * pr.ldo;
         }
-        // ragged M with a row map: this thread's eight rows 4 j + rs go to
-        // output rows orow[j] (-1: not stored)
+        // out: fp32, or (out_f16) fp16 terms of a per-token sum
+        // element offset of each of this thread's eight rows 4 j + rs (-1: not
+        // stored): row base + r, or with a row map (ragged M) out_row_map[r]
         const bool mapped = MODE == MGROUP && pr.out_row_map != nullptr;
-        int orow[8];
-        if (mapped) {
+        long long roff[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int r = 4 * j + rs;
-            orow[j] = -1;
-            if (r < nrows) {
+        for (int j = 0; j < 8; ++j) {
+          const int r = 4 * j + rs;
+          roff[j] = -1;
+          if (r < nrows) {
+            if (mapped) {
               const int v = __ldg(pr.out_row_map + row0 + r);
               if (v < 0 || v >= pr.out_map_rows) record_status(P.status, MOE_ERR_DEVICE_BOUNDS);
-              else orow[j] = v;
+              else roff[j] = (long long)v * pr.ldo;
+            } else {
+              roff[j] = base + (long long)r * pr.ldo;
             }
           }
         }
         const bool comb = MODE == MGROUP && pr.comb_y != nullptr;
         const int ck = pr.comb_k;
+        const __half* comb_o = reinterpret_cast<const __half*>(pr.comb_o);
         const int c_end = ti.half ? col_shift + pr.mma_n / 2 : pr.n_tile;
         for (int c0 = col_shift; c0 < c_end; c0 += 32) {
           if (ti.n0 + c0 >= pr.N) break;
@@ -1125,22 +1119,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           if (has_acc) tmem_chunk_quad(taddr + c0 - col_shift, tb, lane, v);
           else zero_quad(v);
           const int col = ti.n0 + c0 + cq;
-          const bool col_ok = col < pr.N;  // N is a multiple of 4
-          float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (EPI == EPI_F32 && pr.bias && col_ok) b = __ldg(reinterpret_cast<const float4*>(pr.bias + col));
+          if (col >= pr.N) continue;  // N is a multiple of 4
+          if (EPI == EPI_F32 && pr.bias) {
+            const float4 b = __ldg(reinterpret_cast<const float4*>(pr.bias + col));
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int r = 4 * j + rs;
-            if (r >= nrows || !col_ok) continue;
-            float4 a = make_float4(v[j].x + b.x, v[j].y + b.y, v[j].z + b.z, v[j].w + b.w);
-            if (comb) {
-              // token t = row0 + r: its kept slots' expert outputs, gate-
-              // weighted, added in slot order (the combine's own order)
+            for (int j = 0; j < 8; ++j) v[j] = make_float4(v[j].x + b.x, v[j].y + b.y, v[j].z + b.z, v[j].w + b.w);
+          }
+          if (comb) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int r = 4 * j + rs;
+              if (r >= nrows) continue;
+              // token t = row0 + r: s rounded through fp16 (as the unfused
+              // path stores it), then its kept slots' expert outputs, gate-
+              // weighted, added in slot order (the combine's own order); a
+              // non-finite sum (a term beyond the fp16 range) is reported
+              float4 a = unpack_f16x4(f16x4(v[j]));
               const long long slot0 = (long long)(row0 + r) * ck;
               float4 o[kMaxK];
 #pragma unroll
               for (int q = 0; q < kMaxK; ++q)
-                if (q < ck) o[q] = __ldg(reinterpret_cast<const float4*>(pr.comb_o + (slot0 + q) * pr.ldo + col));
+                if (q < ck) o[q] = unpack_f16x4(__ldg(reinterpret_cast<const uint2*>(comb_o + (slot0 + q) * pr.ldo + col)));
 #pragma unroll
               for (int q = 0; q < kMaxK; ++q) {
                 if (q >= ck) break;
@@ -1149,12 +1148,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
                 a = make_float4(fmaf(gq, o[q].x, a.x), fmaf(gq, o[q].y, a.y), fmaf(gq, o[q].z, a.z),
                                 fmaf(gq, o[q].w, a.w));
               }
+              if (!(isfinite(a.x) && isfinite(a.y) && isfinite(a.z) && isfinite(a.w)))
+                record_status(P.status, MOE_ERR_RANGE);
               store4(reinterpret_cast<__nv_bfloat16*>(pr.comb_y) + (long long)(row0 + r) * pr.ldo + col, a);
-            } else if (mapped) {
-              if (orow[j] >= 0) store4(outp + (long long)orow[j] * pr.ldo + col, a);
-            } else {
-              store4(outp + base + (long long)r * pr.ldo + col, a);
             }
+          } else if (pr.out_f16) {
+            // fp16 terms of a per-token sum
+            __half* outp = reinterpret_cast<__half*>(outv) + col;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (roff[j] >= 0) *reinterpret_cast<uint2*>(outp + roff[j]) = f16x4(v[j]);
+          } else {
+            float* outp = reinterpret_cast<float*>(outv) + col;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (roff[j] >= 0) store4(outp + roff[j], v[j]);
           }
         }
       } else if (EPI == EPI_SWIGLU_FWD && MX) {

@@ -86,6 +86,7 @@ bool fill_dgrad_gu(Params& P, Problem& pr, const DgradGuArgs& a) {
   pr.ksplit = a.H;
   pr.tx_bytes = A_BYTES + PairCfg<kPair>::B_BYTES;
   pr.out = a.dx;
+  pr.out_f16 = 1;  // input-gradient rows: fp16 terms of the unpermute's sum
   pr.ldo = a.d;
   return true;
 }

@@ -63,6 +63,7 @@ bool fill_down_fwd(Params& P, Problem& pr, const DownFwdArgs& a) {
   pr.map_b = ib;
   pr.tx_bytes = A_BYTES + b_bytes(pair);
   pr.out = a.o;
+  pr.out_f16 = 1;  // expert / shared outputs: fp16 terms of the combine's sum
   pr.ldo = a.d;
   pr.out_row_map = a.out_row_map;
   pr.out_map_rows = a.out_map_rows;

@@ -51,8 +51,8 @@ cudaError_t launch_permute_mx(const void* x, const int32_t* idx, int T, int d, i
                               int32_t* counts_raw, int32_t* counts, int32_t* offsets, int32_t* mx_offsets,
                               int32_t* row_of_slot, int32_t* slot_of_row, void* codes, void* scales, void* ws,
                               int* status, cudaStream_t s);
-// o_perm, s_out fp32; y bf16
-cudaError_t launch_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
+// o_perm, s_out fp16 (the per-token sum terms); y bf16
+cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
                            int T, int d, int k, void* y, int* status, cudaStream_t s);
 // dY_perm[row_of_slot[t*k+s]] = dY[t] for every kept slot
 cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
@@ -63,9 +63,9 @@ inline int dgp_slots(int H) { return 2 * ((H + 255) / 256); }
 // dgates[t,s] = sum_p dgp[row_of_slot[t*k+s], p] (0 for dropped slots)
 cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_slot, int T, int k, float* dgates,
                                  cudaStream_t s);
-// dx[t] = sum_s dx_perm[row(t,s)] + dx_s[t] + dx_r[t]   (fp32 terms, dx_s and dx_r
-// nullable; dx bf16)
-cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const float* dx_r,
+// dx[t] = sum_s dx_perm[row(t,s)] + dx_s[t] + dx_r[t]   (fp16 terms, fp32 sum;
+// dx_s and dx_r nullable; dx bf16)
+cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const void* dx_r,
                                     const int32_t* row_of_slot, int T, int d, int k, void* dx, int* status,
                                     cudaStream_t s);
 // dlogits [T,E] fp32 (dense, + add[T,E] if add != NULL) and, if dl_hi != NULL,
@@ -109,12 +109,12 @@ struct DownFwdArgs {
   const int32_t* offsets;
   int G, d, H;
   const void* Wd;       // [G, d, H]
-  float* o;             // [rows, d] fp32 (unused with comb_y)
+  void* o;              // [rows, d] fp16 (unused with comb_y)
   const int32_t* out_row_map;  // row r stored at row out_row_map[r] of o (NULL: r)
   int out_map_rows;            // rows of o with a row map
   // combine fused into this (dense, shared-expert) problem's epilogue:
   // y[t] = bf16(o[t] + sum_{kept j} gates[t,j] comb_o[t*k+j]), o not stored
-  const float* comb_o;         // [T*k, d] fp32, slot order
+  const void* comb_o;          // [T*k, d] fp16, slot order
   const float* comb_gates;
   const int32_t* comb_row_of_slot;
   int comb_k;
@@ -152,7 +152,7 @@ struct DgradGuArgs {      // dx = (dau_hi + dau_lo) [W_g; W_u]
   int G, d, H;
   const void* Wg;         // [G, H, d]
   const void* Wu;
-  float* dx;              // [rows, d] fp32
+  void* dx;               // [rows, d] fp16
 };
 struct WgradArgs {        // out[g] = A_g^T B_g over rows [off[g], off[g+1])
   const void* A;          // [rows, M] bf16
@@ -186,9 +186,9 @@ cudaError_t launch_group_maps(const CUtensorMap* whole, const CUtensorMap* whole
 // dW_r partials: part[S, E, d] = split-K pieces of (dl_hi + dl_lo)^T x; dl halves [T, E] bf16
 cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* x, int T, int d, int E, int S,
                            float* part, int* status, cudaStream_t s);
-// dx_r [T, d] fp32 = (dl_hi + dl_lo) W_r, the router's term of the input gradient
+// dx_r [T, d] fp16 = (dl_hi + dl_lo) W_r, the router's term of the input gradient
 cudaError_t gemm_router_dx(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, int T, int d, int E,
-                           float* dx_r, int* status, cudaStream_t s);
+                           void* dx_r, int* status, cudaStream_t s);
 
 // MXFP8 expert GEMMs (E4M3 operands, tile-atom E8M0 scales).  A: [rows_total,
 // K] codes; rows of group g start at offsets[g] (a multiple of 128, or dense
@@ -210,12 +210,13 @@ struct MxGemmArgs {
 };
 cudaError_t gemm_mx_swiglu(const MxGemmArgs& routed, const MxGemmArgs* shared, cudaStream_t s);
 cudaError_t gemm_mx_down(const MxGemmArgs& routed, const MxGemmArgs* shared, cudaStream_t s);
-cudaError_t launch_combine_rows(const float* o_perm, const float* s_out, const float* gates,
+// o_perm, s_out fp16 (f16) or fp32 (the MXFP8 path), o_rows rows of o_perm
+cudaError_t launch_combine_rows(const void* o_perm, const void* s_out, bool f16, const float* gates,
                                 const int32_t* row_of_slot, int T, int d, int k, long long o_rows, void* y,
                                 int* status, cudaStream_t s);
 // the same with the expert outputs stored by slot: y[t] = s[t] + sum_{kept j}
 // g[t,j] o_slot[t*k+j]
-cudaError_t launch_combine_slots(const float* o_slot, const float* s_out, const float* gates,
+cudaError_t launch_combine_slots(const void* o_slot, const void* s_out, const float* gates,
                                  const int32_t* row_of_slot, int T, int d, int k, void* y, int* status,
                                  cudaStream_t s);
 

@@ -47,7 +47,7 @@ size_t ws_route_topk_bwd(int T, int d, int E) {
   return 2 * align256((size_t)T * E * 2) + (S > 1 ? align256((size_t)S * E * d * 4) : 0);
 }
 // dlogits as bf16 hi + lo [T,E] x2, the router's fp32 term of dx [T,d]
-size_t ws_permute_bwd(int T, int d, int E) { return 2 * align256((size_t)T * E * 2) + align256((size_t)T * d * 4); }
+size_t ws_permute_bwd(int T, int d, int E) { return 2 * align256((size_t)T * E * 2) + align256((size_t)T * d * 2); }
 
 // grouped SwiGLU backward scratch: da|du hi+lo [rows,2H] x2, g*h hi+lo [rows,H] x2,
 // gate-gradient partials [rows, ceil(H/256)], for the routed rows (T*k) and the
@@ -147,6 +147,7 @@ const char* moe_status_string(int status) {
     case MOE_ERR_CUDA: return "CUDA call failed";
     case MOE_ERR_TIMEOUT: return "device: bounded wait expired";
     case MOE_ERR_DEVICE_BOUNDS: return "device: index out of range";
+    case MOE_ERR_RANGE: return "device: a per-token sum was not finite (an fp16 term beyond its range, or inf / NaN)";
     default: return "unknown status";
   }
 }
@@ -256,7 +257,7 @@ int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int
 
 int moe_grouped_swiglu(const void* x_perm, const int32_t* offsets, const void* x, int T, int d, int E, int k, int H,
                        int Hs, const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
-                       const void* Ws_d, float* au, void* h, float* o_perm, float* au_s, void* h_s, float* s_out,
+                       const void* Ws_d, float* au, void* h, void* o_perm, float* au_s, void* h_s, void* s_out,
                        void* ws, size_t ws_bytes, void* stream) {
   (void)ws;
   (void)ws_bytes;
@@ -305,7 +306,7 @@ int moe_grouped_swiglu_recompute(const void* x_perm, const int32_t* offsets, con
 int moe_grouped_swiglu_fused(const void* x, const int32_t* slot_of_row, const int32_t* row_of_slot,
                              const float* gates, const int32_t* offsets, int T, int d, int E, int k, int H, int Hs,
                              const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
-                             const void* Ws_d, float* au, void* h, float* o_slot, float* au_s, void* h_s, void* y,
+                             const void* Ws_d, float* au, void* h, void* o_slot, float* au_s, void* h_s, void* y,
                              void* stream) {
   int rc = check_dims(T, d, E, k);
   if (rc) return rc;
@@ -361,7 +362,7 @@ int moe_grouped_swiglu_recompute_fused(const void* x, const int32_t* slot_of_row
   return check(gemm_swiglu_fwd(r, Hs > 0 ? &sh : nullptr, device_status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 
-int moe_unpermute_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
+int moe_unpermute_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
                           int T, int d, int k, void* y, void* stream) {
   if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
   if (k > kMaxK || (d % 64) != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
@@ -385,7 +386,7 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
                            const int32_t* slot_of_row, const int32_t* offsets, const void* x_perm, const void* x,
                            const float* au, const float* au_s, int T, int d, int E, int k, int H, int Hs,
                            const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
-                           const void* Ws_d, float* dx_perm, float* dx_s, void* dW_g, void* dW_u, void* dW_d,
+                           const void* Ws_d, void* dx_perm, void* dx_s, void* dW_g, void* dW_u, void* dW_d,
                            void* dWs_g, void* dWs_u, void* dWs_d, float* dgates, void* ws, size_t ws_bytes,
                            void* stream) {
   int rc = check_dims(T, d, E, k);
@@ -579,11 +580,11 @@ int moe_unpermute_combine_mxfp8(const float* o_perm, const float* s_out, const f
     return MOE_ERR_UNSUPPORTED;
   if (!o_perm || !gates || !row_of_slot || !y) return MOE_ERR_INVALID_ARG;
   if (!al16(o_perm) || !al16(y) || (s_out && !al16(s_out))) return MOE_ERR_INVALID_ARG;
-  return check(launch_combine_rows(o_perm, s_out, gates, row_of_slot, T, d, k, mx_rows_max(T, E, k), y,
+  return check(launch_combine_rows(o_perm, s_out, false, gates, row_of_slot, T, d, k, mx_rows_max(T, E, k), y,
                                    device_status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 
-int moe_permute_bwd(const float* dx_perm, const float* dx_s, const int32_t* row_of_slot, const float* dlogits,
+int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot, const float* dlogits,
                     const void* W_r, int T, int d, int E, int k, void* dx, void* ws, size_t ws_bytes, void* stream) {
   if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
   if (k > kMaxK || (d % 64) != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
@@ -601,7 +602,7 @@ int moe_permute_bwd(const float* dx_perm, const float* dx_s, const int32_t* row_
   uint16_t* dl_lo = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + align256((size_t)T * E * 2));
   cudaError_t e = launch_f32_to_bf16_split(dlogits, dl_hi, dl_lo, (long long)T * E, st);
   if (e != cudaSuccess) return fail_cuda(e);
-  float* dx_r = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * align256((size_t)T * E * 2));
+  void* dx_r = static_cast<char*>(ws) + 2 * align256((size_t)T * E * 2);  // fp16 [T, d]
   e = gemm_router_dx(dl_hi, dl_lo, W_r, T, d, E, dx_r, device_status_ptr(), st);
   if (e != cudaSuccess) return fail_cuda(e);
   return check(launch_unpermute_reduce(dx_perm, dx_s, dx_r, row_of_slot, T, d, k, dx, device_status_ptr(), st));

@@ -251,10 +251,20 @@ __global__ void perm_scatter_kernel(const uint4* __restrict__ x, const int32_t* 
 }
 
 // ------------------------------------------------------------------ combine
-// fp32 expert / shared outputs, fp32 accumulation, one bf16 rounding of y.
-// slot_order: the expert outputs are stored by slot (o[t*k+s]) instead of by
-// permuted row
-__global__ void combine_kernel(const float4* __restrict__ o_perm, const float4* __restrict__ s_out,
+// Eight consecutive values of a row of fp32 or fp16 terms, as fp32.
+__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __half* p, float (&f)[8]) {
+  unpack_f16x8(__ldg(reinterpret_cast<const uint4*>(p)), f);
+}
+
+// Expert / shared outputs (fp16 terms, or fp32 from the MXFP8 path), fp32
+// accumulation, one bf16 rounding of y.  slot_order: the expert outputs are
+// stored by slot (o[t*k+s]) instead of by permuted row.
+template <typename In>
+__global__ void combine_kernel(const In* __restrict__ o_perm, const In* __restrict__ s_out,
                                const float* __restrict__ gates, const int32_t* __restrict__ row_of_slot, int T, int d,
                                int k, long long max_rows, int slot_order, uint4* __restrict__ y, int* status) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -278,12 +288,11 @@ __global__ void combine_kernel(const float4* __restrict__ o_perm, const float4* 
     rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
     gs[s] = __shfl_sync(0xffffffffu, g, s < k ? s : 0);
   }
-  const int vpr = d / 8;  // 8 elements per step: two float4 in, one uint4 out
+  const int vpr = d / 8;  // 8 elements per step, one uint4 out
   for (int c = lane; c < vpr; c += 32) {
     float acc[8];
     if (s_out) {
-      float4 a = __ldg(s_out + (long long)t * 2 * vpr + 2 * c), b = __ldg(s_out + (long long)t * 2 * vpr + 2 * c + 1);
-      acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w; acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+      load8(s_out + (long long)t * d + 8 * c, acc);
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
@@ -292,13 +301,17 @@ __global__ void combine_kernel(const float4* __restrict__ o_perm, const float4* 
     for (int s = 0; s < kMaxK; ++s) {
       if (s >= k) break;
       if (rows[s] < 0) continue;
-      const float4* src = o_perm + (long long)rows[s] * 2 * vpr + 2 * c;
-      float4 a = __ldg(src), b = __ldg(src + 1);
-      acc[0] = fmaf(gs[s], a.x, acc[0]); acc[1] = fmaf(gs[s], a.y, acc[1]);
-      acc[2] = fmaf(gs[s], a.z, acc[2]); acc[3] = fmaf(gs[s], a.w, acc[3]);
-      acc[4] = fmaf(gs[s], b.x, acc[4]); acc[5] = fmaf(gs[s], b.y, acc[5]);
-      acc[6] = fmaf(gs[s], b.z, acc[6]); acc[7] = fmaf(gs[s], b.w, acc[7]);
+      float v[8];
+      load8(o_perm + (long long)rows[s] * d + 8 * c, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(gs[s], v[e], acc[e]);
     }
+    // an infinite term (an fp16 term beyond its range) or NaN makes the sum
+    // non-finite
+    bool fin = true;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fin &= isfinite(acc[e]);
+    if (!fin) record_status(status, MOE_ERR_RANGE);
     y[(long long)t * vpr + c] = pack8(acc);
   }
 }
@@ -354,8 +367,9 @@ __global__ void dgates_reduce_kernel(const float* __restrict__ dgp, int P, const
   }
 }
 
-__global__ void unpermute_reduce_kernel(const float4* __restrict__ dx_perm, const float4* __restrict__ dx_s,
-                                        const float4* __restrict__ dx_r, const int32_t* __restrict__ row_of_slot,
+// fp16 terms, fp32 accumulation, one bf16 rounding of dx
+__global__ void unpermute_reduce_kernel(const __half* __restrict__ dx_perm, const __half* __restrict__ dx_s,
+                                        const __half* __restrict__ dx_r, const int32_t* __restrict__ row_of_slot,
                                         int T, int d, int k, long long max_rows, uint4* __restrict__ dx, int* status) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -377,24 +391,28 @@ __global__ void unpermute_reduce_kernel(const float4* __restrict__ dx_perm, cons
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
     // the per-token terms (shared expert, router), then the kept rows
-    const float4* tok_terms[2] = {dx_s, dx_r};
+    const __half* tok_terms[2] = {dx_s, dx_r};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       if (!tok_terms[i]) continue;
-      const float4* src = tok_terms[i] + (long long)t * 2 * vpr + 2 * c;
-      float4 a = __ldg(src), b = __ldg(src + 1);
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      float v[8];
+      load8(tok_terms[i] + (long long)t * d + 8 * c, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += v[e];
     }
 #pragma unroll
     for (int s = 0; s < kMaxK; ++s) {
       if (s >= k) break;
       if (rows[s] < 0) continue;
-      const float4* src = dx_perm + (long long)rows[s] * 2 * vpr + 2 * c;
-      float4 a = __ldg(src), b = __ldg(src + 1);
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      float v[8];
+      load8(dx_perm + (long long)rows[s] * d + 8 * c, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += v[e];
     }
+    bool fin = true;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fin &= isfinite(acc[e]);
+    if (!fin) record_status(status, MOE_ERR_RANGE);
     dx[(long long)t * vpr + c] = pack8(acc);
   }
 }
@@ -648,29 +666,34 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_rows(const float* o_perm, const float* s_out, const float* gates,
+cudaError_t launch_combine_rows(const void* o_perm, const void* s_out, bool f16, const float* gates,
                                 const int32_t* row_of_slot, int T, int d, int k, long long o_rows, void* y,
                                 int* status, cudaStream_t s) {
   timing_mark(s, "combine");
-  combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-      reinterpret_cast<const float4*>(o_perm), reinterpret_cast<const float4*>(s_out), gates, row_of_slot, T, d, k,
-      o_rows, 0, static_cast<uint4*>(y), status);
+  if (f16)
+    combine_kernel<__half><<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+        static_cast<const __half*>(o_perm), static_cast<const __half*>(s_out), gates, row_of_slot, T, d, k, o_rows, 0,
+        static_cast<uint4*>(y), status);
+  else
+    combine_kernel<float><<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+        static_cast<const float*>(o_perm), static_cast<const float*>(s_out), gates, row_of_slot, T, d, k, o_rows, 0,
+        static_cast<uint4*>(y), status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_slots(const float* o_slot, const float* s_out, const float* gates,
+cudaError_t launch_combine_slots(const void* o_slot, const void* s_out, const float* gates,
                                  const int32_t* row_of_slot, int T, int d, int k, void* y, int* status,
                                  cudaStream_t s) {
   timing_mark(s, "combine_slots");
-  combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-      reinterpret_cast<const float4*>(o_slot), reinterpret_cast<const float4*>(s_out), gates, row_of_slot, T, d, k,
+  combine_kernel<__half><<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+      static_cast<const __half*>(o_slot), static_cast<const __half*>(s_out), gates, row_of_slot, T, d, k,
       (long long)T * k, 1, static_cast<uint4*>(y), status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float* o_perm, const float* s_out, const float* gates, const int32_t* row_of_slot,
+cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
                            int T, int d, int k, void* y, int* status, cudaStream_t s) {
-  return launch_combine_rows(o_perm, s_out, gates, row_of_slot, T, d, k, (long long)T * k, y, status, s);
+  return launch_combine_rows(o_perm, s_out, true, gates, row_of_slot, T, d, k, (long long)T * k, y, status, s);
 }
 
 cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
@@ -689,15 +712,13 @@ cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpermute_reduce(const float* dx_perm, const float* dx_s, const float* dx_r,
+cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const void* dx_r,
                                     const int32_t* row_of_slot, int T, int d, int k, void* dx, int* status,
                                     cudaStream_t s) {
   timing_mark(s, "unpermute_reduce");
   unpermute_reduce_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-      reinterpret_cast<const float4*>(dx_perm), reinterpret_cast<const float4*>(dx_s),
-      reinterpret_cast<const float4*>(dx_r), row_of_slot, T, d, k,
-      (long long)T * k,
-      static_cast<uint4*>(dx), status);
+      static_cast<const __half*>(dx_perm), static_cast<const __half*>(dx_s), static_cast<const __half*>(dx_r),
+      row_of_slot, T, d, k, (long long)T * k, static_cast<uint4*>(dx), status);
   return cudaGetLastError();
 }
 

@@ -46,10 +46,12 @@ class MoELayer:
         self.x_perm = None if self.fused else e(R, d)
         self.au = e(R, 2 * H, dt=torch.float32) if backward else None
         self.h = e(R, H)
-        self.o_perm = e(R, d, dt=torch.float32)
+        # the terms of the per-token sums (expert outputs, shared output,
+        # input-gradient rows) in fp16
+        self.o_perm = e(R, d, dt=torch.float16)
         self.au_s = e(T, 2 * Hs, dt=torch.float32) if (Hs and backward) else None
         self.h_s = e(T, Hs) if Hs else None
-        self.s = e(T, d, dt=torch.float32) if (Hs and not self.fused) else None
+        self.s = e(T, d, dt=torch.float16) if (Hs and not self.fused) else None
         self.y = e(T, d)
         if self.balance_alpha > 0:
             # auxiliary load-balancing loss (device scalar), mean router
@@ -62,8 +64,8 @@ class MoELayer:
         if backward:
             self.dY_perm = None if self.fused else e(R, d)
             self.dgates = e(T, k, dt=torch.float32)
-            self.dx_perm = e(R, d, dt=torch.float32)
-            self.dx_s = e(T, d, dt=torch.float32) if Hs else None
+            self.dx_perm = e(R, d, dt=torch.float16)
+            self.dx_s = e(T, d, dt=torch.float16) if Hs else None
             self.dW_g = e(E, H, d)
             self.dW_u = e(E, H, d)
             self.dW_d = e(E, d, H)
