@@ -521,8 +521,8 @@ def main_ours(args):
                "gu_c": u8(E * 2 * H * d), "gu_s": u8(sb(E * 2 * H, d)), "d_c": u8(E * d * H), "d_s": u8(sb(E * d, H)),
                "sgu_c": u8(2 * Hs * d), "sgu_s": u8(sb(2 * Hs, d)), "sd_c": u8(d * Hs), "sd_s": u8(sb(d, Hs)),
                "xsc": u8(T * d), "xss": u8(sb(T, d)), "hsc": u8(T * Hs), "hss": u8(sb(T, Hs)),
-               "o": torch.empty(mrows, d, dtype=torch.float32, device="cuda"),
-               "s": torch.empty(T, d, dtype=torch.float32, device="cuda"),
+               "o": torch.empty(mrows, d, dtype=torch.float16, device="cuda"),
+               "s": torch.empty(T, d, dtype=torch.float16, device="cuda"),
                "y": torch.empty(T, d, dtype=torch.bfloat16, device="cuda")}
         B.moe_mxfp8_quantize_gate_up(dev["W_g"], dev["W_u"], E, H, d, mxb["gu_c"], mxb["gu_s"])
         B.moe_mxfp8_quantize(dev["W_d"], E * d, H, mxb["d_c"], mxb["d_s"])

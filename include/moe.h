@@ -46,7 +46,7 @@
  * Weight layouts (out_features x in_features):
  *   W_r [E,d]; W_g, W_u [E,H,d]; W_d [E,d,H]; Ws_g, Ws_u [Hs,d]; Ws_d [d,Hs].
  * Buffers sized for the dropless maximum R <= T*k (rows >= R are left as
- * they were): x_perm, dY_perm [T*k, d] bf16; o_perm, dx_perm [T*k, d] fp32;
+ * they were): x_perm, dY_perm [T*k, d] bf16; o_perm, dx_perm [T*k, d] fp16;
  * au [T*k, 2H] fp32; h [T*k, H] bf16; slot_of_row [T*k].
  */
 #ifndef MOE_GB300_H
@@ -468,9 +468,10 @@ MOE_API int moe_permute_mxfp8(const void* x, const int32_t* topk_idx, int T, int
  * space),
  *   a = MX(x) MX(W_g[e])^T, u = MX(x) MX(W_u[e])^T   (fp32 accumulate)
  *   h = silu(a) u, quantized along H (blocks of 32) into h_codes / h_scales
- *   o = MX(h) MX(W_d[e])^T  -> o_perm [moe_mxfp8_rows, d] fp32
+ *   o = MX(h) MX(W_d[e])^T  -> o_perm [moe_mxfp8_rows, d] fp16
  * and the same on every token with the shared weights (xs = MX(x) from
- * moe_mxfp8_quantize, h_s -> hs_codes [T, Hs] / hs_scales, s [T, d] fp32).
+ * moe_mxfp8_quantize, h_s -> hs_codes [T, Hs] / hs_scales, s [T, d] fp16:
+ * o and s are the combine's sum terms, as in moe_grouped_swiglu).
  * Wgu: the packed gate/up codes and scales (moe_mxfp8_quantize_gate_up);
  * Wd: W_d quantized as E*d rows of H.  The products run on the tensor cores
  * as block-scaled E4M3 MMAs (tcgen05 kind::mxf8f6f4, E8M0 scales in tensor
@@ -481,11 +482,11 @@ MOE_API int moe_grouped_swiglu_mxfp8(const void* x_codes, const void* x_scales, 
                                      const void* Wgu_scales, const void* Wd_codes, const void* Wd_scales,
                                      const void* Wsgu_codes, const void* Wsgu_scales, const void* Wsd_codes,
                                      const void* Wsd_scales, void* h_codes, void* h_scales, void* hs_codes,
-                                     void* hs_scales, float* o_perm, float* s, void* stream);
+                                     void* hs_scales, void* o_perm, void* s, void* stream);
 
 /* moe_unpermute_combine for o_perm in the padded row space of the MXFP8
  * path (moe_mxfp8_rows(T, E, k) rows; row_of_slot from moe_permute_mxfp8). */
-MOE_API int moe_unpermute_combine_mxfp8(const float* o_perm, const float* s, const float* gates,
+MOE_API int moe_unpermute_combine_mxfp8(const void* o_perm, const void* s, const float* gates,
                                         const int32_t* row_of_slot, int T, int d, int E, int k, void* y,
                                         void* stream);
 

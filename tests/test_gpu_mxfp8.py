@@ -129,7 +129,9 @@ def run_mx_layer(B, w, inp):
     B.moe_mxfp8_quantize(dev["x"], T, d, xs_c, xs_s)
     h_c, h_s = u8(rows * H), u8(B.moe_mxfp8_scales_bytes(rows, H))
     hs_c, hs_s = u8(T * Hs), u8(B.moe_mxfp8_scales_bytes(T, Hs))
-    o_perm, s = torch.full((rows, d), float("nan"), device="cuda"), f32(T, d)
+    # fp16 sum terms; padding rows stay NaN
+    o_perm = torch.full((rows, d), float("nan"), dtype=torch.float16, device="cuda")
+    s = torch.empty(T, d, dtype=torch.float16, device="cuda")
     B.moe_grouped_swiglu_mxfp8(x_codes, x_scales, mxoff, counts, xs_c, xs_s, T, d, E, k, H, Hs, Wgu_c, Wgu_s,
                                Wd_c, Wd_s, Wsgu_c, Wsgu_s, Wsd_c, Wsd_s, h_c, h_s, hs_c, hs_s, o_perm, s)
     y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")

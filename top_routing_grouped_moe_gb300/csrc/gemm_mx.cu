@@ -1,5 +1,5 @@
 // MXFP8 expert GEMMs: gate/up with the SwiGLU epilogue that quantizes h, and
-// down with fp32 rows out, on block-scaled E4M3 operands (tcgen05
+// down with fp16 rows out (terms of the combine's sum), on block-scaled E4M3 operands (tcgen05
 // kind::mxf8f6f4 with E8M0 scales in tensor memory).
 #include "gemm_host.cuh"
 
@@ -31,6 +31,7 @@ bool fill_mx(Params& P, Problem& pr, const MxGemmArgs& a, bool swiglu) {
   pr.nkq = a.K / 128;
   pr.sfb_gstride = (long long)(Nb / 128) * pr.nkq * 512;
   pr.out = a.out;
+  pr.out_f16 = swiglu ? 0 : 1;  // down: fp16 terms of the combine's sum
   pr.ldo = a.N;
   pr.out_sf = a.out_scales;
   pr.out_sf_nq = a.N / 128;

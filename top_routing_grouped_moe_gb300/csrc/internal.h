@@ -210,8 +210,8 @@ struct MxGemmArgs {
 };
 cudaError_t gemm_mx_swiglu(const MxGemmArgs& routed, const MxGemmArgs* shared, cudaStream_t s);
 cudaError_t gemm_mx_down(const MxGemmArgs& routed, const MxGemmArgs* shared, cudaStream_t s);
-// o_perm, s_out fp16 (f16) or fp32 (the MXFP8 path), o_rows rows of o_perm
-cudaError_t launch_combine_rows(const void* o_perm, const void* s_out, bool f16, const float* gates,
+// o_perm (o_rows rows), s_out fp16; y bf16
+cudaError_t launch_combine_rows(const void* o_perm, const void* s_out, const float* gates,
                                 const int32_t* row_of_slot, int T, int d, int k, long long o_rows, void* y,
                                 int* status, cudaStream_t s);
 // the same with the expert outputs stored by slot: y[t] = s[t] + sum_{kept j}

@@ -539,7 +539,7 @@ int moe_grouped_swiglu_mxfp8(const void* x_codes, const void* x_scales, const in
                              int k, int H, int Hs, const void* Wgu_codes, const void* Wgu_scales,
                              const void* Wd_codes, const void* Wd_scales, const void* Wsgu_codes,
                              const void* Wsgu_scales, const void* Wsd_codes, const void* Wsd_scales, void* h_codes,
-                             void* h_scales, void* hs_codes, void* hs_scales, float* o_perm, float* s_out,
+                             void* h_scales, void* hs_codes, void* hs_scales, void* o_perm, void* s_out,
                              void* stream) {
   int rc = check_dims(T, d, E, k);
   if (rc) return rc;
@@ -573,14 +573,14 @@ int moe_grouped_swiglu_mxfp8(const void* x_codes, const void* x_scales, const in
   return check(gemm_mx_down(r2, Hs > 0 ? &s2 : nullptr, st));
 }
 
-int moe_unpermute_combine_mxfp8(const float* o_perm, const float* s_out, const float* gates,
+int moe_unpermute_combine_mxfp8(const void* o_perm, const void* s_out, const float* gates,
                                 const int32_t* row_of_slot, int T, int d, int E, int k, void* y, void* stream) {
   if (T < 1 || d < 1 || k < 1 || E < 1) return MOE_ERR_INVALID_ARG;
   if (k > kMaxK || k > E || E > kMaxE || (d % 64) != 0 || (long long)T * k >= (1LL << 31))
     return MOE_ERR_UNSUPPORTED;
   if (!o_perm || !gates || !row_of_slot || !y) return MOE_ERR_INVALID_ARG;
   if (!al16(o_perm) || !al16(y) || (s_out && !al16(s_out))) return MOE_ERR_INVALID_ARG;
-  return check(launch_combine_rows(o_perm, s_out, false, gates, row_of_slot, T, d, k, mx_rows_max(T, E, k), y,
+  return check(launch_combine_rows(o_perm, s_out, gates, row_of_slot, T, d, k, mx_rows_max(T, E, k), y,
                                    device_status_ptr(), static_cast<cudaStream_t>(stream)));
 }
 

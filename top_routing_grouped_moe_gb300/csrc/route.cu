@@ -251,20 +251,15 @@ __global__ void perm_scatter_kernel(const uint4* __restrict__ x, const int32_t* 
 }
 
 // ------------------------------------------------------------------ combine
-// Eight consecutive values of a row of fp32 or fp16 terms, as fp32.
-__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
+// Eight consecutive fp16 terms of a row, as fp32.
 __device__ __forceinline__ void load8(const __half* p, float (&f)[8]) {
   unpack_f16x8(__ldg(reinterpret_cast<const uint4*>(p)), f);
 }
 
-// Expert / shared outputs (fp16 terms, or fp32 from the MXFP8 path), fp32
-// accumulation, one bf16 rounding of y.  slot_order: the expert outputs are
-// stored by slot (o[t*k+s]) instead of by permuted row.
-template <typename In>
-__global__ void combine_kernel(const In* __restrict__ o_perm, const In* __restrict__ s_out,
+// Expert / shared outputs (fp16 terms), fp32 accumulation, one bf16 rounding
+// of y.  slot_order: the expert outputs are stored by slot (o[t*k+s]) instead
+// of by permuted row.
+__global__ void combine_kernel(const __half* __restrict__ o_perm, const __half* __restrict__ s_out,
                                const float* __restrict__ gates, const int32_t* __restrict__ row_of_slot, int T, int d,
                                int k, long long max_rows, int slot_order, uint4* __restrict__ y, int* status) {
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -666,18 +661,13 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_rows(const void* o_perm, const void* s_out, bool f16, const float* gates,
+cudaError_t launch_combine_rows(const void* o_perm, const void* s_out, const float* gates,
                                 const int32_t* row_of_slot, int T, int d, int k, long long o_rows, void* y,
                                 int* status, cudaStream_t s) {
   timing_mark(s, "combine");
-  if (f16)
-    combine_kernel<__half><<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-        static_cast<const __half*>(o_perm), static_cast<const __half*>(s_out), gates, row_of_slot, T, d, k, o_rows, 0,
-        static_cast<uint4*>(y), status);
-  else
-    combine_kernel<float><<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-        static_cast<const float*>(o_perm), static_cast<const float*>(s_out), gates, row_of_slot, T, d, k, o_rows, 0,
-        static_cast<uint4*>(y), status);
+  combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+      static_cast<const __half*>(o_perm), static_cast<const __half*>(s_out), gates, row_of_slot, T, d, k, o_rows, 0,
+      static_cast<uint4*>(y), status);
   return cudaGetLastError();
 }
 
@@ -685,7 +675,7 @@ cudaError_t launch_combine_slots(const void* o_slot, const void* s_out, const fl
                                  const int32_t* row_of_slot, int T, int d, int k, void* y, int* status,
                                  cudaStream_t s) {
   timing_mark(s, "combine_slots");
-  combine_kernel<__half><<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+  combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
       static_cast<const __half*>(o_slot), static_cast<const __half*>(s_out), gates, row_of_slot, T, d, k,
       (long long)T * k, 1, static_cast<uint4*>(y), status);
   return cudaGetLastError();
@@ -693,7 +683,7 @@ cudaError_t launch_combine_slots(const void* o_slot, const void* s_out, const fl
 
 cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
                            int T, int d, int k, void* y, int* status, cudaStream_t s) {
-  return launch_combine_rows(o_perm, s_out, true, gates, row_of_slot, T, d, k, (long long)T * k, y, status, s);
+  return launch_combine_rows(o_perm, s_out, gates, row_of_slot, T, d, k, (long long)T * k, y, status, s);
 }
 
 cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
