@@ -618,43 +618,67 @@ def main_ours(args):
             pin["logits_in"] = torch.from_numpy(inp["logits_in"]).pin_memory()
         y_host = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
         dx_host = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
-        xin = torch.empty_like(dev["x"])
-        dyin = torch.empty_like(dev["dY"])
-        lin = torch.empty_like(dev["logits_in"]) if "logits_in" in dev else None
-        h2d = pin["x"].numel() * 2 + pin["dY"].numel() * 2 + (pin["logits_in"].numel() * 4 if lin is not None else 0)
+        h2d = pin["x"].numel() * 2 + pin["dY"].numel() * 2 + (pin["logits_in"].numel() * 4 if "logits_in" in pin else 0)
         d2h = 2 * T * d * 2
 
-        # a second stream carries the transfers that need not wait: dY's
-        # upload runs beside the forward, y's download beside the backward
-        side = torch.cuda.Stream()
+        # The loop a training job runs: every step uploads its x and dY from
+        # pinned host memory and downloads y and dx, through the layer API.
+        # Inputs are double-buffered: step i+1's upload runs (on its own
+        # stream) beside step i's backward, y's download beside the backward,
+        # dx's beside the next forward.  Events order every reuse: a buffer is
+        # refilled only after the backward that read it, and y / dx are
+        # overwritten only after their downloads.
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        xin = [torch.empty_like(dev["x"]) for _ in range(2)]
+        dyin = [torch.empty_like(dev["dY"]) for _ in range(2)]
+        lin = [torch.empty_like(dev["logits_in"]) for _ in range(2)] if "logits_in" in dev else None
 
-        def e2e_step():
+        def upload(b, after):
+            with torch.cuda.stream(up):
+                if after is not None:
+                    up.wait_event(after)
+                xin[b].copy_(pin["x"], non_blocking=True)
+                if lin is not None:
+                    lin[b].copy_(pin["logits_in"], non_blocking=True)
+                dyin[b].copy_(pin["dY"], non_blocking=True)
+                return up.record_event()
+
+        def e2e_run(n):
             main = torch.cuda.current_stream()
-            xin.copy_(pin["x"], non_blocking=True)
-            if lin is not None:
-                lin.copy_(pin["logits_in"], non_blocking=True)
-            side.wait_stream(main)
-            with torch.cuda.stream(side):
-                dyin.copy_(pin["dY"], non_blocking=True)
+            ready = upload(0, None)
+            freed = [None, None]
+            y_copied = dx_copied = None
             p = dict(dev)
-            layer.forward(xin, p, logits_in=lin)
-            fwd_done = main.record_event()
-            main.wait_stream(side)
-            with torch.cuda.stream(side):
-                side.wait_event(fwd_done)
-                y_host.copy_(layer.y, non_blocking=True)
-            layer.backward(xin, dyin, p, learned_router=learned)
-            dx_host.copy_(layer.dx, non_blocking=True)
+            for i in range(n):
+                b = i & 1
+                main.wait_event(ready)
+                if y_copied is not None:
+                    main.wait_event(y_copied)
+                layer.forward(xin[b], p, logits_in=lin[b] if lin is not None else None)
+                fwd_done = main.record_event()
+                with torch.cuda.stream(down):
+                    down.wait_event(fwd_done)
+                    y_host.copy_(layer.y, non_blocking=True)
+                    y_copied = down.record_event()
+                if i + 1 < n:
+                    ready = upload(1 - b, freed[1 - b])
+                if dx_copied is not None:
+                    main.wait_event(dx_copied)
+                layer.backward(xin[b], dyin[b], p, learned_router=learned)
+                freed[b] = main.record_event()
+                with torch.cuda.stream(down):
+                    down.wait_event(freed[b])
+                    dx_host.copy_(layer.dx, non_blocking=True)
+                    dx_copied = down.record_event()
             main.synchronize()
-            side.synchronize()
+            down.synchronize()
+            up.synchronize()
 
-        for _ in range(3):
-            e2e_step()
+        e2e_run(3)
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
+        e2e_run(args.steps)
         el = max_over_ranks([time.perf_counter() - t0], "cuda")[0]
         e2e = {"value": tokens_per_s(T, args.steps, world, el * 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
