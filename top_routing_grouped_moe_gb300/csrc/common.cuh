@@ -1,6 +1,7 @@
 // Shared definitions of the CUDA path (device side and host side).
 #pragma once
 #include <cstdint>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -113,6 +114,37 @@ __device__ __forceinline__ uint32_t mx_codes4(float v0, float v1, float v2, floa
 
 __device__ __forceinline__ long long mx_atom_offset(long long row, int block, int nq) {
   return ((row >> 7) * nq + (block >> 2)) * 512 + 16 * (row & 31) + 4 * ((row & 127) >> 5) + (block & 3);
+}
+
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialization (launch_pdl below, and the GEMM
+// launcher): its CTAs may be scheduled while the kernel before it on the
+// stream is still retiring, run a prologue that touches only shared memory,
+// tensor memory and kernel parameters, and then wait in dependency_wait()
+// until the previous kernel has completed and its memory is visible.  Every
+// thread waits before its first global access (read or write), and every CTA
+// waits before it exits, so the chain stays ordered however far back a
+// kernel's inputs were written.  No kernel signals its dependents early: a
+// trigger at kernel entry (dependents resident for the whole kernel) measured
+// slower than none.  Launched without the attribute, or after a non-kernel
+// operation, the wait is a no-op.
+__device__ __forceinline__ void dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kern` on `s` with programmatic stream serialization (see above).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace moe

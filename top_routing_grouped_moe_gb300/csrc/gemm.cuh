@@ -508,6 +508,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
   const int tile0 = blockIdx.x / PAIR;
   const int tile_step = gridDim.x / PAIR;
 
+  // programmatic launch: this prologue touches shared memory, tensor memory
+  // and the kernel parameters only; the wait below (every thread, before the
+  // schedule reads the offsets) orders all global accesses after the
+  // previous kernel
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       // GATHER: the lead's expect-tx arrival and one cp.async arrival per lane
@@ -537,6 +541,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
     ptx::tmem_relinquish<PAIR>();
     ptx::tc_fence_before();
   }
+  dependency_wait();
   build_schedule<MODE, TILE_M>(P, S);  // contains __syncthreads
   if (PAIR == 2) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();

@@ -209,6 +209,7 @@ cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* ti
   const WgradArgs* order[2] = {shared ? shared : &routed, shared ? &routed : nullptr};
   long long bound = 0;
   int with_offsets = 0;
+  bool counter_zeroed = false;  // by the group-maps kernel
   for (int i = 0; i < 2 && order[i]; ++i) {
     const WgradArgs& a = *order[i];
     Problem& pr = P.prob[i];
@@ -235,10 +236,11 @@ cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* ti
         if (!encode_blocks(&whole_1row[m], base[m], cols[m], 1, bkk, nblk[m])) return cudaErrorInvalidValue;
       }
       CUtensorMap* gm = static_cast<CUtensorMap*>(group_maps);
-      cudaError_t e =
-          launch_group_maps(whole, whole_1row, base, rb, nmaps, a.offsets, a.G, a.rows_total, gm, s);
+      cudaError_t e = launch_group_maps(whole, whole_1row, base, rb, nmaps, a.offsets, a.G, a.rows_total, gm,
+                                        tile_counter, s);
       if (e != cudaSuccess) return e;
       pr.gmaps = gm;
+      counter_zeroed = tile_counter != nullptr;
     }
   }
   P.tile_counter = tile_counter;
@@ -249,13 +251,13 @@ cudaError_t gemm_wgrad(const WgradArgs& routed, const WgradArgs* shared, int* ti
   // the routed problem's
   if (shared && shared->gather.src) return cudaErrorInvalidValue;
   if (routed.gather.src) {
-    if (routed.A_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_A, 0, 1>(P, bound, s, name);
-    if (routed.B_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_B, 0, 1>(P, bound, s, name);
+    if (routed.A_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_A, 0, 1>(P, bound, s, name, counter_zeroed);
+    if (routed.B_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_B, 0, 1>(P, bound, s, name, counter_zeroed);
     return cudaErrorInvalidValue;
   }
-  if (routed.A_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_A>(P, bound, s, name);
-  if (routed.B_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_B>(P, bound, s, name);
-  return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_NONE>(P, bound, s, name);
+  if (routed.A_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_A>(P, bound, s, name, counter_zeroed);
+  if (routed.B_lo) return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_B>(P, bound, s, name, counter_zeroed);
+  return launch<1, 1, KGROUP, EPI_BF16, 1, SPLIT_NONE>(P, bound, s, name, counter_zeroed);
 }
 
 }  // namespace moe

@@ -168,9 +168,12 @@ inline Problem blank_problem() {
 
 // Launch a persistent grid for `tile_bound` tiles at most: one CTA per SM
 // (PAIR = 1), or clusters of two CTAs sized by the number of clusters that can
-// be resident at once (PAIR = 2).
+// be resident at once (PAIR = 2), with programmatic stream serialization (the
+// kernel waits for its predecessor after its on-chip prologue).  The dynamic
+// schedule's tile counter is zeroed by a memset unless the kernel launched
+// just before (`counter_ready`) has zeroed it.
 template <int AMN, int BMN, int MODE, int EPI, int PAIR, int SPLIT = SPLIT_NONE, int MX = 0, int GATHER = 0>
-cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s, const char* name) {
+cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s, const char* name, bool counter_ready = false) {
   auto kern = grouped_gemm_kernel<AMN, BMN, MODE, EPI, PAIR, SPLIT, MX, GATHER>;
   constexpr size_t smem = smem_bytes<MODE, EPI, PAIR, SPLIT, MX>();
   static_assert(smem <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
@@ -208,32 +211,35 @@ cudaError_t launch(Params& P, long long tile_bound, cudaStream_t s, const char* 
   }
   if (tile_bound <= 0) return cudaSuccess;
   P.status = device_status_ptr();
-  if (P.tile_counter) {
+  if (P.tile_counter && !counter_ready) {
     timing_mark(s, "memset_tile_counter");
     e = cudaMemsetAsync(P.tile_counter, 0, sizeof(int), s);
     if (e != cudaSuccess) return e;
   }
   timing_mark(s, name);
+  int grid;
   if (PAIR == 1) {
-    int grid = device_sm_count();
+    grid = device_sm_count();
     if (tile_bound < grid) grid = static_cast<int>(tile_bound);
-    kern<<<grid, NUM_THREADS, smem, s>>>(P);
-    return cudaGetLastError();
+  } else {
+    int clusters = max_clusters[dev];
+    if (tile_bound < clusters) clusters = static_cast<int>(tile_bound);
+    grid = 2 * clusters;
   }
-  int clusters = max_clusters[dev];
-  if (tile_bound < clusters) clusters = static_cast<int>(tile_bound);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = PAIR == 2 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, P);
 }
 

@@ -30,6 +30,7 @@ struct GroupMapArgs {
   const int32_t* offsets;  // [G+1]
   int G, extent;
   CUtensorMap* out;        // [G][kMapsPerGroup]
+  int* tile_counter;       // nullable: zeroed for the GEMM that follows (its dynamic tile schedule)
 };
 
 // One warp per group.  The row range is clamped into [0, extent) so that a
@@ -38,7 +39,9 @@ struct GroupMapArgs {
 // row 0, which the GEMM never reads.
 __global__ void __launch_bounds__(32) group_maps_kernel(const __grid_constant__ GroupMapArgs a) {
   __shared__ alignas(128) CUtensorMap sm[kMapsPerGroup];
+  dependency_wait();
   const int g = blockIdx.x, lane = threadIdx.x;
+  if (g == 0 && lane == 0 && a.tile_counter) *a.tile_counter = 0;
   int r0 = __ldg(a.offsets + g), r1 = __ldg(a.offsets + g + 1);
   r0 = min(max(r0, 0), a.extent);
   r1 = min(max(r1, r0), a.extent);
@@ -67,7 +70,7 @@ __global__ void __launch_bounds__(32) group_maps_kernel(const __grid_constant__ 
 
 cudaError_t launch_group_maps(const CUtensorMap* whole, const CUtensorMap* whole_1row, const void* const* base,
                               const uint64_t* row_bytes, int nmaps, const int32_t* offsets, int G, int extent,
-                              CUtensorMap* out, cudaStream_t s) {
+                              CUtensorMap* out, int* tile_counter, cudaStream_t s) {
   if (nmaps < 1 || nmaps > kMapsPerGroup || G < 1 || extent < 1 || !offsets || !out) return cudaErrorInvalidValue;
   if (reinterpret_cast<uintptr_t>(out) % 128 != 0) return cudaErrorInvalidValue;
   GroupMapArgs a;
@@ -85,9 +88,9 @@ cudaError_t launch_group_maps(const CUtensorMap* whole, const CUtensorMap* whole
   a.G = G;
   a.extent = extent;
   a.out = out;
+  a.tile_counter = tile_counter;
   timing_mark(s, "group_maps");
-  group_maps_kernel<<<G, 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(group_maps_kernel, dim3(G), dim3(32), 0, s, a);
 }
 
 }  // namespace moe
@@ -136,7 +139,8 @@ extern "C" MOE_API int moe_selftest_group_maps(void) {
         rc = MOE_ERR_UNSUPPORTED;
     if (rc != MOE_OK) break;
     e = cudaMemcpy(d_off, h_off, (G + 1) * sizeof(int32_t), cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = launch_group_maps(whole, whole_1row, base, row_bytes, 2, d_off, G, rows, d_maps, 0);
+    if (e == cudaSuccess)
+      e = launch_group_maps(whole, whole_1row, base, row_bytes, 2, d_off, G, rows, d_maps, nullptr, 0);
     CUtensorMap got[kMaxGroups * kMapsPerGroup];
     if (e == cudaSuccess) e = cudaMemcpy(got, d_maps, (size_t)G * kMapsPerGroup * sizeof(CUtensorMap),
                                          cudaMemcpyDeviceToHost);

@@ -179,10 +179,12 @@ size_t group_maps_bytes(int G);
 // Per-group maps: for each group g and operand m, a block view of the whole
 // [extent, cols] buffer at base[m] re-based at row off[g] with off[g+1] -
 // off[g] rows; out[g * 3 + m] in device memory.  `whole` is encoded with the
-// buffer's rows, `whole_1row` with one row (same box).
+// buffer's rows, `whole_1row` with one row (same box).  A non-null
+// `tile_counter` is zeroed for the GEMM launched next (in place of a memset,
+// which would break the chain of programmatic launches).
 cudaError_t launch_group_maps(const CUtensorMap* whole, const CUtensorMap* whole_1row, const void* const* base,
                               const uint64_t* row_bytes, int nmaps, const int32_t* offsets, int G, int extent,
-                              CUtensorMap* out, cudaStream_t s);
+                              CUtensorMap* out, int* tile_counter, cudaStream_t s);
 // dW_r partials: part[S, E, d] = split-K pieces of (dl_hi + dl_lo)^T x; dl halves [T, E] bf16
 cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* x, int T, int d, int E, int S,
                            float* part, int* status, cudaStream_t s);

@@ -34,6 +34,7 @@ template <bool GATE_UP>
 __global__ void mx_quantize_rows_kernel(const uint4* __restrict__ src, const uint4* __restrict__ src2,
                                         long long rows, int cols, int H, uint32_t* __restrict__ codes,
                                         uint8_t* __restrict__ scales) {
+  dependency_wait();
   const long long p = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= rows) return;
@@ -89,6 +90,7 @@ __global__ void perm_scatter_mx_kernel(const uint4* __restrict__ x, const int32_
                                        int capacity, long long max_rows, int32_t* __restrict__ row_of_slot,
                                        int32_t* __restrict__ slot_of_row, uint32_t* __restrict__ codes,
                                        uint8_t* __restrict__ scales, int* status) {
+  dependency_wait();
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -156,20 +158,18 @@ size_t mx_scales_bytes(long long rows, int cols) {
 cudaError_t launch_mx_quantize(const void* src, long long rows, int cols, void* codes, void* scales,
                                cudaStream_t s) {
   timing_mark(s, "mx_quantize");
-  mx_quantize_rows_kernel<false><<<warp_blocks(rows), 32 * kWarps, 0, s>>>(
+  return launch_pdl(mx_quantize_rows_kernel<false>, dim3(warp_blocks(rows)), dim3(32 * kWarps), 0, s,
       static_cast<const uint4*>(src), nullptr, rows, cols, 0, static_cast<uint32_t*>(codes),
       static_cast<uint8_t*>(scales));
-  return cudaGetLastError();
 }
 
 cudaError_t launch_mx_quantize_gate_up(const void* W_g, const void* W_u, int E, int H, int d, void* codes,
                                        void* scales, cudaStream_t s) {
   const long long rows = 2LL * E * H;
   timing_mark(s, "mx_quantize_gate_up");
-  mx_quantize_rows_kernel<true><<<warp_blocks(rows), 32 * kWarps, 0, s>>>(
+  return launch_pdl(mx_quantize_rows_kernel<true>, dim3(warp_blocks(rows)), dim3(32 * kWarps), 0, s,
       static_cast<const uint4*>(W_g), static_cast<const uint4*>(W_u), rows, d, H, static_cast<uint32_t*>(codes),
       static_cast<uint8_t*>(scales));
-  return cudaGetLastError();
 }
 
 cudaError_t launch_permute_mx(const void* x, const int32_t* idx, int T, int d, int E, int k, int capacity,
@@ -182,11 +182,10 @@ cudaError_t launch_permute_mx(const void* x, const int32_t* idx, int T, int d, i
                                         &tile_base, &inrank, status, s);
   if (e != cudaSuccess) return e;
   timing_mark(s, "perm_scatter_mx");
-  perm_scatter_mx_kernel<<<warp_blocks(T), 32 * kWarps, 0, s>>>(
+  return launch_pdl(perm_scatter_mx_kernel, dim3(warp_blocks(T)), dim3(32 * kWarps), 0, s,
       static_cast<const uint4*>(x), idx, inrank, tile_base, mx_offsets, T, d, E, k, capacity,
       mx_rows_max(T, E, k), row_of_slot, slot_of_row, static_cast<uint32_t*>(codes), static_cast<uint8_t*>(scales),
       status);
-  return cudaGetLastError();
 }
 
 }  // namespace moe

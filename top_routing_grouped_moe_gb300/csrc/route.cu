@@ -25,6 +25,7 @@ __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
 template <int NJ>
 __global__ void topk_gating_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
                                    float* __restrict__ gates) {
+  dependency_wait();
   const int warp = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -95,6 +96,7 @@ __global__ void topk_gating_kernel(const float* __restrict__ logits, int T, int 
 __global__ void perm_tile_hist_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                       int32_t* __restrict__ tile_counts, int32_t* __restrict__ inrank,
                                       int* status) {
+  dependency_wait();
   __shared__ uint32_t bits[kMaxE][kRouteTile / 32];
   const int tile = blockIdx.x;
   const int t_local = threadIdx.x;  // blockDim.x == kRouteTile
@@ -145,6 +147,7 @@ __global__ void perm_scan_kernel(const int32_t* __restrict__ tile_counts, int nt
                                  int32_t* __restrict__ tile_base, int32_t* __restrict__ counts_raw,
                                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                  int32_t* __restrict__ mx_offsets) {
+  dependency_wait();
   __shared__ int seg[1024];
   __shared__ int cnt[kMaxE];
   const int P = blockDim.x / E;  // segments of tiles per expert
@@ -211,6 +214,7 @@ __global__ void perm_scatter_kernel(const uint4* __restrict__ x, const int32_t* 
                                     const int32_t* __restrict__ offsets, int T, int d, int E, int k, int capacity,
                                     int32_t* __restrict__ row_of_slot, int32_t* __restrict__ slot_of_row,
                                     uint4* __restrict__ x_perm) {
+  dependency_wait();
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -262,6 +266,7 @@ __device__ __forceinline__ void load8(const __half* p, float (&f)[8]) {
 __global__ void combine_kernel(const __half* __restrict__ o_perm, const __half* __restrict__ s_out,
                                const float* __restrict__ gates, const int32_t* __restrict__ row_of_slot, int T, int d,
                                int k, long long max_rows, int slot_order, uint4* __restrict__ y, int* status) {
+  dependency_wait();
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -316,6 +321,7 @@ __global__ void combine_kernel(const __half* __restrict__ o_perm, const __half* 
 // expert backward, where they can be formed from fp32 values).
 __global__ void gather_rows_kernel(const uint4* __restrict__ dY, const int32_t* __restrict__ row_of_slot, int T,
                                    int d, int k, long long max_rows, uint4* __restrict__ dY_perm, int* status) {
+  dependency_wait();
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -352,6 +358,7 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ dY, const int32_t* 
 // dgates[slot] = sum of the per-N-tile partials of its row (0 if dropped)
 __global__ void dgates_reduce_kernel(const float* __restrict__ dgp, int P, const int32_t* __restrict__ row_of_slot,
                                      long long n_slots, float* __restrict__ dgates) {
+  dependency_wait();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_slots;
        i += (long long)gridDim.x * blockDim.x) {
     const int row = row_of_slot[i];
@@ -366,6 +373,7 @@ __global__ void dgates_reduce_kernel(const float* __restrict__ dgp, int P, const
 __global__ void unpermute_reduce_kernel(const __half* __restrict__ dx_perm, const __half* __restrict__ dx_s,
                                         const __half* __restrict__ dx_r, const int32_t* __restrict__ row_of_slot,
                                         int T, int d, int k, long long max_rows, uint4* __restrict__ dx, int* status) {
+  dependency_wait();
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -419,6 +427,7 @@ __global__ void router_bwd_dl_kernel(const float* __restrict__ dgates, const flo
                                      const int32_t* __restrict__ idx, int T, int E, int k,
                                      const float* __restrict__ add, float* __restrict__ dl,
                                      uint16_t* __restrict__ dl_hi, uint16_t* __restrict__ dl_lo) {
+  dependency_wait();
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -459,6 +468,7 @@ __global__ void router_bwd_dl_kernel(const float* __restrict__ dgates, const flo
 // v -> hi = bf16(v), lo = bf16(v - hi)
 __global__ void f32_to_bf16_split_kernel(const float* __restrict__ src, uint16_t* __restrict__ hi,
                                          uint16_t* __restrict__ lo, long long n) {
+  dependency_wait();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const float v = src[i];
     __nv_bfloat16 h = __float2bfloat16_rn(v);
@@ -469,6 +479,7 @@ __global__ void f32_to_bf16_split_kernel(const float* __restrict__ src, uint16_t
 }
 
 __global__ void splitk_reduce_kernel(const float4* __restrict__ part, int S, long long n4, float4* __restrict__ out) {
+  dependency_wait();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
     float4 a = part[i];
     for (int s = 1; s < S; ++s) {
@@ -518,6 +529,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 lbl_kernel(const float* __restrict__ logits, const int32_t* __restrict__ counts_raw, int T, int E, int k, float alpha,
            float* __restrict__ loss, float* __restrict__ P_mean, float* __restrict__ dl, float* __restrict__ partial,
            unsigned* __restrict__ ticket) {
+  dependency_wait();
   __shared__ float acc_s[kWarpsPerBlock][32 * NJ];
   __shared__ float red[32 * kWarpsPerBlock];
   __shared__ bool last;
@@ -609,14 +621,11 @@ cudaError_t launch_topk_gating(const float* logits, int T, int E, int k, int32_t
   const unsigned grid = warp_blocks(T);
   const int nj = (E + 31) / 32;
   timing_mark(s, "topk_gating");
-  switch (nj) {
-    case 1: topk_gating_kernel<1><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
-    case 2: topk_gating_kernel<2><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
-    case 3:
-    case 4: topk_gating_kernel<4><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
-    default: topk_gating_kernel<8><<<grid, 32 * kWarpsPerBlock, 0, s>>>(logits, T, E, k, idx, gates); break;
-  }
-  return cudaGetLastError();
+  auto kern = nj == 1   ? topk_gating_kernel<1>
+              : nj == 2 ? topk_gating_kernel<2>
+              : nj <= 4 ? topk_gating_kernel<4>
+                        : topk_gating_kernel<8>;
+  return launch_pdl(kern, dim3(grid), dim3(32 * kWarpsPerBlock), 0, s, logits, T, E, k, idx, gates);
 }
 
 static inline size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -635,15 +644,14 @@ cudaError_t launch_permute_counts(const int32_t* idx, int T, int E, int k, int c
   int32_t* tile_base = reinterpret_cast<int32_t*>(w + align256((size_t)ntile * E * 4));
   int32_t* inrank = reinterpret_cast<int32_t*>(w + 2 * align256((size_t)ntile * E * 4));
   timing_mark(s, "perm_tile_hist");
-  perm_tile_hist_kernel<<<ntile, kRouteTile, 0, s>>>(idx, T, E, k, tile_counts, inrank, status);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e =
+      launch_pdl(perm_tile_hist_kernel, dim3(ntile), dim3(kRouteTile), 0, s, idx, T, E, k, tile_counts, inrank, status);
   if (e != cudaSuccess) return e;
   timing_mark(s, "perm_scan");
-  perm_scan_kernel<<<1, 1024, 0, s>>>(tile_counts, ntile, E, capacity, tile_base, counts_raw, counts, offsets,
-                                      mx_offsets);
   *tile_base_out = tile_base;
   *inrank_out = inrank;
-  return cudaGetLastError();
+  return launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, tile_counts, ntile, E, capacity, tile_base,
+                    counts_raw, counts, offsets, mx_offsets);
 }
 
 cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int E, int k, int capacity,
@@ -655,30 +663,27 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, int T, int d, int 
                                         &tile_base, &inrank, status, s);
   if (e != cudaSuccess) return e;
   timing_mark(s, x_perm ? "perm_scatter" : "perm_maps");
-  perm_scatter_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
-      static_cast<const uint4*>(x), idx, inrank, tile_base, offsets, T, d, E, k, capacity, row_of_slot, slot_of_row,
-      static_cast<uint4*>(x_perm));
-  return cudaGetLastError();
+  return launch_pdl(perm_scatter_kernel, dim3(warp_blocks(T)), dim3(32 * kWarpsPerBlock), 0, s,
+                    static_cast<const uint4*>(x), idx, inrank, tile_base, offsets, T, d, E, k, capacity, row_of_slot,
+                    slot_of_row, static_cast<uint4*>(x_perm));
 }
 
 cudaError_t launch_combine_rows(const void* o_perm, const void* s_out, const float* gates,
                                 const int32_t* row_of_slot, int T, int d, int k, long long o_rows, void* y,
                                 int* status, cudaStream_t s) {
   timing_mark(s, "combine");
-  combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+  return launch_pdl(combine_kernel, dim3(warp_blocks(T)), dim3(32 * kWarpsPerBlock), 0, s,
       static_cast<const __half*>(o_perm), static_cast<const __half*>(s_out), gates, row_of_slot, T, d, k, o_rows, 0,
       static_cast<uint4*>(y), status);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_combine_slots(const void* o_slot, const void* s_out, const float* gates,
                                  const int32_t* row_of_slot, int T, int d, int k, void* y, int* status,
                                  cudaStream_t s) {
   timing_mark(s, "combine_slots");
-  combine_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+  return launch_pdl(combine_kernel, dim3(warp_blocks(T)), dim3(32 * kWarpsPerBlock), 0, s,
       static_cast<const __half*>(o_slot), static_cast<const __half*>(s_out), gates, row_of_slot, T, d, k,
       (long long)T * k, 1, static_cast<uint4*>(y), status);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* gates, const int32_t* row_of_slot,
@@ -689,49 +694,43 @@ cudaError_t launch_combine(const void* o_perm, const void* s_out, const float* g
 cudaError_t launch_gather_rows(const void* dY, const int32_t* row_of_slot, int T, int d, int k, void* dY_perm,
                                int* status, cudaStream_t s) {
   timing_mark(s, "gather_rows");
-  gather_rows_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+  return launch_pdl(gather_rows_kernel, dim3(warp_blocks(T)), dim3(32 * kWarpsPerBlock), 0, s,
       static_cast<const uint4*>(dY), row_of_slot, T, d, k, (long long)T * k, static_cast<uint4*>(dY_perm), status);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_slot, int T, int k, float* dgates,
                                  cudaStream_t s) {
   const long long n = (long long)T * k;
   timing_mark(s, "dgates_reduce");
-  dgates_reduce_kernel<<<flat_blocks(n, 256), 256, 0, s>>>(dgp, P, row_of_slot, n, dgates);
-  return cudaGetLastError();
+  return launch_pdl(dgates_reduce_kernel, dim3(flat_blocks(n, 256)), dim3(256), 0, s, dgp, P, row_of_slot, n, dgates);
 }
 
 cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const void* dx_r,
                                     const int32_t* row_of_slot, int T, int d, int k, void* dx, int* status,
                                     cudaStream_t s) {
   timing_mark(s, "unpermute_reduce");
-  unpermute_reduce_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(
+  return launch_pdl(unpermute_reduce_kernel, dim3(warp_blocks(T)), dim3(32 * kWarpsPerBlock), 0, s,
       static_cast<const __half*>(dx_perm), static_cast<const __half*>(dx_s), static_cast<const __half*>(dx_r),
       row_of_slot, T, d, k, (long long)T * k, static_cast<uint4*>(dx), status);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
                                  const float* add, float* dlogits, uint16_t* dl_hi, uint16_t* dl_lo, cudaStream_t s) {
   timing_mark(s, "router_bwd_dl");
-  router_bwd_dl_kernel<<<warp_blocks(T), 32 * kWarpsPerBlock, 0, s>>>(dgates, gates, idx, T, E, k, add, dlogits,
-                                                                       dl_hi, dl_lo);
-  return cudaGetLastError();
+  return launch_pdl(router_bwd_dl_kernel, dim3(warp_blocks(T)), dim3(32 * kWarpsPerBlock), 0, s, dgates, gates, idx,
+                    T, E, k, add, dlogits, dl_hi, dl_lo);
 }
 
 cudaError_t launch_f32_to_bf16_split(const float* src, uint16_t* hi, uint16_t* lo, long long n, cudaStream_t s) {
   timing_mark(s, "f32_to_bf16_split");
-  f32_to_bf16_split_kernel<<<flat_blocks(n, 256), 256, 0, s>>>(src, hi, lo, n);
-  return cudaGetLastError();
+  return launch_pdl(f32_to_bf16_split_kernel, dim3(flat_blocks(n, 256)), dim3(256), 0, s, src, hi, lo, n);
 }
 
 cudaError_t launch_splitk_reduce(const float* partial, int S, long long n, float* out, cudaStream_t s) {
   const long long n4 = n / 4;
   timing_mark(s, "splitk_reduce");
-  splitk_reduce_kernel<<<flat_blocks(n4, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(partial), S, n4,
-                                                            reinterpret_cast<float4*>(out));
-  return cudaGetLastError();
+  return launch_pdl(splitk_reduce_kernel, dim3(flat_blocks(n4, 256)), dim3(256), 0, s,
+                    reinterpret_cast<const float4*>(partial), S, n4, reinterpret_cast<float4*>(out));
 }
 
 size_t balance_loss_ws_bytes(int T, int E) {
@@ -750,14 +749,10 @@ cudaError_t launch_balance_loss(const float* logits, const int32_t* counts_raw, 
   if (e != cudaSuccess) return e;
   const unsigned threads = 32 * kWarpsPerBlock;
   timing_mark(s, "balance_loss");
-  switch ((E + 31) / 32) {
-    case 1: lbl_kernel<1><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
-    case 2: lbl_kernel<2><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
-    case 3:
-    case 4: lbl_kernel<4><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
-    default: lbl_kernel<8><<<nblk, threads, 0, s>>>(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl, partial, ticket); break;
-  }
-  return cudaGetLastError();
+  const int nj = (E + 31) / 32;
+  auto kern = nj == 1 ? lbl_kernel<1> : nj == 2 ? lbl_kernel<2> : nj <= 4 ? lbl_kernel<4> : lbl_kernel<8>;
+  return launch_pdl(kern, dim3(nblk), dim3(threads), 0, s, logits, counts_raw, T, E, k, alpha, loss, P_mean, dl,
+                    partial, ticket);
 }
 
 }  // namespace moe
