@@ -29,6 +29,15 @@
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*,
  *     NULL = legacy default stream), performs no host synchronisation and
  *     can be captured in a CUDA graph.
+ *   - Kernels are launched with programmatic stream serialization: a kernel
+ *     may be scheduled while the kernel before it on the stream retires, and
+ *     waits (griddepcontrol.wait) for it to complete before any global
+ *     memory access.  Stream order with the caller's own work is unchanged.
+ *     No kernel of the library signals its dependents early, so a caller's
+ *     kernel launched after one of ours with the same attribute still starts
+ *     only once ours has finished; it should itself wait (griddepcontrol.wait)
+ *     before reading our outputs, as any programmatically launched kernel
+ *     must.
  *   - Return value: MOE_OK, or an error code.  Argument errors are detected
  *     on the host before anything is launched.  MOE_ERR_CUDA reports a launch
  *     failure (moe_last_cuda_error() gives the cudaError_t value).  Device-side
