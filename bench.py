@@ -146,6 +146,36 @@ def kernel_work(w, R, fused=False):
     }
 
 
+def issued_mma_flops(w, R):
+    """MMA FLOPs the split-precision kernels issue per launch, where that is
+    more than their algorithmic FLOPs: every K step of a bf16 hi + lo operand
+    is issued twice (weight gradients: all tiles; dgrad of gate/up: the shared
+    expert's tiles; router weight gradient and router dx: dlogits).  Tile
+    padding is not counted."""
+    T, d, E, k, H, Hs = w.T, w.d, w.E, w.k, w.H, w.Hs
+    gu = 4.0 * d * (R * H + T * Hs)
+    dn = 2.0 * d * (R * H + T * Hs)
+    out = {
+        "gemm_wgrad_gate_up": 2 * gu,
+        "gemm_wgrad_down": 2 * dn,
+        "gemm_dgrad_gate_up": 4.0 * d * (R * H + 2 * T * Hs),
+        "gemm_router_dw": 2 * 2.0 * T * d * E,
+        "gemm_router_dx": 2 * 2.0 * T * d * E,
+    }
+    out["gemm_wgrad_gate_up (gather)"] = out["gemm_wgrad_gate_up"]
+    out["gemm_wgrad_down (gather)"] = out["gemm_wgrad_down"]
+    return out
+
+
+def with_issued(row, name, issued, ms, tensor_peak):
+    """Adds the issued MMA FLOPs of a split-precision kernel and their
+    fraction of the tensor peak (beside the algorithmic fraction)."""
+    if name in issued:
+        row["issued_mma_flops"] = issued[name]
+        row["issued_tensor_frac"] = round(issued[name] / (ms / 1000.0) / (tensor_peak * 1e12), 4)
+    return row
+
+
 def kernel_roofline(work, ms, tensor_peak, hbm_peak):
     """Binding roof of one launch: its algorithmic FLOPs at the tensor peak
     against its algorithmic bytes at the HBM peak; `frac` = the binding roof's
@@ -582,6 +612,7 @@ def main_ours(args):
     hbm_peak = peaks.get("hbm_gbs") or 6800.0
     peak_src = "measured" if peaks else "fallback"
     work = kernel_work(w, R, fused)
+    issued = issued_mma_flops(w, R)
     step_eager = eager_total / args.steps
     kernels = {}
     for name, e in per_kernel.items():
@@ -590,9 +621,11 @@ def main_ours(args):
                "share": round(mean * e["launches_per_step"] / step_eager, 4)}
         if name in work:
             row.update(kernel_roofline(work[name], mean, tensor_peak, hbm_peak))
+            with_issued(row, name, issued, mean, tensor_peak)
         kernels[name] = row
     dom = max((n for n in kernels if n in work), key=lambda n: kernels[n]["share"])
     roof = dict(kernel_roofline(work[dom], kernels[dom]["ms_per_launch"], tensor_peak, hbm_peak))
+    with_issued(roof, dom, issued, kernels[dom]["ms_per_launch"], tensor_peak)
     roof.update({"kernel": dom, "share_of_step": kernels[dom]["share"],
                  "traffic": profiled_traffic(w.name, dom),
                  "traffic_unit": "bytes per launch (ncu dram read + write)",
