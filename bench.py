@@ -26,7 +26,8 @@ at the rate of tiled TMA loads); the other is timed too (`other_path`).
 (the calls are asynchronous and allocate nothing); `fwd_tokens_per_s` does
 the same for the forward calls alone.  `kernels` times every kernel launch
 of the step with CUDA events that the library records just before each of
-its launches (moe_timing_begin), over eager steps; `roofline` is the kernel
+its launches (moe_timing_begin), captured as event-record nodes in a graph
+of the step and replayed like the timed region; `roofline` is the kernel
 with the largest share of the step, against the binding roof (tensor or HBM)
 of its algorithmic work, with the measured burst peaks.
 
@@ -433,9 +434,9 @@ def main_ours(args):
         raise RuntimeError(f"device status {st}: {B.status_string(st)}")
     R = int(layer.offsets[-1].item())
 
-    # ---- every kernel launch of the step, timed by the library's own event
-    # marks (eager steps, L2 flushed before each)
-    per_kernel = {}
+    # ---- eager steps (the calls issued one by one), timed by the library's
+    # own event marks, L2 flushed before each: the eager step time and the
+    # number of kernel launches per step
     eager_ms = []
     n_kernels = 0
     for i in range(args.steps):
@@ -446,12 +447,6 @@ def main_ours(args):
         lst = tm.launches()
         eager_ms.append(sum(ms for _, ms in lst))
         n_kernels = sum(1 for name, _ in lst if not name.startswith("memset"))
-        seen = {}
-        for name, ms in lst:
-            seen.setdefault(name, []).append(ms)
-        for name, v in seen.items():
-            e = per_kernel.setdefault(name, {"launches_per_step": len(v), "ms": []})
-            e["ms"].extend(v)
     eager_total = max_over_ranks([sum(eager_ms)], "cuda")[0]
 
     # ---- the step (and the forward alone) as CUDA-graph replays
@@ -504,6 +499,34 @@ def main_ours(args):
     other_fwd_ms = replay_ms(graphs["other_forward"]) if "other_forward" in graphs else None
     value = tokens_per_s(T, args.steps, world, graph_ms)
     fwd_value = tokens_per_s(T, args.steps, world, fwd_ms)
+
+    def graph_launch_times(fn):
+        """Every kernel launch of fn timed inside the timed region's form of
+        it: fn captured in a CUDA graph with the library's timing marks (an
+        event-record node before each launch), replayed args.steps times with
+        L2 flushed before each.  {name: [ms of each launch]}"""
+        tmr = B.LaunchTimer(capacity=64, stream=gstream)  # events created outside the capture
+        gstream.wait_stream(main_stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gstream):
+            with tmr:
+                fn(gstream)
+        main_stream.wait_stream(gstream)
+        for _ in range(3):
+            flush.fill_(1)
+            g.replay()
+        times = {}
+        for i in range(args.steps):
+            flush.fill_(1)
+            g.replay()
+            torch.cuda.synchronize()
+            for name, ms in tmr.launches():
+                times.setdefault(name, []).append(ms)
+        return times
+
+    per_kernel = {name: {"launches_per_step": len(v) // args.steps, "ms": v}
+                  for name, v in graph_launch_times(step).items()}
+    timed_total = max_over_ranks([sum(sum(e["ms"]) for e in per_kernel.values())], "cuda")[0]
     # the smallest layer's working set fits in L2: its hot-L2 rate (replays
     # back to back, no flush) is reported beside the flushed one
     hot_l2 = None
@@ -589,14 +612,7 @@ def main_ours(args):
         st = B.moe_device_status()
         if st != 0:
             raise RuntimeError(f"device status {st} in the MXFP8 forward: {B.status_string(st)}")
-        mx_kernels = {}
-        for i in range(args.steps):
-            flush.fill_(1)
-            with B.LaunchTimer(capacity=64, stream=main_stream) as tm:
-                mx_forward(main_stream)
-            torch.cuda.synchronize()
-            for name, ms in tm.launches():
-                mx_kernels.setdefault(name, []).append(ms)
+        mx_kernels = graph_launch_times(mx_forward)
         gstream.wait_stream(main_stream)
         gmx = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gmx, stream=gstream):
@@ -624,11 +640,12 @@ def main_ours(args):
     work = kernel_work(w, R, fused)
     issued = issued_mma_flops(w, R)
     step_eager = eager_total / args.steps
+    step_timed = timed_total / args.steps
     kernels = {}
     for name, e in per_kernel.items():
         mean = statistics.mean(e["ms"])
         row = {"launches_per_step": e["launches_per_step"], "ms_per_launch": round(mean, 4),
-               "share": round(mean * e["launches_per_step"] / step_eager, 4)}
+               "share": round(mean * e["launches_per_step"] / step_timed, 4)}
         if name in work:
             row.update(kernel_roofline(work[name], mean, tensor_peak, hbm_peak))
             with_issued(row, name, issued, mean, tensor_peak)
@@ -740,8 +757,9 @@ def main_ours(args):
                        "routing": w.routing, "capacity": w.capacity, "pass": "forward+backward",
                        "l2": "flushed before every step (256 MB write)", "parallelism": f"replicas x{world}",
                        "timing": "value / fwd_tokens_per_s: the C-ABI calls of the step / of the forward "
-                                 "captured once in a CUDA graph and replayed; kernels: every launch of eager "
-                                 "steps, timed by events the library records before each launch"},
+                                 "captured once in a CUDA graph and replayed; kernels: every launch of the "
+                                 "step, timed by event-record nodes the library puts before each launch in a "
+                                 "graph of the step, replayed the same way"},
             "fwd_tokens_per_s": fwd_value,
             "path": args.path,
             "other_path": None if other_ms is None else {

@@ -114,12 +114,21 @@ MOE_API int moe_device_status(int* status_out);
  * launch i took elapsed(events[i], events[i+1]) (queue gaps included).
  * moe_timing_end stops recording and returns the number of launches seen;
  * moe_timing_name(i) is the i-th launch's kernel name (a static string, ""
- * out of range), valid until the next moe_timing_begin in this thread.  Use
- * outside stream capture.  MOE_ERR_INVALID_ARG: NULL events, a negative
- * capacity, or moe_timing_end without a begin. */
+ * out of range), valid until the next moe_timing_begin in this thread.
+ * Inside stream capture the records become event-record nodes of the graph
+ * (cudaEventRecordExternal): every replay records the events again, so the
+ * launches of one replay are timed after it completes.  A record node
+ * between two launches orders them plainly (no programmatic overlap).
+ * MOE_ERR_INVALID_ARG: NULL events, a negative capacity, or moe_timing_end
+ * without a begin.
+ * moe_timing_record: records one caller event on `stream` the same way (an
+ * event-record node when the stream is capturing): the closing event after
+ * the last call.  MOE_ERR_INVALID_ARG: NULL event; MOE_ERR_CUDA: the record
+ * failed. */
 MOE_API int moe_timing_begin(void* const* events, int capacity);
 MOE_API int moe_timing_end(int* n_launches);
 MOE_API const char* moe_timing_name(int i);
+MOE_API int moe_timing_record(void* event, void* stream);
 
 /* Workspace bytes needed by every call below for this shape (the maximum
  * over the calls; a single buffer can serve all of them in sequence on one

@@ -37,6 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         if n not in ("moe_version", "moe_status_string", "moe_last_cuda_error", "moe_device_status",
                      "moe_workspace_size", "moe_timing_begin", "moe_timing_end", "moe_timing_name",
+                     "moe_timing_record",
                      "moe_mxfp8_rows", "moe_mxfp8_scales_bytes"):
             assert n in lib.SIGNATURES, n
 
@@ -149,3 +150,4 @@ def test_launch_timing_host_side(lib):
     assert L.moe_timing_begin(None, 0) == lib.MOE_OK
     assert L.moe_timing_end(ctypes.byref(n)) == lib.MOE_OK and n.value == 0
     assert L.moe_timing_name(0) == b"" and L.moe_timing_name(-1) == b""
+    assert L.moe_timing_record(None, None) == lib.MOE_ERR_INVALID_ARG

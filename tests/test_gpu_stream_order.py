@@ -60,3 +60,34 @@ def test_caller_kernels_around_the_calls_stay_ordered(B, name, fused):
     got = snapshot(layer)
     for n in ref:
         assert torch.equal(ref[n].view(torch.uint8), got[n].view(torch.uint8)), n
+
+
+def test_launch_timing_eager_and_inside_a_graph(B):
+    """The library's timing marks: eager calls and a captured graph of the
+    same step see the same launches in the same order, and the graph's marks
+    are recorded again at each replay (times that add up to more than 0)."""
+    from top_routing_grouped_moe_gb300.layer import MoELayer
+    w = CASES["learned_shared"]
+    dev = upload(workloads.make_inputs(w))
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with B.LaunchTimer(capacity=64, stream=s) as tm:
+        step(layer, w, dev, stream=s)
+    torch.cuda.synchronize()
+    eager = tm.launches()
+    assert len(eager) >= 10 and all(ms >= 0 for _, ms in eager) and sum(ms for _, ms in eager) > 0
+    tg = B.LaunchTimer(capacity=64, stream=s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        with tg:
+            step(layer, w, dev, stream=s)
+    torch.cuda.synchronize()
+    names = [n for n, _ in eager if not n.startswith("memset")]
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        got = tg.launches()
+        assert [n for n, _ in got if not n.startswith("memset")] == names
+        assert all(ms >= 0 for _, ms in got) and sum(ms for _, ms in got) > 0
+    assert B.moe_device_status() == 0

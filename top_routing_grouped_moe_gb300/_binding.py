@@ -93,6 +93,8 @@ _lib.moe_timing_end.restype = _I
 _lib.moe_timing_end.argtypes = [ctypes.POINTER(_I)]
 _lib.moe_timing_name.restype = ctypes.c_char_p
 _lib.moe_timing_name.argtypes = [_I]
+_lib.moe_timing_record.restype = _I
+_lib.moe_timing_record.argtypes = [_P, _P]
 
 
 def _ptr(v):
@@ -162,8 +164,9 @@ class LaunchTimer:
     """Times every kernel launch of the library's calls made inside a `with`
     block in this thread (moe_timing_begin / moe_timing_end), with CUDA
     events recorded on each launch's own stream.  After the block and a
-    synchronize, `launches()` gives [(kernel name, ms)].  Use outside stream
-    capture."""
+    synchronize, `launches()` gives [(kernel name, ms)].  Inside stream
+    capture the records become event-record nodes of the graph: after each
+    replay and a synchronize, `launches()` gives that replay's times."""
 
     def __init__(self, capacity=256, stream=None):
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(capacity + 1)]
@@ -191,8 +194,11 @@ class LaunchTimer:
         if self.n > len(self._arr):
             raise RuntimeError(f"LaunchTimer: {self.n} launches, capacity {len(self._arr)}")
         self.names = [_lib.moe_timing_name(i).decode() for i in range(self.n)]
-        # the end of the last launch
-        self.events[self.n].record(self.stream if self.stream is not None else torch.cuda.current_stream())
+        # the end of the last launch (a graph node too, when capturing)
+        s = self.stream if self.stream is not None else torch.cuda.current_stream()
+        rc = _lib.moe_timing_record(ctypes.c_void_p(self.events[self.n].cuda_event), ctypes.c_void_p(s.cuda_stream))
+        if rc != MOE_OK:
+            raise MoEError("moe_timing_record", rc, status_string(rc))
         return False
 
     def launches(self):

@@ -97,11 +97,21 @@ int check_hidden(int H, int Hs) {
 
 void record_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
 
+// An event record on `s`; while `s` is capturing, an event-record node of
+// the graph (recorded again at every replay).
+cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, s);
+}
+
 void timing_mark(cudaStream_t s, const char* name) {
   LaunchTiming& lt = t_timing;
   if (!lt.on) return;
   if (lt.n < lt.capacity) {
-    cudaEventRecord(static_cast<cudaEvent_t>(lt.events[lt.n]), s);
+    record_timing_event(static_cast<cudaEvent_t>(lt.events[lt.n]), s);
     lt.names.push_back(name);
   }
   ++lt.n;
@@ -194,6 +204,11 @@ int moe_timing_end(int* n_launches) {
   lt.events = nullptr;
   if (n_launches) *n_launches = lt.n;
   return MOE_OK;
+}
+
+int moe_timing_record(void* event, void* stream) {
+  if (!event) return MOE_ERR_INVALID_ARG;
+  return check(record_timing_event(static_cast<cudaEvent_t>(event), static_cast<cudaStream_t>(stream)));
 }
 
 const char* moe_timing_name(int i) {
