@@ -305,7 +305,7 @@ MOE_API int moe_unpermute_combine(const void* o_perm, const void* s, const float
  * GEMMs use (each expert's rows are read through maps re-based on the device
  * from the offsets): builds the per-group maps of two operands for an offsets
  * table with empty, one-row and ragged groups and compares each map byte for
- * byte with the map the driver's encoder gives for the same sub-matrix.  No
+ * byte with the map the CUDA driver's encoder gives for the same sub-matrix.  No
  * tensor copy runs.  Returns MOE_OK, or MOE_ERR_UNSUPPORTED if a map differs.
  * Allocates and frees its own scratch and synchronizes the device. */
 MOE_API int moe_selftest_group_maps(void);

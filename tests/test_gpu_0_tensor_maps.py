@@ -1,7 +1,7 @@
 """The weight-gradient GEMMs read each expert's rows through tensor maps
 patched on the device (base address and row extent re-set per group).  This
 file sorts before every test that runs those GEMMs: the patched maps must be
-byte-identical to the maps the driver's encoder gives for the same
+byte-identical to the maps the CUDA driver's encoder gives for the same
 sub-matrices (empty, one-row and ragged groups)."""
 import pytest
 import torch
