@@ -418,6 +418,16 @@ def main_ours(args):
             lay.backward(dev["x"], dev["dY"], dev, learned_router=learned, stream=stream)
         return forward, step
 
+    def forward_nosave(stream):
+        """The forward alone as a forward-only pass runs it: a|u are not kept
+        for a backward (the activation-recompute form of the forward)."""
+        keep = layer.recompute
+        layer.recompute = True
+        try:
+            layer.forward(dev["x"], dev, logits_in=logits_in, stream=stream)
+        finally:
+            layer.recompute = keep
+
     forward, step = calls(layer)
     other = "unfused" if fused else "fused"
     other_forward, other_step = calls(layers[other])
@@ -452,7 +462,7 @@ def main_ours(args):
     # ---- the step (and the forward alone) as CUDA-graph replays
     gstream = torch.cuda.Stream()
     graphs = {}
-    graph_fns = [("step", step), ("forward", forward)]
+    graph_fns = [("step", step), ("forward", forward), ("forward_nosave", forward_nosave)]
     if not args.no_other_path:
         graph_fns += [("other_step", other_step), ("other_forward", other_forward)]
     for gname, fn in graph_fns:
@@ -495,6 +505,7 @@ def main_ours(args):
     wall = time.perf_counter() - wall0
     fwd_ms = replay_ms(graphs["forward"])
     clocks = sampler.stop()
+    nosave_ms = replay_ms(graphs["forward_nosave"])
     other_ms = replay_ms(graphs["other_step"]) if "other_step" in graphs else None
     other_fwd_ms = replay_ms(graphs["other_forward"]) if "other_forward" in graphs else None
     value = tokens_per_s(T, args.steps, world, graph_ms)
@@ -771,9 +782,17 @@ def main_ours(args):
                         "graph replay, L2 flushed before each"},
             "mxfp8_forward": mx_fwd,
             "fwd_ms_per_step": fwd_ms / args.steps,
+            "fwd_nosave": {"tokens_per_s": tokens_per_s(T, args.steps, world, nosave_ms),
+                           "ms_per_step": nosave_ms / args.steps,
+                           "gemm_tflops": ffl / (nosave_ms / args.steps / 1000.0) / 1e12,
+                           "note": "the forward as a forward-only pass: a|u not kept for a backward; graph "
+                                   "replay, L2 flushed before each"},
             "hot_l2": hot_l2,
             "eager": {"value": tokens_per_s(T, args.steps, world, eager_total), "ms_per_step": step_eager},
             "gemm_tflops_fwd_bwd": (ffl + bfl) / (graph_ms / args.steps / 1000.0) / 1e12,
+            # the forward alone (configurations whose pass is the forward)
+            "gemm_tflops_fwd": ffl / (fwd_ms / args.steps / 1000.0) / 1e12,
+            "gemm_frac_bf16_fwd": round(ffl / (fwd_ms / args.steps / 1000.0) / 1e12 / tensor_peak, 4),
             "gemm_frac_bf16_fwd_bwd": round((ffl + bfl) / (graph_ms / args.steps / 1000.0) / 1e12 / tensor_peak, 4),
             "roofline": roof,
             "kernels": dict(sorted(kernels.items(), key=lambda kv: -kv[1]["share"])),
