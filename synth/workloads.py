@@ -24,6 +24,7 @@ Storage layouts (row-major, the layout the C ABI takes):
 from __future__ import annotations
 
 from dataclasses import dataclass, field
+from fractions import Fraction
 
 import numpy as np
 
@@ -48,11 +49,13 @@ class Workload:
 
     @property
     def capacity(self) -> int:
-        """ceil(cf*T*k/E) computed exactly for cf = 1.25 (= 5/4); 0 = dropless."""
+        """ceil(cf*T*k/E) computed exactly in integers, cf taken as the
+        fraction it denotes (1.25 = 5/4, 0.25 = 1/4); 0 = dropless."""
         if self.capacity_factor == 0.0:
             return 0
-        assert self.capacity_factor == 1.25
-        return (5 * self.T * self.k + 4 * self.E - 1) // (4 * self.E)
+        f = Fraction(self.capacity_factor).limit_denominator(1000)
+        assert f > 0 and abs(float(f) - self.capacity_factor) < 1e-12
+        return (f.numerator * self.T * self.k + f.denominator * self.E - 1) // (f.denominator * self.E)
 
 
 WORKLOADS = {

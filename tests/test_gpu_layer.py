@@ -35,6 +35,11 @@ CASES = {
     # the largest E and k: most experts hold 0-6 rows
     "e256_k8": workloads.custom("e256_k8", T=64, d=256, E=256, k=8, H=128, Hs=0),
     "single_token": workloads.custom("single_token", T=1, d=256, E=8, k=2, H=128, Hs=128),
+    # capacity far below the load: C = 44 rows per expert, three quarters of
+    # the (token, slot) pairs dropped, most experts exactly full
+    "heavy_drops": workloads.custom("heavy_drops", T=700, d=256, E=16, k=4, H=256, Hs=128, capacity_factor=0.25),
+    # k = E: every token in every expert (all segments T rows long)
+    "k_equals_E": workloads.custom("k_equals_E", T=100, d=256, E=8, k=8, H=128, Hs=0),
 }
 
 
@@ -79,7 +84,7 @@ def test_layer_forward_backward_parity(B, name):
     compare_layer(w, inp, layer, ref, refb)
 
 
-@pytest.mark.parametrize("name", ["zipf_capacity", "partial_tiles"])
+@pytest.mark.parametrize("name", ["zipf_capacity", "partial_tiles", "heavy_drops"])
 def test_unwritten_rows_never_leak(B, name):
     """All output and scratch buffers filled with NaN before the step: rows
     past the kept ones (capacity drop) and past each tile's valid rows are

@@ -311,6 +311,11 @@ def test_capacity_formula():
     assert orc.capacity_of(8192, 4, 64) == 640          # 1.25 * 8192 * 4 / 64 exactly
     assert orc.capacity_of(10, 1, 3) == math.ceil(1.25 * 10 / 3)
     assert workloads.WORKLOADS["tiny64e_zipf_cap125"].capacity == 640
+    # other factors, as the fractions they denote: ceil(0.25 * 700 * 4 / 16) =
+    # ceil(43.75) = 44; an exact multiple does not round up
+    assert workloads.custom("c", T=700, d=256, E=16, k=4, H=256, Hs=0, capacity_factor=0.25).capacity == 44
+    assert workloads.custom("c", T=64, d=256, E=16, k=4, H=256, Hs=0, capacity_factor=0.5).capacity == 8
+    assert workloads.custom("c", T=64, d=256, E=16, k=4, H=256, Hs=0).capacity == 0
 
 
 # ---------------------------------------------------------------- balance loss
