@@ -61,3 +61,28 @@ def test_roofline_takes_the_binding_roof():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert r["achieved"] == pytest.approx(1000.0) and r["frac"] == pytest.approx(0.2)
     assert r["tensor_frac"] == pytest.approx(0.05)
+
+
+def test_reference_arm_line_contract():
+    """`bench.py --impl reference` (the C++ oracle on the host cores) prints
+    one JSON line with the keys of the benchmark contract."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                          "--steps", "2", "--warmup", "1", "--cpu-sample-tokens", "16"],
+                         capture_output=True, text=True, timeout=600, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 1
+    assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert d["config"]["workload"] == "tiny" and d["config"]["sample_tokens"] == 16
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
