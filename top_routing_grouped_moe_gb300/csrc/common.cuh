@@ -66,19 +66,6 @@ __device__ __forceinline__ void unpack_f16x8(const uint4& v, float (&f)[8]) {
   f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-// v = hi + lo with hi = bf16(v), lo = bf16(v - hi): about 16 significant bits
-// in two bf16 halves (8 values each, packed).
-__device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
-  float h[8], l[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    h[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
-    l[e] = v[e] - h[e];
-  }
-  hi = pack8(h);
-  lo = pack8(l);
-}
-
 // ------------------------------------------------------------ MXFP8
 // (E4M3 elements, one E8M0 scale 2^(floor(log2 max|v|) - 8) per 32 values along
 // K; scales of rows [128 t, 128 t + 128) x blocks [4 q, 4 q + 4) form one
