@@ -5,9 +5,11 @@ multiple of 64 in [128, 512], E in {8, 16, 24, 40, 64} (E a multiple of 8),
 k in [1, min(8, E)], H and Hs multiples of 128 (Hs = 0: no shared expert),
 learned or random routing, the Zipf bias on some learned cases, and dropless
 or capacity-limited (factors 1.25 and 0.5).  Each uses its own input seed.
-Forward and backward are compared with the C++ oracle exactly as the fixed
-cases are (tests/gpu_util.py): routing and permutation bit for bit on the
-GPU's own fp32 logits, every output and gradient within the layer tolerance."""
+Forward and backward, through both call sequences (unfused, and fused: row
+gathers in the GEMM loads, the combine in the shared down projection), are
+compared with the C++ oracle exactly as the fixed cases are
+(tests/gpu_util.py): routing and permutation bit for bit on the GPU's own
+fp32 logits, every output and gradient within the layer tolerance."""
 import random
 
 import pytest
@@ -48,15 +50,16 @@ def B():
     return _binding
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["unfused", "fused"])
 @pytest.mark.parametrize("case", range(len(CASES)), ids=[
     f"{w.name}-T{w.T}-d{w.d}-E{w.E}-k{w.k}-H{w.H}-Hs{w.Hs}-{w.routing}{'-zipf' if w.zipf_bias else ''}"
     f"-cap{w.capacity}" for w, _ in CASES])
-def test_random_shape_layer_parity(B, case):
+def test_random_shape_layer_parity(B, case, fused):
     from top_routing_grouped_moe_gb300.layer import MoELayer
     w, base = CASES[case]
     inp = workloads.make_inputs(w, base=base)
     dev = upload(inp)
-    layer = MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity, fused=fused)
     layer.forward(dev["x"], dev, logits_in=dev.get("logits_in"))
     layer.backward(dev["x"], dev["dY"], dev, learned_router=w.routing == "learned")
     torch.cuda.synchronize()
