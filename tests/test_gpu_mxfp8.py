@@ -98,6 +98,24 @@ CASES = {
 }
 
 
+def _random_cases(n=5, seed=20261203):
+    """Seeded random shapes within the MXFP8 path's limits: d a multiple of
+    128, E a multiple of 8, k <= min(8, E), H and Hs multiples of 128, a
+    shared expert, learned routing (with the Zipf bias or a capacity on some)."""
+    import random
+    rng = random.Random(seed)
+    out = {}
+    for i in range(n):
+        E = rng.choice([8, 16, 24, 40, 64])
+        out[f"random{i}"] = dict(T=rng.randint(1, 600), d=128 * rng.randint(1, 4), E=E, k=rng.randint(1, min(8, E)),
+                                 H=128 * rng.randint(1, 4), Hs=128 * rng.randint(1, 2), routing="learned",
+                                 zipf_bias=rng.random() < 0.3, capacity_factor=rng.choice([0.0, 1.25, 0.5]))
+    return out
+
+
+CASES.update(_random_cases())
+
+
 def run_mx_layer(B, w, inp):
     """Routing (bf16 path), the MX permutation, the weights quantized, the MX
     expert MLP and the combine; returns every buffer as numpy."""
