@@ -36,16 +36,21 @@ def upload(inp: dict) -> dict:
     return out
 
 
-MARGINS = {}  # name -> (max err/(atol + rtol|ref|), relative Frobenius), of the last comparison
+MARGINS = {}  # name -> (max err/bound, relative Frobenius), of the last comparison
 
 
-def assert_close(name, gpu: np.ndarray, ref: np.ndarray, atol=ATOL, rtol=RTOL, fro=FRO):
+def assert_close(name, gpu: np.ndarray, ref: np.ndarray, atol=ATOL, rtol=RTOL, fro=FRO, allow=None):
+    """allow: an optional per-element absolute allowance added to the bound
+    (a rounding bound derived from the arithmetic, for shapes beyond the
+    layer configurations the bar is stated for)."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert gpu.shape == ref.shape, (name, gpu.shape, ref.shape)
     assert np.all(np.isfinite(gpu)), f"{name}: non-finite values"
     err = np.abs(gpu - ref)
     bound = atol + rtol * np.abs(ref)
+    if allow is not None:
+        bound = bound + np.broadcast_to(np.asarray(allow, dtype=np.float64), bound.shape)
     bad = err > bound
     nref = np.linalg.norm(ref)
     rel = np.linalg.norm(gpu - ref) / nref if nref > 0 else np.linalg.norm(gpu)
@@ -53,11 +58,14 @@ def assert_close(name, gpu: np.ndarray, ref: np.ndarray, atol=ATOL, rtol=RTOL, f
         ratio = float(np.max(np.where(bound > 0, err / np.where(bound > 0, bound, 1), np.where(err > 0, np.inf, 0))))
     MARGINS[name] = (ratio, float(rel))
     if bad.any():
-        i = np.unravel_index(np.argmax(err - (atol + rtol * np.abs(ref))), err.shape)
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError(f"{name}: {bad.sum()} of {bad.size} elements out of tolerance; worst at {i}: "
                              f"gpu {gpu[i]!r} ref {ref[i]!r}; rel fro {rel:.3e}")
     assert rel <= fro, f"{name}: relative Frobenius error {rel:.3e} > {fro}"
     return rel
+
+
+_assert_close = assert_close  # for compare_layer, whose local wrapper shadows the name
 
 
 def near_tie_tokens(logits: np.ndarray, k: int, delta: float) -> np.ndarray:
@@ -146,17 +154,22 @@ def oracle_reference(w, inp, layer, f64=None, impl=None):
     return f64, ref, refb, flips
 
 
-def compare_layer(w, inp, layer, ref, refb):
+def compare_layer(w, inp, layer, ref, refb, allow=None):
     """Compares a finished MoELayer forward+backward with the oracle's
     (`oracle_reference`: the oracle run on the same fp32 logits).  Top-k
     indices, counts, offsets, both row maps, x_perm and dY_perm bit-exact;
     every floating output and gradient within the layer tolerance, every
     token and every expert.  A fused layer (the permutation inside the GEMMs'
     loads, the combine inside the shared down projection) has no x_perm,
-    dY_perm or s, and holds the expert outputs by slot."""
+    dY_perm or s, and holds the expert outputs by slot.  allow: optional
+    per-element allowances by tensor name (assert_close)."""
     import torch
     MARGINS.clear()
     k = w.k
+    allow = allow or {}
+
+    def assert_close(name, gpu, ref_, **kw):
+        return _assert_close(name, gpu, ref_, allow=allow.get(name), **kw)
 
     # routing and permutation: bit-exact
     assert np.array_equal(layer.idx.cpu().numpy(), ref["idx"]), "topk_idx"
