@@ -130,6 +130,7 @@ def kernel_work(w, R, fused=False):
         "gather_rows": (0.0, T * d * 2 + R * d * 2 + T * k * 4),
         "unpermute_reduce": (0.0, R * d * 2 + T * d * 2 * sh + T * d * 2 + T * k * 4),
         "topk_gating": (0.0, T * E * 4 + T * k * 8),
+        "grad_amax": (0.0, T * d * 2),  # the scale word of the backward's fp16 terms: dY read once
         # MXFP8 forward: E4M3 operands (1 byte) with one scale byte per 32
         "gemm_mx_gate_up_swiglu": (gu, (R * d + T * d * sh) * 33 // 32 + wgu // 2 * 33 // 32
                                    + hid * 33 // 32),

@@ -361,6 +361,14 @@ MOE_API int moe_unpermute_combine_bwd(const void* dY, const int32_t* row_of_slot
  * permutation fused into their operand loads, no moe_unpermute_combine_bwd
  * call needed; slower than the permuted copies on GB300);
  * dY and x are required.  Same results as with the permuted copies.
+ * dx_scale (nullable; requires dY): a device uint32 scale word.  The call
+ * writes into it the largest bf16 magnitude of dY (the bit pattern of
+ * max |dY|), whose power of two 2^e (e = floor(log2 max|dY|), 0 for a zero
+ * or non-finite dY) then divides dx_perm and dx_s: the fp16 terms sit where
+ * they sit for gradients of order one whatever the gradient's own scale (a
+ * loss averaged over many tokens gives |dY| far below fp16's normal range),
+ * and moe_permute_bwd, given the same word, multiplies the sum by 2^e.
+ * Both scalings are exact; NULL: the terms are stored unscaled.
  * ws >= moe_workspace_size() bytes. */
 MOE_API int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gates,
                            const int32_t* row_of_slot, const int32_t* slot_of_row,
@@ -372,7 +380,7 @@ MOE_API int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const fl
                            void* dx_perm, void* dx_s,
                            void* dW_g, void* dW_u, void* dW_d,
                            void* dWs_g, void* dWs_u, void* dWs_d,
-                           float* dgates, void* ws, size_t ws_bytes, void* stream);
+                           float* dgates, uint32_t* dx_scale, void* ws, size_t ws_bytes, void* stream);
 
 /* Backward of the top-k softmax gating and of the router product:
  *   dlogits[t,e] = g_s (dgates[t,s] - sum_j g_j dgates[t,j]) if e = topk_idx[t,s],
@@ -419,10 +427,13 @@ MOE_API int moe_router_balance_loss(const float* logits, const int32_t* counts_r
  * MOE_ERR_RANGE).  dx_s may be NULL (no
  * shared expert); dlogits and W_r may both be NULL (given-logits routing).
  * The router term uses the tensor cores with dlogits as a bf16 hi + lo pair
- * and enters the sum as an fp16 term. */
+ * and enters the sum as an fp16 term.  dx_scale (nullable): the scale word
+ * moe_grouped_swiglu_bwd wrote when it produced dx_perm and dx_s; the router
+ * term is stored divided by the same 2^e and the sum multiplied by 2^e
+ * (NULL: e = 0, unscaled terms). */
 MOE_API int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot,
                     const float* dlogits, const void* W_r,
-                    int T, int d, int E, int k, void* dx,
+                    int T, int d, int E, int k, void* dx, const uint32_t* dx_scale,
                     void* ws, size_t ws_bytes, void* stream);
 
 /* ----------------------------------------------------------------- MXFP8 */

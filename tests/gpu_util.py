@@ -2,6 +2,8 @@
 tolerance, and the routing near-tie analysis."""
 from __future__ import annotations
 
+import math
+
 import numpy as np
 import torch
 
@@ -201,14 +203,23 @@ def compare_layer(w, inp, layer, ref, refb, allow=None):
         assert_close("s", host_f64(layer.s), ref["s"])
     assert_close("y", host_f64(layer.y), ref["y"])
 
-    # backward
-    assert_close("dx_perm", host_f64(layer.dx_perm[:R]), refb["dx_perm"])
+    # backward; the stored fp16 input-gradient terms are the values divided by
+    # 2^e, e = floor(log2 max|dY|), when the layer keeps a gradient scale word
+    # (which must hold max|dY|'s bf16 magnitude pattern)
+    up = 1.0
+    if getattr(layer, "dx_scale", None) is not None:
+        m = int((inp["dY"].astype(np.uint32) & 0x7FFF).max())
+        assert (int(layer.dx_scale.item()) & 0xFFFFFFFF) == m, "gradient scale word"
+        amax = float(np.array([m << 16], dtype=np.uint32).view(np.float32)[0])
+        if 0.0 < amax < np.inf:
+            up = 2.0 ** math.floor(math.log2(amax))
+    assert_close("dx_perm", host_f64(layer.dx_perm[:R]) * up, refb["dx_perm"])
     assert_close("dgates", layer.dgates.cpu().numpy(), refb["dgates"])
     assert_close("dW_d", host_f64(layer.dW_d), refb["dW_d"])
     assert_close("dW_g", host_f64(layer.dW_g), refb["dW_g"])
     assert_close("dW_u", host_f64(layer.dW_u), refb["dW_u"])
     if w.Hs:
-        assert_close("dx_s", host_f64(layer.dx_s), refb["dx_s"])
+        assert_close("dx_s", host_f64(layer.dx_s) * up, refb["dx_s"])
         assert_close("dWs_d", host_f64(layer.dWs_d), refb["dWs_d"])
         assert_close("dWs_g", host_f64(layer.dWs_g), refb["dWs_g"])
         assert_close("dWs_u", host_f64(layer.dWs_u), refb["dWs_u"])

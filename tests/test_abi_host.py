@@ -128,6 +128,10 @@ P = 1 << 12  # stand-in device addresses (16-byte aligned); never dereferenced
     # backward, gather form: no dY to gather from
     (lambda L: L.moe_grouped_swiglu_bwd(None, None, P, P, P, P, None, P, P, P, 16, 128, 8, 2, 128, 0, P, P, P,
                                         None, None, None, P, None, P, P, P, None, None, None, P, P, 1 << 30, 0), 1),
+    # backward: a scale word without the dY it is taken from (Hs = 0 allows dY = NULL)
+    (lambda L: L.moe_grouped_swiglu_bwd(P, None, P, P, P, P, P, None, P, None, 16, 128, 8, 2, 128, 0, P, P, P,
+                                        None, None, None, P, None, P, P, P, None, None, None, P, P, 1 << 30, 0,
+                                        dx_scale=P), 1),
     # permute, maps only: still needs its maps
     (lambda L: L.moe_permute(None, P, 16, 128, 64, 4, 0, P, P, P, None, P, None, P, 1 << 20, 0), 1),
 ])

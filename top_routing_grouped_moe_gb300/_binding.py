@@ -53,10 +53,10 @@ SIGNATURES = {
     "moe_grouped_swiglu_recompute_fused": "ppp" + "iiiiii" + "pppp" + "pp" + "s",
     "moe_unpermute_combine": "pppp" + "iii" + "p" + "s",
     "moe_unpermute_combine_bwd": "pp" + "iii" + "p" + "s",
-    "moe_grouped_swiglu_bwd": "pppppppppp" + "iiiiii" + "pppppp" + "pp" + "pppppp" + "p" + "pz" + "s",
+    "moe_grouped_swiglu_bwd": "pppppppppp" + "iiiiii" + "pppppp" + "pp" + "pppppp" + "pp" + "pz" + "s",
     "moe_route_topk_bwd": "pppp" + "iiii" + "ppp" + "pz" + "s",
     "moe_router_balance_loss": "pp" + "iii" + "f" + "ppp" + "pz" + "s",
-    "moe_permute_bwd": "ppppp" + "iiii" + "p" + "pz" + "s",
+    "moe_permute_bwd": "ppppp" + "iiii" + "pp" + "pz" + "s",
     "moe_mxfp8_quantize": "p" + "Li" + "pp" + "s",
     "moe_mxfp8_quantize_gate_up": "pp" + "iii" + "pp" + "s",
     "moe_permute_mxfp8": "pp" + "iiiii" + "pppppp" + "pp" + "pz" + "s",
@@ -256,10 +256,12 @@ def moe_unpermute_combine_bwd(dY, row_of_slot, T, d, k, dY_perm, stream=None):
 
 def moe_grouped_swiglu_bwd(dY_perm, dY, gates, row_of_slot, slot_of_row, offsets, x_perm, x, au, au_s, T, d, E, k,
                            H, Hs, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, dx_perm, dx_s, dW_g, dW_u, dW_d, dWs_g, dWs_u,
-                           dWs_d, dgates, ws, ws_bytes, stream=None):
+                           dWs_d, dgates, ws, ws_bytes, stream=None, dx_scale=None):
+    """dx_scale: optional int32/uint32 [1] device word (see moe.h): the fp16
+    terms dx_perm / dx_s are stored divided by 2^e of max |dY|."""
     return _call("moe_grouped_swiglu_bwd", dY_perm, dY, gates, row_of_slot, slot_of_row, offsets, x_perm, x, au,
                  au_s, T, d, E, k, H, Hs, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, dx_perm, dx_s, dW_g, dW_u, dW_d, dWs_g,
-                 dWs_u, dWs_d, dgates, ws, ws_bytes, stream)
+                 dWs_u, dWs_d, dgates, dx_scale, ws, ws_bytes, stream)
 
 
 def moe_route_topk_bwd(dgates, gates, topk_idx, x, T, d, E, k, dlogits, dW_r, ws, ws_bytes, stream=None,
@@ -273,8 +275,11 @@ def moe_router_balance_loss(logits, counts_raw, T, E, k, alpha, loss, P_mean, dl
                  ws_bytes, stream)
 
 
-def moe_permute_bwd(dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream=None):
-    return _call("moe_permute_bwd", dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream)
+def moe_permute_bwd(dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, ws, ws_bytes, stream=None,
+                    dx_scale=None):
+    """dx_scale: the word moe_grouped_swiglu_bwd wrote for these terms (or None)."""
+    return _call("moe_permute_bwd", dx_perm, dx_s, row_of_slot, dlogits, W_r, T, d, E, k, dx, dx_scale, ws,
+                 ws_bytes, stream)
 
 
 def moe_mxfp8_rows(T, E, k) -> int:

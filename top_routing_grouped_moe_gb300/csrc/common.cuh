@@ -66,6 +66,23 @@ __device__ __forceinline__ void unpack_f16x8(const uint4& v, float (&f)[8]) {
   f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+// ------------------------------------------------------------ gradient-term scale
+// The backward's fp16 sum terms (input-gradient rows) are stored divided by
+// 2^e, e = floor(log2 max|dY|): the terms then sit where they sit for
+// gradients of order one whatever the gradient's own scale, and the sum is
+// multiplied by 2^e again (both exact).  The scale word holds the largest
+// bf16 magnitude pattern of dY (an integer maximum, independent of order).
+
+// e of a bf16 magnitude pattern: 0 for zero, inf or NaN (the finite checks
+// report the latter two), clamped to [-126, 126].
+__device__ __forceinline__ int grad_scale_exp(unsigned word) {
+  const int f = (int)((word >> 7) & 0xFFu);
+  if (word == 0u || f == 0xFF) return 0;
+  return min(max(f - 127, -126), 126);
+}
+// 2^e as an fp32 normal, e in [-126, 127]
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
 // ------------------------------------------------------------ MXFP8
 // (E4M3 elements, one E8M0 scale 2^(floor(log2 max|v|) - 8) per 32 values along
 // K; scales of rows [128 t, 128 t + 128) x blocks [4 q, 4 q + 4) form one

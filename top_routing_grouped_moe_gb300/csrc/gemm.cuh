@@ -128,6 +128,7 @@ struct Problem {
   long long ld_aux;
   const float* bias;   // EPI_F32 (nullable)
   int out_f16;         // EPI_F32: out holds fp16 (a value beyond its range records MOE_ERR_RANGE)
+  const uint32_t* out_scale;  // out_f16: values stored divided by 2^e of this gradient scale word (NULL: e = 0)
   int H;               // SWIGLU: column offset of u within au
   // EPI_SWIGLU_BWD
   const float* gates;      // per-slot gate (nullable: g = 1)
@@ -1115,6 +1116,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
           }
         }
         const bool comb = MODE == MGROUP && pr.comb_y != nullptr;
+        const float down = pr.out_scale ? pow2f(-grad_scale_exp(__ldg(pr.out_scale))) : 1.0f;
         const int ck = pr.comb_k;
         const __half* comb_o = reinterpret_cast<const __half*>(pr.comb_o);
         const int c_end = ti.half ? col_shift + pr.mma_n / 2 : pr.n_tile;
@@ -1158,11 +1160,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_kernel(const __gr
               store4(reinterpret_cast<__nv_bfloat16*>(pr.comb_y) + (long long)(row0 + r) * pr.ldo + col, a);
             }
           } else if (pr.out_f16) {
-            // fp16 terms of a per-token sum
+            // fp16 terms of a per-token sum (gradient terms: divided by 2^e)
             __half* outp = reinterpret_cast<__half*>(outv) + col;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              if (roff[j] >= 0) *reinterpret_cast<uint2*>(outp + roff[j]) = f16x4(v[j]);
+              if (roff[j] >= 0)
+                *reinterpret_cast<uint2*>(outp + roff[j]) =
+                    f16x4(make_float4(v[j].x * down, v[j].y * down, v[j].z * down, v[j].w * down));
           } else {
             float* outp = reinterpret_cast<float*>(outv) + col;
 #pragma unroll

@@ -87,6 +87,7 @@ bool fill_dgrad_gu(Params& P, Problem& pr, const DgradGuArgs& a) {
   pr.tx_bytes = A_BYTES + PairCfg<kPair>::B_BYTES;
   pr.out = a.dx;
   pr.out_f16 = 1;  // input-gradient rows: fp16 terms of the unpermute's sum
+  pr.out_scale = a.scale;
   pr.ldo = a.d;
   return true;
 }

@@ -73,7 +73,7 @@ cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const v
 }
 
 cudaError_t gemm_router_dx(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, int T, int d, int E,
-                           void* dx_r, int* status, cudaStream_t s) {
+                           void* dx_r, const uint32_t* scale, int* status, cudaStream_t s) {
   (void)status;
   Params P;
   std::memset(&P, 0, sizeof(P));
@@ -96,6 +96,7 @@ cudaError_t gemm_router_dx(const uint16_t* dl_hi, const uint16_t* dl_lo, const v
   pr.tx_bytes = A_BYTES + 4 * MN_BLOCK_BYTES;
   pr.out = dx_r;
   pr.out_f16 = 1;  // fp16 term of the unpermute's sum
+  pr.out_scale = scale;
   pr.ldo = d;
   P.num_problems = 1;
   return launch<0, 1, MGROUP, EPI_F32, 1>(P, (long long)cdiv_h(T, BM) * cdiv_h(d, 256), s, "gemm_router_dx");

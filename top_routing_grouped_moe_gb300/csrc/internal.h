@@ -63,11 +63,14 @@ inline int dgp_slots(int H) { return 2 * ((H + 255) / 256); }
 // dgates[t,s] = sum_p dgp[row_of_slot[t*k+s], p] (0 for dropped slots)
 cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_slot, int T, int k, float* dgates,
                                  cudaStream_t s);
-// dx[t] = sum_s dx_perm[row(t,s)] + dx_s[t] + dx_r[t]   (fp16 terms, fp32 sum;
-// dx_s and dx_r nullable; dx bf16)
+// dx[t] = 2^e (sum_s dx_perm[row(t,s)] + dx_s[t] + dx_r[t])   (fp16 terms, fp32
+// sum; dx_s and dx_r nullable; e from the scale word, NULL: e = 0; dx bf16)
 cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const void* dx_r,
-                                    const int32_t* row_of_slot, int T, int d, int k, void* dx, int* status,
-                                    cudaStream_t s);
+                                    const int32_t* row_of_slot, int T, int d, int k, const uint32_t* scale, void* dx,
+                                    int* status, cudaStream_t s);
+// the scale word of the backward's fp16 terms: zeroed, then the largest bf16
+// magnitude pattern of dY[n] (n a multiple of 8)
+cudaError_t launch_grad_scale(const void* dY, long long n, uint32_t* word, cudaStream_t s);
 // dlogits [T,E] fp32 (dense, + add[T,E] if add != NULL) and, if dl_hi != NULL,
 // its bf16 hi + lo halves [T,E]
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,
@@ -152,7 +155,8 @@ struct DgradGuArgs {      // dx = (dau_hi + dau_lo) [W_g; W_u]
   int G, d, H;
   const void* Wg;         // [G, H, d]
   const void* Wu;
-  void* dx;               // [rows, d] fp16
+  void* dx;               // [rows, d] fp16, divided by 2^e of the scale word
+  const uint32_t* scale;  // nullable (e = 0)
 };
 struct WgradArgs {        // out[g] = A_g^T B_g over rows [off[g], off[g+1])
   const void* A;          // [rows, M] bf16
@@ -188,9 +192,10 @@ cudaError_t launch_group_maps(const CUtensorMap* whole, const CUtensorMap* whole
 // dW_r partials: part[S, E, d] = split-K pieces of (dl_hi + dl_lo)^T x; dl halves [T, E] bf16
 cudaError_t gemm_router_dw(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* x, int T, int d, int E, int S,
                            float* part, int* status, cudaStream_t s);
-// dx_r [T, d] fp16 = (dl_hi + dl_lo) W_r, the router's term of the input gradient
+// dx_r [T, d] fp16 = (dl_hi + dl_lo) W_r / 2^e, the router's term of the input
+// gradient (e from the scale word; NULL: e = 0)
 cudaError_t gemm_router_dx(const uint16_t* dl_hi, const uint16_t* dl_lo, const void* W_r, int T, int d, int E,
-                           void* dx_r, int* status, cudaStream_t s);
+                           void* dx_r, const uint32_t* scale, int* status, cudaStream_t s);
 
 // MXFP8 expert GEMMs (E4M3 operands, tile-atom E8M0 scales).  A: [rows_total,
 // K] codes; rows of group g start at offsets[g] (a multiple of 128, or dense

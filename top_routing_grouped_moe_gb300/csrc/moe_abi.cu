@@ -402,8 +402,8 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
                            const float* au, const float* au_s, int T, int d, int E, int k, int H, int Hs,
                            const void* W_g, const void* W_u, const void* W_d, const void* Ws_g, const void* Ws_u,
                            const void* Ws_d, void* dx_perm, void* dx_s, void* dW_g, void* dW_u, void* dW_d,
-                           void* dWs_g, void* dWs_u, void* dWs_d, float* dgates, void* ws, size_t ws_bytes,
-                           void* stream) {
+                           void* dWs_g, void* dWs_u, void* dWs_d, float* dgates, uint32_t* dx_scale, void* ws,
+                           size_t ws_bytes, void* stream) {
   int rc = check_dims(T, d, E, k);
   if (rc) return rc;
   rc = check_hidden(H, Hs);
@@ -419,6 +419,8 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   for (const void* p : req16)
     if (!al16(p)) return MOE_ERR_INVALID_ARG;
   if (gather ? (!dY || !x || !al16(dY) || !al16(x)) : (!al16(dY_perm) || !al16(x_perm))) return MOE_ERR_INVALID_ARG;
+  // the scale of the fp16 input-gradient terms comes from dY
+  if (dx_scale && (!dY || !al16(dY))) return MOE_ERR_INVALID_ARG;
   if (Hs > 0) {
     const void* req_s[] = {dY, x, au_s, Ws_g, Ws_u, Ws_d, dx_s, dWs_g, dWs_u, dWs_d};
     for (const void* p : req_s)
@@ -433,13 +435,18 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   float* dgp = reinterpret_cast<float*>(w + L.dgp);
   const RowGather gdy = gather ? RowGather{dY, T, slot_of_row, k, R} : RowGather{};
   const RowGather gx = gather ? RowGather{x, T, slot_of_row, k, R} : RowGather{};
+  cudaError_t e = cudaSuccess;
+  if (dx_scale) {
+    e = launch_grad_scale(dY, (long long)T * d, dx_scale, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
 
   // 1. dgrad of the down projection with the SwiGLU backward epilogue
   DgradDownArgs r1{dY_perm, R, offsets, E, d, H, W_d, au, w + L.dau_hi, w + L.dau_lo, w + L.gh_hi, w + L.gh_lo,
                    gates, slot_of_row, R, dgp, gdy};
   DgradDownArgs s1{dY, T, nullptr, 1, d, Hs, Ws_d, au_s, w + L.s_dau_hi, w + L.s_dau_lo, w + L.s_gh_hi,
                    w + L.s_gh_lo, nullptr, nullptr, 0, nullptr};
-  cudaError_t e = gemm_dgrad_down(r1, Hs > 0 ? &s1 : nullptr, status, st);
+  e = gemm_dgrad_down(r1, Hs > 0 ? &s1 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
   e = launch_dgates_reduce(dgp, dgp_slots(H), row_of_slot, T, k, dgates, st);
   if (e != cudaSuccess) return fail_cuda(e);
@@ -455,8 +462,8 @@ int moe_grouped_swiglu_bwd(const void* dY_perm, const void* dY, const float* gat
   // 3. dx_perm = [da|du] [W_g; W_u]
   // routed rows carry their gate factor (g < 1), so their bf16 da|du error is
   // small next to the shared expert's; only the shared operand is split
-  DgradGuArgs r3{w + L.dau_hi, nullptr, R, offsets, E, d, H, W_g, W_u, dx_perm};
-  DgradGuArgs s3{w + L.s_dau_hi, w + L.s_dau_lo, T, nullptr, 1, d, Hs, Ws_g, Ws_u, dx_s};
+  DgradGuArgs r3{w + L.dau_hi, nullptr, R, offsets, E, d, H, W_g, W_u, dx_perm, dx_scale};
+  DgradGuArgs s3{w + L.s_dau_hi, w + L.s_dau_lo, T, nullptr, 1, d, Hs, Ws_g, Ws_u, dx_s, dx_scale};
   e = gemm_dgrad_gu(r3, Hs > 0 ? &s3 : nullptr, status, st);
   if (e != cudaSuccess) return fail_cuda(e);
 
@@ -600,7 +607,8 @@ int moe_unpermute_combine_mxfp8(const void* o_perm, const void* s_out, const flo
 }
 
 int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of_slot, const float* dlogits,
-                    const void* W_r, int T, int d, int E, int k, void* dx, void* ws, size_t ws_bytes, void* stream) {
+                    const void* W_r, int T, int d, int E, int k, void* dx, const uint32_t* dx_scale, void* ws,
+                    size_t ws_bytes, void* stream) {
   if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
   if (k > kMaxK || (d % 64) != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   if (!dx_perm || !row_of_slot || !dx) return MOE_ERR_INVALID_ARG;
@@ -608,7 +616,8 @@ int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of
   if ((dlogits == nullptr) != (W_r == nullptr)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!W_r)
-    return check(launch_unpermute_reduce(dx_perm, dx_s, nullptr, row_of_slot, T, d, k, dx, device_status_ptr(), st));
+    return check(
+        launch_unpermute_reduce(dx_perm, dx_s, nullptr, row_of_slot, T, d, k, dx_scale, dx, device_status_ptr(), st));
   int rc = check_dims(T, d, E, k);
   if (rc) return rc;
   if (!al16(W_r)) return MOE_ERR_INVALID_ARG;
@@ -618,9 +627,10 @@ int moe_permute_bwd(const void* dx_perm, const void* dx_s, const int32_t* row_of
   cudaError_t e = launch_f32_to_bf16_split(dlogits, dl_hi, dl_lo, (long long)T * E, st);
   if (e != cudaSuccess) return fail_cuda(e);
   void* dx_r = static_cast<char*>(ws) + 2 * align256((size_t)T * E * 2);  // fp16 [T, d]
-  e = gemm_router_dx(dl_hi, dl_lo, W_r, T, d, E, dx_r, device_status_ptr(), st);
+  e = gemm_router_dx(dl_hi, dl_lo, W_r, T, d, E, dx_r, dx_scale, device_status_ptr(), st);
   if (e != cudaSuccess) return fail_cuda(e);
-  return check(launch_unpermute_reduce(dx_perm, dx_s, dx_r, row_of_slot, T, d, k, dx, device_status_ptr(), st));
+  return check(
+      launch_unpermute_reduce(dx_perm, dx_s, dx_r, row_of_slot, T, d, k, dx_scale, dx, device_status_ptr(), st));
 }
 
 }  // extern "C"

@@ -370,9 +370,26 @@ __global__ void dgates_reduce_kernel(const float* __restrict__ dgp, int P, const
 }
 
 // fp16 terms, fp32 accumulation, one bf16 rounding of dx
+// The scale word of the backward's fp16 terms: the largest bf16 magnitude
+// pattern of the upstream gradient (grid-stride over 16-byte chunks, a warp
+// maximum, one atomicMax per warp into the zeroed word).
+__global__ void grad_amax_kernel(const uint4* __restrict__ src, long long n16, unsigned* __restrict__ word) {
+  dependency_wait();
+  unsigned m = 0u;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = max(m, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0 && m) atomicMax(word, m);
+}
+
 __global__ void unpermute_reduce_kernel(const __half* __restrict__ dx_perm, const __half* __restrict__ dx_s,
                                         const __half* __restrict__ dx_r, const int32_t* __restrict__ row_of_slot,
-                                        int T, int d, int k, long long max_rows, uint4* __restrict__ dx, int* status) {
+                                        int T, int d, int k, long long max_rows, const unsigned* __restrict__ scale,
+                                        uint4* __restrict__ dx, int* status) {
   dependency_wait();
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -388,6 +405,8 @@ __global__ void unpermute_reduce_kernel(const __half* __restrict__ dx_perm, cons
   int rows[kMaxK];
 #pragma unroll
   for (int s = 0; s < kMaxK; ++s) rows[s] = __shfl_sync(0xffffffffu, row, s < k ? s : 0);
+  // the terms hold v / 2^e (scale word; none: e = 0)
+  const float up = scale ? pow2f(grad_scale_exp(__ldg(scale))) : 1.0f;
   const int vpr = d / 8;
   for (int c = lane; c < vpr; c += 32) {
     float acc[8];
@@ -412,6 +431,8 @@ __global__ void unpermute_reduce_kernel(const __half* __restrict__ dx_perm, cons
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] += v[e];
     }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= up;
     bool fin = true;
 #pragma unroll
     for (int e = 0; e < 8; ++e) fin &= isfinite(acc[e]);
@@ -706,12 +727,22 @@ cudaError_t launch_dgates_reduce(const float* dgp, int P, const int32_t* row_of_
 }
 
 cudaError_t launch_unpermute_reduce(const void* dx_perm, const void* dx_s, const void* dx_r,
-                                    const int32_t* row_of_slot, int T, int d, int k, void* dx, int* status,
-                                    cudaStream_t s) {
+                                    const int32_t* row_of_slot, int T, int d, int k, const uint32_t* scale, void* dx,
+                                    int* status, cudaStream_t s) {
   timing_mark(s, "unpermute_reduce");
   return launch_pdl(unpermute_reduce_kernel, dim3(warp_blocks(T)), dim3(32 * kWarpsPerBlock), 0, s,
       static_cast<const __half*>(dx_perm), static_cast<const __half*>(dx_s), static_cast<const __half*>(dx_r),
-      row_of_slot, T, d, k, (long long)T * k, static_cast<uint4*>(dx), status);
+      row_of_slot, T, d, k, (long long)T * k, scale, static_cast<uint4*>(dx), status);
+}
+
+cudaError_t launch_grad_scale(const void* dY, long long n, uint32_t* word, cudaStream_t s) {
+  timing_mark(s, "memset_grad_scale");
+  cudaError_t e = cudaMemsetAsync(word, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  const long long n16 = n / 8;  // 8 bf16 per 16 bytes (rows are multiples of 64 values)
+  timing_mark(s, "grad_amax");
+  return launch_pdl(grad_amax_kernel, dim3(flat_blocks(n16, 256)), dim3(256), 0, s, static_cast<const uint4*>(dY),
+                    n16, word);
 }
 
 cudaError_t launch_router_bwd_dl(const float* dgates, const float* gates, const int32_t* idx, int T, int E, int k,

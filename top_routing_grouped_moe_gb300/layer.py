@@ -73,6 +73,8 @@ class MoELayer:
             self.dWs_u = e(Hs, d) if Hs else None
             self.dWs_d = e(d, Hs) if Hs else None
             self.dlogits = e(T, E, dt=torch.float32)
+            # scale word of the fp16 input-gradient terms (the max |dY| pattern)
+            self.dx_scale = e(1, dt=torch.int32)
             self.dW_r = e(E, d, dt=torch.float32)
             self.dx = e(T, d)
 
@@ -122,11 +124,12 @@ class MoELayer:
                                  self.x_perm, x, self.au, self.au_s, T, d, E, k, H, Hs, p["W_g"], p["W_u"],
                                  p["W_d"], p.get("Ws_g"), p.get("Ws_u"), p.get("Ws_d"), self.dx_perm, self.dx_s,
                                  self.dW_g, self.dW_u, self.dW_d, self.dWs_g, self.dWs_u, self.dWs_d, self.dgates,
-                                 self.ws, self.ws_bytes, stream)
+                                 self.ws, self.ws_bytes, stream, dx_scale=self.dx_scale)
         lr = learned_router and p.get("W_r") is not None
         B.moe_route_topk_bwd(self.dgates, self.gates, self.idx, x if lr else None, T, d, E, k, self.dlogits,
                              self.dW_r if lr else None, self.ws, self.ws_bytes, stream,
                              dlogits_add=self.dlogits_lbl if self.balance_alpha > 0 else None)
         B.moe_permute_bwd(self.dx_perm, self.dx_s, self.row_of_slot, self.dlogits if lr else None,
-                          p.get("W_r") if lr else None, T, d, E, k, self.dx, self.ws, self.ws_bytes, stream)
+                          p.get("W_r") if lr else None, T, d, E, k, self.dx, self.ws, self.ws_bytes, stream,
+                          dx_scale=self.dx_scale)
         return self.dx
