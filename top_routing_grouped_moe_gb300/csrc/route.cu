@@ -371,17 +371,30 @@ __global__ void dgates_reduce_kernel(const float* __restrict__ dgp, int P, const
 
 // fp16 terms, fp32 accumulation, one bf16 rounding of dx
 // The scale word of the backward's fp16 terms: the largest bf16 magnitude
-// pattern of the upstream gradient (grid-stride over 16-byte chunks, a warp
-// maximum, one atomicMax per warp into the zeroed word).
+// pattern of the upstream gradient (grid-stride over 16-byte chunks, four
+// independent loads in flight per thread, a warp maximum, one atomicMax per
+// warp into the zeroed word).
+__device__ __forceinline__ unsigned bf16x8_mag_max(const uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  unsigned m = 0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m = max(m, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+  return m;
+}
+
 __global__ void grad_amax_kernel(const uint4* __restrict__ src, long long n16, unsigned* __restrict__ word) {
   dependency_wait();
   unsigned m = 0u;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
-    const uint4 v = __ldg(src + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const long long step = (long long)gridDim.x * blockDim.x;
+  long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  for (; i + 3 * step < n16; i += 4 * step) {
+    uint4 v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) m = max(m, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(src + i + u * step);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) m = max(m, bf16x8_mag_max(v[u]));
   }
+  for (; i < n16; i += step) m = max(m, bf16x8_mag_max(__ldg(src + i)));
   m = __reduce_max_sync(0xffffffffu, m);
   if ((threadIdx.x & 31) == 0 && m) atomicMax(word, m);
 }
