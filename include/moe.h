@@ -22,7 +22,12 @@
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
  *     documented otherwise.  The library never allocates or frees device
  *     memory; scratch space comes from a caller workspace of at least
- *     moe_workspace_size() bytes, 256-byte aligned.
+ *     moe_workspace_size() bytes, 256-byte aligned.  Every call uses its
+ *     workspace from the start, so calls that share one workspace must be
+ *     ordered on the GPU (one stream, or events between streams); calls on
+ *     different workspaces and buffers may run concurrently.  The host side
+ *     is thread-safe (per-thread error and timing state, per-device caches
+ *     under a lock).
  *   - Tensors are dense and row-major.  "bf16" = IEEE bfloat16 bit patterns
  *     (uint16 storage).  Device pointers of bf16/fp32 tensors must be 16-byte
  *     aligned.
