@@ -91,3 +91,32 @@ def test_launch_timing_eager_and_inside_a_graph(B):
         assert [n for n, _ in got if not n.startswith("memset")] == names
         assert all(ms >= 0 for _, ms in got) and sum(ms for _, ms in got) > 0
     assert B.moe_device_status() == 0
+
+
+def test_two_layers_on_two_streams_at_once(B):
+    """Two layers (their own buffers and workspaces) stepping on two streams
+    at the same time -- persistent GEMMs and programmatic launches of both
+    interleaving on the SMs -- give the same bits as when each steps alone."""
+    from top_routing_grouped_moe_gb300.layer import MoELayer
+    from tests.test_gpu_determinism import snapshot
+    ws = [CASES["learned_shared"], CASES["zipf_capacity"]]
+    devs = [upload(workloads.make_inputs(w)) for w in ws]
+    layers = [MoELayer(w.T, w.d, w.E, w.k, w.H, w.Hs, w.capacity) for w in ws]
+    alone = []
+    for w, dev, layer in zip(ws, devs, layers):
+        step(layer, w, dev)
+        torch.cuda.synchronize()
+        alone.append(snapshot(layer))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        for w, dev, layer, s in zip(ws, devs, layers, streams):
+            with torch.cuda.stream(s):
+                step(layer, w, dev, stream=s)
+    torch.cuda.synchronize()
+    assert B.moe_device_status() == 0
+    for layer, ref in zip(layers, alone):
+        got = snapshot(layer)
+        for n in ref:
+            assert torch.equal(got[n].view(torch.uint8), ref[n].view(torch.uint8)), n
