@@ -376,12 +376,18 @@ def main_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
 
     import __graft_entry__
+    # one build per node: local rank 0 compiles (if anything changed) while
+    # the other ranks wait, then find it up to date
+    if world > 1 and local != 0:
+        dist.barrier()
     __graft_entry__.build()
+    if world > 1 and local == 0:
+        dist.barrier()
     from top_routing_grouped_moe_gb300 import _binding as B
     from top_routing_grouped_moe_gb300.layer import MoELayer
 
